@@ -1,0 +1,361 @@
+/*
+ * oracle.c — plain fp64 CPU reference of the speculative-decoding verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY: see oracle.h for who may call it and for the
+ * sources each function follows. Nothing here is blocked, fused or reordered
+ * beyond what the method states; rows are computed lazily, in the order the
+ * sequential accept test reaches them, as the pages' loops do.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------ storage */
+
+static double load_logit(const void* base, int dtype, int64_t i) {
+  if (dtype == 1) {
+    uint32_t u = (uint32_t)((const uint16_t*)base)[i] << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return (double)f;
+  }
+  return (double)((const float*)base)[i];
+}
+
+static void load_row(const void* base, int dtype, int64_t row, int64_t V, double* l) {
+  for (int64_t v = 0; v < V; ++v) l[v] = load_logit(base, dtype, row * V + v);
+}
+
+/* Sampling mode: a row is usable when it holds no NaN, no +inf, and at least
+ * one finite value (otherwise softmax is undefined). */
+static int row_ok_sampling(const double* l, int64_t V) {
+  int any_finite = 0;
+  for (int64_t v = 0; v < V; ++v) {
+    if (isnan(l[v]) || l[v] == INFINITY) return 0;
+    if (l[v] != -INFINITY) any_finite = 1;
+  }
+  return any_finite;
+}
+
+static int row_has_nan(const double* l, int64_t V) {
+  for (int64_t v = 0; v < V; ++v)
+    if (isnan(l[v])) return 1;
+  return 0;
+}
+
+/* ----------------------------------------------------- distributions */
+
+/* Temperature-scaled softmax, [P2] §3.4 / [P1] §4: z = l / T, then
+ * p_v = exp(z_v - M) / sum_w exp(z_w - M) with M = max z. Returns log of the
+ * normaliser (lse) and M through the pointers. */
+static void softmax_T(const double* l, int64_t V, double T, double* p, double* M_out, double* lse_out) {
+  double M = -INFINITY;
+  for (int64_t v = 0; v < V; ++v) {
+    double z = l[v] / T;
+    if (z > M) M = z;
+  }
+  double S = 0.0;
+  for (int64_t v = 0; v < V; ++v) {
+    double e = (l[v] == -INFINITY) ? 0.0 : exp(l[v] / T - M);
+    p[v] = e;
+    S += e;
+  }
+  for (int64_t v = 0; v < V; ++v) p[v] /= S;
+  if (M_out) *M_out = M;
+  if (lse_out) *lse_out = M + log(S);
+}
+
+typedef struct {
+  double val;
+  int64_t idx;
+} val_idx;
+
+static int by_value_desc(const void* a, const void* b) {
+  const val_idx* x = (const val_idx*)a;
+  const val_idx* y = (const val_idx*)b;
+  if (x->val > y->val) return -1;
+  if (x->val < y->val) return 1;
+  return (x->idx > y->idx) - (x->idx < y->idx);
+}
+
+/* Top-p nucleus, [P2] §3.4 and §5.2: keep the tokens whose stored logit is at
+ * least tau, where tau is the largest stored value whose upper set
+ * {v : l_v >= tau} holds probability >= top_p; every token tied at the cut is
+ * kept. Found by sorting the row in descending order and accumulating p until
+ * it reaches top_p. The kept probabilities are renormalised to sum to one
+ * (p'_v = p_v / P_S), the rest set to zero. Returns P_S and tau; *margin gets
+ * min(top_p - mass strictly above tau, P_S - top_p). */
+static void nucleus(const double* l, double* p, int64_t V, double top_p, val_idx* scratch, double* PS_out,
+                    double* tau_out, double* margin) {
+  for (int64_t v = 0; v < V; ++v) {
+    scratch[v].val = l[v];
+    scratch[v].idx = v;
+  }
+  qsort(scratch, (size_t)V, sizeof(val_idx), by_value_desc);
+  double cum = 0.0, tau = scratch[V - 1].val;
+  for (int64_t r = 0; r < V; ++r) {
+    cum += p[scratch[r].idx];
+    if (cum >= top_p) {
+      tau = scratch[r].val;
+      break;
+    }
+  }
+  double above = 0.0, PS = 0.0;
+  for (int64_t v = 0; v < V; ++v) {
+    if (l[v] > tau) above += p[v];
+    if (l[v] >= tau) PS += p[v];
+  }
+  for (int64_t v = 0; v < V; ++v) p[v] = (l[v] >= tau) ? p[v] / PS : 0.0;
+  if (PS_out) *PS_out = PS;
+  if (tau_out) *tau_out = tau;
+  if (margin) {
+    double m = fmin(top_p - above, PS - top_p);
+    if (m < *margin) *margin = m;
+  }
+}
+
+/* The sampling distribution of one row: softmax at T, then top-p. */
+static void row_dist(const double* l, int64_t V, double T, double top_p, double* p, val_idx* scratch,
+                     double* margin) {
+  softmax_T(l, V, T, p, NULL, NULL);
+  if (top_p < 1.0) nucleus(l, p, V, top_p, scratch, NULL, NULL, margin);
+}
+
+/* Inverse-CDF draw from unnormalised weights w (ascending vocabulary order):
+ * the smallest t with C_t = sum_{v<=t} w_v > u * Z, Z = sum_v w_v. If rounding
+ * leaves u*Z at or past the last partial sum, the largest t with w_t > 0. */
+static int64_t inverse_cdf(const double* w, int64_t V, double u, double* margin) {
+  double Z = 0.0;
+  for (int64_t v = 0; v < V; ++v) Z += w[v];
+  double target = u * Z, C = 0.0;
+  for (int64_t t = 0; t < V; ++t) {
+    double prev = C;
+    C += w[t];
+    if (C > target) {
+      if (margin) {
+        double m = fmin(target - prev, C - target) / Z;
+        if (m < *margin) *margin = m;
+      }
+      return t;
+    }
+  }
+  if (margin) *margin = 0.0;
+  for (int64_t t = V - 1; t >= 0; --t)
+    if (w[t] > 0.0) return t;
+  return V - 1;
+}
+
+/* Argmax with the lowest index among equal maxima (numeric order, so -0 and
+ * +0 tie). */
+static int64_t argmax_lowest(const double* l, int64_t V) {
+  int64_t best = 0;
+  for (int64_t v = 1; v < V; ++v)
+    if (l[v] > l[best]) best = v;
+  return best;
+}
+
+/* ---------------------------------------------------------- sampling */
+
+int oracle_verify_sample(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                         const float* uniforms, int64_t B, int32_t K, int64_t V, float temperature, float top_p,
+                         int32_t* out_tokens, int32_t* out_accept_len, double* out_margin) {
+  if (!target || !draft_tokens || !out_tokens || !out_accept_len) return -1;
+  if (B < 0 || K < 1 || V < 2 || (dtype != 0 && dtype != 1)) return -1;
+  if (!(temperature >= 0.0f) || !(top_p > 0.0f && top_p <= 1.0f)) return -1;
+  const int greedy_limit = (temperature == 0.0f);
+  if (!greedy_limit && (!draft || !uniforms)) return -1;
+  const double T = (double)temperature;
+  const double P = (double)top_p;
+
+  double* lt = (double*)malloc(sizeof(double) * (size_t)V);
+  double* ld = (double*)malloc(sizeof(double) * (size_t)V);
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  double* w = (double*)malloc(sizeof(double) * (size_t)V);
+  val_idx* scratch = (val_idx*)malloc(sizeof(val_idx) * (size_t)V);
+  if (!lt || !ld || !p || !q || !w || !scratch) {
+    free(lt); free(ld); free(p); free(q); free(w); free(scratch);
+    return -1;
+  }
+
+  for (int64_t b = 0; b < B; ++b) {
+    int32_t* out = out_tokens + b * (K + 1);
+    const int32_t* x = draft_tokens + b * K;
+    const float* u = greedy_limit ? NULL : uniforms + b * (K + 1);
+    double margin = INFINITY;
+    for (int i = 0; i <= K; ++i) out[i] = -1;
+
+    /* Input checks cover every row and token of the sequence, whichever the
+     * accept test later reaches. */
+    int ok = 1;
+    for (int i = 0; i < K; ++i) ok &= (x[i] >= 0 && (int64_t)x[i] < V);
+    if (!greedy_limit)
+      for (int i = 0; i <= K; ++i) ok &= (u[i] >= 0.0f && u[i] < 1.0f);
+    for (int i = 0; ok && i <= K; ++i) {
+      load_row(target, dtype, b * (K + 1) + i, V, lt);
+      ok = greedy_limit ? !row_has_nan(lt, V) : row_ok_sampling(lt, V);
+    }
+    for (int i = 0; ok && !greedy_limit && i < K; ++i) {
+      load_row(draft, dtype, b * K + i, V, ld);
+      ok = row_ok_sampling(ld, V);
+    }
+    if (!ok) {
+      out_accept_len[b] = -1;
+      if (out_margin) out_margin[b] = INFINITY;
+      continue;
+    }
+
+    if (greedy_limit) {
+      /* T -> 0: p_i is one-hot at its argmax, so x_i is accepted iff it is
+       * that argmax; the residual at a rejection and the bonus are argmaxes. */
+      int j = K;
+      for (int i = 0; i < K; ++i) {
+        load_row(target, dtype, b * (K + 1) + i, V, lt);
+        int64_t a = argmax_lowest(lt, V);
+        if ((int64_t)x[i] == a) {
+          out[i] = x[i];
+        } else {
+          out[i] = (int32_t)a;
+          j = i;
+          break;
+        }
+      }
+      if (j == K) {
+        load_row(target, dtype, b * (K + 1) + K, V, lt);
+        out[K] = (int32_t)argmax_lowest(lt, V);
+      }
+      out_accept_len[b] = j;
+      if (out_margin) out_margin[b] = INFINITY;
+      continue;
+    }
+
+    /* [P1] §2.3: test x_0, x_1, ... in order; stop at the first rejection. */
+    int j = K;
+    for (int i = 0; i < K; ++i) {
+      load_row(target, dtype, b * (K + 1) + i, V, lt);
+      load_row(draft, dtype, b * K + i, V, ld);
+      row_dist(lt, V, T, P, p, scratch, &margin); /* p_i (target) */
+      row_dist(ld, V, T, P, q, scratch, &margin); /* q_i (draft)  */
+      const double px = p[x[i]], qx = q[x[i]];
+      /* [P1] §2.1, [P2] §3.1: alpha = min(1, p(x)/q(x)). A zero q(x) with a
+       * positive p(x) gives alpha = 1 (the pages' p/(q+eps)); p(x) = 0 gives
+       * alpha = 0. */
+      double alpha;
+      if (px == 0.0)
+        alpha = 0.0;
+      else if (qx == 0.0)
+        alpha = 1.0;
+      else
+        alpha = fmin(1.0, px / qx);
+      double du = fabs((double)u[i] - alpha);
+      if (du < margin) margin = du;
+      if ((double)u[i] < alpha) { /* [P2] §3.1: r < alpha accepts */
+        out[i] = x[i];
+        continue;
+      }
+      /* Rejected at i: draw from norm(max(0, p - q)) ([P1] §2.1-2.2); if that
+       * residual is all zero, draw from p instead ([P1] §4). */
+      double Z = 0.0;
+      for (int64_t v = 0; v < V; ++v) {
+        w[v] = fmax(0.0, p[v] - q[v]);
+        Z += w[v];
+      }
+      out[i] = (int32_t)inverse_cdf(Z > 0.0 ? w : p, V, (double)u[K], &margin);
+      j = i;
+      break;
+    }
+    if (j == K) {
+      /* All K accepted: the bonus token from the target's distribution at
+       * position K ([P1] §2.3, [P2] §3.1). */
+      load_row(target, dtype, b * (K + 1) + K, V, lt);
+      row_dist(lt, V, T, P, p, scratch, &margin);
+      out[K] = (int32_t)inverse_cdf(p, V, (double)u[K], &margin);
+    }
+    out_accept_len[b] = j;
+    if (out_margin) out_margin[b] = margin;
+  }
+  free(lt); free(ld); free(p); free(q); free(w); free(scratch);
+  return 0;
+}
+
+int oracle_row_stats(const void* rows, int dtype, int64_t nrows, int64_t V, float temperature, float top_p,
+                     double* out) {
+  if (!rows || !out || nrows < 0 || V < 1 || (dtype != 0 && dtype != 1)) return -1;
+  if (!(temperature > 0.0f) || !(top_p > 0.0f && top_p <= 1.0f)) return -1;
+  double* l = (double*)malloc(sizeof(double) * (size_t)V);
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  val_idx* scratch = (val_idx*)malloc(sizeof(val_idx) * (size_t)V);
+  if (!l || !p || !scratch) {
+    free(l); free(p); free(scratch);
+    return -1;
+  }
+  for (int64_t r = 0; r < nrows; ++r) {
+    load_row(rows, dtype, r, V, l);
+    double M, lse, PS = 1.0, tau = -INFINITY;
+    softmax_T(l, V, (double)temperature, p, &M, &lse);
+    if (top_p < 1.0f) nucleus(l, p, V, (double)top_p, scratch, &PS, &tau, NULL);
+    out[4 * r + 0] = M;
+    out[4 * r + 1] = lse;
+    out[4 * r + 2] = PS;
+    out[4 * r + 3] = tau;
+  }
+  free(l); free(p); free(scratch);
+  return 0;
+}
+
+/* ------------------------------------------------------------- greedy */
+
+int oracle_verify_greedy(const void* logits, int dtype, const int32_t* cand, int64_t B, int32_t G, int32_t N,
+                         int64_t V, int32_t* out_tokens, int32_t* out_accept_len, int32_t* out_best) {
+  if (!logits || !cand || !out_tokens || !out_accept_len) return -1;
+  if (B < 0 || G < 1 || N < 2 || V < 2 || (dtype != 0 && dtype != 1)) return -1;
+  double* l = (double*)malloc(sizeof(double) * (size_t)V);
+  int64_t* a = (int64_t*)malloc(sizeof(int64_t) * (size_t)G * (size_t)N);
+  if (!l || !a) {
+    free(l); free(a);
+    return -1;
+  }
+  for (int64_t b = 0; b < B; ++b) {
+    int32_t* out = out_tokens + b * N;
+    for (int n = 0; n < N; ++n) out[n] = -1;
+    int ok = 1;
+    for (int64_t k = 0; k < (int64_t)G * (N - 1); ++k) {
+      int32_t c = cand[b * G * (N - 1) + k];
+      ok &= (c >= 0 && (int64_t)c < V);
+    }
+    /* a_{g,n} = argmax of row (g, n), lowest index among equal maxima. */
+    for (int g = 0; ok && g < G; ++g)
+      for (int n = 0; ok && n < N; ++n) {
+        load_row(logits, dtype, (b * G + g) * N + n, V, l);
+        if (row_has_nan(l, V)) ok = 0;
+        a[g * N + n] = argmax_lowest(l, V);
+      }
+    if (!ok) {
+      out_accept_len[b] = -1;
+      if (out_best) out_best[b] = -1;
+      continue;
+    }
+    /* [P4] verify branch: candidate token n must equal the argmax at n; the
+     * longest matched prefix wins (lowest g on ties), then one bonus token. */
+    int best_g = 0, best_L = -1;
+    for (int g = 0; g < G; ++g) {
+      const int32_t* c = cand + (b * G + g) * (N - 1);
+      int L = 0;
+      while (L < N - 1 && (int64_t)c[L] == a[g * N + L]) ++L;
+      if (L > best_L) {
+        best_L = L;
+        best_g = g;
+      }
+    }
+    const int32_t* c = cand + (b * G + best_g) * (N - 1);
+    for (int n = 0; n < best_L; ++n) out[n] = c[n];
+    out[best_L] = (int32_t)a[best_g * N + best_L];
+    out_accept_len[b] = best_L;
+    if (out_best) out_best[b] = best_g;
+  }
+  free(l);
+  free(a);
+  return 0;
+}

@@ -1,0 +1,226 @@
+"""Checks that pin the CPU oracle to what the pages and the mathematics fix.
+
+Each check takes the oracle library to test (``lib``), so the same check can be
+run against the real oracle and against builds with a planted mistake
+(tests/test_oracle_mutations.py), which it must reject.
+
+Sources (page title, section):
+  "Speculative Decoding —— LLM推理优化技术（一）" (hustzhy.cn), §2.2: the output
+      follows p; §2.4: E[accept] = 1 - TV(p, q); §3.1: tokens per round
+      (1 - a^(K+1)) / (1 - a).
+  "Lookahead Decoding 完全拆解" (pinghaoyang.com.cn), scaling-law section,
+      eq. (5): E[#tokens] = (g+1) - sum_{i=1..g} (1 - a^i)^b for b drafts.
+"""
+from __future__ import annotations
+
+import itertools
+import math
+import os
+
+import numpy as np
+from scipy import stats
+
+import oracle
+import specgen as sg
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def softmax(l, T=1.0):
+    z = np.asarray(l, np.float64) / T
+    e = np.exp(z - z.max())
+    return e / e.sum()
+
+
+def nucleus_bruteforce(l, p, top_p):
+    """The largest threshold whose upper set holds >= top_p (all distinct values tried)."""
+    l = np.asarray(l, np.float64)
+    for tau in sorted(set(l.tolist()), reverse=True):
+        if p[l >= tau].sum() >= top_p:
+            return tau
+    return l.min()
+
+
+def dist(l, T, top_p=1.0):
+    p = softmax(l, T)
+    if top_p < 1:
+        tau = nucleus_bruteforce(l, p, top_p)
+        p = np.where(np.asarray(l) >= tau, p, 0.0)
+        p /= p.sum()
+    return p
+
+
+def replicate(target_rows, draft_rows, n):
+    t = np.broadcast_to(np.asarray(target_rows, np.float32), (n,) + np.shape(target_rows)).copy()
+    d = np.broadcast_to(np.asarray(draft_rows, np.float32), (n,) + np.shape(draft_rows)).copy()
+    return t, d
+
+
+# Fixed small rows used by the statistical checks (V = 8).
+LT = np.array([[1.0, 0.5, -0.3, 2.0, 0.0, -1.0, 1.5, 0.2],
+               [0.3, 1.7, -0.5, 0.1, 1.1, -2.0, 0.4, 0.9]], np.float32)
+LD = np.array([[0.2, 1.1, 0.4, 1.2, 0.9, -0.2, 0.3, 1.0]], np.float32)
+
+
+def check_output_is_target_distribution(lib, T=1.0, top_p=1.0, n=1_000_000, seed=11):
+    """§2.2: the emitted token at position 0 follows p_0 (chi-square, df = V-1);
+    given all K=1 draft tokens accepted, the bonus follows p_1."""
+    V = LT.shape[1]
+    target, draft = replicate(LT, LD, n)
+    toks = sg.draft_tokens(draft, sg.F32, T, top_p, seed=seed)
+    u = sg.uniforms(n, 1, seed=seed)
+    out, acc, _ = oracle.verify_sample(target, draft, toks, u, T, top_p, lib=lib)
+    assert (acc >= 0).all()
+    for pos, rows in ((0, np.ones(n, bool)), (1, acc == 1)):
+        p = dist(LT[pos], T, top_p)
+        c = np.bincount(out[rows, pos], minlength=V)
+        keep = p > 0
+        assert c[~keep].sum() == 0, "emitted a token outside the target's support"
+        _, pval = stats.chisquare(c[keep], p[keep] * rows.sum())
+        assert pval > 1e-3, f"position {pos}: chi-square p-value {pval:.3g}"
+
+
+def check_acceptance_is_one_minus_tv(lib, T=1.0, n=1_000_000, seed=12):
+    """§2.4: P(accept x_0) = sum_x min(p, q) = 1 - TV(p, q), within 4 sigma."""
+    target, draft = replicate(LT, LD, n)
+    toks = sg.draft_tokens(draft, sg.F32, T, 1.0, seed=seed)
+    u = sg.uniforms(n, 1, seed=seed)
+    _, acc, _ = oracle.verify_sample(target, draft, toks, u, T, 1.0, lib=lib)
+    p, q = softmax(LT[0], T), softmax(LD[0], T)
+    alpha = np.minimum(p, q).sum()
+    assert abs(alpha - (1 - 0.5 * np.abs(p - q).sum())) < 1e-12
+    rate = (acc == 1).mean()
+    assert abs(rate - alpha) < 4 * math.sqrt(alpha * (1 - alpha) / n), (rate, alpha)
+
+
+def check_tokens_per_round(lib, K, n=200_000, seed=13):
+    """§3.1: with the same (p, q) at every position, acceptances are iid with
+    rate a and E[tokens per round] = (1 - a^(K+1)) / (1 - a)."""
+    lt = LT[0]
+    ld = LD[0]
+    target, draft = replicate(np.tile(lt, (K + 1, 1)), np.tile(ld, (K, 1)), n)
+    toks = sg.draft_tokens(draft, sg.F32, 1.0, 1.0, seed=seed + K)
+    u = sg.uniforms(n, K, seed=seed + K)
+    _, acc, _ = oracle.verify_sample(target, draft, toks, u, 1.0, 1.0, lib=lib)
+    a = np.minimum(softmax(lt), softmax(ld)).sum()
+    expect = (1 - a ** (K + 1)) / (1 - a)
+    tokens = acc + 1.0
+    assert abs(tokens.mean() - expect) < 4 * tokens.std() / math.sqrt(n), (tokens.mean(), expect)
+
+
+# Distributions whose probabilities are multiples of 1/8, so that every accept
+# threshold and every CDF edge is a multiple of 1/16 and a midpoint grid of
+# uniforms integrates the oracle's decisions exactly.
+NICE_P = [np.array([3, 3, 1, 1]) / 8, np.array([1, 2, 4, 1]) / 8, np.array([1, 1, 2, 4]) / 8]
+NICE_Q = [np.array([2, 2, 2, 2]) / 8, np.array([2, 1, 1, 4]) / 8]
+
+
+def closed_form_mass(K, j, t):
+    """§2.2-2.3: P(output = t_0..t_j with accept length j)
+    = prod_{i<j} min(p_i, q_i)(t_i) * (max(0, p_j - q_j)(t_j) if j < K else p_K(t_K))."""
+    m = 1.0
+    for i in range(j):
+        m *= min(NICE_P[i][t[i]], NICE_Q[i][t[i]])
+    if j < K:
+        m *= max(0.0, NICE_P[j][t[j]] - NICE_Q[j][t[j]])
+    else:
+        m *= NICE_P[K][t[K]]
+    return m
+
+
+def check_brute_force(lib, K=2, n=16):
+    """Enumerate every draft tuple (weight prod q_i(x_i)) and a midpoint grid
+    of n^(K+1) uniform vectors; the mass of each output equals the closed form."""
+    V = 4
+    lt = np.log(np.array(NICE_P[: K] + [NICE_P[K]]))
+    ld = np.log(np.array(NICE_Q[:K]))
+    grid = (np.arange(n) + 0.5) / n
+    U = np.array(list(itertools.product(grid, repeat=K + 1)), np.float32)
+    B = U.shape[0]
+    target, draft = replicate(lt, ld, B)
+    mass = {}
+    for x in itertools.product(range(V), repeat=K):
+        w = np.prod([NICE_Q[i][x[i]] for i in range(K)])
+        if w == 0:
+            continue
+        toks = np.tile(np.array(x, np.int32), (B, 1))
+        out, acc, _ = oracle.verify_sample(target, draft, toks, U, 1.0, 1.0, lib=lib)
+        assert (acc >= 0).all()
+        keys, counts = np.unique(np.concatenate([acc[:, None], out], 1), axis=0, return_counts=True)
+        for k, c in zip(keys, counts):
+            key = (int(k[0]),) + tuple(int(v) for v in k[1: 2 + k[0]])
+            mass[key] = mass.get(key, 0.0) + w * c / B
+    total = 0.0
+    for j in range(K + 1):
+        for t in itertools.product(range(V), repeat=j + 1):
+            expect = closed_form_mass(K, j, t)
+            got = mass.get((j,) + t, 0.0)
+            assert abs(got - expect) < 1e-9, ((j,) + t, got, expect)
+            total += expect
+    assert abs(total - 1.0) < 1e-12
+    assert abs(sum(mass.values()) - 1.0) < 1e-9
+
+
+def load_topp_golden():
+    cases = []
+    for line in open(os.path.join(GOLDEN, "topp_ties.txt")):
+        if not line.strip() or line.startswith("#"):
+            continue
+        head, logits, kept, ps, tau = [s.strip() for s in line.split(";")]
+        T, top_p = (float(x) for x in head.split())
+        cases.append((T, top_p, np.array(logits.split(), np.float32), [int(k) for k in kept.split()],
+                      float(ps), float(tau)))
+    return cases
+
+
+def check_topp_golden(lib):
+    for T, top_p, l, kept, ps, tau in load_topp_golden():
+        st = oracle.row_stats(l[None, :], T, top_p, lib=lib)[0]
+        assert abs(st[2] - ps) < 2e-6, (T, top_p, st, ps)
+        assert st[3] == tau, (T, top_p, st, tau)
+        assert sorted(np.nonzero(l >= st[3])[0].tolist()) == kept
+
+
+def load_greedy_golden():
+    lines = [l.strip() for l in open(os.path.join(GOLDEN, "greedy_hand.txt")) if l.strip() and l[0] != "#"]
+    cases, i = [], 0
+    while i < len(lines):
+        _, G, N, V = lines[i].split()
+        G, N, V = int(G), int(N), int(V)
+        rows = [[float(x) for x in lines[i + 1 + r].split()] for r in range(G * N)]
+        cand = [[int(x) for x in lines[i + 1 + G * N + g].split()] for g in range(G)]
+        exp = lines[i + 1 + G * N + G]
+        toks, acc, best = [s.strip() for s in exp[len("expect"):].split(";")]
+        cases.append((np.array(rows, np.float32).reshape(1, G, N, V), np.array(cand, np.int32).reshape(1, G, N - 1),
+                      [int(t) for t in toks.split()], int(acc), int(best)))
+        i += 2 + G * N + G
+    return cases
+
+
+def check_greedy_golden(lib):
+    for logits, cand, toks, acc, best in load_greedy_golden():
+        for dt in (sg.F32, sg.BF16):
+            out, a, b = oracle.verify_greedy(sg.from_float(logits, dt), cand, lib=lib)
+            assert out[0].tolist() == toks and a[0] == acc and b[0] == best, (out, a, b, toks, acc, best)
+
+
+def multi_draft_expected_tokens(gamma, b, a, r=0.0):
+    """Lookahead eq. (5) generalised to chance matches: a candidate token is the
+    argmax with probability a per step until the first miss; a missed or later
+    token is a uniform id that still equals the argmax with probability r.
+    With r = 0 this is (g+1) - sum_i (1 - a^i)^b."""
+    e = 1.0
+    for i in range(1, gamma + 1):
+        p_match = a ** i + sum(a ** k * (1 - a) * r ** (i - k) for k in range(i))
+        e += 1.0 - (1.0 - p_match) ** b
+    return e
+
+
+def check_greedy_multi_draft(lib, V=512, B=12_000):
+    cfg = sg.CONFIGS["cfg4_greedy_v32000_bf16"].with_(B=B, V=V, seed=5)
+    d = sg.greedy_inputs(cfg)
+    _, acc, _ = oracle.verify_greedy(d["logits"], d["cand"], lib=lib)
+    assert (acc >= 0).all()
+    tokens = acc + 1.0
+    expect = multi_draft_expected_tokens(cfg.N - 1, cfg.G, cfg.match_prob, 1.0 / V)
+    assert abs(tokens.mean() - expect) < 4 * tokens.std() / math.sqrt(B), (tokens.mean(), expect)

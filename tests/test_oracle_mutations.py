@@ -1,0 +1,68 @@
+"""Each pin must reject a plausible mistake: build a copy of the oracle with one
+planted mistake (on the CPU, in a temporary directory) and check that at least
+the named pin fails on it. The real oracle source is never modified."""
+import os
+import tempfile
+
+import pytest
+
+import oracle
+from pins import (check_acceptance_is_one_minus_tv, check_brute_force, check_greedy_golden,
+                  check_output_is_target_distribution, check_tokens_per_round)
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+MUTATIONS = {
+    # the residual is max(0, p - q), not max(0, q - p)
+    "residual_sign": ("w[v] = fmax(0.0, p[v] - q[v]);", "w[v] = fmax(0.0, q[v] - p[v]);",
+                      lambda lib: check_brute_force(lib, K=2)),
+    # alpha = min(1, p/q), not min(1, q/p)
+    "ratio_inverted": ("alpha = fmin(1.0, px / qx);", "alpha = fmin(1.0, qx / px);",
+                       check_acceptance_is_one_minus_tv),
+    # the residual must be renormalised (the draw compares against u * Z)
+    "no_renormalise": ("double target = u * Z, C = 0.0;", "double target = u, C = 0.0;",
+                       lambda lib: check_brute_force(lib, K=2)),
+    # the bonus comes from target row K
+    "bonus_wrong_row": ("      load_row(target, dtype, b * (K + 1) + K, V, lt);\n      row_dist(",
+                        "      load_row(target, dtype, b * (K + 1) + K - 1, V, lt);\n      row_dist(",
+                        lambda lib: check_brute_force(lib, K=2)),
+    # draft token i is tested against target row i
+    "target_row_off_by_one": ("load_row(target, dtype, b * (K + 1) + i, V, lt);\n      load_row(draft",
+                              "load_row(target, dtype, b * (K + 1) + i + 1, V, lt);\n      load_row(draft",
+                              lambda lib: check_brute_force(lib, K=2)),
+    # the accept test uses u_i, not the sample's uniform
+    "wrong_uniform": ("if ((double)u[i] < alpha) {", "if ((double)u[K] < alpha) {",
+                      lambda lib: check_tokens_per_round(lib, 4)),
+    # temperature on both sides
+    "temperature_one_side": ("row_dist(ld, V, T, P, q, scratch, &margin);",
+                             "row_dist(ld, V, 1.0, P, q, scratch, &margin);",
+                             lambda lib: check_output_is_target_distribution(lib, 0.7, 1.0)),
+    # top-p on both sides
+    "top_p_one_side": ("row_dist(ld, V, T, P, q, scratch, &margin);",
+                       "row_dist(ld, V, T, 1.0, q, scratch, &margin);",
+                       lambda lib: check_output_is_target_distribution(lib, 1.0, 0.8)),
+    # argmax ties go to the lowest index
+    "argmax_highest_index": ("if (l[v] > l[best]) best = v;", "if (l[v] >= l[best]) best = v;",
+                             check_greedy_golden),
+    # equal prefix lengths: the lowest candidate wins
+    "greedy_last_candidate": ("if (L > best_L) {", "if (L >= best_L) {", check_greedy_golden),
+}
+
+
+@pytest.fixture(scope="module")
+def tmpdir_mod():
+    with tempfile.TemporaryDirectory() as d:
+        yield d
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pin_rejects_planted_mistake(name, tmpdir_mod):
+    old, new, check = MUTATIONS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} must occur exactly once"
+    path = os.path.join(tmpdir_mod, f"oracle_{name}.c")
+    with open(path, "w") as f:
+        f.write(src.replace(old, new))
+    lib = oracle.load_library(oracle.compile_oracle(path, os.path.join(tmpdir_mod, f"lib_{name}.so")))
+    with pytest.raises(AssertionError):
+        check(lib)
