@@ -1,0 +1,416 @@
+#!/usr/bin/env python3
+"""Benchmark of the speculative-decoding verify step (libspecverify, GB300).
+
+One step = one verify call over one batch of the workload: every row of
+target and draft logits read once, the accept scan, and the residual or bonus
+draw. Default workload: B=64, K=5, V=32000 bf16, T=1 (the workload the
+headline metric is quoted on). Metric: verified positions per second
+(B*(K+1) target positions per call), with the achieved algorithmic HBM
+bandwidth against the measured peak.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME|all] [--impl reference]
+
+Timing: inputs are resident in HBM before the timed region; the K timed calls
+are replayed from CUDA graphs, cycling through enough copies of the inputs
+that the working set exceeds the 129 MB L2 (so no call finds its inputs in
+L2); CUDA events on the launching stream bracket the timed replays, with a
+barrier and a device synchronise on both sides. ``e2e`` repeats the metric
+through the public API with pinned host buffers, copies included.
+``--impl reference`` times the CPU oracle (the baseline this project is
+checked against) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import specgen as sg  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+DEFAULT_CONFIG = "cfg2_v32000_bf16"
+KERNEL = "verify_kernel"
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ------------------------------------------------------------------ workload
+
+def workload(name: str):
+    cfg = sg.CONFIGS[name]
+    greedy = isinstance(cfg, sg.GreedyConfig)
+    esz = 2 if cfg.dtype == sg.BF16 else 4
+    if greedy:
+        positions = cfg.B * cfg.G * cfg.N
+        logit_bytes = cfg.B * cfg.G * cfg.N * cfg.V * esz
+        small_in = cfg.B * cfg.G * (cfg.N - 1) * 4
+        out_bytes = cfg.B * cfg.N * 4 + cfg.B * 4
+    else:
+        positions = cfg.B * (cfg.K + 1)
+        logit_bytes = cfg.B * (2 * cfg.K + 1) * cfg.V * esz
+        small_in = cfg.B * cfg.K * 4 + cfg.B * (cfg.K + 1) * 4
+        out_bytes = cfg.B * (cfg.K + 1) * 4 + cfg.B * 4
+    return cfg, greedy, positions, logit_bytes, small_in, out_bytes
+
+
+def config_json(cfg, greedy, rotation):
+    c = {"workload": cfg.name, "B": cfg.B, "V": cfg.V, "logits": "bf16" if cfg.dtype == sg.BF16 else "f32"}
+    if greedy:
+        c.update({"mode": "greedy", "G": cfg.G, "N": cfg.N})
+    else:
+        c.update({"mode": "sample", "K": cfg.K, "temperature": cfg.temperature, "top_p": cfg.top_p})
+    c["l2"] = (f"inputs larger than L2: {rotation} rotating input sets" if rotation > 1
+               else "inputs larger than L2 (one set)")
+    return c
+
+
+def to_torch(a, torch, pin=False):
+    t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == np.uint16 else torch.from_numpy(a)
+    return t.pin_memory() if pin else t
+
+
+# -------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ helpers
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_39_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary of this workload,
+    or None if there is none or the kernel sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{KERNEL}_{workload_name}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    h = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
+    if not m or not h or h.group(1) != kernel_source_hash():
+        return None
+    return float(m.group(1))
+
+
+def oracle_cpu_rate(cfg, greedy, budget_s: float, nthreads: int):
+    """Positions per second of the CPU oracle over a bounded sample of the
+    workload, fanned out over sequences on ``nthreads`` host threads."""
+    import oracle
+    chunk = max(1, min(cfg.B, 8 if cfg.V > 50000 else 32))
+    inputs = (sg.greedy_inputs(cfg, B=chunk * nthreads) if greedy else sg.sample_inputs(cfg, B=chunk * nthreads))
+    oracle._lib()
+
+    def one(i):
+        sl = slice(i * chunk, (i + 1) * chunk)
+        if greedy:
+            oracle.verify_greedy(inputs["logits"][sl], inputs["cand"][sl])
+        else:
+            oracle.verify_sample(inputs["target"][sl], inputs["draft"][sl], inputs["draft_tokens"][sl],
+                                 inputs["uniforms"][sl], cfg.temperature, cfg.top_p)
+        return chunk
+
+    per_seq = cfg.G * cfg.N if greedy else cfg.K + 1
+    done, t0 = 0, time.perf_counter()
+    with ThreadPoolExecutor(nthreads) as ex:
+        while True:
+            done += sum(ex.map(one, range(nthreads)))
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                break
+    return done * per_seq / el, done, el
+
+
+# --------------------------------------------------------------- GPU arm
+
+def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
+    import torch
+    import speculative_decoding_verification_39_gb300 as svpkg
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    svpkg.build()
+    cfg, greedy, positions, logit_bytes, small_in, out_bytes = workload(name)
+    rotation = 1 if logit_bytes > L2_BYTES else int(math.ceil(3 * L2_BYTES / logit_bytes)) + 1
+    log(f"[bench] {name}: {logit_bytes / 1e6:.1f} MB of logits per call, {rotation} input set(s)")
+    t0 = time.perf_counter()
+    host = sg.greedy_inputs(cfg, seq_offset=rank * cfg.B) if greedy else sg.sample_inputs(cfg, seq_offset=rank * cfg.B)
+    log(f"[bench] inputs generated in {time.perf_counter() - t0:.1f} s")
+    keys = ("logits", "cand") if greedy else ("target", "draft", "draft_tokens", "uniforms")
+    pinned = {k: to_torch(host[k], torch, pin=True) for k in keys}
+    sets = []
+    for r in range(rotation):
+        sets.append({k: pinned[k].to(dev, non_blocking=True) for k in keys})
+    torch.cuda.synchronize()
+    outs = [(torch.empty((cfg.B, cfg.N if greedy else cfg.K + 1), dtype=torch.int32, device=dev),
+             torch.empty((cfg.B,), dtype=torch.int32, device=dev)) for _ in range(rotation)]
+
+    def call(i):
+        s, (ot, oa) = sets[i % rotation], outs[i % rotation]
+        if greedy:
+            svpkg.verify_greedy(s["logits"], s["cand"], out_tokens=ot, out_accept_len=oa)
+        else:
+            svpkg.verify_sample(s["target"], s["draft"], s["draft_tokens"], s["uniforms"], cfg.temperature,
+                                cfg.top_p, out_tokens=ot, out_accept_len=oa)
+
+    stream = torch.cuda.Stream(dev)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            call(i)
+    stream.synchronize()
+    with torch.cuda.stream(stream):
+        if svpkg.get_status() != 0:
+            raise RuntimeError("device status set during warm-up")
+    # graphs of at most 1000 calls; the timed region replays exactly K calls
+    chunk = min(args.steps, 1000)
+    graphs = []
+    n_left = args.steps
+    launches_before = svpkg.launch_count()
+    idx = 0
+    while n_left > 0:
+        n = min(chunk, n_left)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for _ in range(n):
+                call(idx)
+                idx += 1
+        graphs.append((g, n))
+        n_left -= n
+    captured = svpkg.launch_count() - launches_before
+    # pre-roll: replay for ~1 s so that clocks settle and the sampler sees the load
+    with ClockSampler(local) as clk:
+        t_pre = time.perf_counter()
+        with torch.cuda.stream(stream):
+            while time.perf_counter() - t_pre < 1.0:
+                graphs[0][0].replay()
+                stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for g, _ in graphs:
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        ms = e0.elapsed_time(e1)
+    with torch.cuda.stream(stream):
+        status = svpkg.get_status()
+    if status != 0:
+        raise RuntimeError(f"device status {status} after the timed region")
+    if world > 1:
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = positions * world * args.steps / (ms / 1e3)
+    achieved_gbs = logit_bytes / (ms_per_step / 1e3) / 1e9
+    peak, peak_kind = measured_peak()
+
+    # end to end through the public API with pinned host buffers
+    e2e_steps = max(3, min(20, args.steps))
+    host_args = [pinned[k] for k in keys]
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            (svpkg.verify_greedy(*host_args) if greedy else
+             svpkg.verify_sample(*host_args, cfg.temperature, cfg.top_p))
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        for _ in range(e2e_steps):
+            (svpkg.verify_greedy(*host_args) if greedy else
+             svpkg.verify_sample(*host_args, cfg.temperature, cfg.top_p))
+        e2e_s = (time.perf_counter() - t1) / e2e_steps
+    h2d = logit_bytes + small_in
+
+    line = {
+        "metric": "verified positions/sec and achieved HBM GB/s (% of GB300 peak) per verify call",
+        "value": value,
+        "unit": "positions/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded Philox inputs of the workload's shapes)",
+        "config": config_json(cfg, greedy, rotation),
+        "rounds_per_s": cfg.B * world / (ms_per_step / 1e3),
+        "achieved_gbs": achieved_gbs,
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
+                     "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
+                     "traffic": profiled_traffic(name), "algorithmic_bytes_per_launch": logit_bytes,
+                     "kernel": KERNEL, "timing": "CUDA events over graph replays of the timed calls"},
+        "clocks": clk.summary(),
+        "e2e": {"value": positions * world / e2e_s, "unit": "positions/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": out_bytes},
+        "gpu_launches": int(captured),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nth = os.cpu_count() or 1
+        rate, n, el = oracle_cpu_rate(cfg, greedy, args.cpu_budget, nth)
+        line["cpu_baseline"] = {"value": rate, "unit": "positions/s", "cores": nth, "kind": "oracle",
+                                "sample": f"{n} sequences of the workload in {el:.1f} s, "
+                                          f"one oracle call per thread per batch"}
+    if print_line and rank == 0:
+        print(json.dumps(line), flush=True)
+    return line
+
+
+# ---------------------------------------------------------- reference arm
+
+def run_reference(args, name: str):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    cfg, greedy, positions, logit_bytes, _, _ = workload(name)
+    nth = os.cpu_count() or 1
+    per_step = max(5.0, 60.0 / max(1, args.steps + args.warmup))
+    rates = []
+    for i in range(args.warmup + args.steps):
+        rate, n, el = oracle_cpu_rate(cfg, greedy, min(per_step, 20.0), nth)
+        if i >= args.warmup:
+            rates.append(rate)
+    value = float(np.mean(rates))
+    line = {
+        "impl": "reference",
+        "metric": "verified positions/sec and achieved HBM GB/s (% of GB300 peak) per verify call",
+        "value": value,
+        "unit": "positions/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": positions / value * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic (seeded Philox inputs of the workload's shapes)",
+        "config": config_json(cfg, greedy, 1),
+        "cpu_baseline": {"value": value, "unit": "positions/s", "cores": nth, "kind": "oracle",
+                         "sample": f"per step: a bounded sample of the workload's sequences, about "
+                                   f"{min(per_step, 20.0):.0f} s of CPU work"},
+        "e2e": {"value": value, "unit": "positions/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, help="workload name, or 'all'")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    names = list(sg.CONFIGS) if args.config == "all" else [args.config]
+    if args.impl == "reference":
+        for n in names:
+            run_reference(args, n)
+        return
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world != args.gpus:
+        log(f"[bench] --gpus {args.gpus} but WORLD_SIZE {world}; using WORLD_SIZE")
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    try:
+        for n in names:
+            run_gpu(args, n, rank, world, print_line=True)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,151 @@
+/*
+ * specverify.h — C ABI of libspecverify, the GB300 (sm_103a) speculative-
+ * decoding verify step.
+ *
+ * The operation. A draft model proposed K tokens x_0..x_{K-1}; the target
+ * model scored K+1 positions. Verification turns both models' logits into
+ * distributions p (target) and q (draft), accepts x_i while
+ * u_i < min(1, p_i(x_i) / q_i(x_i)), stops at the first rejection j, and
+ * replaces x_j by a draw from norm(max(0, p_j - q_j)); if all K are accepted
+ * it draws one bonus token from p_K. The emitted tokens then follow the target
+ * model's distribution exactly. Sources (page title, section):
+ *   "Speculative Decoding —— LLM推理优化技术（一）" (hustzhy.cn), §2.1 accept
+ *     probability and residual distribution, §2.2 proof, §2.3 sequential test
+ *     with a bonus token, §4 temperature on both sides and the fallback to p
+ *     when the residual is all zero;
+ *   kwkr.cn "投机解码" §3.1 the verify steps (r < alpha accepts), §3.2 fp32
+ *     probabilities, §3.4 temperature and top-p applied identically to both
+ *     sides, resampling only inside the truncated set;
+ *   "Lookahead Decoding 完全拆解" (pinghaoyang.com.cn), verify branch: greedy
+ *     verification of n-gram candidates against the per-position argmax,
+ *     longest matched prefix plus one bonus token.
+ *
+ * Conventions shared by every entry point:
+ *   - Every array argument is a DEVICE pointer owned by the caller; the
+ *     library never frees or retains it past the call's completion on the
+ *     stream. Arrays are dense, row-major, with the vocabulary innermost.
+ *   - Calls are asynchronous: they validate arguments on the host, enqueue
+ *     one kernel on `stream` (a cudaStream_t; NULL = the legacy default
+ *     stream) and return. Results are valid once the stream reaches them.
+ *   - The library keeps a small scratch area per (device, stream), allocated
+ *     on the first call that needs it (or a larger one) and reused after.
+ *     Calls on the same stream are ordered; calls on different streams use
+ *     different scratch areas. sv_release() frees them all.
+ *   - Host-checkable errors return a negative sv_status and enqueue nothing.
+ *   - Input errors found on the device (a token id outside [0,V), a uniform
+ *     outside [0,1), a NaN logit, a +inf logit or an all -inf row in sampling
+ *     mode, a NaN logit in greedy mode) mark that sequence only:
+ *     out_accept_len[b] = -1 and out_tokens[b,:] = -1. They also set a sticky
+ *     flag that sv_get_status() reports. Kernels never trap.
+ *   - Every internal wait is bounded; a wait that runs out sets
+ *     SV_ERR_TIMEOUT, reported by sv_get_status().
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+typedef enum {
+  SV_OK = 0,
+  SV_ERR_ARG = -1,     /* bad shape, null pointer, temperature < 0, top_p outside (0,1] */
+  SV_ERR_DTYPE = -2,   /* dtype not SV_F32 / SV_BF16, or a misaligned pointer for it */
+  SV_ERR_CUDA = -3,    /* a CUDA runtime call failed (launch, allocation, copy) */
+  SV_ERR_INPUT = -4,   /* device-detected bad input in at least one sequence */
+  SV_ERR_TIMEOUT = -5, /* a bounded device wait ran out; the scratch was reset */
+  SV_ERR_NOMEM = -6    /* scratch allocation failed */
+} sv_status;
+
+/*
+ * Sampling-mode verify ("Speculative Decoding" §2.1-2.3; kwkr.cn §3.1, §3.4).
+ *
+ *   target_logits [B, K+1, V] dtype: row i is the target distribution that
+ *                 draft token i is tested against; row K is the bonus
+ *                 distribution.
+ *   draft_logits  [B, K, V] dtype: row i is the draft distribution that
+ *                 produced draft token i. Not read when temperature == 0.
+ *   draft_tokens  [B, K] int32.
+ *   uniforms      [B, K+1] fp32 in [0,1): u_0..u_{K-1} are the accept tests;
+ *                 u_K drives the single inverse-CDF draw (residual or bonus).
+ *                 Not read when temperature == 0.
+ *   B >= 0, K >= 1, V >= 2; dtype SV_F32 or SV_BF16 (pointers aligned to
+ *   the element size).
+ *   temperature   > 0: p = softmax(l/T), q likewise, on both sides;
+ *                 == 0: the greedy limit: x_i is accepted iff it is the
+ *                 argmax of target row i (lowest index among equal maxima);
+ *                 at a rejection the token is that argmax; the bonus is the
+ *                 argmax of row K.
+ *   top_p         in (0,1]; < 1 restricts p and q each to its nucleus — the
+ *                 tokens whose stored logit is >= tau, tau the largest value
+ *                 whose upper set holds >= top_p of the mass (ties at the cut
+ *                 are kept) — and renormalises; 1 = no filter.
+ * Outputs:
+ *   out_tokens     [B, K+1] int32: x_0..x_{j-1}, then the drawn token at j,
+ *                  then -1.
+ *   out_accept_len [B] int32: j in [0, K] (-1 for a sequence with bad input).
+ *   out_row_stats  nullable [B, 2K+1, 4] fp32, rows in the order target
+ *                  0..K, draft 0..K-1: {m = max l/T, lse = log sum exp(l/T),
+ *                  P_S = nucleus mass (1 without top-p), tau = stored logit
+ *                  at the nucleus cut (-inf without top-p)}. Written only
+ *                  when temperature > 0.
+ * The selected token is the smallest t with sum_{v<=t} w_v > u_K * sum_v w_v
+ * (ascending vocabulary order), w = max(0, p'_j - q'_j) after a rejection
+ * (p'_j itself if that is all zero) or p'_K for the bonus.
+ */
+int sv_verify_sample(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                     const float* uniforms, int64_t B, int32_t K, int64_t V, int32_t dtype, float temperature,
+                     float top_p, int32_t* out_tokens, int32_t* out_accept_len, float* out_row_stats,
+                     void* stream);
+
+/*
+ * Greedy verify of Lookahead n-gram candidates ("Lookahead Decoding 完全拆解",
+ * verify branch; "Speculative Decoding" §5.3).
+ *
+ *   logits [B, G, N, V] dtype: candidate g's N positions (its N-1 tokens and
+ *          the bonus position after them).
+ *   cand   [B, G, N-1] int32: the candidate n-grams.
+ *   B >= 0, G >= 1, N >= 2, V >= 2.
+ * a_{g,n} = argmax_v logits[b,g,n,v] (lowest index among equal maxima; -0
+ * and +0 are equal). L_g = the longest n with cand[b,g,0..n-1] equal to
+ * a_{g,0..n-1}. The winner g* has the largest L_g (lowest g on ties).
+ * Outputs:
+ *   out_tokens     [B, N] int32: cand[b,g*,0..L-1], then a_{g*,L}, then -1.
+ *   out_accept_len [B] int32: L in [0, N-1] (-1 for bad input).
+ *   out_best_cand  nullable [B] int32: g*.
+ */
+int sv_verify_greedy(const void* logits, const int32_t* cand, int64_t B, int32_t G, int32_t N, int64_t V,
+                     int32_t dtype, int32_t* out_tokens, int32_t* out_accept_len, int32_t* out_best_cand,
+                     void* stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the sticky device status of
+ * that stream's scratch: SV_OK, SV_ERR_INPUT (some sequence had bad input
+ * since the last call) or SV_ERR_TIMEOUT (a bounded wait ran out; the scratch
+ * has been re-zeroed so later calls start clean). SV_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+int sv_get_status(void* stream);
+
+/* A static, human-readable name for an sv_status value. */
+const char* sv_status_string(int status);
+
+/* Frees every scratch area on every device (synchronises those devices). */
+int sv_release(void);
+
+/* Launch-shape knobs, for tuning and tests: stages of the shared-memory ring
+ * (1..8) and CTAs per SM (1..4); 0 restores the default. Applies to calls
+ * made after it on any device. */
+int sv_set_launch_shape(int32_t stages, int32_t ctas_per_sm);
+
+/* How many kernel launches the library has enqueued since it was loaded. */
+uint64_t sv_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

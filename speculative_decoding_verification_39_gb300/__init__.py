@@ -1,0 +1,254 @@
+"""libspecverify — the speculative-decoding verify step on GB300 (sm_103a).
+
+This module is a thin binding over the C ABI in ``include/specverify.h``: it
+checks and marshals torch tensors (device memory, the current stream) into the
+library's entry points, which run every step of the verify path in the CUDA
+kernels of ``csrc/``. There is no CPU fallback: if ``libspecverify.so`` is
+missing or cannot be loaded, every call raises.
+
+Entry points (same names as the C ABI):
+  verify_sample(target, draft, draft_tokens, uniforms, temperature, top_p)
+  verify_greedy(logits, cand)
+  get_status()
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from concurrent.futures import ThreadPoolExecutor
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_CSRC = os.path.join(_HERE, "csrc")
+_INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
+_SO = os.path.join(_HERE, "libspecverify.so")
+_SOURCES = ["sv_kernels.cu", "sv_api.cu"]
+_DEPS = _SOURCES + ["sv_kernels.h", "sv_device.cuh"]
+
+SV_F32, SV_BF16 = 0, 1
+STATUS = {0: "SV_OK", -1: "SV_ERR_ARG", -2: "SV_ERR_DTYPE", -3: "SV_ERR_CUDA", -4: "SV_ERR_INPUT",
+          -5: "SV_ERR_TIMEOUT", -6: "SV_ERR_NOMEM"}
+
+NVCC_FLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
+              "-Xcompiler", "-fPIC"]
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, rc: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(rc, rc)}")
+        self.rc = rc
+
+
+def _stale() -> bool:
+    if not os.path.exists(_SO):
+        return True
+    t = os.path.getmtime(_SO)
+    deps = [os.path.join(_CSRC, f) for f in _DEPS] + [os.path.join(_INCLUDE, "specverify.h")]
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile ``libspecverify.so`` in-tree for sm_103a (nvcc; no GPU needed)."""
+    if not force and not _stale():
+        return _SO
+    objs = []
+
+    def cc(src):
+        obj = os.path.join(_CSRC, os.path.splitext(src)[0] + f".{os.getpid()}.o")
+        cmd = ["nvcc", *NVCC_FLAGS, "-c", os.path.join(_CSRC, src), "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for {src}:\n{r.stderr}")
+        if verbose:
+            print(r.stderr)
+        return obj
+
+    with ThreadPoolExecutor(len(_SOURCES)) as ex:
+        objs = list(ex.map(cc, _SOURCES))
+    tmp = _SO + f".tmp{os.getpid()}"
+    try:
+        subprocess.run(["nvcc", "-shared", "-gencode", "arch=compute_103a,code=sm_103a", *objs, "-o", tmp],
+                       check=True, capture_output=True, text=True)
+        os.replace(tmp, _SO)
+    finally:
+        for o in objs:
+            if os.path.exists(o):
+                os.remove(o)
+    return _SO
+
+
+_lib_handle = None
+
+
+def lib():
+    """The loaded ``libspecverify.so``; raises if it has not been built."""
+    global _lib_handle
+    if _lib_handle is None:
+        if not os.path.exists(_SO):
+            raise RuntimeError(f"libspecverify.so is not built ({_SO}); run __graft_entry__.build()")
+        h = ctypes.CDLL(_SO)
+        vp, i64, i32, f32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_float
+        h.sv_verify_sample.argtypes = [vp, vp, vp, vp, i64, i32, i64, i32, f32, f32, vp, vp, vp, vp]
+        h.sv_verify_sample.restype = ctypes.c_int
+        h.sv_verify_greedy.argtypes = [vp, vp, i64, i32, i32, i64, i32, vp, vp, vp, vp]
+        h.sv_verify_greedy.restype = ctypes.c_int
+        h.sv_get_status.argtypes = [vp]
+        h.sv_get_status.restype = ctypes.c_int
+        h.sv_status_string.argtypes = [ctypes.c_int]
+        h.sv_status_string.restype = ctypes.c_char_p
+        h.sv_release.argtypes = []
+        h.sv_release.restype = ctypes.c_int
+        h.sv_set_launch_shape.argtypes = [i32, i32]
+        h.sv_set_launch_shape.restype = ctypes.c_int
+        h.sv_launch_count.argtypes = []
+        h.sv_launch_count.restype = ctypes.c_uint64
+        _lib_handle = h
+    return _lib_handle
+
+
+def exported_symbols() -> list:
+    return ["sv_verify_sample", "sv_verify_greedy", "sv_get_status", "sv_status_string", "sv_release",
+            "sv_set_launch_shape", "sv_launch_count"]
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    if t.dtype == torch.float32:
+        return SV_F32
+    raise TypeError(f"logits must be torch.bfloat16 or torch.float32, got {t.dtype}")
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _on_device(t: torch.Tensor, device, name: str) -> torch.Tensor:
+    if t.device.type == "cpu":
+        return t.to(device, non_blocking=True)
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    return t
+
+
+def _check(t: torch.Tensor, shape, dtype, name):
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def verify_sample(target, draft, draft_tokens, uniforms, temperature: float, top_p: float = 1.0,
+                  row_stats: bool = False, out_tokens=None, out_accept_len=None, device=None):
+    """Sampling-mode verify (sv_verify_sample).
+
+    target [B,K+1,V] and draft [B,K,V] logits (bf16 or fp32), draft_tokens
+    [B,K] int32, uniforms [B,K+1] fp32. Tensors on a CUDA device are used in
+    place on the current stream (asynchronous). CPU tensors are copied to
+    ``device`` (default: the current CUDA device), verified there, and the
+    results copied back; that call returns after the results are on the host.
+    Returns (out_tokens [B,K+1] int32, out_accept_len [B] int32) and, with
+    ``row_stats``, a third tensor [B,2K+1,4] fp32 {m, lse, P_S, tau}.
+    """
+    host = target.device.type == "cpu"
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if not host:
+        dev = target.device
+    B, K1, V = target.shape
+    K = K1 - 1
+    limit = float(temperature) == 0.0
+    t = _on_device(target, dev, "target")
+    d = _on_device(draft, dev, "draft") if draft is not None else None
+    x = _on_device(draft_tokens, dev, "draft_tokens")
+    u = _on_device(uniforms, dev, "uniforms") if uniforms is not None else None
+    _check(t, (B, K + 1, V), None, "target")
+    dt = _dtype_code(t)
+    if d is not None:
+        _check(d, (B, K, V), t.dtype, "draft")
+    _check(x, (B, K), torch.int32, "draft_tokens")
+    if u is not None:
+        _check(u, (B, K + 1), torch.float32, "uniforms")
+    if not limit and (d is None or u is None):
+        raise ValueError("draft and uniforms are required when temperature > 0")
+    ot = torch.empty((B, K + 1), dtype=torch.int32, device=dev) if (out_tokens is None or host) else out_tokens
+    oa = torch.empty((B,), dtype=torch.int32, device=dev) if (out_accept_len is None or host) else out_accept_len
+    rs = torch.empty((B, 2 * K + 1, 4), dtype=torch.float32, device=dev) if row_stats else None
+    with torch.cuda.device(dev):
+        rc = lib().sv_verify_sample(_ptr(t), _ptr(d), _ptr(x), _ptr(u), B, K, V, dt, float(temperature),
+                                    float(top_p), _ptr(ot), _ptr(oa), _ptr(rs), _stream_handle(dev))
+    if rc != 0:
+        raise SpecVerifyError(rc, "sv_verify_sample")
+    res = [ot, oa] + ([rs] if row_stats else [])
+    if host:
+        outs = [r.to("cpu", non_blocking=True) if out is None else out.copy_(r, non_blocking=True)
+                for r, out in zip(res, [out_tokens, out_accept_len, None])]
+        torch.cuda.current_stream(dev).synchronize()
+        res = outs
+    return tuple(res)
+
+
+def verify_greedy(logits, cand, out_tokens=None, out_accept_len=None, best=False, device=None):
+    """Greedy Lookahead verify (sv_verify_greedy).
+
+    logits [B,G,N,V] (bf16 or fp32), cand [B,G,N-1] int32. Returns
+    (out_tokens [B,N], out_accept_len [B]) and, with ``best``, the winning
+    candidate [B]. CPU tensors are handled as in verify_sample.
+    """
+    host = logits.device.type == "cpu"
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if not host:
+        dev = logits.device
+    B, G, N, V = logits.shape
+    lg = _on_device(logits, dev, "logits")
+    c = _on_device(cand, dev, "cand")
+    _check(lg, (B, G, N, V), None, "logits")
+    dt = _dtype_code(lg)
+    _check(c, (B, G, N - 1), torch.int32, "cand")
+    ot = torch.empty((B, N), dtype=torch.int32, device=dev) if (out_tokens is None or host) else out_tokens
+    oa = torch.empty((B,), dtype=torch.int32, device=dev) if (out_accept_len is None or host) else out_accept_len
+    ob = torch.empty((B,), dtype=torch.int32, device=dev) if best else None
+    with torch.cuda.device(dev):
+        rc = lib().sv_verify_greedy(_ptr(lg), _ptr(c), B, G, N, V, dt, _ptr(ot), _ptr(oa), _ptr(ob),
+                                    _stream_handle(dev))
+    if rc != 0:
+        raise SpecVerifyError(rc, "sv_verify_greedy")
+    res = [ot, oa] + ([ob] if best else [])
+    if host:
+        outs = [r.to("cpu", non_blocking=True) if out is None else out.copy_(r, non_blocking=True)
+                for r, out in zip(res, [out_tokens, out_accept_len, None])]
+        torch.cuda.current_stream(dev).synchronize()
+        res = outs
+    return tuple(res)
+
+
+def get_status(device=None) -> int:
+    """Synchronise the current stream and return (and clear) its sticky device status."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        return lib().sv_get_status(_stream_handle(dev))
+
+
+def set_launch_shape(stages: int = 0, ctas_per_sm: int = 0) -> None:
+    rc = lib().sv_set_launch_shape(stages, ctas_per_sm)
+    if rc != 0:
+        raise SpecVerifyError(rc, "sv_set_launch_shape")
+
+
+def launch_count() -> int:
+    return int(lib().sv_launch_count())
+
+
+def release() -> None:
+    rc = lib().sv_release()
+    if rc != 0:
+        raise SpecVerifyError(rc, "sv_release")

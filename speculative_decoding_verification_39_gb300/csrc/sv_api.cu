@@ -1,0 +1,256 @@
+// sv_api.cu — the C ABI of libspecverify (declared in include/specverify.h):
+// host-side argument checks, the per-(device, stream) scratch areas and the
+// launch of the verify kernel.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
+
+#include "../../include/specverify.h"
+#include "sv_kernels.h"
+
+namespace {
+
+constexpr int kDefaultStages = 4;
+constexpr int kDefaultCtasPerSm = 2;
+constexpr int64_t kMaxV = (int64_t)1 << 31;
+
+std::atomic<int> g_stages{kDefaultStages};
+std::atomic<int> g_ctas_per_sm{kDefaultCtasPerSm};
+std::atomic<uint64_t> g_launches{0};
+
+struct Scratch {
+  void* base = nullptr;
+  size_t bytes = 0;
+};
+
+std::mutex g_mu;
+std::map<std::pair<int, uintptr_t>, Scratch> g_scratch;
+std::map<int, int> g_sm_count;
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Layout {
+  size_t ctl, row_cnt, seq_cnt, part, rowstat, total;
+};
+
+Layout layout_for(int64_t B, int64_t rows, int64_t W) {
+  Layout L;
+  L.ctl = 0;
+  L.row_cnt = align256(L.ctl + 64);
+  L.seq_cnt = align256(L.row_cnt + (size_t)rows * 4);
+  L.part = align256(L.seq_cnt + (size_t)B * 4);
+  L.rowstat = align256(L.part + (size_t)W * 8);
+  L.total = align256(L.rowstat + (size_t)rows * 16);
+  return L;
+}
+
+// Returns a zero-initialised scratch area of at least `bytes` for the current
+// device and `stream`. Counters inside it are self-cleaning, so it is zeroed
+// only when (re)allocated.
+int get_scratch(cudaStream_t stream, size_t bytes, void** out, int* device) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  *device = dev;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Scratch& s = g_scratch[{dev, reinterpret_cast<uintptr_t>(stream)}];
+  if (s.bytes < bytes) {
+    if (s.base) {
+      cudaStreamSynchronize(stream);
+      cudaFree(s.base);
+      s.base = nullptr;
+      s.bytes = 0;
+    }
+    size_t want = bytes < (1u << 20) ? (1u << 20) : bytes;
+    if (cudaMalloc(&s.base, want) != cudaSuccess) {
+      s.base = nullptr;
+      cudaGetLastError();
+      return SV_ERR_NOMEM;
+    }
+    if (cudaMemsetAsync(s.base, 0, want, stream) != cudaSuccess) return SV_ERR_CUDA;
+    s.bytes = want;
+  }
+  *out = s.base;
+  return SV_OK;
+}
+
+int sm_count(int dev) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_sm_count.find(dev);
+  if (it != g_sm_count.end()) return it->second;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  g_sm_count[dev] = n;
+  return n;
+}
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t stream) {
+  const int esz = dtype == SV_BF16 ? 2 : 4;
+  p.TE = sv::kTileBytes / esz;
+  p.NT = (p.V + p.TE - 1) / p.TE;
+  p.W = rows_total * p.NT;
+  p.stages = g_stages.load();
+  const Layout L = layout_for(p.B, rows_total, p.W);
+  void* base = nullptr;
+  int dev = 0;
+  int rc = get_scratch(stream, L.total, &base, &dev);
+  if (rc != SV_OK) return rc;
+  char* b = static_cast<char*>(base);
+  p.ctl = reinterpret_cast<uint32_t*>(b + L.ctl);
+  p.row_cnt = reinterpret_cast<uint32_t*>(b + L.row_cnt);
+  p.seq_cnt = reinterpret_cast<uint32_t*>(b + L.seq_cnt);
+  p.part = reinterpret_cast<float2*>(b + L.part);
+  p.rowstat = reinterpret_cast<float4*>(b + L.rowstat);
+  int64_t grid = (int64_t)sm_count(dev) * g_ctas_per_sm.load();
+  if (grid > p.W) grid = p.W;
+  if (grid < 1) grid = 1;
+  cudaError_t e = sv::launch(p, dtype, mode, (int)grid, stream);
+  if (e != cudaSuccess) return SV_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" int sv_verify_sample(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                                const float* uniforms, int64_t B, int32_t K, int64_t V, int32_t dtype,
+                                float temperature, float top_p, int32_t* out_tokens, int32_t* out_accept_len,
+                                float* out_row_stats, void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (B < 0 || K < 1 || V < 2 || V >= kMaxV || K > (1 << 20)) return SV_ERR_ARG;
+  if (!(temperature >= 0.f) || std::isinf(temperature)) return SV_ERR_ARG;
+  if (!(top_p > 0.f && top_p <= 1.f)) return SV_ERR_ARG;
+  if (B == 0) return SV_OK;
+  const bool limit = temperature == 0.f;
+  if (!target_logits || !draft_tokens || !out_tokens || !out_accept_len) return SV_ERR_ARG;
+  if (!limit && (!draft_logits || !uniforms)) return SV_ERR_ARG;
+  const size_t esz = dtype == SV_BF16 ? 2 : 4;
+  if (!aligned_to(target_logits, esz) || (!limit && !aligned_to(draft_logits, esz))) return SV_ERR_DTYPE;
+  if (!aligned_to(draft_tokens, 4) || !aligned_to(out_tokens, 4) || !aligned_to(out_accept_len, 4) ||
+      (uniforms && !aligned_to(uniforms, 4)) || (out_row_stats && !aligned_to(out_row_stats, 16)))
+    return SV_ERR_ARG;
+  const float c = limit ? 0.f : (float)(1.4426950408889634 / (double)temperature);
+  if (!limit && !std::isfinite(c)) return SV_ERR_ARG;
+  sv::Params p{};
+  p.a = static_cast<const char*>(target_logits);
+  p.d = static_cast<const char*>(limit ? target_logits : draft_logits);
+  p.tokens = draft_tokens;
+  p.uniforms = uniforms;
+  p.out_tokens = out_tokens;
+  p.out_accept_len = out_accept_len;
+  p.out_best = nullptr;
+  p.out_row_stats = limit ? nullptr : out_row_stats;
+  p.B = B;
+  p.V = V;
+  p.K = K;
+  p.G = 0;
+  p.N = 0;
+  p.RS = limit ? K + 1 : 2 * K + 1;
+  p.c = c;
+  p.T = temperature;
+  p.top_p = top_p;
+  p.topp = (!limit && top_p < 1.f) ? 1 : 0;
+  return run(p, dtype, limit ? sv::kArgmaxLimit : sv::kSample, B * (int64_t)p.RS, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int sv_verify_greedy(const void* logits, const int32_t* cand, int64_t B, int32_t G, int32_t N, int64_t V,
+                                int32_t dtype, int32_t* out_tokens, int32_t* out_accept_len, int32_t* out_best_cand,
+                                void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (B < 0 || G < 1 || G > 65535 || N < 2 || N > 32767 || V < 2 || V >= kMaxV) return SV_ERR_ARG;
+  if ((int64_t)G * N > (1 << 24)) return SV_ERR_ARG;
+  if (B == 0) return SV_OK;
+  if (!logits || !cand || !out_tokens || !out_accept_len) return SV_ERR_ARG;
+  const size_t esz = dtype == SV_BF16 ? 2 : 4;
+  if (!aligned_to(logits, esz)) return SV_ERR_DTYPE;
+  if (!aligned_to(cand, 4) || !aligned_to(out_tokens, 4) || !aligned_to(out_accept_len, 4) ||
+      (out_best_cand && !aligned_to(out_best_cand, 4)))
+    return SV_ERR_ARG;
+  sv::Params p{};
+  p.a = static_cast<const char*>(logits);
+  p.d = p.a;
+  p.tokens = cand;
+  p.uniforms = nullptr;
+  p.out_tokens = out_tokens;
+  p.out_accept_len = out_accept_len;
+  p.out_best = out_best_cand;
+  p.out_row_stats = nullptr;
+  p.B = B;
+  p.V = V;
+  p.K = 0;
+  p.G = G;
+  p.N = N;
+  p.RS = G * N;
+  p.c = 0.f;
+  p.T = 0.f;
+  p.top_p = 1.f;
+  p.topp = 0;
+  return run(p, dtype, sv::kGreedy, B * (int64_t)p.RS, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int sv_get_status(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SV_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  Scratch sc;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_scratch.find({dev, reinterpret_cast<uintptr_t>(s)});
+    if (it == g_scratch.end()) return SV_OK;
+    sc = it->second;
+  }
+  uint32_t status = 0;
+  char* ctl = static_cast<char*>(sc.base);
+  if (cudaMemcpy(&status, ctl + 12, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return SV_ERR_CUDA;
+  if (status == 0) return SV_OK;
+  if (status & 2u) {  // a wait ran out: counters may be left half-way, start clean
+    if (cudaMemset(sc.base, 0, sc.bytes) != cudaSuccess) return SV_ERR_CUDA;
+    return SV_ERR_TIMEOUT;
+  }
+  if (cudaMemset(ctl + 12, 0, 4) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_ERR_INPUT;
+}
+
+extern "C" const char* sv_status_string(int status) {
+  switch (status) {
+    case SV_OK: return "ok";
+    case SV_ERR_ARG: return "invalid argument";
+    case SV_ERR_DTYPE: return "unsupported dtype or misaligned logits";
+    case SV_ERR_CUDA: return "CUDA runtime error";
+    case SV_ERR_INPUT: return "bad input in at least one sequence";
+    case SV_ERR_TIMEOUT: return "a bounded device wait ran out";
+    case SV_ERR_NOMEM: return "scratch allocation failed";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int sv_release(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  int rc = SV_OK;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  for (auto& kv : g_scratch) {
+    if (!kv.second.base) continue;
+    cudaSetDevice(kv.first.first);
+    cudaDeviceSynchronize();
+    if (cudaFree(kv.second.base) != cudaSuccess) rc = SV_ERR_CUDA;
+  }
+  g_scratch.clear();
+  cudaSetDevice(cur);
+  return rc;
+}
+
+extern "C" int sv_set_launch_shape(int32_t stages, int32_t ctas_per_sm) {
+  if (stages < 0 || stages > sv::kMaxStages || ctas_per_sm < 0 || ctas_per_sm > 4) return SV_ERR_ARG;
+  g_stages.store(stages == 0 ? kDefaultStages : stages);
+  g_ctas_per_sm.store(ctas_per_sm == 0 ? kDefaultCtasPerSm : ctas_per_sm);
+  return SV_OK;
+}
+
+extern "C" uint64_t sv_launch_count(void) { return g_launches.load(); }

@@ -1,0 +1,1028 @@
+// sv_kernels.cu — the verify-step kernels of libspecverify (sm_103a).
+//
+// One persistent kernel per call. Each CTA has one producer warp and eight
+// consumer warps around a ring of shared-memory stages. The producer takes
+// the next tile of the call from a global work counter and moves it from HBM
+// into a stage with a 1-D bulk copy (TMA) that completes on the stage's
+// mbarrier; the consumers reduce the tile and hand the stage back. A tile is
+// up to 16 KB of one logit row; tiles are numbered sequence-major, so the
+// rows of one sequence are read close together in time and stay in L2 for
+// the second look the sampler needs.
+//
+// Cross-CTA hand-off is "the last arriver does the work", never a wait: the
+// CTA that publishes the last tile partial of a row finalises the row (its
+// normaliser, its top-p cut or its argmax), and the CTA that finalises the
+// last row of a sequence runs the sequence's decision and draw.
+//
+// Per-row quantities (sampling mode), with c = log2(e)/T:
+//   M   = max_v l_v                       (raw stored logit)
+//   Mc  = fl(M * c)
+//   s   = sum_v 2^(l_v * c - Mc)           = sum_v exp((l_v - M)/T)
+//   cum = sum_{v : l_v >= tau} 2^(l_v * c - Mc)   (= s without top-p)
+// so p'(v) = 2^(l_v * c - Mc) / cum on the nucleus {l_v >= tau}, and
+//   alpha_i = min(1, p'_i(x_i) / q'_i(x_i))
+//           = min(1, 2^(a_p - a_q) * cum_q / cum_p),  a = fma(l_x, c, -Mc).
+#include "sv_device.cuh"
+#include "sv_kernels.h"
+
+#include <climits>
+#include <cfloat>
+
+namespace sv {
+
+// ------------------------------------------------------------------ layout ---
+
+struct RowStat {
+  float M;       // sampling: row max (NaN = invalid row); argmax: max value (NaN = invalid)
+  float s;       // sampling: normaliser relative to Mc
+  float cum;     // sampling: nucleus mass relative to Mc (= s without top-p)
+  uint32_t tau;  // sampling: nucleus cut key (0 = keep all); argmax: the argmax index
+};
+
+__device__ __forceinline__ RowStat rs_load(const Params& p, int64_t idx) {
+  const float4 v = __ldcg(p.rowstat + idx);
+  RowStat r;
+  r.M = v.x;
+  r.s = v.y;
+  r.cum = v.z;
+  r.tau = __float_as_uint(v.w);
+  return r;
+}
+__device__ __forceinline__ void rs_store(const Params& p, int64_t idx, const RowStat& r) {
+  p.rowstat[idx] = make_float4(r.M, r.s, r.cum, __uint_as_float(r.tau));
+}
+
+struct alignas(16) Shared {
+  uint64_t full[kMaxStages];
+  uint64_t empty[kMaxStages];
+  int64_t meta[kMaxStages];
+  union {
+    uint32_t u[kHistBins];
+    float f[kHistBins];
+  } hist;
+  float cells[kMaxCells];
+  float red_m[kConsumerWarps];
+  float red_s[kConsumerWarps];
+  int64_t red_i[kConsumerWarps];
+  float bf[8];
+  int64_t bl[4];
+  int bi[8];
+  int flag;
+};
+
+size_t shared_bytes(int stages) { return (size_t)stages * kTileBytes + sizeof(Shared); }
+
+template <typename E>
+struct ET;
+template <>
+struct ET<float> {
+  static constexpr int kSize = 4;
+  static constexpr int kPerVec = 4;  // elements per 16-byte vector
+  static constexpr int kKeyBits = 32;
+  __device__ static float load(const char* row, int64_t e) { return __ldg(reinterpret_cast<const float*>(row) + e); }
+  __device__ static uint32_t key(float x) { return key_f32(x); }
+  __device__ static float val(uint32_t k) { return val_f32(k); }
+};
+template <>
+struct ET<uint16_t> {
+  static constexpr int kSize = 2;
+  static constexpr int kPerVec = 8;
+  static constexpr int kKeyBits = 16;
+  __device__ static float load(const char* row, int64_t e) {
+    return __uint_as_float(static_cast<uint32_t>(__ldg(reinterpret_cast<const unsigned short*>(row) + e)) << 16);
+  }
+  __device__ static uint32_t key(float x) { return key_bf16(x); }
+  __device__ static float val(uint32_t k) { return val_bf16(k); }
+};
+
+// Start of row r of sequence b.
+template <typename E, int MODE>
+__device__ __forceinline__ const char* row_ptr(const Params& p, int64_t b, int r) {
+  constexpr int S = ET<E>::kSize;
+  if (MODE == kGreedy) return p.a + ((b * p.RS + r) * p.V) * S;
+  if (r <= p.K) return p.a + ((b * (p.K + 1) + r) * p.V) * S;
+  return p.d + ((b * p.K + (r - p.K - 1)) * p.V) * S;
+}
+
+struct Tile {
+  int64_t b;
+  int r;
+  const char* row;
+  int64_t e0, e1;       // element range of the tile in its row
+  const char* ip;       // interior (16-byte aligned) start
+  uint32_t ibytes;      // interior bytes (multiple of 16), 0 if none
+  int64_t ie0;          // first interior element
+  int nh;               // head elements [e0, e0 + nh), read directly
+  int nt;               // tail elements [e1 - nt, e1), read directly
+};
+
+template <typename E, int MODE>
+__device__ __forceinline__ Tile decode(const Params& p, int64_t w) {
+  constexpr int S = ET<E>::kSize;
+  Tile t;
+  const int64_t per = (int64_t)p.RS * p.NT;
+  t.b = w / per;
+  const int64_t rem = w - t.b * per;
+  t.r = (int)(rem / p.NT);
+  const int64_t k = rem - (int64_t)t.r * p.NT;
+  t.row = row_ptr<E, MODE>(p, t.b, t.r);
+  t.e0 = k * p.TE;
+  t.e1 = min(t.e0 + p.TE, p.V);
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(t.row + t.e0 * S);
+  const uintptr_t a1 = reinterpret_cast<uintptr_t>(t.row + t.e1 * S);
+  const uintptr_t A = (a0 + 15) & ~uintptr_t(15);
+  const uintptr_t Z = a1 & ~uintptr_t(15);
+  if (A < Z) {
+    t.ip = reinterpret_cast<const char*>(A);
+    t.ibytes = (uint32_t)(Z - A);
+    t.nh = (int)((A - a0) / S);
+    t.nt = (int)((a1 - Z) / S);
+    t.ie0 = t.e0 + t.nh;
+  } else {
+    t.ip = nullptr;
+    t.ibytes = 0;
+    t.nh = (int)(t.e1 - t.e0);
+    t.nt = 0;
+    t.ie0 = t.e1;
+  }
+  return t;
+}
+
+// ------------------------------------------------ online (max, sum) ---------
+// (m, s): m the running raw max, s = sum 2^(l*c - fl(m*c)).
+__device__ __forceinline__ void ms_rescale(float& m, float& s, float nm, float c) {
+  if (nm != m) {  // also taken when nm is NaN
+    s = (m == -INFINITY) ? 0.f : s * ex2(m * c - nm * c);
+    m = nm;
+  }
+}
+__device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s2, float c) {
+  const float nm = fmax_nan(m, m2);
+  if (nm == -INFINITY) {
+    m = nm;
+    s = 0.f;
+    return;
+  }
+  const float f1 = (m == -INFINITY) ? 0.f : ex2(m * c - nm * c);
+  const float f2 = (m2 == -INFINITY) ? 0.f : ex2(m2 * c - nm * c);
+  s = s * f1 + s2 * f2;
+  m = nm;
+}
+__device__ __forceinline__ void ms_scalar(float& m, float& s, float x, float c) {
+  ms_rescale(m, s, fmax_nan(m, x), c);
+  if (m == -INFINITY) return;
+  s += ex2(fmaf(x, c, -(m * c)));
+}
+__device__ __forceinline__ void ms_vec(float& m, float& s0, float& s1, const uint4 q, float c, uint16_t) {
+  const uint32_t mm = bf2_max_nan(bf2_max_nan(q.x, q.y), bf2_max_nan(q.z, q.w));
+  const float vmax = fmax_nan(bf_lo(mm), bf_hi(mm));
+  const float nm = fmax_nan(m, vmax);
+  if (nm != m) {
+    const float f = (m == -INFINITY) ? 0.f : ex2(m * c - nm * c);
+    s0 *= f;
+    s1 *= f;
+    m = nm;
+  }
+  if (m == -INFINITY) return;
+  const float nmc = -(m * c);
+  s0 += ex2(fmaf(bf_lo(q.x), c, nmc));
+  s1 += ex2(fmaf(bf_hi(q.x), c, nmc));
+  s0 += ex2(fmaf(bf_lo(q.y), c, nmc));
+  s1 += ex2(fmaf(bf_hi(q.y), c, nmc));
+  s0 += ex2(fmaf(bf_lo(q.z), c, nmc));
+  s1 += ex2(fmaf(bf_hi(q.z), c, nmc));
+  s0 += ex2(fmaf(bf_lo(q.w), c, nmc));
+  s1 += ex2(fmaf(bf_hi(q.w), c, nmc));
+}
+__device__ __forceinline__ void ms_vec(float& m, float& s0, float& s1, const uint4 q, float c, float) {
+  const float x0 = __uint_as_float(q.x), x1 = __uint_as_float(q.y), x2 = __uint_as_float(q.z),
+              x3 = __uint_as_float(q.w);
+  const float vmax = fmax_nan(fmax_nan(x0, x1), fmax_nan(x2, x3));
+  const float nm = fmax_nan(m, vmax);
+  if (nm != m) {
+    const float f = (m == -INFINITY) ? 0.f : ex2(m * c - nm * c);
+    s0 *= f;
+    s1 *= f;
+    m = nm;
+  }
+  if (m == -INFINITY) return;
+  const float nmc = -(m * c);
+  s0 += ex2(fmaf(x0, c, nmc));
+  s1 += ex2(fmaf(x1, c, nmc));
+  s0 += ex2(fmaf(x2, c, nmc));
+  s1 += ex2(fmaf(x3, c, nmc));
+}
+
+// ---------------------------------------------------- argmax (lowest index) --
+// (v, i): best value and its index; i < 0 means "nothing seen but -inf".
+__device__ __forceinline__ bool am_better(float v2, int64_t i2, float v1, int64_t i1) {
+  if (i2 < 0) return false;
+  if (i1 < 0) return true;
+  return (v2 > v1) || (v2 == v1 && i2 < i1);
+}
+__device__ __forceinline__ void am_scalar(float& v, int64_t& i, bool& nan, float x, int64_t e) {
+  if (x != x) {
+    nan = true;
+    return;
+  }
+  if (am_better(x, e, v, i)) {
+    v = x;
+    i = e;
+  }
+}
+__device__ __forceinline__ void am_vec(float& v, int64_t& i, bool& nan, const uint4 q, int64_t e, uint16_t) {
+  const uint32_t mm = bf2_max_nan(bf2_max_nan(q.x, q.y), bf2_max_nan(q.z, q.w));
+  const float vmax = fmax_nan(bf_lo(mm), bf_hi(mm));
+  if (vmax != vmax) {
+    nan = true;
+    return;
+  }
+  if (vmax > v || i < 0) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    int k = 0;
+#pragma unroll
+    for (int j = 7; j >= 0; --j) {
+      const float x = (j & 1) ? bf_hi(w[j >> 1]) : bf_lo(w[j >> 1]);
+      if (x == vmax) k = j;
+    }
+    v = vmax;
+    i = e + k;
+  }
+}
+__device__ __forceinline__ void am_vec(float& v, int64_t& i, bool& nan, const uint4 q, int64_t e, float) {
+  const float x[4] = {__uint_as_float(q.x), __uint_as_float(q.y), __uint_as_float(q.z), __uint_as_float(q.w)};
+  const float vmax = fmax_nan(fmax_nan(x[0], x[1]), fmax_nan(x[2], x[3]));
+  if (vmax != vmax) {
+    nan = true;
+    return;
+  }
+  if (vmax > v || i < 0) {
+    int k = 0;
+#pragma unroll
+    for (int j = 3; j >= 0; --j)
+      if (x[j] == vmax) k = j;
+    v = vmax;
+    i = e + k;
+  }
+}
+
+// ---------------------------------------------- weights for the inverse CDF --
+// Eight consecutive elements starting at e (a multiple of 8); -inf past V.
+template <typename E>
+__device__ __forceinline__ void load8(const char* row, int64_t e, int64_t V, bool aligned, float out[8]) {
+  if (aligned && e + 8 <= V) {
+    if (ET<E>::kSize == 2) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(row + e * 2));
+      out[0] = bf_lo(q.x); out[1] = bf_hi(q.x); out[2] = bf_lo(q.y); out[3] = bf_hi(q.y);
+      out[4] = bf_lo(q.z); out[5] = bf_hi(q.z); out[6] = bf_lo(q.w); out[7] = bf_hi(q.w);
+    } else {
+      const uint4 q0 = __ldg(reinterpret_cast<const uint4*>(row + e * 4));
+      const uint4 q1 = __ldg(reinterpret_cast<const uint4*>(row + e * 4 + 16));
+      out[0] = __uint_as_float(q0.x); out[1] = __uint_as_float(q0.y);
+      out[2] = __uint_as_float(q0.z); out[3] = __uint_as_float(q0.w);
+      out[4] = __uint_as_float(q1.x); out[5] = __uint_as_float(q1.y);
+      out[6] = __uint_as_float(q1.z); out[7] = __uint_as_float(q1.w);
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) out[k] = (e + k < V) ? ET<E>::load(row, e + k) : -INFINITY;
+  }
+}
+
+// The sampler's weights over one row: w_v = p'(v) up to a constant, or, with
+// two rows, w_v = max(0, p'(v) - q'(v)).
+template <typename E, bool kResidual>
+struct Weights {
+  const char* rp;
+  const char* rq;
+  int64_t V;
+  float c, nMcp, nMcq, ip, iq;
+  uint32_t taup, tauq;
+  int topp;
+  bool aligned;
+  __device__ __forceinline__ void w8(int64_t e, float w[8]) const {
+    float lp[8];
+    load8<E>(rp, e, V, aligned, lp);
+    if (kResidual) {
+      float lq[8];
+      load8<E>(rq, e, V, aligned, lq);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float ep = ex2(fmaf(lp[k], c, nMcp));
+        float eq = ex2(fmaf(lq[k], c, nMcq));
+        if (topp) {
+          if (ET<E>::key(lp[k]) < taup) ep = 0.f;
+          if (ET<E>::key(lq[k]) < tauq) eq = 0.f;
+        }
+        w[k] = fmaxf(0.f, fmaf(ep, ip, -eq * iq));
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float ep = ex2(fmaf(lp[k], c, nMcp));
+        if (topp && ET<E>::key(lp[k]) < taup) ep = 0.f;
+        w[k] = ep;
+      }
+    }
+  }
+};
+
+// Inverse-CDF draw by the 256 consumer threads: the smallest t with
+// sum_{v<=t} w_v > u * sum_v w_v. Returns -1 when every weight is zero.
+// The row is cut into cells of 256*m elements (at most kMaxCells cells); a
+// first pass sums each cell, one warp scans the cell sums to find the cell
+// holding the crossing, and rescans that cell alone.
+template <class WF>
+__device__ int64_t cdf_draw(const WF& wf, int64_t V, float u, Shared& sh, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const int64_t m = (V + 256LL * kMaxCells - 1) / (256LL * kMaxCells) > 1 ? (V + 256LL * kMaxCells - 1) / (256LL * kMaxCells) : 1;
+  const int64_t CE = 256 * m;
+  const int ncells = (int)((V + CE - 1) / CE);
+  for (int cc = warp; cc < ncells; cc += kConsumerWarps) {
+    float sum = 0.f;
+    for (int64_t q = 0; q < m; ++q) {
+      float w[8];
+      wf.w8(cc * CE + (lane * m + q) * 8, w);
+      sum += ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+    }
+    sum = warp_sum(sum);
+    if (lane == 0) sh.cells[cc] = sum;
+  }
+  cbar();
+  if (warp == 0) {
+    const int cpl = (ncells + 31) / 32;
+    const int c0 = min(ncells, lane * cpl), c1 = min(ncells, c0 + cpl);
+    float ls = 0.f;
+    for (int cc = c0; cc < c1; ++cc) ls += sh.cells[cc];
+    const float incl = warp_incl_scan(ls, lane);
+    const float Z = __shfl_sync(0xffffffffu, incl, 31);
+    int64_t t = -1;
+    if (Z > 0.f) {
+      const float Tg = u * Z;
+      float run = incl - ls;
+      int hit = -1;
+      for (int cc = c0; cc < c1; ++cc) {
+        if (run + sh.cells[cc] > Tg) {
+          hit = cc;
+          break;
+        }
+        run += sh.cells[cc];
+      }
+      const unsigned bal = __ballot_sync(0xffffffffu, hit >= 0);
+      int cstar;
+      float Tl = 0.f;
+      bool last_positive = false;
+      if (bal) {
+        const int fl = __ffs(bal) - 1;
+        cstar = __shfl_sync(0xffffffffu, hit, fl);
+        Tl = Tg - __shfl_sync(0xffffffffu, run, fl);
+      } else {  // u*Z at or past the total after rounding: the last positive weight
+        int last = -1;
+        for (int cc = c0; cc < c1; ++cc)
+          if (sh.cells[cc] > 0.f) last = cc;
+        for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+        cstar = last;
+        last_positive = true;
+      }
+      // the crossing cell: lane l owns elements [cstar*CE + l*8m, +8m)
+      const int64_t base = (int64_t)cstar * CE + (int64_t)lane * 8 * m;
+      float ls2 = 0.f;
+      for (int64_t q = 0; q < m; ++q) {
+        float w[8];
+        wf.w8(base + q * 8, w);
+        ls2 += ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+      }
+      const float incl2 = warp_incl_scan(ls2, lane);
+      const float excl2 = incl2 - ls2;
+      int64_t mine = -1;
+      if (!last_positive) {
+        const unsigned bal2 = __ballot_sync(0xffffffffu, excl2 + ls2 > Tl);
+        if (bal2) {
+          const int fl2 = __ffs(bal2) - 1;
+          if (lane == fl2) {
+            float acc = excl2;
+            int64_t lastpos = -1;
+            for (int64_t q = 0; q < m && mine < 0; ++q) {
+              float w[8];
+              wf.w8(base + q * 8, w);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) {
+                if (mine < 0) {
+                  acc += w[k];
+                  if (w[k] > 0.f) lastpos = base + q * 8 + k;
+                  if (acc > Tl) mine = base + q * 8 + k;
+                }
+              }
+            }
+            if (mine < 0) mine = lastpos;  // rounding inside the lane
+          }
+          mine = __shfl_sync(0xffffffffu, mine, fl2);
+        } else {
+          last_positive = true;
+        }
+      }
+      if (last_positive) {
+        int64_t lastpos = -1;
+        for (int64_t q = 0; q < m; ++q) {
+          float w[8];
+          wf.w8(base + q * 8, w);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            if (w[k] > 0.f) lastpos = base + q * 8 + k;
+        }
+        for (int o = 16; o > 0; o >>= 1) {
+          const long long other = __shfl_xor_sync(0xffffffffu, (long long)lastpos, o);
+          lastpos = max((long long)lastpos, other);
+        }
+        mine = lastpos;
+      }
+      t = mine;
+    }
+    if (lane == 0) sh.bl[0] = t;
+  }
+  cbar();
+  const int64_t t = sh.bl[0];
+  cbar();
+  return t;
+}
+
+// ------------------------------------------------ block-wide helpers ---------
+// Exclusive prefix of one float per consumer thread; also returns the total.
+__device__ __forceinline__ float block_excl_scan(float v, float& total, Shared& sh, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const float incl = warp_incl_scan(v, lane);
+  if (lane == 31) sh.red_s[warp] = incl;
+  cbar();
+  float off = 0.f, tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kConsumerWarps; ++w) {
+    const float x = sh.red_s[w];
+    if (w < warp) off += x;
+    tot += x;
+  }
+  cbar();
+  total = tot;
+  return off + incl - v;
+}
+
+// Calls f(element value) for every element of a row, spread over the
+// consumer threads (16-byte loads when the row is aligned).
+template <typename E, class F>
+__device__ __forceinline__ void for_each_elem(const char* row, int64_t V, int tid, F&& f) {
+  constexpr int PV = ET<E>::kPerVec;
+  if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+    const int64_t nv = V / PV;
+    const uint4* rv = reinterpret_cast<const uint4*>(row);
+    for (int64_t v = tid; v < nv; v += kConsumerThreads) {
+      const uint4 q = __ldg(rv + v);
+      if (PV == 8) {
+        f(bf_lo(q.x)); f(bf_hi(q.x)); f(bf_lo(q.y)); f(bf_hi(q.y));
+        f(bf_lo(q.z)); f(bf_hi(q.z)); f(bf_lo(q.w)); f(bf_hi(q.w));
+      } else {
+        f(__uint_as_float(q.x)); f(__uint_as_float(q.y)); f(__uint_as_float(q.z)); f(__uint_as_float(q.w));
+      }
+    }
+    for (int64_t e = nv * PV + tid; e < V; e += kConsumerThreads) f(ET<E>::load(row, e));
+  } else {
+    for (int64_t e = tid; e < V; e += kConsumerThreads) f(ET<E>::load(row, e));
+  }
+}
+
+// Top-p cut of one row: the largest key tau whose upper set
+// {v : key(l_v) >= tau} holds mass >= top_p * s, and that mass.
+// Windows of kHistBins bins are laid below the current upper key; a bin is
+// one exact key (counts times the key's weight) or, for fp32 rows first, a
+// run of 2^sh keys (weights added per element). The window that holds the
+// crossing is refined until the bins are exact keys.
+template <typename E>
+__device__ void topp_cut(const Params& p, Shared& sh, const char* row, float M, float s, int tid, uint32_t& tau,
+                         float& cum) {
+  const float c = p.c, nMc = -(M * c);
+  const float target = p.top_p * s;
+  uint32_t hi = ET<E>::key(M);
+  int shf = (ET<E>::kKeyBits == 16) ? 0 : 16;
+  float above = 0.f;
+  for (int iter = 0; iter < 4096; ++iter) {
+    const uint64_t span = (uint64_t)kHistBins << shf;
+    const uint32_t lo = ((uint64_t)hi + 1 >= span) ? (uint32_t)((uint64_t)hi + 1 - span) : 0u;
+    const int nb = (int)(((uint64_t)hi - lo) >> shf) + 1;
+    for (int k = tid; k < kHistBins; k += kConsumerThreads) sh.hist.u[k] = 0u;
+    cbar();
+    const int s_ = shf;
+    for_each_elem<E>(row, p.V, tid, [&](float x) {
+      const uint32_t k = ET<E>::key(x);
+      if (k >= lo && k <= hi) {
+        const int bin = (int)((hi - k) >> s_);
+        if (s_ == 0)
+          atomicAdd(&sh.hist.u[bin], 1u);
+        else
+          atomicAdd(&sh.hist.f[bin], ex2(fmaf(x, c, nMc)));
+      }
+    });
+    cbar();
+    constexpr int PER = kHistBins / kConsumerThreads;
+    float m[PER];
+    float ls = 0.f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      const int bin = tid * PER + j;
+      float mj = 0.f;
+      if (bin < nb) {
+        if (shf == 0) {
+          const uint32_t cnt = sh.hist.u[bin];
+          mj = cnt ? (float)cnt * ex2(fmaf(ET<E>::val(hi - (uint32_t)bin), c, nMc)) : 0.f;
+        } else {
+          mj = sh.hist.f[bin];
+        }
+      }
+      m[j] = mj;
+      ls += mj;
+    }
+    float total;
+    const float excl = block_excl_scan(ls, total, sh, tid);
+    if (tid == 0) sh.bi[0] = INT_MAX;
+    cbar();
+    float run = excl;
+    int hit = -1;
+    float before = 0.f, mh = 0.f;
+#pragma unroll
+    for (int j = 0; j < PER; ++j) {
+      if (hit < 0 && above + run + m[j] >= target) {
+        hit = tid * PER + j;
+        before = run;
+        mh = m[j];
+      }
+      run += m[j];
+    }
+    if (hit >= 0) atomicMin(&sh.bi[0], hit);
+    cbar();
+    const int b = sh.bi[0];
+    if (b != INT_MAX && hit == b) {
+      sh.bf[0] = before;
+      sh.bf[1] = mh;
+    }
+    cbar();
+    if (b != INT_MAX) {
+      const float bb = sh.bf[0], bm = sh.bf[1];
+      if (shf == 0) {
+        tau = hi - (uint32_t)b;
+        cum = above + bb + bm;
+        cbar();
+        return;
+      }
+      above += bb;
+      hi = hi - ((uint32_t)b << shf);
+      shf = (shf > 11) ? shf - 11 : 0;
+    } else {
+      above += total;
+      if (lo == 0u) {  // every key seen: rounding left the mass short of top_p * s
+        tau = 0u;
+        cum = above;
+        cbar();
+        return;
+      }
+      hi = lo - 1u;
+    }
+    cbar();
+  }
+  tau = 0u;
+  cum = s;
+}
+
+// ------------------------------------------------------ sequence tails -------
+
+template <typename E>
+__device__ void seq_sample(const Params& p, Shared& sh, int64_t b, int tid) {
+  const int K = p.K;
+  const float c = p.c;
+  if (tid == 0) sh.bi[1] = K;
+  cbar();
+  int bad = 0;
+  for (int i = tid; i < K; i += kConsumerThreads) {
+    const int32_t x = p.tokens[b * K + i];
+    const float u = p.uniforms[b * (K + 1) + i];
+    const RowStat rp = rs_load(p, b * p.RS + i);
+    const RowStat rq = rs_load(p, b * p.RS + K + 1 + i);
+    if (x < 0 || (int64_t)x >= p.V || !(u >= 0.f && u < 1.f) || rp.M != rp.M || rq.M != rq.M) {
+      bad = 1;
+      continue;
+    }
+    const float lp = ET<E>::load(row_ptr<E, kSample>(p, b, i), x);
+    const float lq = ET<E>::load(row_ptr<E, kSample>(p, b, K + 1 + i), x);
+    float alpha;
+    const bool in_p = !p.topp || ET<E>::key(lp) >= rp.tau;
+    const bool in_q = !p.topp || ET<E>::key(lq) >= rq.tau;
+    if (!in_p || lp == -INFINITY) {
+      alpha = 0.f;
+    } else if (!in_q || lq == -INFINITY) {
+      alpha = 1.f;
+    } else {
+      const float ap = fmaf(lp, c, -(rp.M * c));
+      const float aq = fmaf(lq, c, -(rq.M * c));
+      alpha = fminf(1.f, ex2(ap - aq) * (rq.cum / rp.cum));
+    }
+    if (!(u < alpha)) atomicMin(&sh.bi[1], i);
+  }
+  {
+    const RowStat rk = rs_load(p, b * p.RS + K);
+    const float uK = p.uniforms[b * (K + 1) + K];
+    if (tid == 0 && (rk.M != rk.M || !(uK >= 0.f && uK < 1.f))) bad = 1;
+  }
+  bad = cbar_or(bad);
+  const int j = sh.bi[1];
+  int32_t* out = p.out_tokens + b * (K + 1);
+  if (bad) {
+    for (int i = tid; i <= K; i += kConsumerThreads) out[i] = -1;
+    if (tid == 0) {
+      p.out_accept_len[b] = -1;
+      atomicOr(p.ctl + 3, kStatusInput);
+    }
+    return;
+  }
+  const float uK = p.uniforms[b * (K + 1) + K];
+  const RowStat rp = rs_load(p, b * p.RS + j);
+  const bool aligned = (p.V * ET<E>::kSize) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.a) & 15) == 0 &&
+                       (reinterpret_cast<uintptr_t>(p.d) & 15) == 0;
+  int64_t t = -1;
+  if (j < K) {
+    const RowStat rq = rs_load(p, b * p.RS + K + 1 + j);
+    Weights<E, true> wf{row_ptr<E, kSample>(p, b, j), row_ptr<E, kSample>(p, b, K + 1 + j), p.V, c, -(rp.M * c),
+                        -(rq.M * c), 1.f / rp.cum, 1.f / rq.cum, rp.tau, rq.tau, p.topp, aligned};
+    t = cdf_draw(wf, p.V, uK, sh, tid);
+  }
+  if (t < 0) {  // bonus row, or a residual that is all zero: draw from p'_j
+    Weights<E, false> wf{row_ptr<E, kSample>(p, b, j), nullptr, p.V, c, -(rp.M * c), 0.f, 1.f, 0.f, rp.tau, 0u,
+                         p.topp, aligned};
+    t = cdf_draw(wf, p.V, uK, sh, tid);
+  }
+  for (int i = tid; i <= K; i += kConsumerThreads)
+    out[i] = i < j ? p.tokens[b * K + i] : (i == j ? (int32_t)t : -1);
+  if (tid == 0) p.out_accept_len[b] = j;
+}
+
+template <typename E>
+__device__ void seq_argmax_limit(const Params& p, Shared& sh, int64_t b, int tid) {
+  const int K = p.K;
+  if (tid == 0) sh.bi[1] = K;
+  cbar();
+  int bad = 0;
+  for (int i = tid; i <= K; i += kConsumerThreads) {
+    const RowStat r = rs_load(p, b * p.RS + i);
+    if (r.M != r.M) bad = 1;
+    if (i < K) {
+      const int32_t x = p.tokens[b * K + i];
+      if (x < 0 || (int64_t)x >= p.V) bad = 1;
+      else if ((uint32_t)x != r.tau) atomicMin(&sh.bi[1], i);
+    }
+  }
+  bad = cbar_or(bad);
+  const int j = sh.bi[1];
+  int32_t* out = p.out_tokens + b * (K + 1);
+  if (bad) {
+    for (int i = tid; i <= K; i += kConsumerThreads) out[i] = -1;
+    if (tid == 0) {
+      p.out_accept_len[b] = -1;
+      atomicOr(p.ctl + 3, kStatusInput);
+    }
+    return;
+  }
+  const RowStat rj = rs_load(p, b * p.RS + j);
+  for (int i = tid; i <= K; i += kConsumerThreads)
+    out[i] = i < j ? p.tokens[b * K + i] : (i == j ? (int32_t)rj.tau : -1);
+  if (tid == 0) p.out_accept_len[b] = j;
+}
+
+__device__ void seq_greedy(const Params& p, Shared& sh, int64_t b, int tid) {
+  const int G = p.G, N = p.N;
+  if (tid == 0) sh.bi[1] = -1;
+  cbar();
+  int bad = 0;
+  for (int r = tid; r < G * N; r += kConsumerThreads) {
+    const RowStat rs = rs_load(p, b * p.RS + r);
+    if (rs.M != rs.M) bad = 1;
+  }
+  for (int k = tid; k < G * (N - 1); k += kConsumerThreads) {
+    const int32_t x = p.tokens[b * G * (N - 1) + k];
+    if (x < 0 || (int64_t)x >= p.V) bad = 1;
+  }
+  bad = cbar_or(bad);
+  int32_t* out = p.out_tokens + b * N;
+  if (bad) {
+    for (int n = tid; n < N; n += kConsumerThreads) out[n] = -1;
+    if (tid == 0) {
+      p.out_accept_len[b] = -1;
+      if (p.out_best) p.out_best[b] = -1;
+      atomicOr(p.ctl + 3, kStatusInput);
+    }
+    return;
+  }
+  for (int g = tid; g < G; g += kConsumerThreads) {
+    const int32_t* cg = p.tokens + (b * G + g) * (N - 1);
+    const float4* rg = p.rowstat + b * p.RS + (int64_t)g * N;
+    int L = 0;
+    while (L < N - 1 && (uint32_t)cg[L] == __float_as_uint(__ldcg(rg + L).w)) ++L;
+    atomicMax(&sh.bi[1], L * 65536 + (65535 - g));
+  }
+  cbar();
+  const int key = sh.bi[1];
+  const int L = key >> 16, g = 65535 - (key & 0xFFFF);
+  const int32_t* cg = p.tokens + (b * G + g) * (N - 1);
+  const float4* rg = p.rowstat + b * p.RS + (int64_t)g * N;
+  for (int n = tid; n < N; n += kConsumerThreads)
+    out[n] = n < L ? cg[n] : (n == L ? (int32_t)__float_as_uint(__ldcg(rg + L).w) : -1);
+  if (tid == 0) {
+    p.out_accept_len[b] = L;
+    if (p.out_best) p.out_best[b] = g;
+  }
+}
+
+// ------------------------------------------------------------- row tails -----
+
+template <typename E, int MODE>
+__device__ void finish_row(const Params& p, Shared& sh, int64_t b, int r, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const int64_t row = b * p.RS + r;
+  __threadfence();
+  if (warp == 0) {
+    const float2* part = p.part + row * p.NT;
+    if (MODE == kSample) {
+      float m = -INFINITY, s = 0.f;
+      for (int64_t k = lane; k < p.NT; k += 32) {
+        const float2 v = __ldcg(part + k);
+        ms_combine(m, s, v.x, v.y, p.c);
+      }
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        ms_combine(m, s, m2, s2, p.c);
+      }
+      if (lane == 0) {
+        sh.bf[2] = m;
+        sh.bf[3] = s;
+      }
+    } else {
+      float v = -INFINITY;
+      int64_t i = -1;
+      bool nan = false;
+      for (int64_t k = lane; k < p.NT; k += 32) {
+        const float2 pv = __ldcg(part + k);
+        const int64_t pi = (int64_t)__float_as_int(pv.y);
+        if (pv.x != pv.x) nan = true;
+        else if (am_better(pv.x, pi, v, i)) {
+          v = pv.x;
+          i = pi;
+        }
+      }
+      for (int o = 16; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        const long long i2 = __shfl_xor_sync(0xffffffffu, (long long)i, o);
+        if (am_better(v2, i2, v, i)) {
+          v = v2;
+          i = i2;
+        }
+      }
+      nan = __any_sync(0xffffffffu, nan);
+      if (lane == 0) {
+        RowStat rs;
+        rs.M = nan ? __int_as_float(0x7fc00000) : v;
+        rs.s = 0.f;
+        rs.cum = 0.f;
+        rs.tau = (uint32_t)(i < 0 ? 0 : i);  // all -inf: every element ties, index 0 wins
+        rs_store(p, row, rs);
+      }
+    }
+  }
+  cbar();
+  if (MODE == kSample) {
+    const float M = sh.bf[2], s = sh.bf[3];
+    const bool valid = (M > -INFINITY) && (M < INFINITY);  // NaN fails both
+    uint32_t tau = 0u;
+    float cum = s;
+    const char* rowp = row_ptr<E, MODE>(p, b, r);
+    if (valid && p.topp) topp_cut<E>(p, sh, rowp, M, s, tid, tau, cum);
+    if (tid == 0) {
+      RowStat rs;
+      rs.M = valid ? M : __int_as_float(0x7fc00000);
+      rs.s = s;
+      rs.cum = cum;
+      rs.tau = tau;
+      rs_store(p, row, rs);
+      if (p.out_row_stats) {
+        float4 o;
+        const float Mc = M * p.c;
+        o.x = valid ? __fdiv_rn(M, p.T) : __int_as_float(0x7fc00000);
+        o.y = valid ? (Mc + lg2(s)) * 0.69314718055994531f : __int_as_float(0x7fc00000);
+        o.z = valid ? cum / s : __int_as_float(0x7fc00000);
+        o.w = (valid && p.topp) ? ET<E>::val(tau) : -INFINITY;
+        reinterpret_cast<float4*>(p.out_row_stats)[row] = o;
+      }
+    }
+  }
+  if (tid == 0) {
+    p.row_cnt[row] = 0u;
+    __threadfence();
+    const uint32_t old = atomicAdd(p.seq_cnt + b, 1u);
+    sh.flag = (old == (uint32_t)p.RS - 1u);
+    if (sh.flag) p.seq_cnt[b] = 0u;
+  }
+  cbar();
+  if (sh.flag) {
+    __threadfence();
+    if (MODE == kSample) seq_sample<E>(p, sh, b, tid);
+    else if (MODE == kArgmaxLimit) seq_argmax_limit<E>(p, sh, b, tid);
+    else seq_greedy(p, sh, b, tid);
+  }
+  cbar();
+}
+
+// --------------------------------------------------------------- kernel -------
+
+template <typename E, int MODE>
+__device__ void producer_loop(const Params& p, char* ring, Shared& sh) {
+  unsigned long long* next = reinterpret_cast<unsigned long long*>(p.ctl);
+  int last_parity[kMaxStages];
+  for (int i = 0; i < kMaxStages; ++i) last_parity[i] = -1;
+  bool aborted = false;
+  for (int64_t it = 0;; ++it) {
+    const int slot = (int)(it % p.stages);
+    const uint32_t ph = (uint32_t)((it / p.stages) & 1);
+    if (it >= p.stages && !mbar_wait(&sh.empty[slot], ph ^ 1u)) {
+      atomicOr(p.ctl + 3, kStatusTimeout);
+      aborted = true;
+      break;
+    }
+    const int64_t w = (int64_t)atomicAdd(next, 1ull);
+    sh.meta[slot] = w;
+    if (w >= p.W) {
+      mbar_arrive(&sh.full[slot]);
+      break;
+    }
+    const Tile t = decode<E, MODE>(p, w);
+    if (t.ibytes) {
+      mbar_arrive_expect_tx(&sh.full[slot], t.ibytes);
+      bulk_g2s(ring + (size_t)slot * kTileBytes, t.ip, t.ibytes, &sh.full[slot]);
+      last_parity[slot] = (int)ph;
+    } else {
+      mbar_arrive(&sh.full[slot]);
+    }
+  }
+  if (aborted) {  // let copies still in flight land before the CTA exits
+    for (int i = 0; i < p.stages; ++i)
+      if (last_parity[i] >= 0) (void)mbar_wait(&sh.full[i], (uint32_t)last_parity[i]);
+  }
+  // The last producer to finish re-arms the work counter for the next call.
+  __threadfence();
+  const uint32_t prev = atomicAdd(p.ctl + 2, 1u);
+  if (prev == gridDim.x - 1) {
+    *next = 0ull;
+    p.ctl[2] = 0u;
+    __threadfence();
+  }
+}
+
+template <typename E, int MODE>
+__device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int tid) {
+  constexpr int PV = ET<E>::kPerVec;
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int64_t it = 0;; ++it) {
+    const int slot = (int)(it % p.stages);
+    const uint32_t ph = (uint32_t)((it / p.stages) & 1);
+    const bool ok = mbar_wait(&sh.full[slot], ph);
+    if (cbar_or(!ok)) {
+      if (tid == 0) atomicOr(p.ctl + 3, kStatusTimeout);
+      return;
+    }
+    const int64_t w = sh.meta[slot];
+    if (w >= p.W) return;
+    const Tile t = decode<E, MODE>(p, w);
+    const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)slot * kTileBytes);
+    const int nvec = (int)(t.ibytes >> 4);
+    float2 res;
+    if (MODE == kSample) {
+      float m = -INFINITY, s0 = 0.f, s1 = 0.f;
+      for (int v = tid; v < nvec; v += kConsumerThreads) ms_vec(m, s0, s1, sv[v], p.c, E());
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[slot]);
+      if (tid < t.nh) ms_scalar(m, s0, ET<E>::load(t.row, t.e0 + tid), p.c);
+      if (tid >= 32 && tid < 32 + t.nt) ms_scalar(m, s0, ET<E>::load(t.row, t.e1 - t.nt + (tid - 32)), p.c);
+      float s = s0 + s1;
+      for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        ms_combine(m, s, m2, s2, p.c);
+      }
+      if (lane == 0) {
+        sh.red_m[warp] = m;
+        sh.red_s[warp] = s;
+      }
+      cbar();
+      if (tid == 0) {
+        float M = sh.red_m[0], S = sh.red_s[0];
+        for (int k = 1; k < kConsumerWarps; ++k) ms_combine(M, S, sh.red_m[k], sh.red_s[k], p.c);
+        res = make_float2(M, S);
+      }
+    } else {
+      float v = -INFINITY;
+      int64_t i = -1;
+      bool nan = false;
+      for (int q = tid; q < nvec; q += kConsumerThreads) am_vec(v, i, nan, sv[q], t.ie0 + (int64_t)q * PV, E());
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[slot]);
+      if (tid < t.nh) am_scalar(v, i, nan, ET<E>::load(t.row, t.e0 + tid), t.e0 + tid);
+      if (tid >= 32 && tid < 32 + t.nt) {
+        const int64_t e = t.e1 - t.nt + (tid - 32);
+        am_scalar(v, i, nan, ET<E>::load(t.row, e), e);
+      }
+      for (int o = 16; o > 0; o >>= 1) {
+        const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        const long long i2 = __shfl_xor_sync(0xffffffffu, (long long)i, o);
+        if (am_better(v2, i2, v, i)) {
+          v = v2;
+          i = i2;
+        }
+      }
+      nan = __any_sync(0xffffffffu, nan);
+      if (lane == 0) {
+        sh.red_m[warp] = nan ? __int_as_float(0x7fc00000) : v;
+        sh.red_i[warp] = i;
+      }
+      cbar();
+      if (tid == 0) {
+        float V_ = sh.red_m[0];
+        int64_t I = sh.red_i[0];
+        bool N_ = V_ != V_;
+        for (int k = 1; k < kConsumerWarps; ++k) {
+          const float v2 = sh.red_m[k];
+          if (v2 != v2) N_ = true;
+          else if (am_better(v2, sh.red_i[k], V_, I)) {
+            V_ = v2;
+            I = sh.red_i[k];
+          }
+        }
+        if (N_ && !(V_ != V_)) V_ = __int_as_float(0x7fc00000);
+        res = make_float2(V_, __int_as_float((int)I));
+      }
+    }
+    if (tid == 0) {
+      const int64_t row = t.b * p.RS + t.r;
+      p.part[w] = res;
+      __threadfence();
+      const uint32_t old = atomicAdd(p.row_cnt + row, 1u);
+      sh.flag = (old == (uint32_t)(p.NT - 1));
+    }
+    cbar();
+    if (sh.flag) finish_row<E, MODE>(p, sh, t.b, t.r, tid);
+  }
+}
+
+template <typename E, int MODE>
+__global__ void __launch_bounds__(kThreads, 2) verify_kernel(const Params p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  char* ring = reinterpret_cast<char*>(smem);
+  Shared& sh = *reinterpret_cast<Shared*>(smem + (size_t)p.stages * kTileBytes);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      mbar_init(&sh.full[i], 1u);
+      mbar_init(&sh.empty[i], (uint32_t)kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid >= kConsumerThreads) {
+    if (tid == kConsumerThreads) producer_loop<E, MODE>(p, ring, sh);
+    return;
+  }
+  consumer_loop<E, MODE>(p, ring, sh, tid);
+}
+
+// ------------------------------------------------------------- launching ------
+
+template <typename E, int MODE>
+static cudaError_t launch_t(const Params& p, int grid, cudaStream_t stream) {
+  const size_t smem = shared_bytes(p.stages);
+  auto* k = verify_kernel<E, MODE>;
+  // Raise the dynamic shared-memory limit once per size (not a stream
+  // operation, but kept out of later calls so they can be graph-captured).
+  static size_t raised = 0;
+  if (smem > raised) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(shared_bytes(kMaxStages)));
+    if (e != cudaSuccess) return e;
+    raised = shared_bytes(kMaxStages);
+  }
+  k<<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+int kernel_threads() { return kThreads; }
+
+cudaError_t launch(const Params& p, int dtype, int mode, int grid, cudaStream_t stream) {
+  if (dtype == 1) {
+    if (mode == kSample) return launch_t<uint16_t, kSample>(p, grid, stream);
+    if (mode == kArgmaxLimit) return launch_t<uint16_t, kArgmaxLimit>(p, grid, stream);
+    return launch_t<uint16_t, kGreedy>(p, grid, stream);
+  }
+  if (mode == kSample) return launch_t<float, kSample>(p, grid, stream);
+  if (mode == kArgmaxLimit) return launch_t<float, kArgmaxLimit>(p, grid, stream);
+  return launch_t<float, kGreedy>(p, grid, stream);
+}
+
+}  // namespace sv

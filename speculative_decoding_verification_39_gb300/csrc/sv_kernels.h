@@ -1,0 +1,44 @@
+// sv_kernels.h — internal interface between the C ABI (sv_api.cu) and the
+// kernels (sv_kernels.cu). Not installed; not part of the public ABI.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+enum Mode { kSample = 0, kArgmaxLimit = 1, kGreedy = 2 };
+constexpr int kMaxStages = 8;
+constexpr int kTileBytes = 16384;  // one ring stage holds one tile
+
+struct Params {
+  const char* a;           // target logits [B,K+1,V] (sampling) or logits [B,G,N,V] (greedy)
+  const char* d;           // draft logits [B,K,V] (sampling, T > 0)
+  const int32_t* tokens;   // draft tokens [B,K] or candidates [B,G,N-1]
+  const float* uniforms;   // [B,K+1]
+  int32_t* out_tokens;
+  int32_t* out_accept_len;
+  int32_t* out_best;       // nullable (greedy)
+  float* out_row_stats;    // nullable (sampling)
+  int64_t B, V;
+  int K, G, N;
+  int RS;                  // rows per sequence
+  int64_t NT;              // tiles per row
+  int64_t TE;              // elements per tile
+  int64_t W;               // tiles in the call = B * RS * NT
+  float c;                 // log2(e) / T
+  float T;
+  float top_p;
+  int topp;                // top_p < 1
+  uint32_t* ctl;           // [0..1] work counter (u64), [2] finished producers, [3] status bits
+  uint32_t* row_cnt;       // [B*RS] tiles published per row
+  uint32_t* seq_cnt;       // [B] rows finished per sequence
+  float2* part;            // [W] per-tile partials
+  float4* rowstat;         // [B*RS] per-row results
+  int stages;
+};
+
+size_t shared_bytes(int stages);
+cudaError_t launch(const Params& p, int dtype, int mode, int grid, cudaStream_t stream);
+int kernel_threads();
+
+}  // namespace sv

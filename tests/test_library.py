@@ -1,0 +1,85 @@
+"""The C-ABI library builds, loads and exports every symbol the header
+declares; host-side argument checks reject bad calls before any launch. No
+GPU is needed: every call here fails its checks before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import speculative_decoding_verification_39_gb300 as svpkg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "specverify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    svpkg.build()
+    return svpkg.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(sv_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    assert "sv_verify_sample" in names and "sv_verify_greedy" in names
+    assert set(names) == set(svpkg.exported_symbols())
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = os.popen(f"nm -D --defined-only {svpkg._SO}").read()
+    exported = set(re.findall(r" T (sv_[a-z_]+)", out))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for rc in range(-6, 1):
+        assert lib.sv_status_string(rc)
+    assert lib.sv_status_string(0) == b"ok"
+
+
+def test_host_argument_checks(lib):
+    f = lib.sv_verify_sample
+    p = ctypes.c_void_p(16)  # never dereferenced: the checks fail first
+    # dtype
+    assert f(p, p, p, p, 4, 3, 100, 7, 1.0, 1.0, p, p, None, None) == -2
+    # shapes
+    assert f(p, p, p, p, -1, 3, 100, 1, 1.0, 1.0, p, p, None, None) == -1
+    assert f(p, p, p, p, 4, 0, 100, 1, 1.0, 1.0, p, p, None, None) == -1
+    assert f(p, p, p, p, 4, 3, 1, 1, 1.0, 1.0, p, p, None, None) == -1
+    assert f(p, p, p, p, 4, 3, 1 << 31, 1, 1.0, 1.0, p, p, None, None) == -1
+    # temperature / top_p
+    assert f(p, p, p, p, 4, 3, 100, 1, -0.5, 1.0, p, p, None, None) == -1
+    assert f(p, p, p, p, 4, 3, 100, 1, float("nan"), 1.0, p, p, None, None) == -1
+    assert f(p, p, p, p, 4, 3, 100, 1, 1.0, 0.0, p, p, None, None) == -1
+    assert f(p, p, p, p, 4, 3, 100, 1, 1.0, 1.5, p, p, None, None) == -1
+    # null pointers
+    assert f(None, p, p, p, 4, 3, 100, 1, 1.0, 1.0, p, p, None, None) == -1
+    assert f(p, None, p, p, 4, 3, 100, 1, 1.0, 1.0, p, p, None, None) == -1
+    assert f(p, p, p, None, 4, 3, 100, 1, 1.0, 1.0, p, p, None, None) == -1
+    # misaligned logits for the dtype
+    q = ctypes.c_void_p(17)
+    assert f(q, p, p, p, 4, 3, 100, 1, 1.0, 1.0, p, p, None, None) == -2
+    # B == 0 is a no-op, even with null pointers
+    assert f(None, None, None, None, 0, 3, 100, 1, 1.0, 1.0, None, None, None, None) == 0
+    g = lib.sv_verify_greedy
+    assert g(p, p, 4, 0, 5, 100, 1, p, p, None, None) == -1
+    assert g(p, p, 4, 7, 1, 100, 1, p, p, None, None) == -1
+    assert g(p, p, 4, 7, 5, 100, 9, p, p, None, None) == -2
+    assert g(None, None, 0, 7, 5, 100, 1, None, None, None, None) == 0
+    assert lib.sv_set_launch_shape(9, 1) == -1
+    assert lib.sv_set_launch_shape(0, 0) == 0
+
+
+def test_binding_refuses_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(svpkg, "_SO", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(svpkg, "_lib_handle", None)
+    with pytest.raises(RuntimeError):
+        svpkg.lib()
