@@ -22,8 +22,16 @@ std::atomic<int> g_stages{kDefaultStages};
 std::atomic<int> g_ctas_per_sm{kDefaultCtasPerSm};
 std::atomic<uint64_t> g_launches{0};
 
+// A scratch area has three parts at fixed places: the control block, a
+// counter region and a data region. Every counter is back at zero when a call
+// completes (the kernel resets what it used), and the counter region never
+// holds anything else, so calls of any shape can follow each other without a
+// memset. The data region (per-tile partials, per-row results) is written
+// before it is read in every call.
 struct Scratch {
   void* base = nullptr;
+  size_t cnt_words = 0;   // capacity of the counter region, in 32-bit words
+  size_t data_bytes = 0;  // capacity of the data region
   size_t bytes = 0;
 };
 
@@ -31,49 +39,39 @@ std::mutex g_mu;
 std::map<std::pair<int, uintptr_t>, Scratch> g_scratch;
 std::map<int, int> g_sm_count;
 
+constexpr size_t kCtlBytes = 256;
+
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-struct Layout {
-  size_t ctl, row_cnt, seq_cnt, part, rowstat, total;
-};
+size_t counter_offset() { return kCtlBytes; }
+size_t data_offset(const Scratch& s) { return kCtlBytes + align256(s.cnt_words * 4); }
 
-Layout layout_for(int64_t B, int64_t rows, int64_t W) {
-  Layout L;
-  L.ctl = 0;
-  L.row_cnt = align256(L.ctl + 64);
-  L.seq_cnt = align256(L.row_cnt + (size_t)rows * 4);
-  L.part = align256(L.seq_cnt + (size_t)B * 4);
-  L.rowstat = align256(L.part + (size_t)W * 8);
-  L.total = align256(L.rowstat + (size_t)rows * 16);
-  return L;
-}
-
-// Returns a zero-initialised scratch area of at least `bytes` for the current
-// device and `stream`. Counters inside it are self-cleaning, so it is zeroed
-// only when (re)allocated.
-int get_scratch(cudaStream_t stream, size_t bytes, void** out, int* device) {
+// Returns the scratch of the current device and `stream`, grown (and zeroed)
+// if it has fewer than `cnt_words` counters or `data_bytes` of data room.
+int get_scratch(cudaStream_t stream, size_t cnt_words, size_t data_bytes, Scratch* out, int* device) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
   *device = dev;
   std::lock_guard<std::mutex> lk(g_mu);
   Scratch& s = g_scratch[{dev, reinterpret_cast<uintptr_t>(stream)}];
-  if (s.bytes < bytes) {
+  if (s.cnt_words < cnt_words || s.data_bytes < data_bytes) {
     if (s.base) {
       cudaStreamSynchronize(stream);
       cudaFree(s.base);
-      s.base = nullptr;
-      s.bytes = 0;
+      s = Scratch{};
     }
-    size_t want = bytes < (1u << 20) ? (1u << 20) : bytes;
-    if (cudaMalloc(&s.base, want) != cudaSuccess) {
-      s.base = nullptr;
+    Scratch n;
+    n.cnt_words = cnt_words < 65536 ? 65536 : cnt_words;
+    n.data_bytes = align256(data_bytes < (1u << 20) ? (1u << 20) : data_bytes);
+    n.bytes = data_offset(n) + n.data_bytes;
+    if (cudaMalloc(&n.base, n.bytes) != cudaSuccess) {
       cudaGetLastError();
       return SV_ERR_NOMEM;
     }
-    if (cudaMemsetAsync(s.base, 0, want, stream) != cudaSuccess) return SV_ERR_CUDA;
-    s.bytes = want;
+    if (cudaMemsetAsync(n.base, 0, n.bytes, stream) != cudaSuccess) return SV_ERR_CUDA;
+    s = n;
   }
-  *out = s.base;
+  *out = s;
   return SV_OK;
 }
 
@@ -93,19 +91,29 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   const int esz = dtype == SV_BF16 ? 2 : 4;
   p.TE = sv::kTileBytes / esz;
   p.NT = (p.V + p.TE - 1) / p.TE;
-  p.W = rows_total * p.NT;
   p.stages = g_stages.load();
-  const Layout L = layout_for(p.B, rows_total, p.W);
-  void* base = nullptr;
+  int dev0 = 0;
+  if (cudaGetDevice(&dev0) != cudaSuccess) return SV_ERR_CUDA;
+  const int64_t slots = (int64_t)sm_count(dev0) * g_ctas_per_sm.load();
+  // Chunks of up to 8 tiles, small enough that every CTA gets about eight of them.
+  int64_t ct = rows_total * p.NT / (slots * 8);
+  p.CT = ct < 1 ? 1 : (ct > 8 ? 8 : ct);
+  if (p.CT > p.NT) p.CT = p.NT;
+  p.NC = (p.NT + p.CT - 1) / p.CT;
+  p.W = rows_total * p.NC;
+  const size_t cnt_words = (size_t)rows_total + (size_t)p.B;
+  const size_t part_bytes = align256((size_t)p.W * 8);
+  const size_t data_bytes = part_bytes + (size_t)rows_total * 16;
+  Scratch sc;
   int dev = 0;
-  int rc = get_scratch(stream, L.total, &base, &dev);
+  int rc = get_scratch(stream, cnt_words, data_bytes, &sc, &dev);
   if (rc != SV_OK) return rc;
-  char* b = static_cast<char*>(base);
-  p.ctl = reinterpret_cast<uint32_t*>(b + L.ctl);
-  p.row_cnt = reinterpret_cast<uint32_t*>(b + L.row_cnt);
-  p.seq_cnt = reinterpret_cast<uint32_t*>(b + L.seq_cnt);
-  p.part = reinterpret_cast<float2*>(b + L.part);
-  p.rowstat = reinterpret_cast<float4*>(b + L.rowstat);
+  char* b = static_cast<char*>(sc.base);
+  p.ctl = reinterpret_cast<uint32_t*>(b);
+  p.row_cnt = reinterpret_cast<uint32_t*>(b + counter_offset());
+  p.seq_cnt = p.row_cnt + rows_total;
+  p.part = reinterpret_cast<float2*>(b + data_offset(sc));
+  p.rowstat = reinterpret_cast<float4*>(b + data_offset(sc) + part_bytes);
   int64_t grid = (int64_t)sm_count(dev) * g_ctas_per_sm.load();
   if (grid > p.W) grid = p.W;
   if (grid < 1) grid = 1;

@@ -73,6 +73,15 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ---- global atomics ------------------------------------------------------------
+// Add with release (orders this thread's earlier writes before it) and acquire
+// (orders its later reads after it) semantics at GPU scope.
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
 // ---- consumer-group named barrier (barrier 1, the 256 consumer threads) ------
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory"); }
 __device__ __forceinline__ int cbar_or(int pred) {

@@ -55,15 +55,19 @@ __device__ __forceinline__ void rs_store(const Params& p, int64_t idx, const Row
 struct alignas(16) Shared {
   uint64_t full[kMaxStages];
   uint64_t empty[kMaxStages];
-  int64_t meta[kMaxStages];
+  int64_t meta_w[kMaxStages];   // chunk id of the tile in the stage (-1: no more work)
+  int meta_k[kMaxStages];       // tile index within its row
+  int meta_last[kMaxStages];    // last tile of its chunk
   union {
     uint32_t u[kHistBins];
     float f[kHistBins];
   } hist;
   float cells[kMaxCells];
-  float red_m[kConsumerWarps];
-  float red_s[kConsumerWarps];
-  int64_t red_i[kConsumerWarps];
+  float red_m[2][kConsumerWarps];  // per-warp chunk partials, double-buffered by chunk parity
+  float red_s[2][kConsumerWarps];
+  int64_t red_i[2][kConsumerWarps];
+  int64_t pend[2];                 // row completed by the chunk of that parity, or -1
+  float scan[kConsumerWarps];
   float bf[8];
   int64_t bl[4];
   int bi[8];
@@ -105,8 +109,6 @@ __device__ __forceinline__ const char* row_ptr(const Params& p, int64_t b, int r
 }
 
 struct Tile {
-  int64_t b;
-  int r;
   const char* row;
   int64_t e0, e1;       // element range of the tile in its row
   const char* ip;       // interior (16-byte aligned) start
@@ -116,16 +118,32 @@ struct Tile {
   int nt;               // tail elements [e1 - nt, e1), read directly
 };
 
+// A chunk is up to CT consecutive tiles of one row, the unit of scheduling and
+// of publishing a partial. Chunk ids run sequence-major: (b, r, ci).
+struct ChunkId {
+  int64_t b;
+  int r;
+  int64_t k0;  // first tile
+  int n;       // tiles in the chunk
+};
+
+__device__ __forceinline__ ChunkId decode_chunk(const Params& p, int64_t w) {
+  ChunkId c;
+  const int64_t per = (int64_t)p.RS * p.NC;
+  c.b = w / per;
+  const int64_t rem = w - c.b * per;
+  c.r = (int)(rem / p.NC);
+  const int64_t ci = rem - (int64_t)c.r * p.NC;
+  c.k0 = ci * p.CT;
+  c.n = (int)min((int64_t)p.CT, p.NT - c.k0);
+  return c;
+}
+
 template <typename E, int MODE>
-__device__ __forceinline__ Tile decode(const Params& p, int64_t w) {
+__device__ __forceinline__ Tile tile_of(const Params& p, int64_t b, int r, int64_t k) {
   constexpr int S = ET<E>::kSize;
   Tile t;
-  const int64_t per = (int64_t)p.RS * p.NT;
-  t.b = w / per;
-  const int64_t rem = w - t.b * per;
-  t.r = (int)(rem / p.NT);
-  const int64_t k = rem - (int64_t)t.r * p.NT;
-  t.row = row_ptr<E, MODE>(p, t.b, t.r);
+  t.row = row_ptr<E, MODE>(p, b, r);
   t.e0 = k * p.TE;
   t.e1 = min(t.e0 + p.TE, p.V);
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(t.row + t.e0 * S);
@@ -149,12 +167,13 @@ __device__ __forceinline__ Tile decode(const Params& p, int64_t w) {
 }
 
 // ------------------------------------------------ online (max, sum) ---------
-// (m, s): m the running raw max, s = sum 2^(l*c - fl(m*c)).
-__device__ __forceinline__ void ms_rescale(float& m, float& s, float nm, float c) {
-  if (nm != m) {  // also taken when nm is NaN
-    s = (m == -INFINITY) ? 0.f : s * ex2(m * c - nm * c);
-    m = nm;
-  }
+// (m, s): m the running raw max, s = sum 2^(l*c - mref(m)) with
+// mref(m) = fl(m*c). The reference is rounded explicitly (never fused into a
+// neighbouring add), so that every rescale factor 2^(mref(m) - mref(m')) is
+// exactly the shift between the references the terms were summed against.
+__device__ __forceinline__ float mref(float m, float c) { return __fmul_rn(m, c); }
+__device__ __forceinline__ float rescale(float m_old, float m_new, float c) {
+  return (m_old == -INFINITY) ? 0.f : ex2(__fsub_rn(mref(m_old, c), mref(m_new, c)));
 }
 __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s2, float c) {
   const float nm = fmax_nan(m, m2);
@@ -163,28 +182,30 @@ __device__ __forceinline__ void ms_combine(float& m, float& s, float m2, float s
     s = 0.f;
     return;
   }
-  const float f1 = (m == -INFINITY) ? 0.f : ex2(m * c - nm * c);
-  const float f2 = (m2 == -INFINITY) ? 0.f : ex2(m2 * c - nm * c);
-  s = s * f1 + s2 * f2;
+  s = s * rescale(m, nm, c) + s2 * rescale(m2, nm, c);
   m = nm;
 }
 __device__ __forceinline__ void ms_scalar(float& m, float& s, float x, float c) {
-  ms_rescale(m, s, fmax_nan(m, x), c);
+  const float nm = fmax_nan(m, x);
+  if (nm != m) {  // also taken when nm is NaN
+    s *= rescale(m, nm, c);
+    m = nm;
+  }
   if (m == -INFINITY) return;
-  s += ex2(fmaf(x, c, -(m * c)));
+  s += ex2(fmaf(x, c, -mref(m, c)));
 }
 __device__ __forceinline__ void ms_vec(float& m, float& s0, float& s1, const uint4 q, float c, uint16_t) {
   const uint32_t mm = bf2_max_nan(bf2_max_nan(q.x, q.y), bf2_max_nan(q.z, q.w));
   const float vmax = fmax_nan(bf_lo(mm), bf_hi(mm));
   const float nm = fmax_nan(m, vmax);
   if (nm != m) {
-    const float f = (m == -INFINITY) ? 0.f : ex2(m * c - nm * c);
+    const float f = rescale(m, nm, c);
     s0 *= f;
     s1 *= f;
     m = nm;
   }
   if (m == -INFINITY) return;
-  const float nmc = -(m * c);
+  const float nmc = -mref(m, c);
   s0 += ex2(fmaf(bf_lo(q.x), c, nmc));
   s1 += ex2(fmaf(bf_hi(q.x), c, nmc));
   s0 += ex2(fmaf(bf_lo(q.y), c, nmc));
@@ -200,13 +221,13 @@ __device__ __forceinline__ void ms_vec(float& m, float& s0, float& s1, const uin
   const float vmax = fmax_nan(fmax_nan(x0, x1), fmax_nan(x2, x3));
   const float nm = fmax_nan(m, vmax);
   if (nm != m) {
-    const float f = (m == -INFINITY) ? 0.f : ex2(m * c - nm * c);
+    const float f = rescale(m, nm, c);
     s0 *= f;
     s1 *= f;
     m = nm;
   }
   if (m == -INFINITY) return;
-  const float nmc = -(m * c);
+  const float nmc = -mref(m, c);
   s0 += ex2(fmaf(x0, c, nmc));
   s1 += ex2(fmaf(x1, c, nmc));
   s0 += ex2(fmaf(x2, c, nmc));
@@ -451,12 +472,12 @@ __device__ int64_t cdf_draw(const WF& wf, int64_t V, float u, Shared& sh, int ti
 __device__ __forceinline__ float block_excl_scan(float v, float& total, Shared& sh, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   const float incl = warp_incl_scan(v, lane);
-  if (lane == 31) sh.red_s[warp] = incl;
+  if (lane == 31) sh.scan[warp] = incl;
   cbar();
   float off = 0.f, tot = 0.f;
 #pragma unroll
   for (int w = 0; w < kConsumerWarps; ++w) {
-    const float x = sh.red_s[w];
+    const float x = sh.scan[w];
     if (w < warp) off += x;
     tot += x;
   }
@@ -497,7 +518,7 @@ __device__ __forceinline__ void for_each_elem(const char* row, int64_t V, int ti
 template <typename E>
 __device__ void topp_cut(const Params& p, Shared& sh, const char* row, float M, float s, int tid, uint32_t& tau,
                          float& cum) {
-  const float c = p.c, nMc = -(M * c);
+  const float c = p.c, nMc = -mref(M, p.c);
   const float target = p.top_p * s;
   uint32_t hi = ET<E>::key(M);
   int shf = (ET<E>::kKeyBits == 16) ? 0 : 16;
@@ -617,8 +638,8 @@ __device__ void seq_sample(const Params& p, Shared& sh, int64_t b, int tid) {
     } else if (!in_q || lq == -INFINITY) {
       alpha = 1.f;
     } else {
-      const float ap = fmaf(lp, c, -(rp.M * c));
-      const float aq = fmaf(lq, c, -(rq.M * c));
+      const float ap = fmaf(lp, c, -mref(rp.M, c));
+      const float aq = fmaf(lq, c, -mref(rq.M, c));
       alpha = fminf(1.f, ex2(ap - aq) * (rq.cum / rp.cum));
     }
     if (!(u < alpha)) atomicMin(&sh.bi[1], i);
@@ -646,12 +667,12 @@ __device__ void seq_sample(const Params& p, Shared& sh, int64_t b, int tid) {
   int64_t t = -1;
   if (j < K) {
     const RowStat rq = rs_load(p, b * p.RS + K + 1 + j);
-    Weights<E, true> wf{row_ptr<E, kSample>(p, b, j), row_ptr<E, kSample>(p, b, K + 1 + j), p.V, c, -(rp.M * c),
-                        -(rq.M * c), 1.f / rp.cum, 1.f / rq.cum, rp.tau, rq.tau, p.topp, aligned};
+    Weights<E, true> wf{row_ptr<E, kSample>(p, b, j), row_ptr<E, kSample>(p, b, K + 1 + j), p.V, c, -mref(rp.M, c),
+                        -mref(rq.M, c), 1.f / rp.cum, 1.f / rq.cum, rp.tau, rq.tau, p.topp, aligned};
     t = cdf_draw(wf, p.V, uK, sh, tid);
   }
   if (t < 0) {  // bonus row, or a residual that is all zero: draw from p'_j
-    Weights<E, false> wf{row_ptr<E, kSample>(p, b, j), nullptr, p.V, c, -(rp.M * c), 0.f, 1.f, 0.f, rp.tau, 0u,
+    Weights<E, false> wf{row_ptr<E, kSample>(p, b, j), nullptr, p.V, c, -mref(rp.M, c), 0.f, 1.f, 0.f, rp.tau, 0u,
                          p.topp, aligned};
     t = cdf_draw(wf, p.V, uK, sh, tid);
   }
@@ -744,10 +765,10 @@ __device__ void finish_row(const Params& p, Shared& sh, int64_t b, int r, int ti
   const int64_t row = b * p.RS + r;
   __threadfence();
   if (warp == 0) {
-    const float2* part = p.part + row * p.NT;
+    const float2* part = p.part + row * p.NC;
     if (MODE == kSample) {
       float m = -INFINITY, s = 0.f;
-      for (int64_t k = lane; k < p.NT; k += 32) {
+      for (int64_t k = lane; k < p.NC; k += 32) {
         const float2 v = __ldcg(part + k);
         ms_combine(m, s, v.x, v.y, p.c);
       }
@@ -763,7 +784,7 @@ __device__ void finish_row(const Params& p, Shared& sh, int64_t b, int r, int ti
       float v = -INFINITY;
       int64_t i = -1;
       bool nan = false;
-      for (int64_t k = lane; k < p.NT; k += 32) {
+      for (int64_t k = lane; k < p.NC; k += 32) {
         const float2 pv = __ldcg(part + k);
         const int64_t pi = (int64_t)__float_as_int(pv.y);
         if (pv.x != pv.x) nan = true;
@@ -808,7 +829,7 @@ __device__ void finish_row(const Params& p, Shared& sh, int64_t b, int r, int ti
       rs_store(p, row, rs);
       if (p.out_row_stats) {
         float4 o;
-        const float Mc = M * p.c;
+        const float Mc = mref(M, p.c);
         o.x = valid ? __fdiv_rn(M, p.T) : __int_as_float(0x7fc00000);
         o.y = valid ? (Mc + lg2(s)) * 0.69314718055994531f : __int_as_float(0x7fc00000);
         o.z = valid ? cum / s : __int_as_float(0x7fc00000);
@@ -819,8 +840,7 @@ __device__ void finish_row(const Params& p, Shared& sh, int64_t b, int r, int ti
   }
   if (tid == 0) {
     p.row_cnt[row] = 0u;
-    __threadfence();
-    const uint32_t old = atomicAdd(p.seq_cnt + b, 1u);
+    const uint32_t old = atom_add_acq_rel(p.seq_cnt + b, 1u);
     sh.flag = (old == (uint32_t)p.RS - 1u);
     if (sh.flag) p.seq_cnt[b] = 0u;
   }
@@ -836,36 +856,48 @@ __device__ void finish_row(const Params& p, Shared& sh, int64_t b, int r, int ti
 
 // --------------------------------------------------------------- kernel -------
 
+// The producer: one elected thread takes chunks from the call's work counter
+// and streams their tiles into the ring, one stage per tile, each stage a
+// single bulk copy completing on the stage's "full" barrier.
 template <typename E, int MODE>
 __device__ void producer_loop(const Params& p, char* ring, Shared& sh) {
   unsigned long long* next = reinterpret_cast<unsigned long long*>(p.ctl);
   int last_parity[kMaxStages];
   for (int i = 0; i < kMaxStages; ++i) last_parity[i] = -1;
   bool aborted = false;
-  for (int64_t it = 0;; ++it) {
-    const int slot = (int)(it % p.stages);
-    const uint32_t ph = (uint32_t)((it / p.stages) & 1);
-    if (it >= p.stages && !mbar_wait(&sh.empty[slot], ph ^ 1u)) {
-      atomicOr(p.ctl + 3, kStatusTimeout);
-      aborted = true;
-      break;
-    }
+  int64_t it = 0;
+  while (!aborted) {
     const int64_t w = (int64_t)atomicAdd(next, 1ull);
-    sh.meta[slot] = w;
-    if (w >= p.W) {
-      mbar_arrive(&sh.full[slot]);
-      break;
+    const ChunkId ch = decode_chunk(p, w < p.W ? w : 0);
+    const int n = w < p.W ? ch.n : 1;  // the end of work takes one stage too
+    for (int j = 0; j < n; ++j, ++it) {
+      const int slot = (int)(it % p.stages);
+      const uint32_t ph = (uint32_t)((it / p.stages) & 1);
+      if (it >= p.stages && !mbar_wait(&sh.empty[slot], ph ^ 1u)) {
+        aborted = true;
+        break;
+      }
+      if (w >= p.W) {
+        sh.meta_w[slot] = -1;
+        mbar_arrive(&sh.full[slot]);
+        break;
+      }
+      const Tile t = tile_of<E, MODE>(p, ch.b, ch.r, ch.k0 + j);
+      sh.meta_w[slot] = w;
+      sh.meta_k[slot] = (int)(ch.k0 + j);
+      sh.meta_last[slot] = (j == n - 1);
+      if (t.ibytes) {
+        mbar_arrive_expect_tx(&sh.full[slot], t.ibytes);
+        bulk_g2s(ring + (size_t)slot * kTileBytes, t.ip, t.ibytes, &sh.full[slot]);
+        last_parity[slot] = (int)ph;
+      } else {
+        mbar_arrive(&sh.full[slot]);
+      }
     }
-    const Tile t = decode<E, MODE>(p, w);
-    if (t.ibytes) {
-      mbar_arrive_expect_tx(&sh.full[slot], t.ibytes);
-      bulk_g2s(ring + (size_t)slot * kTileBytes, t.ip, t.ibytes, &sh.full[slot]);
-      last_parity[slot] = (int)ph;
-    } else {
-      mbar_arrive(&sh.full[slot]);
-    }
+    if (w >= p.W) break;
   }
-  if (aborted) {  // let copies still in flight land before the CTA exits
+  if (aborted) {  // a wait ran out: let copies still in flight land before the CTA exits
+    atomicOr(p.ctl + 3, kStatusTimeout);
     for (int i = 0; i < p.stages; ++i)
       if (last_parity[i] >= 0) (void)mbar_wait(&sh.full[i], (uint32_t)last_parity[i]);
   }
@@ -879,98 +911,135 @@ __device__ void producer_loop(const Params& p, char* ring, Shared& sh) {
   }
 }
 
+// Publishing a chunk: combine the eight warps' partials, store the chunk's
+// partial and count it against its row with a release-acquire atomic. Run by
+// one lane of a rotating warp; the other warps go on with the next chunk, and
+// learn whether the row completed at the next chunk boundary.
+template <int MODE>
+__device__ __forceinline__ void publish(const Params& p, Shared& sh, int par, int64_t w, int64_t row) {
+  float2 res;
+  if (MODE == kSample) {
+    float M = sh.red_m[par][0], S = sh.red_s[par][0];
+    for (int k = 1; k < kConsumerWarps; ++k) ms_combine(M, S, sh.red_m[par][k], sh.red_s[par][k], p.c);
+    res = make_float2(M, S);
+  } else {
+    float V_ = sh.red_m[par][0];
+    int64_t I = sh.red_i[par][0];
+    bool N_ = V_ != V_;
+    for (int k = 1; k < kConsumerWarps; ++k) {
+      const float v2 = sh.red_m[par][k];
+      if (v2 != v2) N_ = true;
+      else if (am_better(v2, sh.red_i[par][k], V_, I)) {
+        V_ = v2;
+        I = sh.red_i[par][k];
+      }
+    }
+    if (N_) V_ = __int_as_float(0x7fc00000);
+    res = make_float2(V_, __int_as_float((int)I));
+  }
+  p.part[w] = res;
+  const uint32_t old = atom_add_acq_rel(p.row_cnt + row, 1u);
+  sh.pend[par] = (old == (uint32_t)(p.NC - 1)) ? row : -1;
+}
+
+// The consumers: per-thread accumulation over every tile of a chunk, then one
+// barrier per chunk (which also carries the abort vote of bounded waits).
 template <typename E, int MODE>
 __device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int tid) {
   constexpr int PV = ET<E>::kPerVec;
   const int warp = tid >> 5, lane = tid & 31;
+  float m = -INFINITY, s0 = 0.f, s1 = 0.f;   // sampling: online (max, sum)
+  float av = -INFINITY;                      // argmax: value, index, NaN seen
+  int64_t ai = -1;
+  bool an = false;
+  int timed_out = 0;
+  int64_t chunks = 0;
   for (int64_t it = 0;; ++it) {
     const int slot = (int)(it % p.stages);
     const uint32_t ph = (uint32_t)((it / p.stages) & 1);
-    const bool ok = mbar_wait(&sh.full[slot], ph);
-    if (cbar_or(!ok)) {
-      if (tid == 0) atomicOr(p.ctl + 3, kStatusTimeout);
-      return;
+    if (!mbar_wait(&sh.full[slot], ph)) {
+      timed_out = 1;
+      break;
     }
-    const int64_t w = sh.meta[slot];
-    if (w >= p.W) return;
-    const Tile t = decode<E, MODE>(p, w);
+    const int64_t w = sh.meta_w[slot];
+    if (w < 0) break;  // no more work
+    const ChunkId ch = decode_chunk(p, w);
+    const Tile t = tile_of<E, MODE>(p, ch.b, ch.r, sh.meta_k[slot]);
+    const bool last = sh.meta_last[slot] != 0;
     const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)slot * kTileBytes);
     const int nvec = (int)(t.ibytes >> 4);
-    float2 res;
     if (MODE == kSample) {
-      float m = -INFINITY, s0 = 0.f, s1 = 0.f;
       for (int v = tid; v < nvec; v += kConsumerThreads) ms_vec(m, s0, s1, sv[v], p.c, E());
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.empty[slot]);
-      if (tid < t.nh) ms_scalar(m, s0, ET<E>::load(t.row, t.e0 + tid), p.c);
-      if (tid >= 32 && tid < 32 + t.nt) ms_scalar(m, s0, ET<E>::load(t.row, t.e1 - t.nt + (tid - 32)), p.c);
+      if (t.nh | t.nt) {
+        // head and tail elements (rows not 16-byte aligned) join one
+        // accumulator, so that a new maximum among them rescales everything
+        s0 += s1;
+        s1 = 0.f;
+        if (tid < t.nh) ms_scalar(m, s0, ET<E>::load(t.row, t.e0 + tid), p.c);
+        if (tid >= 32 && tid < 32 + t.nt) ms_scalar(m, s0, ET<E>::load(t.row, t.e1 - t.nt + (tid - 32)), p.c);
+      }
+    } else {
+      for (int q = tid; q < nvec; q += kConsumerThreads) am_vec(av, ai, an, sv[q], t.ie0 + (int64_t)q * PV, E());
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.empty[slot]);
+      if (tid < t.nh) am_scalar(av, ai, an, ET<E>::load(t.row, t.e0 + tid), t.e0 + tid);
+      if (tid >= 32 && tid < 32 + t.nt) {
+        const int64_t e = t.e1 - t.nt + (tid - 32);
+        am_scalar(av, ai, an, ET<E>::load(t.row, e), e);
+      }
+    }
+    if (!last) continue;
+
+    // ---- end of a chunk: warp partials, one barrier, publish, pending row
+    const int par = (int)(chunks & 1);
+    if (MODE == kSample) {
       float s = s0 + s1;
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
         ms_combine(m, s, m2, s2, p.c);
       }
       if (lane == 0) {
-        sh.red_m[warp] = m;
-        sh.red_s[warp] = s;
+        sh.red_m[par][warp] = m;
+        sh.red_s[par][warp] = s;
       }
-      cbar();
-      if (tid == 0) {
-        float M = sh.red_m[0], S = sh.red_s[0];
-        for (int k = 1; k < kConsumerWarps; ++k) ms_combine(M, S, sh.red_m[k], sh.red_s[k], p.c);
-        res = make_float2(M, S);
-      }
+      m = -INFINITY;
+      s0 = s1 = 0.f;
     } else {
-      float v = -INFINITY;
-      int64_t i = -1;
-      bool nan = false;
-      for (int q = tid; q < nvec; q += kConsumerThreads) am_vec(v, i, nan, sv[q], t.ie0 + (int64_t)q * PV, E());
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.empty[slot]);
-      if (tid < t.nh) am_scalar(v, i, nan, ET<E>::load(t.row, t.e0 + tid), t.e0 + tid);
-      if (tid >= 32 && tid < 32 + t.nt) {
-        const int64_t e = t.e1 - t.nt + (tid - 32);
-        am_scalar(v, i, nan, ET<E>::load(t.row, e), e);
-      }
       for (int o = 16; o > 0; o >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-        const long long i2 = __shfl_xor_sync(0xffffffffu, (long long)i, o);
-        if (am_better(v2, i2, v, i)) {
-          v = v2;
-          i = i2;
+        const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
+        const long long i2 = __shfl_xor_sync(0xffffffffu, (long long)ai, o);
+        if (am_better(v2, i2, av, ai)) {
+          av = v2;
+          ai = i2;
         }
       }
-      nan = __any_sync(0xffffffffu, nan);
+      an = __any_sync(0xffffffffu, an);
       if (lane == 0) {
-        sh.red_m[warp] = nan ? __int_as_float(0x7fc00000) : v;
-        sh.red_i[warp] = i;
+        sh.red_m[par][warp] = an ? __int_as_float(0x7fc00000) : av;
+        sh.red_i[par][warp] = ai;
       }
-      cbar();
-      if (tid == 0) {
-        float V_ = sh.red_m[0];
-        int64_t I = sh.red_i[0];
-        bool N_ = V_ != V_;
-        for (int k = 1; k < kConsumerWarps; ++k) {
-          const float v2 = sh.red_m[k];
-          if (v2 != v2) N_ = true;
-          else if (am_better(v2, sh.red_i[k], V_, I)) {
-            V_ = v2;
-            I = sh.red_i[k];
-          }
-        }
-        if (N_ && !(V_ != V_)) V_ = __int_as_float(0x7fc00000);
-        res = make_float2(V_, __int_as_float((int)I));
-      }
+      av = -INFINITY;
+      ai = -1;
+      an = false;
     }
-    if (tid == 0) {
-      const int64_t row = t.b * p.RS + t.r;
-      p.part[w] = res;
-      __threadfence();
-      const uint32_t old = atomicAdd(p.row_cnt + row, 1u);
-      sh.flag = (old == (uint32_t)(p.NT - 1));
-    }
-    cbar();
-    if (sh.flag) finish_row<E, MODE>(p, sh, t.b, t.r, tid);
+    if (cbar_or(0)) return;  // another warp's wait ran out
+    const int64_t prow = chunks > 0 ? sh.pend[par ^ 1] : -1;
+    if (warp == (int)(chunks % kConsumerWarps) && lane == 0)
+      publish<MODE>(p, sh, par, w, ch.b * p.RS + ch.r);
+    __syncwarp();
+    ++chunks;
+    if (prow >= 0) finish_row<E, MODE>(p, sh, prow / p.RS, (int)(prow % p.RS), tid);
   }
+  // End of work (or a wait that ran out): one last vote, then the row the
+  // final chunk may have completed.
+  if (cbar_or(timed_out)) {
+    if (tid == 0) atomicOr(p.ctl + 3, kStatusTimeout);
+    return;
+  }
+  const int64_t prow = chunks > 0 ? sh.pend[(chunks - 1) & 1] : -1;
+  if (prow >= 0) finish_row<E, MODE>(p, sh, prow / p.RS, (int)(prow % p.RS), tid);
 }
 
 template <typename E, int MODE>
@@ -984,6 +1053,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const Params p) {
       mbar_init(&sh.full[i], 1u);
       mbar_init(&sh.empty[i], (uint32_t)kConsumerWarps);
     }
+    sh.pend[0] = sh.pend[1] = -1;
     fence_mbar_init();
   }
   __syncthreads();

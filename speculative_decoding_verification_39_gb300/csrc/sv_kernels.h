@@ -24,15 +24,17 @@ struct Params {
   int RS;                  // rows per sequence
   int64_t NT;              // tiles per row
   int64_t TE;              // elements per tile
-  int64_t W;               // tiles in the call = B * RS * NT
+  int64_t CT;              // tiles per chunk (the unit of scheduling)
+  int64_t NC;              // chunks per row = ceil(NT / CT)
+  int64_t W;               // chunks in the call = B * RS * NC
   float c;                 // log2(e) / T
   float T;
   float top_p;
   int topp;                // top_p < 1
   uint32_t* ctl;           // [0..1] work counter (u64), [2] finished producers, [3] status bits
-  uint32_t* row_cnt;       // [B*RS] tiles published per row
+  uint32_t* row_cnt;       // [B*RS] chunks published per row
   uint32_t* seq_cnt;       // [B] rows finished per sequence
-  float2* part;            // [W] per-tile partials
+  float2* part;            // [W] per-chunk partials
   float4* rowstat;         // [B*RS] per-row results
   int stages;
 };

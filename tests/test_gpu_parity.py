@@ -50,9 +50,8 @@ def test_sample_parity(name):
     cfg = SAMPLE_CASES[name]
     d = sg.sample_inputs(cfg)
     gpu = run_sample(d, cfg.temperature, cfg.top_p, row_stats=True)
-    summary = compare_sample(d, cfg.temperature, cfg.top_p, gpu=gpu)
+    compare_sample(d, cfg.temperature, cfg.top_p, gpu=gpu, max_mismatch=1)
     compare_row_stats(d, gpu[2], cfg.temperature, cfg.top_p)
-    assert summary["near_ties"] <= 1
 
 
 GREEDY_CASES = {
@@ -211,7 +210,7 @@ def test_full_size_sample(name):
     cfg = C[name]
     d = sg.sample_inputs(cfg)
     gpu = run_sample(d, cfg.temperature, cfg.top_p, row_stats=True)
-    summary = compare_sample(d, cfg.temperature, cfg.top_p, gpu=gpu, near_tie_frac=1e-4)
+    summary = compare_sample(d, cfg.temperature, cfg.top_p, gpu=gpu, max_mismatch=1)
     rows = np.random.default_rng(0).choice(cfg.rows, size=min(cfg.rows, 48), replace=False)
     compare_row_stats(d, gpu[2], cfg.temperature, cfg.top_p, rows=rows)
     print(name, summary)
@@ -220,3 +219,33 @@ def test_full_size_sample(name):
 def test_full_size_greedy():
     s = compare_greedy(sg.greedy_inputs(C["cfg4_greedy_v32000_bf16"]))
     print("cfg4", s)
+
+
+def test_alternating_shapes_on_one_stream():
+    # calls of different shapes and modes reuse one scratch area: every call
+    # must start from clean counters whatever ran before it
+    cases = [sg.sample_inputs(C["cfg2_v32000_bf16"].with_(B=9, V=3001)),
+             sg.greedy_inputs(C["cfg4_greedy_v32000_bf16"].with_(B=5, V=777, dtype=sg.F32)),
+             sg.sample_inputs(C["cfg1_v1000_f32"].with_(B=70, K=2, V=129)),
+             sg.greedy_inputs(C["cfg4_greedy_v32000_bf16"].with_(B=2, G=3, N=3, V=20000))]
+    for _ in range(2):
+        for d in cases:
+            if "logits" in d:
+                compare_greedy(d)
+            else:
+                temp = 1.0
+                compare_sample(d, temp)
+
+
+def test_near_tie_mismatch_rate():
+    """Over many decisions of the headline workload's shape, GPU/oracle
+    mismatches (each one a near-tie) stay at or below 1e-4 of decisions."""
+    base = C["cfg2_v32000_bf16"]
+    total = {"mismatch": 0, "near_ties": 0, "decisions": 0}
+    for seed in range(1, 61):
+        d = sg.sample_inputs(base.with_(seed=seed))
+        s = compare_sample(d, base.temperature, base.top_p, max_mismatch=None)
+        for k in total:
+            total[k] += s[k]
+    print("near-tie mismatch rate", total)
+    assert total["mismatch"] <= max(1, 1e-4 * total["decisions"]), total
