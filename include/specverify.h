@@ -138,7 +138,7 @@ const char* sv_status_string(int status);
 int sv_release(void);
 
 /* Launch-shape knobs, for tuning and tests: stages of the shared-memory ring
- * (1..8) and CTAs per SM (1..4); 0 restores the default. Applies to calls
+ * (1..6) and CTAs per SM (1..4); 0 restores the default. Applies to calls
  * made after it on any device. */
 int sv_set_launch_shape(int32_t stages, int32_t ctas_per_sm);
 

@@ -14,7 +14,7 @@
 
 namespace {
 
-constexpr int kDefaultStages = 4;
+constexpr int kDefaultStages = 3;
 constexpr int kDefaultCtasPerSm = 2;
 constexpr int64_t kMaxV = (int64_t)1 << 31;
 
@@ -95,13 +95,15 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   int dev0 = 0;
   if (cudaGetDevice(&dev0) != cudaSuccess) return SV_ERR_CUDA;
   const int64_t slots = (int64_t)sm_count(dev0) * g_ctas_per_sm.load();
-  // Chunks of up to 8 tiles, small enough that every CTA gets about eight of them.
-  int64_t ct = rows_total * p.NT / (slots * 8);
-  p.CT = ct < 1 ? 1 : (ct > 8 ? 8 : ct);
-  if (p.CT > p.NT) p.CT = p.NT;
-  p.NC = (p.NT + p.CT - 1) / p.CT;
+  // Chunks of up to 8 tiles, small enough that every CTA gets about four of
+  // them, and of near-equal size within a row.
+  int64_t ct = rows_total * p.NT / (slots * 4);
+  ct = ct < 1 ? 1 : (ct > 8 ? 8 : ct);
+  if (ct > p.NT) ct = p.NT;
+  p.NC = (p.NT + ct - 1) / ct;
+  p.CT = (p.NT + p.NC - 1) / p.NC;
   p.W = rows_total * p.NC;
-  const size_t cnt_words = (size_t)rows_total + (size_t)p.B;
+  const size_t cnt_words = (size_t)rows_total + 2 * (size_t)p.B;
   const size_t part_bytes = align256((size_t)p.W * 8);
   const size_t data_bytes = part_bytes + (size_t)rows_total * 16;
   Scratch sc;
@@ -112,6 +114,7 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   p.ctl = reinterpret_cast<uint32_t*>(b);
   p.row_cnt = reinterpret_cast<uint32_t*>(b + counter_offset());
   p.seq_cnt = p.row_cnt + rows_total;
+  p.tail_q = p.seq_cnt + p.B;
   p.part = reinterpret_cast<float2*>(b + data_offset(sc));
   p.rowstat = reinterpret_cast<float4*>(b + data_offset(sc) + part_bytes);
   int64_t grid = (int64_t)sm_count(dev) * g_ctas_per_sm.load();

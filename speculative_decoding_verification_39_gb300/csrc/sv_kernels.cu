@@ -52,21 +52,48 @@ __device__ __forceinline__ void rs_store(const Params& p, int64_t idx, const Row
   p.rowstat[idx] = make_float4(r.M, r.s, r.cum, __uint_as_float(r.tau));
 }
 
+struct TileDesc {
+  const char* row;
+  int64_t e0, e1;    // element range of the tile in its row
+  int64_t ie0;       // first interior element
+  int64_t w;         // chunk id (-1: no more work)
+  int64_t rowid;     // b * RS + r
+  uint32_t ibytes;   // interior bytes (multiple of 16), 0 if none
+  int nh;            // head elements [e0, e0 + nh)
+  int nt;            // tail elements [e1 - nt, e1)
+  int last;          // last tile of its chunk
+};
+
+// Warp roles: warps 0-7 consume tiles, warp 8 (one lane) produces them,
+// warp 9 (one lane) publishes chunk partials and finishes rows.
+constexpr int kProducerWarp = kConsumerWarps;
+constexpr int kPublisherWarp = kConsumerWarps + 1;
+constexpr int kAllThreads = (kConsumerWarps + 2) * 32;
+constexpr int kPartSlots = 4;   // chunk partials in flight from consumers to the publisher
+constexpr int kTaskSlots = 64;  // collective tasks in flight from the publisher to the consumers
+
 struct alignas(16) Shared {
-  uint64_t full[kMaxStages];
-  uint64_t empty[kMaxStages];
-  int64_t meta_w[kMaxStages];   // chunk id of the tile in the stage (-1: no more work)
-  int meta_k[kMaxStages];       // tile index within its row
-  int meta_last[kMaxStages];    // last tile of its chunk
+  uint64_t full[kMaxStages];     // tile landed in the stage (producer -> consumers)
+  uint64_t empty[kMaxStages];    // stage read by all consumer warps (consumers -> producer)
+  uint64_t pfull[kPartSlots];    // chunk partial written by all consumer warps
+  uint64_t pempty[kPartSlots];   // chunk partial taken by the publisher
+  uint64_t pdone;                // publisher finished
+  TileDesc td[kMaxStages];       // what the stage holds, decoded once by the producer
+  float red_m[kPartSlots][kConsumerWarps];
+  float red_s[kPartSlots][kConsumerWarps];
+  int64_t red_i[kPartSlots][kConsumerWarps];
+  int64_t pw[kPartSlots];        // chunk id of the partial (-1: consumers are done)
+  int64_t prow[kPartSlots];      // row of that chunk (b * RS + r)
+  int64_t tq[kTaskSlots];        // task: row id (top-p cut) or -(b+1) (sequence tail)
+  float tq_m[kTaskSlots], tq_s[kTaskSlots];
+  int tq_tail;                   // written by the publisher only
+  int tq_head;                   // written by consumer thread 0 only
+  int snap[2];                   // tq_tail as seen at a chunk boundary, by chunk parity
   union {
     uint32_t u[kHistBins];
     float f[kHistBins];
   } hist;
   float cells[kMaxCells];
-  float red_m[2][kConsumerWarps];  // per-warp chunk partials, double-buffered by chunk parity
-  float red_s[2][kConsumerWarps];
-  int64_t red_i[2][kConsumerWarps];
-  int64_t pend[2];                 // row completed by the chunk of that parity, or -1
   float scan[kConsumerWarps];
   float bf[8];
   int64_t bl[4];
@@ -108,16 +135,10 @@ __device__ __forceinline__ const char* row_ptr(const Params& p, int64_t b, int r
   return p.d + ((b * p.K + (r - p.K - 1)) * p.V) * S;
 }
 
-struct Tile {
-  const char* row;
-  int64_t e0, e1;       // element range of the tile in its row
-  const char* ip;       // interior (16-byte aligned) start
-  uint32_t ibytes;      // interior bytes (multiple of 16), 0 if none
-  int64_t ie0;          // first interior element
-  int nh;               // head elements [e0, e0 + nh), read directly
-  int nt;               // tail elements [e1 - nt, e1), read directly
-};
-
+// One ring stage's tile, decoded once by the producer. The interior is the
+// 16-byte aligned part of the tile, moved by the bulk copy; the unaligned
+// head and tail elements (rows whose byte length is not a multiple of 16)
+// are read directly by the consumers.
 // A chunk is up to CT consecutive tiles of one row, the unit of scheduling and
 // of publishing a partial. Chunk ids run sequence-major: (b, r, ci).
 struct ChunkId {
@@ -140,10 +161,10 @@ __device__ __forceinline__ ChunkId decode_chunk(const Params& p, int64_t w) {
 }
 
 template <typename E, int MODE>
-__device__ __forceinline__ Tile tile_of(const Params& p, int64_t b, int r, int64_t k) {
+__device__ __forceinline__ void decode_tile(const Params& p, const ChunkId& ch, int64_t k, TileDesc& t) {
   constexpr int S = ET<E>::kSize;
-  Tile t;
-  t.row = row_ptr<E, MODE>(p, b, r);
+  t.row = row_ptr<E, MODE>(p, ch.b, ch.r);
+  t.rowid = ch.b * p.RS + ch.r;
   t.e0 = k * p.TE;
   t.e1 = min(t.e0 + p.TE, p.V);
   const uintptr_t a0 = reinterpret_cast<uintptr_t>(t.row + t.e0 * S);
@@ -151,19 +172,16 @@ __device__ __forceinline__ Tile tile_of(const Params& p, int64_t b, int r, int64
   const uintptr_t A = (a0 + 15) & ~uintptr_t(15);
   const uintptr_t Z = a1 & ~uintptr_t(15);
   if (A < Z) {
-    t.ip = reinterpret_cast<const char*>(A);
     t.ibytes = (uint32_t)(Z - A);
     t.nh = (int)((A - a0) / S);
     t.nt = (int)((a1 - Z) / S);
     t.ie0 = t.e0 + t.nh;
   } else {
-    t.ip = nullptr;
     t.ibytes = 0;
     t.nh = (int)(t.e1 - t.e0);
     t.nt = 0;
     t.ie0 = t.e1;
   }
-  return t;
 }
 
 // ------------------------------------------------ online (max, sum) ---------
@@ -359,15 +377,30 @@ __device__ int64_t cdf_draw(const WF& wf, int64_t V, float u, Shared& sh, int ti
   const int64_t m = (V + 256LL * kMaxCells - 1) / (256LL * kMaxCells) > 1 ? (V + 256LL * kMaxCells - 1) / (256LL * kMaxCells) : 1;
   const int64_t CE = 256 * m;
   const int ncells = (int)((V + CE - 1) / CE);
-  for (int cc = warp; cc < ncells; cc += kConsumerWarps) {
-    float sum = 0.f;
-    for (int64_t q = 0; q < m; ++q) {
-      float w[8];
-      wf.w8(cc * CE + (lane * m + q) * 8, w);
-      sum += ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+  // Pass A: cell sums. Each warp takes four cells at a time, so that their
+  // loads are in flight together.
+  constexpr int U = 4;
+  for (int c0 = warp; c0 < ncells; c0 += kConsumerWarps * U) {
+    float sum[U];
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const int cc = c0 + k * kConsumerWarps;
+      float acc = 0.f;
+      if (cc < ncells) {
+        for (int64_t q = 0; q < m; ++q) {
+          float w[8];
+          wf.w8(cc * CE + (lane * m + q) * 8, w);
+          acc += ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+        }
+      }
+      sum[k] = acc;
     }
-    sum = warp_sum(sum);
-    if (lane == 0) sh.cells[cc] = sum;
+#pragma unroll
+    for (int k = 0; k < U; ++k) {
+      const float t = warp_sum(sum[k]);
+      const int cc = c0 + k * kConsumerWarps;
+      if (lane == 0 && cc < ncells) sh.cells[cc] = t;
+    }
   }
   cbar();
   if (warp == 0) {
@@ -491,18 +524,27 @@ __device__ __forceinline__ float block_excl_scan(float v, float& total, Shared& 
 template <typename E, class F>
 __device__ __forceinline__ void for_each_elem(const char* row, int64_t V, int tid, F&& f) {
   constexpr int PV = ET<E>::kPerVec;
+  auto apply = [&](const uint4 q) {
+    if (PV == 8) {
+      f(bf_lo(q.x)); f(bf_hi(q.x)); f(bf_lo(q.y)); f(bf_hi(q.y));
+      f(bf_lo(q.z)); f(bf_hi(q.z)); f(bf_lo(q.w)); f(bf_hi(q.w));
+    } else {
+      f(__uint_as_float(q.x)); f(__uint_as_float(q.y)); f(__uint_as_float(q.z)); f(__uint_as_float(q.w));
+    }
+  };
   if ((reinterpret_cast<uintptr_t>(row) & 15) == 0) {
     const int64_t nv = V / PV;
     const uint4* rv = reinterpret_cast<const uint4*>(row);
-    for (int64_t v = tid; v < nv; v += kConsumerThreads) {
-      const uint4 q = __ldg(rv + v);
-      if (PV == 8) {
-        f(bf_lo(q.x)); f(bf_hi(q.x)); f(bf_lo(q.y)); f(bf_hi(q.y));
-        f(bf_lo(q.z)); f(bf_hi(q.z)); f(bf_lo(q.w)); f(bf_hi(q.w));
-      } else {
-        f(__uint_as_float(q.x)); f(__uint_as_float(q.y)); f(__uint_as_float(q.z)); f(__uint_as_float(q.w));
-      }
+    int64_t v = tid;
+    // four 16-byte loads in flight per thread before any is used
+    for (; v + 3 * kConsumerThreads < nv; v += 4 * kConsumerThreads) {
+      uint4 q[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) q[k] = __ldg(rv + v + k * kConsumerThreads);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) apply(q[k]);
     }
+    for (; v < nv; v += kConsumerThreads) apply(__ldg(rv + v));
     for (int64_t e = nv * PV + tid; e < V; e += kConsumerThreads) f(ET<E>::load(row, e));
   } else {
     for (int64_t e = tid; e < V; e += kConsumerThreads) f(ET<E>::load(row, e));
@@ -760,141 +802,249 @@ __device__ void seq_greedy(const Params& p, Shared& sh, int64_t b, int tid) {
 // ------------------------------------------------------------- row tails -----
 
 template <typename E, int MODE>
-__device__ void finish_row(const Params& p, Shared& sh, int64_t b, int r, int tid) {
-  const int warp = tid >> 5, lane = tid & 31;
-  const int64_t row = b * p.RS + r;
+__device__ __forceinline__ void seq_tail(const Params& p, Shared& sh, int64_t b, int tid) {
   __threadfence();
-  if (warp == 0) {
-    const float2* part = p.part + row * p.NC;
-    if (MODE == kSample) {
-      float m = -INFINITY, s = 0.f;
-      for (int64_t k = lane; k < p.NC; k += 32) {
-        const float2 v = __ldcg(part + k);
-        ms_combine(m, s, v.x, v.y, p.c);
+  if (MODE == kSample) seq_sample<E>(p, sh, b, tid);
+  else if (MODE == kArgmaxLimit) seq_argmax_limit<E>(p, sh, b, tid);
+  else seq_greedy(p, sh, b, tid);
+  cbar();
+}
+
+// A finished sampling row: its record for the sequence tail and, if asked,
+// the caller-visible {m, lse, P_S, tau}.
+template <typename E>
+__device__ void store_sample_row(const Params& p, int64_t row, float M, float s, float cum, uint32_t tau) {
+  const bool valid = (M > -INFINITY) && (M < INFINITY);  // NaN fails both
+  RowStat rs;
+  rs.M = valid ? M : __int_as_float(0x7fc00000);
+  rs.s = s;
+  rs.cum = cum;
+  rs.tau = tau;
+  rs_store(p, row, rs);
+  if (p.out_row_stats) {
+    float4 o;
+    o.x = valid ? __fdiv_rn(M, p.T) : __int_as_float(0x7fc00000);
+    o.y = valid ? (mref(M, p.c) + lg2(s)) * 0.69314718055994531f : __int_as_float(0x7fc00000);
+    o.z = valid ? cum / s : __int_as_float(0x7fc00000);
+    o.w = (valid && p.topp) ? ET<E>::val(tau) : -INFINITY;
+    reinterpret_cast<float4*>(p.out_row_stats)[row] = o;
+  }
+}
+
+// Publisher side: hand a collective task to the consumers.
+__device__ void enqueue_task(const Params& p, Shared& sh, int64_t task, float m, float s) {
+  const int t = sh.tq_tail;
+  if (t - *reinterpret_cast<volatile int*>(&sh.tq_head) >= kTaskSlots) {  // full: wait for the consumers
+    const uint64_t t0 = globaltimer_ns();
+    while (t - *reinterpret_cast<volatile int*>(&sh.tq_head) >= kTaskSlots) {
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        atomicOr(p.ctl + 3, kStatusTimeout);
+        return;
       }
-      for (int o = 16; o > 0; o >>= 1) {
-        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
-        ms_combine(m, s, m2, s2, p.c);
-      }
-      if (lane == 0) {
-        sh.bf[2] = m;
-        sh.bf[3] = s;
-      }
-    } else {
-      float v = -INFINITY;
-      int64_t i = -1;
-      bool nan = false;
-      for (int64_t k = lane; k < p.NC; k += 32) {
-        const float2 pv = __ldcg(part + k);
-        const int64_t pi = (int64_t)__float_as_int(pv.y);
-        if (pv.x != pv.x) nan = true;
-        else if (am_better(pv.x, pi, v, i)) {
-          v = pv.x;
+    }
+  }
+  sh.tq[t % kTaskSlots] = task;
+  sh.tq_m[t % kTaskSlots] = m;
+  sh.tq_s[t % kTaskSlots] = s;
+  __threadfence_block();
+  *reinterpret_cast<volatile int*>(&sh.tq_tail) = t + 1;
+}
+
+// Sequence tails go to a queue in global memory: ctl[4] counts the entries
+// written, ctl[5] the entries taken, tq_global[k] holds b+1 (0 = not yet
+// written). CTAs take entries only once their own streaming work is done, so
+// a tail never holds up tiles that other sequences are waiting for.
+__device__ __forceinline__ void tail_enqueue(const Params& p, int64_t b) {
+  const uint32_t k = atomicAdd(p.ctl + 4, 1u);
+  st_release_gpu(p.tail_q + k, (uint32_t)(b + 1));
+}
+
+// One more row of sequence b is final; the last one queues the sequence tail.
+__device__ __forceinline__ void seq_arrive(const Params& p, int64_t b) {
+  const uint32_t old = atom_add_acq_rel(p.seq_cnt + b, 1u);
+  if (old == (uint32_t)p.RS - 1u) {
+    p.seq_cnt[b] = 0u;
+    tail_enqueue(p, b);
+  }
+}
+
+// Publisher side: the row's result is complete (m, s for sampling; best
+// value and index for argmax). Finish the row here unless it needs the
+// collective top-p pass.
+template <typename E, int MODE>
+__device__ void publisher_row_done(const Params& p, Shared& sh, int64_t row, float2 r) {
+  if (MODE == kSample) {
+    const float m = r.x, s = r.y;
+    const bool valid = (m > -INFINITY) && (m < INFINITY);
+    if (valid && p.topp) {
+      enqueue_task(p, sh, row, m, s);
+      return;
+    }
+    store_sample_row<E>(p, row, m, s, s, 0u);
+  } else {
+    const int64_t i = (int64_t)__float_as_int(r.y);
+    RowStat rs;
+    rs.M = r.x;  // NaN marks a row with a NaN logit
+    rs.s = 0.f;
+    rs.cum = 0.f;
+    rs.tau = (uint32_t)(i < 0 ? 0 : i);  // all -inf: every element ties, index 0 wins
+    rs_store(p, row, rs);
+  }
+  seq_arrive(p, row / p.RS);
+}
+
+// Publisher side: every chunk of `row` is published; combine the partials.
+template <typename E, int MODE>
+__device__ void publisher_finish_row(const Params& p, Shared& sh, int64_t row) {
+  p.row_cnt[row] = 0u;
+  const float2* part = p.part + row * p.NC;
+  if (MODE == kSample) {
+    float m = -INFINITY, s = 0.f;
+    for (int64_t k = 0; k < p.NC; k += 4) {
+      float2 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] = (k + j < p.NC) ? __ldcg(part + k + j) : make_float2(-INFINITY, 0.f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ms_combine(m, s, v[j].x, v[j].y, p.c);
+    }
+    publisher_row_done<E, MODE>(p, sh, row, make_float2(m, s));
+  } else {
+    float v = -INFINITY;
+    int64_t i = -1;
+    bool nan = false;
+    for (int64_t k = 0; k < p.NC; k += 4) {
+      float2 pv[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        pv[j] = (k + j < p.NC) ? __ldcg(part + k + j) : make_float2(-INFINITY, __int_as_float(-1));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int64_t pi = (int64_t)__float_as_int(pv[j].y);
+        if (pv[j].x != pv[j].x) nan = true;
+        else if (am_better(pv[j].x, pi, v, i)) {
+          v = pv[j].x;
           i = pi;
         }
       }
-      for (int o = 16; o > 0; o >>= 1) {
-        const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-        const long long i2 = __shfl_xor_sync(0xffffffffu, (long long)i, o);
-        if (am_better(v2, i2, v, i)) {
-          v = v2;
-          i = i2;
-        }
-      }
-      nan = __any_sync(0xffffffffu, nan);
-      if (lane == 0) {
-        RowStat rs;
-        rs.M = nan ? __int_as_float(0x7fc00000) : v;
-        rs.s = 0.f;
-        rs.cum = 0.f;
-        rs.tau = (uint32_t)(i < 0 ? 0 : i);  // all -inf: every element ties, index 0 wins
-        rs_store(p, row, rs);
-      }
     }
+    publisher_row_done<E, MODE>(p, sh, row,
+                                make_float2(nan ? __int_as_float(0x7fc00000) : v, __int_as_float((int)i)));
   }
-  cbar();
+}
+
+// Consumer side: one queued top-p cut, run by all 256 consumer threads.
+template <typename E, int MODE>
+__device__ void run_task(const Params& p, Shared& sh, int64_t row, float m, float s, int tid) {
   if (MODE == kSample) {
-    const float M = sh.bf[2], s = sh.bf[3];
-    const bool valid = (M > -INFINITY) && (M < INFINITY);  // NaN fails both
+    const int64_t b = row / p.RS;
+    const int r = (int)(row % p.RS);
+    __threadfence();
     uint32_t tau = 0u;
     float cum = s;
-    const char* rowp = row_ptr<E, MODE>(p, b, r);
-    if (valid && p.topp) topp_cut<E>(p, sh, rowp, M, s, tid, tau, cum);
+    topp_cut<E>(p, sh, row_ptr<E, MODE>(p, b, r), m, s, tid, tau, cum);
     if (tid == 0) {
-      RowStat rs;
-      rs.M = valid ? M : __int_as_float(0x7fc00000);
-      rs.s = s;
-      rs.cum = cum;
-      rs.tau = tau;
-      rs_store(p, row, rs);
-      if (p.out_row_stats) {
-        float4 o;
-        const float Mc = mref(M, p.c);
-        o.x = valid ? __fdiv_rn(M, p.T) : __int_as_float(0x7fc00000);
-        o.y = valid ? (Mc + lg2(s)) * 0.69314718055994531f : __int_as_float(0x7fc00000);
-        o.z = valid ? cum / s : __int_as_float(0x7fc00000);
-        o.w = (valid && p.topp) ? ET<E>::val(tau) : -INFINITY;
-        reinterpret_cast<float4*>(p.out_row_stats)[row] = o;
-      }
+      store_sample_row<E>(p, row, m, s, cum, tau);
+      seq_arrive(p, b);
     }
+    cbar();
   }
-  if (tid == 0) {
-    p.row_cnt[row] = 0u;
-    const uint32_t old = atom_add_acq_rel(p.seq_cnt + b, 1u);
-    sh.flag = (old == (uint32_t)p.RS - 1u);
-    if (sh.flag) p.seq_cnt[b] = 0u;
+}
+
+// Consumer side, after the CTA's streaming is done: take tickets for queued
+// sequence tails until every sequence of the call has one. Ticket k is the
+// k-th tail queued; it may not be written yet, but whoever will write it holds
+// the rows it waits for and needs nothing from this CTA, so the wait ends.
+template <typename E, int MODE>
+__device__ void drain_tails(const Params& p, Shared& sh, int tid) {
+  for (;;) {
+    if (tid == 0) {
+      const uint32_t k = atomicAdd(p.ctl + 5, 1u);
+      int64_t b = -1;
+      if ((int64_t)k < p.B) {
+        uint32_t v = ld_acquire_gpu(p.tail_q + k);
+        if (v == 0u) {
+          const uint64_t t0 = globaltimer_ns();
+          while (v == 0u && globaltimer_ns() - t0 < kWaitLimitNs) v = ld_acquire_gpu(p.tail_q + k);
+        }
+        if (v == 0u) atomicOr(p.ctl + 3, kStatusTimeout);
+        else b = (int64_t)v - 1;
+        p.tail_q[k] = 0u;
+      }
+      sh.bl[1] = b;
+    }
+    cbar();
+    const int64_t b = sh.bl[1];
+    cbar();
+    if (b < 0) return;
+    seq_tail<E, MODE>(p, sh, b, tid);
   }
-  cbar();
-  if (sh.flag) {
-    __threadfence();
-    if (MODE == kSample) seq_sample<E>(p, sh, b, tid);
-    else if (MODE == kArgmaxLimit) seq_argmax_limit<E>(p, sh, b, tid);
-    else seq_greedy(p, sh, b, tid);
+}
+
+template <typename E, int MODE>
+__device__ __forceinline__ int drain_tasks(const Params& p, Shared& sh, int head, int snap, int tid) {
+  while (head < snap) {
+    const int i = head % kTaskSlots;
+    run_task<E, MODE>(p, sh, sh.tq[i], sh.tq_m[i], sh.tq_s[i], tid);  // top-p cuts
+    ++head;
   }
-  cbar();
+  if (tid == 0) *reinterpret_cast<volatile int*>(&sh.tq_head) = head;
+  return head;
 }
 
 // --------------------------------------------------------------- kernel -------
 
-// The producer: one elected thread takes chunks from the call's work counter
-// and streams their tiles into the ring, one stage per tile, each stage a
-// single bulk copy completing on the stage's "full" barrier.
+// The producer: one thread takes chunks from the call's work counter (one
+// fetch ahead) and streams their tiles into the ring, one stage per tile,
+// each stage one bulk copy completing on the stage's "full" barrier.
 template <typename E, int MODE>
 __device__ void producer_loop(const Params& p, char* ring, Shared& sh) {
   unsigned long long* next = reinterpret_cast<unsigned long long*>(p.ctl);
   int last_parity[kMaxStages];
   for (int i = 0; i < kMaxStages; ++i) last_parity[i] = -1;
   bool aborted = false;
-  int64_t it = 0;
+  int slot = 0;
+  uint32_t ph = 0u;
+  bool wrapped = false;  // every stage has been used once
+  // Two work indices are always in flight ahead of the chunk being streamed,
+  // so the round trip of the counter never stalls the ring.
+  int64_t w = (int64_t)atomicAdd(next, 1ull);
+  int64_t w1 = w < p.W ? (int64_t)atomicAdd(next, 1ull) : w;
   while (!aborted) {
-    const int64_t w = (int64_t)atomicAdd(next, 1ull);
-    const ChunkId ch = decode_chunk(p, w < p.W ? w : 0);
+    const int64_t w2 = w1 < p.W ? (int64_t)atomicAdd(next, 1ull) : w1;
+    ChunkId ch;
+    if (w < p.W) ch = decode_chunk(p, w);
     const int n = w < p.W ? ch.n : 1;  // the end of work takes one stage too
-    for (int j = 0; j < n; ++j, ++it) {
-      const int slot = (int)(it % p.stages);
-      const uint32_t ph = (uint32_t)((it / p.stages) & 1);
-      if (it >= p.stages && !mbar_wait(&sh.empty[slot], ph ^ 1u)) {
+    for (int j = 0; j < n; ++j) {
+      if (wrapped && !mbar_wait(&sh.empty[slot], ph ^ 1u)) {
         aborted = true;
         break;
       }
+      TileDesc& t = sh.td[slot];
       if (w >= p.W) {
-        sh.meta_w[slot] = -1;
+        t.w = -1;
         mbar_arrive(&sh.full[slot]);
         break;
       }
-      const Tile t = tile_of<E, MODE>(p, ch.b, ch.r, ch.k0 + j);
-      sh.meta_w[slot] = w;
-      sh.meta_k[slot] = (int)(ch.k0 + j);
-      sh.meta_last[slot] = (j == n - 1);
+      decode_tile<E, MODE>(p, ch, ch.k0 + j, t);
+      t.w = w;
+      t.last = (j == n - 1);
       if (t.ibytes) {
+        const char* src = t.row + t.ie0 * ET<E>::kSize;
         mbar_arrive_expect_tx(&sh.full[slot], t.ibytes);
-        bulk_g2s(ring + (size_t)slot * kTileBytes, t.ip, t.ibytes, &sh.full[slot]);
+        bulk_g2s(ring + (size_t)slot * kTileBytes, src, t.ibytes, &sh.full[slot]);
         last_parity[slot] = (int)ph;
       } else {
         mbar_arrive(&sh.full[slot]);
       }
+      if (++slot == p.stages) {
+        slot = 0;
+        ph ^= 1u;
+        wrapped = true;
+      }
     }
     if (w >= p.W) break;
+    w = w1;
+    w1 = w2;
   }
   if (aborted) {  // a wait ran out: let copies still in flight land before the CTA exits
     atomicOr(p.ctl + 3, kStatusTimeout);
@@ -911,67 +1061,96 @@ __device__ void producer_loop(const Params& p, char* ring, Shared& sh) {
   }
 }
 
-// Publishing a chunk: combine the eight warps' partials, store the chunk's
-// partial and count it against its row with a release-acquire atomic. Run by
-// one lane of a rotating warp; the other warps go on with the next chunk, and
-// learn whether the row completed at the next chunk boundary.
-template <int MODE>
-__device__ __forceinline__ void publish(const Params& p, Shared& sh, int par, int64_t w, int64_t row) {
-  float2 res;
-  if (MODE == kSample) {
-    float M = sh.red_m[par][0], S = sh.red_s[par][0];
-    for (int k = 1; k < kConsumerWarps; ++k) ms_combine(M, S, sh.red_m[par][k], sh.red_s[par][k], p.c);
-    res = make_float2(M, S);
-  } else {
-    float V_ = sh.red_m[par][0];
-    int64_t I = sh.red_i[par][0];
-    bool N_ = V_ != V_;
-    for (int k = 1; k < kConsumerWarps; ++k) {
-      const float v2 = sh.red_m[par][k];
-      if (v2 != v2) N_ = true;
-      else if (am_better(v2, sh.red_i[par][k], V_, I)) {
-        V_ = v2;
-        I = sh.red_i[par][k];
-      }
+// The publisher: combines the consumer warps' chunk partials, stores the
+// chunk's partial and counts it against its row (release/acquire atomic,
+// whose result is looked at one chunk later so that its round trip overlaps
+// the next chunk). The last chunk of a row finishes the row.
+template <typename E, int MODE>
+__device__ void publisher_loop(const Params& p, Shared& sh) {
+  int64_t pend_row = -1;
+  uint32_t pend_old = 0u;
+  for (int64_t c = 0;; ++c) {
+    const int ps = (int)(c % kPartSlots);
+    const uint32_t pph = (uint32_t)((c / kPartSlots) & 1);
+    if (!mbar_wait(&sh.pfull[ps], pph)) {
+      atomicOr(p.ctl + 3, kStatusTimeout);
+      break;
     }
-    if (N_) V_ = __int_as_float(0x7fc00000);
-    res = make_float2(V_, __int_as_float((int)I));
+    const int64_t w = sh.pw[ps];
+    if (w < 0) break;
+    float2 res;
+    if (MODE == kSample) {
+      float M = sh.red_m[ps][0], S = sh.red_s[ps][0];
+      for (int k = 1; k < kConsumerWarps; ++k) ms_combine(M, S, sh.red_m[ps][k], sh.red_s[ps][k], p.c);
+      res = make_float2(M, S);
+    } else {
+      float V_ = sh.red_m[ps][0];
+      int64_t I = sh.red_i[ps][0];
+      bool N_ = V_ != V_;
+      for (int k = 1; k < kConsumerWarps; ++k) {
+        const float v2 = sh.red_m[ps][k];
+        if (v2 != v2) N_ = true;
+        else if (am_better(v2, sh.red_i[ps][k], V_, I)) {
+          V_ = v2;
+          I = sh.red_i[ps][k];
+        }
+      }
+      if (N_) V_ = __int_as_float(0x7fc00000);
+      res = make_float2(V_, __int_as_float((int)I));
+    }
+    const int64_t row = sh.prow[ps];
+    mbar_arrive(&sh.pempty[ps]);
+    if (p.NC == 1) {  // the chunk is the whole row: no partial to combine
+      publisher_row_done<E, MODE>(p, sh, row, res);
+      continue;
+    }
+    p.part[w] = res;
+    const uint32_t old = atom_add_acq_rel(p.row_cnt + row, 1u);
+    if (pend_row >= 0 && pend_old == (uint32_t)(p.NC - 1)) publisher_finish_row<E, MODE>(p, sh, pend_row);
+    pend_row = row;
+    pend_old = old;
   }
-  p.part[w] = res;
-  const uint32_t old = atom_add_acq_rel(p.row_cnt + row, 1u);
-  sh.pend[par] = (old == (uint32_t)(p.NC - 1)) ? row : -1;
+  if (pend_row >= 0 && pend_old == (uint32_t)(p.NC - 1)) publisher_finish_row<E, MODE>(p, sh, pend_row);
+  mbar_arrive(&sh.pdone);
 }
 
-// The consumers: per-thread accumulation over every tile of a chunk, then one
-// barrier per chunk (which also carries the abort vote of bounded waits).
+// The consumers: per-thread accumulation over every tile of a chunk; at the
+// end of a chunk, per-warp partials go to the publisher and one barrier (which
+// carries the abort vote of the bounded waits) lets all consumers see the
+// same task-queue snapshot.
 template <typename E, int MODE>
 __device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int tid) {
   constexpr int PV = ET<E>::kPerVec;
   const int warp = tid >> 5, lane = tid & 31;
-  float m = -INFINITY, s0 = 0.f, s1 = 0.f;   // sampling: online (max, sum)
-  float av = -INFINITY;                      // argmax: value, index, NaN seen
+  float m = -INFINITY, s0 = 0.f, s1 = 0.f;  // sampling: online (max, sum)
+  float av = -INFINITY;                     // argmax: value, index, NaN seen
   int64_t ai = -1;
   bool an = false;
   int timed_out = 0;
   int64_t chunks = 0;
-  for (int64_t it = 0;; ++it) {
-    const int slot = (int)(it % p.stages);
-    const uint32_t ph = (uint32_t)((it / p.stages) & 1);
-    if (!mbar_wait(&sh.full[slot], ph)) {
+  int head = 0;
+  int slot = 0;
+  uint32_t ph = 0u;
+  for (;;) {
+    const int cur = slot;
+    if (!mbar_wait(&sh.full[cur], ph)) {
       timed_out = 1;
       break;
     }
-    const int64_t w = sh.meta_w[slot];
+    if (++slot == p.stages) {
+      slot = 0;
+      ph ^= 1u;
+    }
+    const TileDesc t = sh.td[cur];  // a copy: the stage (and its descriptor) is released below
+    const int64_t w = t.w;
     if (w < 0) break;  // no more work
-    const ChunkId ch = decode_chunk(p, w);
-    const Tile t = tile_of<E, MODE>(p, ch.b, ch.r, sh.meta_k[slot]);
-    const bool last = sh.meta_last[slot] != 0;
-    const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)slot * kTileBytes);
+    const bool last = t.last != 0;
+    const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)cur * kTileBytes);
     const int nvec = (int)(t.ibytes >> 4);
     if (MODE == kSample) {
       for (int v = tid; v < nvec; v += kConsumerThreads) ms_vec(m, s0, s1, sv[v], p.c, E());
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.empty[slot]);
+      if (lane == 0) mbar_arrive(&sh.empty[cur]);
       if (t.nh | t.nt) {
         // head and tail elements (rows not 16-byte aligned) join one
         // accumulator, so that a new maximum among them rescales everything
@@ -983,7 +1162,7 @@ __device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int
     } else {
       for (int q = tid; q < nvec; q += kConsumerThreads) am_vec(av, ai, an, sv[q], t.ie0 + (int64_t)q * PV, E());
       __syncwarp();
-      if (lane == 0) mbar_arrive(&sh.empty[slot]);
+      if (lane == 0) mbar_arrive(&sh.empty[cur]);
       if (tid < t.nh) am_scalar(av, ai, an, ET<E>::load(t.row, t.e0 + tid), t.e0 + tid);
       if (tid >= 32 && tid < 32 + t.nt) {
         const int64_t e = t.e1 - t.nt + (tid - 32);
@@ -992,18 +1171,19 @@ __device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int
     }
     if (!last) continue;
 
-    // ---- end of a chunk: warp partials, one barrier, publish, pending row
-    const int par = (int)(chunks & 1);
+    // ---- end of a chunk
+    const int ps = (int)(chunks % kPartSlots);
+    const uint32_t pph = (uint32_t)((chunks / kPartSlots) & 1);
+    float rm, rs_;
+    int64_t ri = -1;
     if (MODE == kSample) {
       float s = s0 + s1;
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
         ms_combine(m, s, m2, s2, p.c);
       }
-      if (lane == 0) {
-        sh.red_m[par][warp] = m;
-        sh.red_s[par][warp] = s;
-      }
+      rm = m;
+      rs_ = s;
       m = -INFINITY;
       s0 = s1 = 0.f;
     } else {
@@ -1016,34 +1196,77 @@ __device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int
         }
       }
       an = __any_sync(0xffffffffu, an);
-      if (lane == 0) {
-        sh.red_m[par][warp] = an ? __int_as_float(0x7fc00000) : av;
-        sh.red_i[par][warp] = ai;
-      }
+      rm = an ? __int_as_float(0x7fc00000) : av;
+      rs_ = 0.f;
+      ri = ai;
       av = -INFINITY;
       ai = -1;
       an = false;
     }
-    if (cbar_or(0)) return;  // another warp's wait ran out
-    const int64_t prow = chunks > 0 ? sh.pend[par ^ 1] : -1;
-    if (warp == (int)(chunks % kConsumerWarps) && lane == 0)
-      publish<MODE>(p, sh, par, w, ch.b * p.RS + ch.r);
-    __syncwarp();
+    if (chunks >= kPartSlots && !mbar_wait(&sh.pempty[ps], pph ^ 1u)) timed_out = 1;
+    if (lane == 0) {
+      sh.red_m[ps][warp] = rm;
+      sh.red_s[ps][warp] = rs_;
+      sh.red_i[ps][warp] = ri;
+      if (warp == 0) {
+        sh.pw[ps] = w;
+        sh.prow[ps] = t.rowid;
+      }
+      mbar_arrive(&sh.pfull[ps]);
+    }
+    const int par = (int)(chunks & 1);
     ++chunks;
-    if (prow >= 0) finish_row<E, MODE>(p, sh, prow / p.RS, (int)(prow % p.RS), tid);
+    if (tid == 0) {
+      sh.snap[par] = *reinterpret_cast<volatile int*>(&sh.tq_tail);
+      __threadfence_block();
+    }
+    if (cbar_or(timed_out)) {
+      if (tid == 0) atomicOr(p.ctl + 3, kStatusTimeout);
+      return;
+    }
+    head = drain_tasks<E, MODE>(p, sh, head, sh.snap[par], tid);
   }
-  // End of work (or a wait that ran out): one last vote, then the row the
-  // final chunk may have completed.
+  // End of work (or a wait that ran out): tell the publisher, wait for it to
+  // finish, and run what it queued.
+  if (!timed_out) {
+    const int ps = (int)(chunks % kPartSlots);
+    const uint32_t pph = (uint32_t)((chunks / kPartSlots) & 1);
+    if (chunks >= kPartSlots && !mbar_wait(&sh.pempty[ps], pph ^ 1u)) timed_out = 1;
+    if (lane == 0) {
+      if (warp == 0) sh.pw[ps] = -1;
+      mbar_arrive(&sh.pfull[ps]);
+    }
+  }
   if (cbar_or(timed_out)) {
     if (tid == 0) atomicOr(p.ctl + 3, kStatusTimeout);
     return;
   }
-  const int64_t prow = chunks > 0 ? sh.pend[(chunks - 1) & 1] : -1;
-  if (prow >= 0) finish_row<E, MODE>(p, sh, prow / p.RS, (int)(prow % p.RS), tid);
+  const int done = mbar_wait(&sh.pdone, 0u) ? 1 : 0;
+  if (tid == 0) {
+    sh.snap[0] = *reinterpret_cast<volatile int*>(&sh.tq_tail);
+    __threadfence_block();
+  }
+  if (cbar_or(!done)) {
+    if (tid == 0) atomicOr(p.ctl + 3, kStatusTimeout);
+    return;
+  }
+  drain_tasks<E, MODE>(p, sh, head, sh.snap[0], tid);
+  drain_tails<E, MODE>(p, sh, tid);
+  // The last CTA out re-arms the tail queue for the next call.
+  if (tid == 0) {
+    __threadfence();
+    const uint32_t prev = atomicAdd(p.ctl + 6, 1u);
+    if (prev == gridDim.x - 1) {
+      p.ctl[4] = 0u;
+      p.ctl[5] = 0u;
+      p.ctl[6] = 0u;
+      __threadfence();
+    }
+  }
 }
 
 template <typename E, int MODE>
-__global__ void __launch_bounds__(kThreads, 2) verify_kernel(const Params p) {
+__global__ void __launch_bounds__(kAllThreads, 2) verify_kernel(const Params p) {
   extern __shared__ __align__(1024) unsigned char smem[];
   char* ring = reinterpret_cast<char*>(smem);
   Shared& sh = *reinterpret_cast<Shared*>(smem + (size_t)p.stages * kTileBytes);
@@ -1053,12 +1276,23 @@ __global__ void __launch_bounds__(kThreads, 2) verify_kernel(const Params p) {
       mbar_init(&sh.full[i], 1u);
       mbar_init(&sh.empty[i], (uint32_t)kConsumerWarps);
     }
-    sh.pend[0] = sh.pend[1] = -1;
+    for (int i = 0; i < kPartSlots; ++i) {
+      mbar_init(&sh.pfull[i], (uint32_t)kConsumerWarps);
+      mbar_init(&sh.pempty[i], 1u);
+    }
+    mbar_init(&sh.pdone, 1u);
+    sh.tq_tail = 0;
+    sh.tq_head = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  if (tid >= kConsumerThreads) {
-    if (tid == kConsumerThreads) producer_loop<E, MODE>(p, ring, sh);
+  const int warp = tid >> 5;
+  if (warp == kProducerWarp) {
+    if ((tid & 31) == 0) producer_loop<E, MODE>(p, ring, sh);
+    return;
+  }
+  if (warp == kPublisherWarp) {
+    if ((tid & 31) == 0) publisher_loop<E, MODE>(p, sh);
     return;
   }
   consumer_loop<E, MODE>(p, ring, sh, tid);
@@ -1078,11 +1312,11 @@ static cudaError_t launch_t(const Params& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     raised = shared_bytes(kMaxStages);
   }
-  k<<<grid, kThreads, smem, stream>>>(p);
+  k<<<grid, kAllThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
-int kernel_threads() { return kThreads; }
+int kernel_threads() { return kAllThreads; }
 
 cudaError_t launch(const Params& p, int dtype, int mode, int grid, cudaStream_t stream) {
   if (dtype == 1) {

@@ -7,8 +7,8 @@
 namespace sv {
 
 enum Mode { kSample = 0, kArgmaxLimit = 1, kGreedy = 2 };
-constexpr int kMaxStages = 8;
-constexpr int kTileBytes = 16384;  // one ring stage holds one tile
+constexpr int kMaxStages = 6;  // 6 x 32 KB + control stays under the 227 KB a CTA may use
+constexpr int kTileBytes = 32768;  // one ring stage holds one tile
 
 struct Params {
   const char* a;           // target logits [B,K+1,V] (sampling) or logits [B,G,N,V] (greedy)
@@ -31,9 +31,11 @@ struct Params {
   float T;
   float top_p;
   int topp;                // top_p < 1
-  uint32_t* ctl;           // [0..1] work counter (u64), [2] finished producers, [3] status bits
+  uint32_t* ctl;           // [0..1] work counter (u64), [2] finished producers, [3] status bits,
+                           // [4] tails queued, [5] tails taken, [6] finished CTAs
   uint32_t* row_cnt;       // [B*RS] chunks published per row
   uint32_t* seq_cnt;       // [B] rows finished per sequence
+  uint32_t* tail_q;        // [B] queued sequence tails (b + 1; 0 = empty)
   float2* part;            // [W] per-chunk partials
   float4* rowstat;         // [B*RS] per-row results
   int stages;

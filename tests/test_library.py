@@ -74,7 +74,7 @@ def test_host_argument_checks(lib):
     assert g(p, p, 4, 7, 1, 100, 1, p, p, None, None) == -1
     assert g(p, p, 4, 7, 5, 100, 9, p, p, None, None) == -2
     assert g(None, None, 0, 7, 5, 100, 1, None, None, None, None) == 0
-    assert lib.sv_set_launch_shape(9, 1) == -1
+    assert lib.sv_set_launch_shape(7, 1) == -1
     assert lib.sv_set_launch_shape(0, 0) == 0
 
 
