@@ -52,8 +52,10 @@ def log(*a):
 
 # ------------------------------------------------------------------ workload
 
-def workload(name: str):
+def workload(name: str, batch: int | None = None):
     cfg = sg.CONFIGS[name]
+    if batch:
+        cfg = cfg.with_(B=batch)
     greedy = isinstance(cfg, sg.GreedyConfig)
     esz = 2 if cfg.dtype == sg.BF16 else 4
     if greedy:
@@ -70,7 +72,7 @@ def workload(name: str):
 
 
 def config_json(cfg, greedy, rotation):
-    c = {"workload": cfg.name, "B": cfg.B, "V": cfg.V, "logits": "bf16" if cfg.dtype == sg.BF16 else "f32"}
+    c = {"workload": cfg.name if cfg.B == sg.CONFIGS[cfg.name].B else f"{cfg.name}_b{cfg.B}", "B": cfg.B, "V": cfg.V, "logits": "bf16" if cfg.dtype == sg.BF16 else "f32"}
     if greedy:
         c.update({"mode": "greedy", "G": cfg.G, "N": cfg.N})
     else:
@@ -148,12 +150,16 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ("sv_kernels.cu", "sv_device.cuh", "sv_kernels.h")
+
+
 def kernel_source_hash() -> str:
+    """Hash of the verify kernel's sources; a profiled traffic figure is only
+    reported while the kernel is the one that was profiled."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_39_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -170,6 +176,23 @@ def profiled_traffic(workload_name: str):
     if not m or not h or h.group(1) != kernel_source_hash():
         return None
     return float(m.group(1))
+
+
+def shard_offset(rank: int, batch: int) -> int:
+    """First global sequence of a rank's shard: every rank verifies its own
+    ``batch`` sequences of the global batch (weak scaling, no collective)."""
+    return rank * batch
+
+
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest of the ranks' values (the timed region's duration)."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_initialized() or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
 
 def oracle_cpu_rate(cfg, greedy, budget_s: float, nthreads: int):
@@ -210,11 +233,12 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     svpkg.build()
-    cfg, greedy, positions, logit_bytes, small_in, out_bytes = workload(name)
+    cfg, greedy, positions, logit_bytes, small_in, out_bytes = workload(name, args.batch)
     rotation = 1 if logit_bytes > L2_BYTES else int(math.ceil(3 * L2_BYTES / logit_bytes)) + 1
     log(f"[bench] {name}: {logit_bytes / 1e6:.1f} MB of logits per call, {rotation} input set(s)")
     t0 = time.perf_counter()
-    host = sg.greedy_inputs(cfg, seq_offset=rank * cfg.B) if greedy else sg.sample_inputs(cfg, seq_offset=rank * cfg.B)
+    off = shard_offset(rank, cfg.B)
+    host = sg.greedy_inputs(cfg, seq_offset=off) if greedy else sg.sample_inputs(cfg, seq_offset=off)
     log(f"[bench] inputs generated in {time.perf_counter() - t0:.1f} s")
     keys = ("logits", "cand") if greedy else ("target", "draft", "draft_tokens", "uniforms")
     pinned = {k: to_torch(host[k], torch, pin=True) for k in keys}
@@ -281,10 +305,7 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
         status = svpkg.get_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     ms_per_step = ms / args.steps
     value = positions * world * args.steps / (ms / 1e3)
     achieved_gbs = logit_bytes / (ms_per_step / 1e3) / 1e9
@@ -348,7 +369,7 @@ def run_reference(args, name: str):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
-    cfg, greedy, positions, logit_bytes, _, _ = workload(name)
+    cfg, greedy, positions, logit_bytes, _, _ = workload(name, args.batch)
     nth = os.cpu_count() or 1
     per_step = max(5.0, 60.0 / max(1, args.steps + args.warmup))
     rates = []
@@ -389,6 +410,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size (profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     names = list(sg.CONFIGS) if args.config == "all" else [args.config]
