@@ -58,7 +58,8 @@ typedef enum {
   SV_ERR_CUDA = -3,    /* a CUDA runtime call failed (launch, allocation, copy) */
   SV_ERR_INPUT = -4,   /* device-detected bad input in at least one sequence */
   SV_ERR_TIMEOUT = -5, /* a bounded device wait ran out; the scratch was reset */
-  SV_ERR_NOMEM = -6    /* scratch allocation failed */
+  SV_ERR_NOMEM = -6,   /* scratch allocation failed */
+  SV_ERR_SCRATCH_LIMIT = -7 /* sv_verify_sample_noalloc: the call needs more than its fixed scratch */
 } sv_status;
 
 /*
@@ -121,6 +122,42 @@ int sv_verify_sample(const void* target_logits, const void* draft_logits, const 
 int sv_verify_greedy(const void* logits, const int32_t* cand, int64_t B, int32_t G, int32_t N, int64_t V,
                      int32_t dtype, int32_t* out_tokens, int32_t* out_accept_len, int32_t* out_best_cand,
                      void* stream);
+
+/*
+ * sv_verify_sample_noalloc: sv_verify_sample for callers that cannot allocate
+ * device memory. The pages have no counterpart to this entry point; it exists
+ * for deployment constraints, not for the method.
+ *
+ * Who needs it: code that runs inside a caller-managed memory pool or arena
+ * that must account for every byte, allocator hooks that would recurse into
+ * themselves if the library called cudaMalloc, and services that reserve all
+ * device memory at start-up and treat any later allocation as a failure.
+ * sv_verify_sample allocates a scratch area per stream on its first call; this
+ * entry point never allocates: it uses a fixed 4 MiB scratch array that is
+ * part of the library image and that every GPU which loads the library holds
+ * until the process exits.
+ *
+ * Arguments, outputs and results are exactly those of sv_verify_sample (the
+ * same kernel runs). Differences:
+ *   - A call whose scratch would exceed 4 MiB returns SV_ERR_SCRATCH_LIMIT and
+ *     enqueues nothing. The scratch needed is about
+ *     256 + 4*(B*R + 2*B) + 8*B*R*ceil(NT/CT) + 16*B*R bytes (R = 2K+1 rows
+ *     per sequence), e.g. about 0.2 MiB for B=256, K=8, V=128256.
+ *   - The first call on a device looks up the array's device address on that
+ *     device (cudaGetSymbolAddress, with the device current) and caches it;
+ *     make that first call before any stream capture.
+ *   - Each call clears the array's control block and counters with a memset
+ *     on `stream` before its kernel.
+ *   - All calls on all streams share the one array, which keeps the contents
+ *     the last call left. Calls whose kernels overlap on the GPU race on it:
+ *     issue them on one stream, or otherwise keep them from overlapping.
+ *   - sv_get_status() does not report this entry point's device-side input
+ *     errors; out_accept_len[b] == -1 still marks a sequence with bad input.
+ */
+int sv_verify_sample_noalloc(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                             const float* uniforms, int64_t B, int32_t K, int64_t V, int32_t dtype, float temperature,
+                             float top_p, int32_t* out_tokens, int32_t* out_accept_len, float* out_row_stats,
+                             void* stream);
 
 /*
  * Synchronises `stream`, then returns and clears the sticky device status of

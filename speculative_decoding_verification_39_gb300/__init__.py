@@ -24,12 +24,12 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _SO = os.path.join(_HERE, "libspecverify.so")
-_SOURCES = ["sv_kernels.cu", "sv_api.cu"]
+_SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_noalloc.cu"]
 _DEPS = _SOURCES + ["sv_kernels.h", "sv_device.cuh"]
 
 SV_F32, SV_BF16 = 0, 1
 STATUS = {0: "SV_OK", -1: "SV_ERR_ARG", -2: "SV_ERR_DTYPE", -3: "SV_ERR_CUDA", -4: "SV_ERR_INPUT",
-          -5: "SV_ERR_TIMEOUT", -6: "SV_ERR_NOMEM"}
+          -5: "SV_ERR_TIMEOUT", -6: "SV_ERR_NOMEM", -7: "SV_ERR_SCRATCH_LIMIT"}
 
 NVCC_FLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
               "-Xcompiler", "-fPIC"]
@@ -106,13 +106,15 @@ def lib():
         h.sv_set_launch_shape.restype = ctypes.c_int
         h.sv_launch_count.argtypes = []
         h.sv_launch_count.restype = ctypes.c_uint64
+        h.sv_verify_sample_noalloc.argtypes = [vp, vp, vp, vp, i64, i32, i64, i32, f32, f32, vp, vp, vp, vp]
+        h.sv_verify_sample_noalloc.restype = ctypes.c_int
         _lib_handle = h
     return _lib_handle
 
 
 def exported_symbols() -> list:
     return ["sv_verify_sample", "sv_verify_greedy", "sv_get_status", "sv_status_string", "sv_release",
-            "sv_set_launch_shape", "sv_launch_count"]
+            "sv_set_launch_shape", "sv_launch_count", "sv_verify_sample_noalloc"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:

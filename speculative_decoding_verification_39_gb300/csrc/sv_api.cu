@@ -237,6 +237,7 @@ extern "C" const char* sv_status_string(int status) {
     case SV_ERR_INPUT: return "bad input in at least one sequence";
     case SV_ERR_TIMEOUT: return "a bounded device wait ran out";
     case SV_ERR_NOMEM: return "scratch allocation failed";
+    case SV_ERR_SCRATCH_LIMIT: return "the call needs more than the fixed no-allocation scratch";
     default: return "unknown status";
   }
 }
