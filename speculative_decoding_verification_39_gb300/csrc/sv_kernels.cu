@@ -78,6 +78,8 @@ struct alignas(16) Shared {
   uint64_t pfull[kPartSlots];    // chunk partial written by all consumer warps
   uint64_t pempty[kPartSlots];   // chunk partial taken by the publisher
   uint64_t pdone;                // publisher finished
+  uint64_t dbar[2];              // the draw's row pieces landed in ring half 0 / 1
+  uint32_t dcount[2];            // pieces issued so far on dbar[0] / dbar[1]
   TileDesc td[kMaxStages];       // what the stage holds, decoded once by the producer
   float red_m[kPartSlots][kConsumerWarps];
   float red_s[kPartSlots][kConsumerWarps];
@@ -252,6 +254,65 @@ __device__ __forceinline__ void ms_vec(float& m, float& s0, float& s1, const uin
   s1 += ex2(fmaf(x3, c, nmc));
 }
 
+// A thread's share of a tile, eight 16-byte vectors at a time: all eight are
+// loaded first, one packed max covers them, the running reference moves once,
+// and the exponentials are independent of each other (four accumulators).
+// Vectors past the tile are -inf, which adds nothing.
+constexpr int kVecBatch = 8;
+__device__ __forceinline__ uint4 neg_inf_vec(uint16_t) { return make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u); }
+__device__ __forceinline__ uint4 neg_inf_vec(float) { return make_uint4(0xFF800000u, 0xFF800000u, 0xFF800000u, 0xFF800000u); }
+__device__ __forceinline__ float vec_max(const uint4& q, uint16_t) {
+  const uint32_t mm = bf2_max_nan(bf2_max_nan(q.x, q.y), bf2_max_nan(q.z, q.w));
+  return fmax_nan(bf_lo(mm), bf_hi(mm));
+}
+__device__ __forceinline__ float vec_max(const uint4& q, float) {
+  return fmax_nan(fmax_nan(__uint_as_float(q.x), __uint_as_float(q.y)),
+                  fmax_nan(__uint_as_float(q.z), __uint_as_float(q.w)));
+}
+__device__ __forceinline__ void vec_exp_add(const uint4& q, float c, float nmc, float s[4], uint16_t) {
+  s[0] += ex2(fmaf(bf_lo(q.x), c, nmc));
+  s[1] += ex2(fmaf(bf_hi(q.x), c, nmc));
+  s[2] += ex2(fmaf(bf_lo(q.y), c, nmc));
+  s[3] += ex2(fmaf(bf_hi(q.y), c, nmc));
+  s[0] += ex2(fmaf(bf_lo(q.z), c, nmc));
+  s[1] += ex2(fmaf(bf_hi(q.z), c, nmc));
+  s[2] += ex2(fmaf(bf_lo(q.w), c, nmc));
+  s[3] += ex2(fmaf(bf_hi(q.w), c, nmc));
+}
+__device__ __forceinline__ void vec_exp_add(const uint4& q, float c, float nmc, float s[4], float) {
+  s[0] += ex2(fmaf(__uint_as_float(q.x), c, nmc));
+  s[1] += ex2(fmaf(__uint_as_float(q.y), c, nmc));
+  s[2] += ex2(fmaf(__uint_as_float(q.z), c, nmc));
+  s[3] += ex2(fmaf(__uint_as_float(q.w), c, nmc));
+}
+template <typename E>
+__device__ __forceinline__ void ms_tile(const uint4* sv, int nvec, int tid, float c, float& m, float s[4]) {
+  for (int v0 = tid; v0 < nvec; v0 += kVecBatch * kConsumerThreads) {
+    uint4 q[kVecBatch];
+#pragma unroll
+    for (int k = 0; k < kVecBatch; ++k) {
+      const int v = v0 + k * kConsumerThreads;
+      q[k] = v < nvec ? sv[v] : neg_inf_vec(E());
+    }
+    float vmax = vec_max(q[0], E());
+#pragma unroll
+    for (int k = 1; k < kVecBatch; ++k) vmax = fmax_nan(vmax, vec_max(q[k], E()));
+    const float nm = fmax_nan(m, vmax);
+    if (nm != m) {  // also taken when nm is NaN
+      const float f = rescale(m, nm, c);
+      s[0] *= f;
+      s[1] *= f;
+      s[2] *= f;
+      s[3] *= f;
+      m = nm;
+    }
+    if (m == -INFINITY) continue;
+    const float nmc = -mref(m, c);
+#pragma unroll
+    for (int k = 0; k < kVecBatch; ++k) vec_exp_add(q[k], c, nmc, s, E());
+  }
+}
+
 // ---------------------------------------------------- argmax (lowest index) --
 // (v, i): best value and its index; i < 0 means "nothing seen but -inf".
 __device__ __forceinline__ bool am_better(float v2, int64_t i2, float v1, int64_t i1) {
@@ -328,6 +389,30 @@ __device__ __forceinline__ void load8(const char* row, int64_t e, int64_t V, boo
   }
 }
 
+// Eight consecutive elements of a row piece staged in shared memory (the
+// piece starts at element e0 of the row; -inf past V).
+template <typename E>
+__device__ __forceinline__ void load8_smem(const char* piece, int64_t e_in_piece, int64_t e, int64_t V,
+                                           float out[8]) {
+  if (ET<E>::kSize == 2) {
+    const uint4 q = *reinterpret_cast<const uint4*>(piece + e_in_piece * 2);
+    out[0] = bf_lo(q.x); out[1] = bf_hi(q.x); out[2] = bf_lo(q.y); out[3] = bf_hi(q.y);
+    out[4] = bf_lo(q.z); out[5] = bf_hi(q.z); out[6] = bf_lo(q.w); out[7] = bf_hi(q.w);
+  } else {
+    const uint4 q0 = *reinterpret_cast<const uint4*>(piece + e_in_piece * 4);
+    const uint4 q1 = *reinterpret_cast<const uint4*>(piece + e_in_piece * 4 + 16);
+    out[0] = __uint_as_float(q0.x); out[1] = __uint_as_float(q0.y);
+    out[2] = __uint_as_float(q0.z); out[3] = __uint_as_float(q0.w);
+    out[4] = __uint_as_float(q1.x); out[5] = __uint_as_float(q1.y);
+    out[6] = __uint_as_float(q1.z); out[7] = __uint_as_float(q1.w);
+  }
+  if (e + 8 > V) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      if (e + k >= V) out[k] = -INFINITY;
+  }
+}
+
 // The sampler's weights over one row: w_v = p'(v) up to a constant, or, with
 // two rows, w_v = max(0, p'(v) - q'(v)).
 template <typename E, bool kResidual>
@@ -340,11 +425,21 @@ struct Weights {
   int topp;
   bool aligned;
   __device__ __forceinline__ void w8(int64_t e, float w[8]) const {
-    float lp[8];
+    float lp[8], lq[8];
     load8<E>(rp, e, V, aligned, lp);
+    if (kResidual) load8<E>(rq, e, V, aligned, lq);
+    weigh(lp, lq, w);
+  }
+  // The same weights for elements staged in shared memory.
+  __device__ __forceinline__ void w8_staged(const char* sp, const char* sq, int64_t e_in_piece, int64_t e,
+                                            float w[8]) const {
+    float lp[8], lq[8];
+    load8_smem<E>(sp, e_in_piece, e, V, lp);
+    if (kResidual) load8_smem<E>(sq, e_in_piece, e, V, lq);
+    weigh(lp, lq, w);
+  }
+  __device__ __forceinline__ void weigh(const float lp[8], const float lq[8], float w[8]) const {
     if (kResidual) {
-      float lq[8];
-      load8<E>(rq, e, V, aligned, lq);
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
         float ep = ex2(fmaf(lp[k], c, nMcp));
@@ -371,16 +466,95 @@ struct Weights {
 // The row is cut into cells of 256*m elements (at most kMaxCells cells); a
 // first pass sums each cell, one warp scans the cell sums to find the cell
 // holding the crossing, and rescans that cell alone.
-template <class WF>
-__device__ int64_t cdf_draw(const WF& wf, int64_t V, float u, Shared& sh, int tid) {
+// Pass A from shared memory: the row (or the two rows) is moved in pieces of
+// whole cells into the two halves of the idle tile ring by bulk copies, the
+// next piece landing while the current one is summed. Returns false (having
+// touched nothing) when it cannot run: unaligned rows, or a ring too small for
+// one cell per row.
+template <typename E, class WF>
+__device__ bool cells_staged(const WF& wf, int64_t V, int64_t CE, int ncells, char* ring, size_t ring_bytes,
+                             Shared& sh, int tid, const uint32_t* ctl_status) {
+  constexpr int S = ET<E>::kSize;
+  const int nrows = wf.rq ? 2 : 1;
+  if (!wf.aligned || ring_bytes == 0) return false;
+  const size_t half = (ring_bytes / 2) & ~size_t(15);
+  int64_t cells_per_piece = (int64_t)(half / nrows / S) / CE;
+  if (cells_per_piece < 1) return false;
+  const int64_t P = cells_per_piece * CE;  // elements per row per piece
+  const int64_t npieces = (V + P - 1) / P;
+  const int warp = tid >> 5, lane = tid & 31;
+  cbar();  // everyone has read dcount, and nothing reads the ring any more
+  const uint32_t c0 = sh.dcount[0], c1 = sh.dcount[1];
+  auto issue = [&](int64_t k) {  // thread 0 only
+    const int buf = (int)(k & 1);
+    const int64_t e0 = k * P;
+    const int64_t n = min(P, V - e0);
+    const uint32_t bytes = (uint32_t)(n * S);
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    mbar_arrive_expect_tx(&sh.dbar[buf], bytes * (uint32_t)nrows);
+    char* dst = ring + (size_t)buf * half;
+    bulk_g2s(dst, wf.rp + e0 * S, bytes, &sh.dbar[buf]);
+    if (nrows == 2) bulk_g2s(dst + (size_t)P * S, wf.rq + e0 * S, bytes, &sh.dbar[buf]);
+  };
+  if (tid == 0) {
+    issue(0);
+    if (npieces > 1) issue(1);
+  }
+  bool ok = true;
+  for (int64_t k = 0; k < npieces; ++k) {
+    const int buf = (int)(k & 1);
+    const uint32_t use = (buf ? c1 : c0) + (uint32_t)(k >> 1);  // uses of this barrier before this one
+    if (!mbar_wait(&sh.dbar[buf], use & 1u)) ok = false;
+    if (cbar_or(!ok)) {
+      ok = false;
+      break;
+    }
+    const char* sp = ring + (size_t)buf * half;
+    const char* sq = sp + (size_t)P * S;
+    const int64_t e0 = k * P;
+    const int cfirst = (int)(e0 / CE);
+    const int clast = (int)min((int64_t)ncells, (e0 + P) / CE + ((e0 + P) % CE ? 1 : 0));
+    const int64_t m = CE / 256;
+    for (int cc = cfirst + warp; cc < clast; cc += kConsumerWarps) {
+      float acc = 0.f;
+      for (int64_t q = 0; q < m; ++q) {
+        const int64_t e = (int64_t)cc * CE + (lane * m + q) * 8;
+        float w[8];
+        wf.w8_staged(sp, sq, e - e0, e, w);
+        acc += ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+      }
+      acc = warp_sum(acc);
+      if (lane == 0) sh.cells[cc] = acc;
+    }
+    cbar();  // the half is free again
+    if (tid == 0 && k + 2 < npieces) issue(k + 2);
+  }
+  if (tid == 0) {
+    const int64_t used0 = (npieces + 1) / 2, used1 = npieces / 2;
+    sh.dcount[0] = c0 + (uint32_t)used0;
+    sh.dcount[1] = c1 + (uint32_t)used1;
+    if (!ok) {  // a wait ran out: let what is in flight land, then report
+      atomicOr(const_cast<uint32_t*>(ctl_status), kStatusTimeout);
+      (void)mbar_wait(&sh.dbar[0], (c0 + (uint32_t)used0 - 1u) & 1u);
+      if (used1) (void)mbar_wait(&sh.dbar[1], (c1 + (uint32_t)used1 - 1u) & 1u);
+    }
+  }
+  cbar();
+  return ok;
+}
+
+template <typename E, class WF>
+__device__ int64_t cdf_draw(const WF& wf, int64_t V, float u, Shared& sh, int tid, char* ring, size_t ring_bytes,
+                            const uint32_t* ctl_status) {
   const int warp = tid >> 5, lane = tid & 31;
   const int64_t m = (V + 256LL * kMaxCells - 1) / (256LL * kMaxCells) > 1 ? (V + 256LL * kMaxCells - 1) / (256LL * kMaxCells) : 1;
   const int64_t CE = 256 * m;
   const int ncells = (int)((V + CE - 1) / CE);
-  // Pass A: cell sums. Each warp takes four cells at a time, so that their
-  // loads are in flight together.
+  const bool staged = cells_staged<E>(wf, V, CE, ncells, ring, ring_bytes, sh, tid, ctl_status);
+  // Pass A without staging: cell sums from global memory, four cells per warp
+  // at a time so that their loads are in flight together.
   constexpr int U = 4;
-  for (int c0 = warp; c0 < ncells; c0 += kConsumerWarps * U) {
+  for (int c0 = staged ? ncells : warp; c0 < ncells; c0 += kConsumerWarps * U) {
     float sum[U];
 #pragma unroll
     for (int k = 0; k < U; ++k) {
@@ -706,17 +880,21 @@ __device__ void seq_sample(const Params& p, Shared& sh, int64_t b, int tid) {
   const RowStat rp = rs_load(p, b * p.RS + j);
   const bool aligned = (p.V * ET<E>::kSize) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.a) & 15) == 0 &&
                        (reinterpret_cast<uintptr_t>(p.d) & 15) == 0;
+  // The tile ring is idle while sequence tails run (they run only after the
+  // CTA's streaming is over), so the draw stages its rows there.
+  char* ring = reinterpret_cast<char*>(&sh) - (size_t)p.stages * kTileBytes;
+  const size_t ring_bytes = (size_t)p.stages * kTileBytes;
   int64_t t = -1;
   if (j < K) {
     const RowStat rq = rs_load(p, b * p.RS + K + 1 + j);
     Weights<E, true> wf{row_ptr<E, kSample>(p, b, j), row_ptr<E, kSample>(p, b, K + 1 + j), p.V, c, -mref(rp.M, c),
                         -mref(rq.M, c), 1.f / rp.cum, 1.f / rq.cum, rp.tau, rq.tau, p.topp, aligned};
-    t = cdf_draw(wf, p.V, uK, sh, tid);
+    t = cdf_draw<E>(wf, p.V, uK, sh, tid, ring, ring_bytes, p.ctl + 3);
   }
   if (t < 0) {  // bonus row, or a residual that is all zero: draw from p'_j
     Weights<E, false> wf{row_ptr<E, kSample>(p, b, j), nullptr, p.V, c, -mref(rp.M, c), 0.f, 1.f, 0.f, rp.tau, 0u,
                          p.topp, aligned};
-    t = cdf_draw(wf, p.V, uK, sh, tid);
+    t = cdf_draw<E>(wf, p.V, uK, sh, tid, ring, ring_bytes, p.ctl + 3);
   }
   for (int i = tid; i <= K; i += kConsumerThreads)
     out[i] = i < j ? p.tokens[b * K + i] : (i == j ? (int32_t)t : -1);
@@ -859,11 +1037,33 @@ __device__ __forceinline__ void tail_enqueue(const Params& p, int64_t b) {
   st_release_gpu(p.tail_q + k, (uint32_t)(b + 1));
 }
 
-// One more row of sequence b is final; the last one queues the sequence tail.
-__device__ __forceinline__ void seq_arrive(const Params& p, int64_t b) {
+// A tail that this CTA runs itself (its streaming is over, so running it here
+// holds up nothing): the queue entry is only marked as claimed, which keeps
+// the count of entries equal to the number of sequences.
+constexpr uint32_t kTailClaimed = 0x80000000u;
+__device__ __forceinline__ void tail_claim(const Params& p, int64_t b) {
+  const uint32_t k = atomicAdd(p.ctl + 4, 1u);
+  st_release_gpu(p.tail_q + k, kTailClaimed | (uint32_t)(b + 1));
+}
+
+// One more row of sequence b is final. Returns true if it was the last one.
+__device__ __forceinline__ bool seq_row_final(const Params& p, int64_t b) {
   const uint32_t old = atom_add_acq_rel(p.seq_cnt + b, 1u);
   if (old == (uint32_t)p.RS - 1u) {
     p.seq_cnt[b] = 0u;
+    return true;
+  }
+  return false;
+}
+
+// Publisher side: the last row of a sequence queues its tail, globally while
+// this CTA still streams, locally once it does not.
+__device__ __forceinline__ void seq_arrive(const Params& p, Shared& sh, int64_t b, bool local) {
+  if (!seq_row_final(p, b)) return;
+  if (local) {
+    enqueue_task(p, sh, -(b + 1), 0.f, 0.f);
+    tail_claim(p, b);
+  } else {
     tail_enqueue(p, b);
   }
 }
@@ -872,7 +1072,7 @@ __device__ __forceinline__ void seq_arrive(const Params& p, int64_t b) {
 // value and index for argmax). Finish the row here unless it needs the
 // collective top-p pass.
 template <typename E, int MODE>
-__device__ void publisher_row_done(const Params& p, Shared& sh, int64_t row, float2 r) {
+__device__ void publisher_row_done(const Params& p, Shared& sh, int64_t row, float2 r, bool local) {
   if (MODE == kSample) {
     const float m = r.x, s = r.y;
     const bool valid = (m > -INFINITY) && (m < INFINITY);
@@ -890,12 +1090,12 @@ __device__ void publisher_row_done(const Params& p, Shared& sh, int64_t row, flo
     rs.tau = (uint32_t)(i < 0 ? 0 : i);  // all -inf: every element ties, index 0 wins
     rs_store(p, row, rs);
   }
-  seq_arrive(p, row / p.RS);
+  seq_arrive(p, sh, row / p.RS, local);
 }
 
 // Publisher side: every chunk of `row` is published; combine the partials.
 template <typename E, int MODE>
-__device__ void publisher_finish_row(const Params& p, Shared& sh, int64_t row) {
+__device__ void publisher_finish_row(const Params& p, Shared& sh, int64_t row, bool local) {
   p.row_cnt[row] = 0u;
   const float2* part = p.part + row * p.NC;
   if (MODE == kSample) {
@@ -907,7 +1107,7 @@ __device__ void publisher_finish_row(const Params& p, Shared& sh, int64_t row) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) ms_combine(m, s, v[j].x, v[j].y, p.c);
     }
-    publisher_row_done<E, MODE>(p, sh, row, make_float2(m, s));
+    publisher_row_done<E, MODE>(p, sh, row, make_float2(m, s), local);
   } else {
     float v = -INFINITY;
     int64_t i = -1;
@@ -928,25 +1128,43 @@ __device__ void publisher_finish_row(const Params& p, Shared& sh, int64_t row) {
       }
     }
     publisher_row_done<E, MODE>(p, sh, row,
-                                make_float2(nan ? __int_as_float(0x7fc00000) : v, __int_as_float((int)i)));
+                                make_float2(nan ? __int_as_float(0x7fc00000) : v, __int_as_float((int)i)), local);
   }
 }
 
-// Consumer side: one queued top-p cut, run by all 256 consumer threads.
+// Consumer side: one queued task, run by all 256 consumer threads: a top-p
+// cut (row >= 0) or, once streaming is over, a sequence tail (-(b+1)).
+// `local` says the CTA's streaming is over.
 template <typename E, int MODE>
-__device__ void run_task(const Params& p, Shared& sh, int64_t row, float m, float s, int tid) {
+__device__ void run_task(const Params& p, Shared& sh, int64_t task, float m, float s, int tid, bool local) {
+  if (task < 0) {
+    seq_tail<E, MODE>(p, sh, -task - 1, tid);
+    return;
+  }
   if (MODE == kSample) {
-    const int64_t b = row / p.RS;
-    const int r = (int)(row % p.RS);
+    const int64_t b = task / p.RS;
+    const int r = (int)(task % p.RS);
     __threadfence();
     uint32_t tau = 0u;
     float cum = s;
     topp_cut<E>(p, sh, row_ptr<E, MODE>(p, b, r), m, s, tid, tau, cum);
     if (tid == 0) {
-      store_sample_row<E>(p, row, m, s, cum, tau);
-      seq_arrive(p, b);
+      store_sample_row<E>(p, task, m, s, cum, tau);
+      int run_here = 0;
+      if (seq_row_final(p, b)) {
+        if (local) {
+          tail_claim(p, b);
+          run_here = 1;
+        } else {
+          tail_enqueue(p, b);
+        }
+      }
+      sh.flag = run_here;
     }
     cbar();
+    const int run_here = sh.flag;
+    cbar();
+    if (run_here) seq_tail<E, MODE>(p, sh, b, tid);
   }
 }
 
@@ -967,6 +1185,7 @@ __device__ void drain_tails(const Params& p, Shared& sh, int tid) {
           while (v == 0u && globaltimer_ns() - t0 < kWaitLimitNs) v = ld_acquire_gpu(p.tail_q + k);
         }
         if (v == 0u) atomicOr(p.ctl + 3, kStatusTimeout);
+        else if (v & kTailClaimed) b = -2;  // run by the CTA that completed it
         else b = (int64_t)v - 1;
         p.tail_q[k] = 0u;
       }
@@ -975,16 +1194,17 @@ __device__ void drain_tails(const Params& p, Shared& sh, int tid) {
     cbar();
     const int64_t b = sh.bl[1];
     cbar();
+    if (b == -2) continue;
     if (b < 0) return;
     seq_tail<E, MODE>(p, sh, b, tid);
   }
 }
 
 template <typename E, int MODE>
-__device__ __forceinline__ int drain_tasks(const Params& p, Shared& sh, int head, int snap, int tid) {
+__device__ __forceinline__ int drain_tasks(const Params& p, Shared& sh, int head, int snap, int tid, bool local) {
   while (head < snap) {
     const int i = head % kTaskSlots;
-    run_task<E, MODE>(p, sh, sh.tq[i], sh.tq_m[i], sh.tq_s[i], tid);  // top-p cuts
+    run_task<E, MODE>(p, sh, sh.tq[i], sh.tq_m[i], sh.tq_s[i], tid, local);
     ++head;
   }
   if (tid == 0) *reinterpret_cast<volatile int*>(&sh.tq_head) = head;
@@ -1067,8 +1287,17 @@ __device__ void producer_loop(const Params& p, char* ring, Shared& sh) {
 // the next chunk). The last chunk of a row finishes the row.
 template <typename E, int MODE>
 __device__ void publisher_loop(const Params& p, Shared& sh) {
+  // The row a chunk completes is finished one chunk later, so that the
+  // counter's round trip overlaps the next chunk and the CTA's last row is
+  // known to be its last (its sequence tail can then run here).
   int64_t pend_row = -1;
   uint32_t pend_old = 0u;
+  float2 pend_res = make_float2(0.f, 0.f);
+  auto finish_pending = [&](bool local) {
+    if (pend_row < 0 || pend_old != (uint32_t)(p.NC - 1)) return;
+    if (p.NC == 1) publisher_row_done<E, MODE>(p, sh, pend_row, pend_res, local);
+    else publisher_finish_row<E, MODE>(p, sh, pend_row, local);
+  };
   for (int64_t c = 0;; ++c) {
     const int ps = (int)(c % kPartSlots);
     const uint32_t pph = (uint32_t)((c / kPartSlots) & 1);
@@ -1100,17 +1329,18 @@ __device__ void publisher_loop(const Params& p, Shared& sh) {
     }
     const int64_t row = sh.prow[ps];
     mbar_arrive(&sh.pempty[ps]);
-    if (p.NC == 1) {  // the chunk is the whole row: no partial to combine
-      publisher_row_done<E, MODE>(p, sh, row, res);
-      continue;
+    uint32_t old = 0u;  // a row that is a single chunk is complete with it
+    if (p.NC > 1) {
+      p.part[w] = res;
+      old = atom_add_acq_rel(p.row_cnt + row, 1u);
     }
-    p.part[w] = res;
-    const uint32_t old = atom_add_acq_rel(p.row_cnt + row, 1u);
-    if (pend_row >= 0 && pend_old == (uint32_t)(p.NC - 1)) publisher_finish_row<E, MODE>(p, sh, pend_row);
+    finish_pending(false);
     pend_row = row;
     pend_old = old;
+    pend_res = res;
   }
-  if (pend_row >= 0 && pend_old == (uint32_t)(p.NC - 1)) publisher_finish_row<E, MODE>(p, sh, pend_row);
+  // The consumers are done streaming: a sequence completed from here on runs here.
+  finish_pending(true);
   mbar_arrive(&sh.pdone);
 }
 
@@ -1122,7 +1352,8 @@ template <typename E, int MODE>
 __device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int tid) {
   constexpr int PV = ET<E>::kPerVec;
   const int warp = tid >> 5, lane = tid & 31;
-  float m = -INFINITY, s0 = 0.f, s1 = 0.f;  // sampling: online (max, sum)
+  float m = -INFINITY;                      // sampling: online (max, sum)
+  float sa[4] = {0.f, 0.f, 0.f, 0.f};
   float av = -INFINITY;                     // argmax: value, index, NaN seen
   int64_t ai = -1;
   bool an = false;
@@ -1148,19 +1379,38 @@ __device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int
     const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)cur * kTileBytes);
     const int nvec = (int)(t.ibytes >> 4);
     if (MODE == kSample) {
-      for (int v = tid; v < nvec; v += kConsumerThreads) ms_vec(m, s0, s1, sv[v], p.c, E());
+      ms_tile<E>(sv, nvec, tid, p.c, m, sa);
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.empty[cur]);
       if (t.nh | t.nt) {
         // head and tail elements (rows not 16-byte aligned) join one
         // accumulator, so that a new maximum among them rescales everything
-        s0 += s1;
-        s1 = 0.f;
-        if (tid < t.nh) ms_scalar(m, s0, ET<E>::load(t.row, t.e0 + tid), p.c);
-        if (tid >= 32 && tid < 32 + t.nt) ms_scalar(m, s0, ET<E>::load(t.row, t.e1 - t.nt + (tid - 32)), p.c);
+        sa[0] += (sa[1] + sa[2]) + sa[3];
+        sa[1] = sa[2] = sa[3] = 0.f;
+        if (tid < t.nh) ms_scalar(m, sa[0], ET<E>::load(t.row, t.e0 + tid), p.c);
+        if (tid >= 32 && tid < 32 + t.nt) ms_scalar(m, sa[0], ET<E>::load(t.row, t.e1 - t.nt + (tid - 32)), p.c);
       }
     } else {
-      for (int q = tid; q < nvec; q += kConsumerThreads) am_vec(av, ai, an, sv[q], t.ie0 + (int64_t)q * PV, E());
+      for (int v0 = tid; v0 < nvec; v0 += kVecBatch * kConsumerThreads) {
+        uint4 q[kVecBatch];
+#pragma unroll
+        for (int k = 0; k < kVecBatch; ++k) {
+          const int v = v0 + k * kConsumerThreads;
+          q[k] = v < nvec ? sv[v] : neg_inf_vec(E());
+        }
+        float vmax = vec_max(q[0], E());
+#pragma unroll
+        for (int k = 1; k < kVecBatch; ++k) vmax = fmax_nan(vmax, vec_max(q[k], E()));
+        if (vmax != vmax) {
+          an = true;
+        } else if (vmax > av || ai < 0) {  // a new best somewhere in the batch: find its first occurrence
+#pragma unroll
+          for (int k = 0; k < kVecBatch; ++k) {
+            const int v = v0 + k * kConsumerThreads;
+            if (v < nvec) am_vec(av, ai, an, q[k], t.ie0 + (int64_t)v * PV, E());
+          }
+        }
+      }
       __syncwarp();
       if (lane == 0) mbar_arrive(&sh.empty[cur]);
       if (tid < t.nh) am_scalar(av, ai, an, ET<E>::load(t.row, t.e0 + tid), t.e0 + tid);
@@ -1177,7 +1427,7 @@ __device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int
     float rm, rs_;
     int64_t ri = -1;
     if (MODE == kSample) {
-      float s = s0 + s1;
+      float s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
       for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
         ms_combine(m, s, m2, s2, p.c);
@@ -1185,7 +1435,7 @@ __device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int
       rm = m;
       rs_ = s;
       m = -INFINITY;
-      s0 = s1 = 0.f;
+      sa[0] = sa[1] = sa[2] = sa[3] = 0.f;
     } else {
       for (int o = 16; o > 0; o >>= 1) {
         const float v2 = __shfl_xor_sync(0xffffffffu, av, o);
@@ -1224,7 +1474,7 @@ __device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int
       if (tid == 0) atomicOr(p.ctl + 3, kStatusTimeout);
       return;
     }
-    head = drain_tasks<E, MODE>(p, sh, head, sh.snap[par], tid);
+    head = drain_tasks<E, MODE>(p, sh, head, sh.snap[par], tid, false);
   }
   // End of work (or a wait that ran out): tell the publisher, wait for it to
   // finish, and run what it queued.
@@ -1250,7 +1500,7 @@ __device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int
     if (tid == 0) atomicOr(p.ctl + 3, kStatusTimeout);
     return;
   }
-  drain_tasks<E, MODE>(p, sh, head, sh.snap[0], tid);
+  drain_tasks<E, MODE>(p, sh, head, sh.snap[0], tid, true);
   drain_tails<E, MODE>(p, sh, tid);
   // The last CTA out re-arms the tail queue for the next call.
   if (tid == 0) {
@@ -1281,6 +1531,9 @@ __global__ void __launch_bounds__(kAllThreads, 2) verify_kernel(const Params p) 
       mbar_init(&sh.pempty[i], 1u);
     }
     mbar_init(&sh.pdone, 1u);
+    mbar_init(&sh.dbar[0], 1u);
+    mbar_init(&sh.dbar[1], 1u);
+    sh.dcount[0] = sh.dcount[1] = 0u;
     sh.tq_tail = 0;
     sh.tq_head = 0;
     fence_mbar_init();
