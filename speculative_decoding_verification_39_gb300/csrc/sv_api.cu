@@ -99,6 +99,9 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   // them, and of near-equal size within a row.
   int64_t ct = rows_total * p.NT / (slots * 4);
   ct = ct < 1 ? 1 : (ct > 8 ? 8 : ct);
+  // A row of up to four tiles is one chunk: its CTA finishes it alone, with
+  // no partial to store and no row counter to count it against.
+  if (p.NT <= 4) ct = p.NT;
   if (ct > p.NT) ct = p.NT;
   p.NC = (p.NT + ct - 1) / ct;
   p.CT = (p.NT + p.NC - 1) / p.NC;

@@ -515,16 +515,37 @@ __device__ bool cells_staged(const WF& wf, int64_t V, int64_t CE, int ncells, ch
     const int cfirst = (int)(e0 / CE);
     const int clast = (int)min((int64_t)ncells, (e0 + P) / CE + ((e0 + P) % CE ? 1 : 0));
     const int64_t m = CE / 256;
-    for (int cc = cfirst + warp; cc < clast; cc += kConsumerWarps) {
-      float acc = 0.f;
-      for (int64_t q = 0; q < m; ++q) {
-        const int64_t e = (int64_t)cc * CE + (lane * m + q) * 8;
-        float w[8];
-        wf.w8_staged(sp, sq, e - e0, e, w);
-        acc += ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+    // A warp's cells of the piece, four at a time: all their weights first,
+    // then the four warp reductions interleaved.
+    constexpr int UC = 4;
+    for (int cb = cfirst + warp; cb < clast; cb += kConsumerWarps * UC) {
+      float acc[UC];
+#pragma unroll
+      for (int k = 0; k < UC; ++k) {
+        const int cc = cb + k * kConsumerWarps;
+        float a = 0.f;
+        if (cc < clast) {
+          for (int64_t q = 0; q < m; ++q) {
+            const int64_t e = (int64_t)cc * CE + (lane * m + q) * 8;
+            float w[8];
+            wf.w8_staged(sp, sq, e - e0, e, w);
+            a += ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+          }
+        }
+        acc[k] = a;
       }
-      acc = warp_sum(acc);
-      if (lane == 0) sh.cells[cc] = acc;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+        for (int k = 0; k < UC; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < UC; ++k) {
+          const int cc = cb + k * kConsumerWarps;
+          if (cc < clast) sh.cells[cc] = acc[k];
+        }
+      }
     }
     cbar();  // the half is free again
     if (tid == 0 && k + 2 < npieces) issue(k + 2);
@@ -618,8 +639,13 @@ __device__ int64_t cdf_draw(const WF& wf, int64_t V, float u, Shared& sh, int ti
       for (int64_t q = 0; q < m; ++q) {
         float w[8];
         wf.w8(base + q * 8, w);
+        if (q == 0) {  // kept in shared memory for the walk below (no second load)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) sh.hist.f[lane * 8 + k] = w[k];
+        }
         ls2 += ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
       }
+      __syncwarp();
       const float incl2 = warp_incl_scan(ls2, lane);
       const float excl2 = incl2 - ls2;
       int64_t mine = -1;
@@ -632,7 +658,12 @@ __device__ int64_t cdf_draw(const WF& wf, int64_t V, float u, Shared& sh, int ti
             int64_t lastpos = -1;
             for (int64_t q = 0; q < m && mine < 0; ++q) {
               float w[8];
-              wf.w8(base + q * 8, w);
+              if (q == 0) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) w[k] = sh.hist.f[lane * 8 + k];
+              } else {
+                wf.w8(base + q * 8, w);
+              }
 #pragma unroll
               for (int k = 0; k < 8; ++k) {
                 if (mine < 0) {

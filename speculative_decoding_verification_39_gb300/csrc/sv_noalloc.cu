@@ -117,6 +117,7 @@ extern "C" int sv_verify_sample_noalloc(const void* target_logits, const void* d
   const int64_t slots = (int64_t)sms * kCtasPerSm;
   int64_t ct = rows * p.NT / (slots * 4);
   ct = ct < 1 ? 1 : (ct > 8 ? 8 : ct);
+  if (p.NT <= 4) ct = p.NT;  // as sv_verify_sample chooses
   if (ct > p.NT) ct = p.NT;
   p.NC = (p.NT + ct - 1) / ct;
   p.CT = (p.NT + p.NC - 1) / p.NC;
