@@ -120,10 +120,14 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   p.tail_q = p.seq_cnt + p.B;
   p.part = reinterpret_cast<float2*>(b + data_offset(sc));
   p.rowstat = reinterpret_cast<float4*>(b + data_offset(sc) + part_bytes);
+  // Short rows: one CTA per sequence, the whole sequence staged in shared memory.
+  const bool seq_mode = mode == sv::kSample && !p.topp && sv::seq_mode_fits(p.K, p.V, esz) &&
+                        aligned_to(p.a, 16) && aligned_to(p.d, 16);
   int64_t grid = (int64_t)sm_count(dev) * g_ctas_per_sm.load();
-  if (grid > p.W) grid = p.W;
+  const int64_t items = seq_mode ? p.B : p.W;
+  if (grid > items) grid = items;
   if (grid < 1) grid = 1;
-  cudaError_t e = sv::launch(p, dtype, mode, (int)grid, stream);
+  cudaError_t e = seq_mode ? sv::launch_seq(p, dtype, (int)grid, stream) : sv::launch(p, dtype, mode, (int)grid, stream);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   g_launches.fetch_add(1);
   return SV_OK;

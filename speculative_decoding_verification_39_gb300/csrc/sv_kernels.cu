@@ -1582,6 +1582,352 @@ __global__ void __launch_bounds__(kAllThreads, 2) verify_kernel(const Params p) 
   consumer_loop<E, MODE>(p, ring, sh, tid);
 }
 
+// ------------------------------------------- whole sequences in one CTA -----
+//
+// For short rows (a whole sequence of 2K+1 rows fits in 48 KB), one work item
+// is one sequence: the producer moves its target block and its draft block
+// into a shared-memory stage with two bulk copies; the consumers compute every
+// row's (max, sum), the accept scan and the draw from shared memory. No row or
+// sequence crosses a CTA, so there are no partials, counters or queues.
+
+constexpr int kSeqStageBytes = 49152;
+constexpr int kSeqStages = 2;
+constexpr int kSeqMaxRows = 64;
+constexpr int kSeqThreads = kConsumerThreads + 32;
+constexpr int kSeqMaxCells = kSeqStageBytes / 2 / 256;
+
+struct alignas(16) SeqShared {
+  uint64_t full[kSeqStages];
+  uint64_t empty[kSeqStages];
+  int64_t seq[kSeqStages];  // sequence in the stage (-1: no more work)
+  float rm[kSeqMaxRows];    // per row: max and sum relative to mref(max)
+  float rsum[kSeqMaxRows];
+  float cells[kSeqMaxCells];
+  float wl[256];            // the crossing cell's weights
+  float bf[4];
+  int bi[4];
+  int64_t bl[2];
+};
+
+size_t seq_shared_bytes() { return (size_t)kSeqStages * kSeqStageBytes + sizeof(SeqShared); }
+
+template <typename E>
+__device__ __forceinline__ float smem_elem(const char* row, int64_t e) {
+  if (ET<E>::kSize == 2)
+    return __uint_as_float((uint32_t)reinterpret_cast<const uint16_t*>(row)[e] << 16);
+  return reinterpret_cast<const float*>(row)[e];
+}
+
+template <typename E>
+__device__ void seq_producer(const Params& p, char* ring, SeqShared& sh) {
+  constexpr int S = ET<E>::kSize;
+  unsigned long long* next = reinterpret_cast<unsigned long long*>(p.ctl);
+  const uint32_t tbytes = (uint32_t)((p.K + 1) * p.V * S), dbytes = (uint32_t)(p.K * p.V * S);
+  int stage = 0;
+  uint32_t ph = 0u;
+  bool wrapped = false, aborted = false;
+  int last_parity[kSeqStages] = {-1, -1};
+  int64_t b = (int64_t)atomicAdd(next, 1ull);
+  for (;;) {
+    const int64_t bn = b < p.B ? (int64_t)atomicAdd(next, 1ull) : b;
+    if (wrapped && !mbar_wait(&sh.empty[stage], ph ^ 1u)) {
+      aborted = true;
+      break;
+    }
+    if (b >= p.B) {
+      sh.seq[stage] = -1;
+      mbar_arrive(&sh.full[stage]);
+      break;
+    }
+    sh.seq[stage] = b;
+    char* dst = ring + (size_t)stage * kSeqStageBytes;
+    mbar_arrive_expect_tx(&sh.full[stage], tbytes + dbytes);
+    bulk_g2s(dst, p.a + b * (int64_t)tbytes, tbytes, &sh.full[stage]);
+    bulk_g2s(dst + tbytes, p.d + b * (int64_t)dbytes, dbytes, &sh.full[stage]);
+    last_parity[stage] = (int)ph;
+    if (++stage == kSeqStages) {
+      stage = 0;
+      ph ^= 1u;
+      wrapped = true;
+    }
+    b = bn;
+  }
+  if (aborted) {
+    atomicOr(p.ctl + 3, kStatusTimeout);
+    for (int i = 0; i < kSeqStages; ++i)
+      if (last_parity[i] >= 0) (void)mbar_wait(&sh.full[i], (uint32_t)last_parity[i]);
+  }
+  __threadfence();
+  const uint32_t prev = atomicAdd(p.ctl + 2, 1u);
+  if (prev == gridDim.x - 1) {
+    *next = 0ull;
+    p.ctl[2] = 0u;
+    __threadfence();
+  }
+}
+
+// One staged sequence, by the 256 consumer threads.
+template <typename E>
+__device__ void seq_in_smem(const Params& p, SeqShared& sh, const char* st, int64_t b, int tid) {
+  constexpr int S = ET<E>::kSize;
+  constexpr int PV = ET<E>::kPerVec;
+  const int warp = tid >> 5, lane = tid & 31;
+  const int K = p.K, R = p.RS;
+  const int64_t V = p.V;
+  const float c = p.c;
+  const int64_t tb = (K + 1) * V * S;
+  auto rowp = [&](int r) { return r <= K ? st + r * V * S : st + tb + (r - K - 1) * V * S; };
+  // ---- per-row (max, sum): one warp per row
+  const int nvec = (int)(V / PV);
+  for (int r = warp; r < R; r += kConsumerWarps) {
+    const uint4* rv = reinterpret_cast<const uint4*>(rowp(r));
+    float m = -INFINITY, sa[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int v0 = lane; v0 < nvec; v0 += 32 * kVecBatch) {
+      uint4 q[kVecBatch];
+#pragma unroll
+      for (int k = 0; k < kVecBatch; ++k) {
+        const int v = v0 + 32 * k;
+        q[k] = v < nvec ? rv[v] : neg_inf_vec(E());
+      }
+      float vmax = vec_max(q[0], E());
+#pragma unroll
+      for (int k = 1; k < kVecBatch; ++k) vmax = fmax_nan(vmax, vec_max(q[k], E()));
+      const float nm = fmax_nan(m, vmax);
+      if (nm != m) {
+        const float f = rescale(m, nm, c);
+        sa[0] *= f; sa[1] *= f; sa[2] *= f; sa[3] *= f;
+        m = nm;
+      }
+      if (m == -INFINITY) continue;
+      const float nmc = -mref(m, c);
+#pragma unroll
+      for (int k = 0; k < kVecBatch; ++k) vec_exp_add(q[k], c, nmc, sa, E());
+    }
+    float sum = (sa[0] + sa[1]) + (sa[2] + sa[3]);
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+      ms_combine(m, sum, m2, s2, c);
+    }
+    if (lane == 0) {
+      sh.rm[r] = m;
+      sh.rsum[r] = sum;
+    }
+  }
+  if (tid == 0) sh.bi[1] = K;
+  cbar();
+  // ---- row stats out, validity, accept scan
+  int bad = 0;
+  for (int r = tid; r < R; r += kConsumerThreads) {
+    const float M = sh.rm[r], s = sh.rsum[r];
+    const bool valid = (M > -INFINITY) && (M < INFINITY);
+    if (!valid) bad = 1;
+    if (p.out_row_stats) {
+      float4 o;
+      o.x = valid ? __fdiv_rn(M, p.T) : __int_as_float(0x7fc00000);
+      o.y = valid ? (mref(M, c) + lg2(s)) * 0.69314718055994531f : __int_as_float(0x7fc00000);
+      o.z = valid ? 1.f : __int_as_float(0x7fc00000);
+      o.w = -INFINITY;
+      reinterpret_cast<float4*>(p.out_row_stats)[b * R + r] = o;
+    }
+  }
+  for (int i = tid; i < K; i += kConsumerThreads) {
+    const int32_t x = p.tokens[b * K + i];
+    const float u = p.uniforms[b * (K + 1) + i];
+    if (x < 0 || (int64_t)x >= V || !(u >= 0.f && u < 1.f)) {
+      bad = 1;
+      continue;
+    }
+    const float Mp = sh.rm[i], Mq = sh.rm[K + 1 + i];
+    if (!(Mp > -INFINITY && Mp < INFINITY && Mq > -INFINITY && Mq < INFINITY)) continue;  // counted above
+    const float lp = smem_elem<E>(rowp(i), x), lq = smem_elem<E>(rowp(K + 1 + i), x);
+    float alpha;
+    if (lp == -INFINITY) alpha = 0.f;
+    else if (lq == -INFINITY) alpha = 1.f;
+    else alpha = fminf(1.f, ex2(fmaf(lp, c, -mref(Mp, c)) - fmaf(lq, c, -mref(Mq, c))) * (sh.rsum[K + 1 + i] / sh.rsum[i]));
+    if (!(u < alpha)) atomicMin(&sh.bi[1], i);
+  }
+  const float uK = p.uniforms[b * (K + 1) + K];
+  if (tid == 0 && !(uK >= 0.f && uK < 1.f)) bad = 1;
+  bad = cbar_or(bad);
+  const int j = sh.bi[1];
+  int32_t* out = p.out_tokens + b * (K + 1);
+  if (bad) {
+    for (int i = tid; i <= K; i += kConsumerThreads) out[i] = -1;
+    if (tid == 0) {
+      p.out_accept_len[b] = -1;
+      atomicOr(p.ctl + 3, kStatusInput);
+    }
+    return;
+  }
+  // ---- the draw, from shared memory: cells of 256 elements, eight per lane
+  const char* rp = rowp(j);
+  const char* rq = j < K ? rowp(K + 1 + j) : nullptr;
+  const float nMp = -mref(sh.rm[j], c), ip = 1.f / sh.rsum[j];
+  const float nMq = rq ? -mref(sh.rm[K + 1 + j], c) : 0.f, iq = rq ? 1.f / sh.rsum[K + 1 + j] : 0.f;
+  const int ncells = (int)((V + 255) / 256);
+  int64_t t = -1;
+  for (int attempt = 0; attempt < 2 && t < 0; ++attempt) {
+    const bool resid = (attempt == 0) && rq != nullptr;
+    auto w8 = [&](int64_t e, float w[8]) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int64_t ek = e + k;
+        if (ek >= V) {
+          w[k] = 0.f;
+          continue;
+        }
+        const float ep = ex2(fmaf(smem_elem<E>(rp, ek), c, nMp));
+        w[k] = resid ? fmaxf(0.f, fmaf(ep, ip, -ex2(fmaf(smem_elem<E>(rq, ek), c, nMq)) * iq)) : ep;
+      }
+    };
+    for (int cc = warp; cc < ncells; cc += kConsumerWarps) {
+      float w[8];
+      w8((int64_t)cc * 256 + lane * 8, w);
+      const float a = warp_sum(((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7])));
+      if (lane == 0) sh.cells[cc] = a;
+    }
+    cbar();
+    if (warp == 0) {
+      const int cpl = (ncells + 31) / 32;
+      const int c0 = min(ncells, lane * cpl), c1 = min(ncells, c0 + cpl);
+      float ls = 0.f;
+      for (int cc = c0; cc < c1; ++cc) ls += sh.cells[cc];
+      const float incl = warp_incl_scan(ls, lane);
+      const float Z = __shfl_sync(0xffffffffu, incl, 31);
+      int64_t tt = -1;
+      if (Z > 0.f) {
+        const float Tg = uK * Z;
+        float run = incl - ls;
+        int hit = -1;
+        for (int cc = c0; cc < c1; ++cc) {
+          if (run + sh.cells[cc] > Tg) {
+            hit = cc;
+            break;
+          }
+          run += sh.cells[cc];
+        }
+        const unsigned bal = __ballot_sync(0xffffffffu, hit >= 0);
+        int cstar;
+        float Tl = 0.f;
+        bool lastpos_mode = false;
+        if (bal) {
+          const int fl = __ffs(bal) - 1;
+          cstar = __shfl_sync(0xffffffffu, hit, fl);
+          Tl = Tg - __shfl_sync(0xffffffffu, run, fl);
+        } else {
+          int last = -1;
+          for (int cc = c0; cc < c1; ++cc)
+            if (sh.cells[cc] > 0.f) last = cc;
+          for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+          cstar = last;
+          lastpos_mode = true;
+        }
+        const int64_t base = (int64_t)cstar * 256 + lane * 8;
+        float w[8];
+        w8(base, w);
+        const float l8 = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+        const float incl2 = warp_incl_scan(l8, lane);
+        const float excl2 = incl2 - l8;
+        int64_t mine = -1, lastp = -1;
+        float acc = excl2;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (w[k] > 0.f) lastp = base + k;
+          acc += w[k];
+          if (mine < 0 && !lastpos_mode && acc > Tl) mine = base + k;
+        }
+        const unsigned bal2 = __ballot_sync(0xffffffffu, mine >= 0);
+        if (bal2) {
+          tt = __shfl_sync(0xffffffffu, (long long)mine, __ffs(bal2) - 1);
+        } else {  // rounding or u*Z past the total: the last positive weight
+          long long lp = lastp;
+          for (int o = 16; o > 0; o >>= 1) lp = max(lp, __shfl_xor_sync(0xffffffffu, lp, o));
+          tt = lp;
+        }
+      }
+      if (lane == 0) sh.bl[0] = tt;
+    }
+    cbar();
+    t = sh.bl[0];
+    cbar();
+    if (!resid) break;  // the bonus or the fallback to p'_j always has mass
+    if (t < 0) {        // a residual that is all zero: draw from p'_j instead
+      rq = nullptr;
+    }
+  }
+  for (int i = tid; i <= K; i += kConsumerThreads)
+    out[i] = i < j ? p.tokens[b * K + i] : (i == j ? (int32_t)t : -1);
+  if (tid == 0) p.out_accept_len[b] = j;
+}
+
+template <typename E>
+__device__ void seq_consumer(const Params& p, const char* ring, SeqShared& sh, int tid) {
+  const int lane = tid & 31;
+  int stage = 0;
+  uint32_t ph = 0u;
+  for (;;) {
+    const int cur = stage;
+    const int ok = mbar_wait(&sh.full[cur], ph) ? 1 : 0;
+    if (++stage == kSeqStages) {
+      stage = 0;
+      ph ^= 1u;
+    }
+    if (cbar_or(!ok)) {
+      if (tid == 0) atomicOr(p.ctl + 3, kStatusTimeout);
+      return;
+    }
+    const int64_t b = sh.seq[cur];
+    if (b < 0) return;
+    seq_in_smem<E>(p, sh, ring + (size_t)cur * kSeqStageBytes, b, tid);
+    cbar();  // every consumer is done with the stage
+    if (lane == 0) mbar_arrive(&sh.empty[cur]);
+  }
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kSeqThreads, 2) verify_seq_kernel(const Params p) {
+  extern __shared__ __align__(1024) unsigned char smem[];
+  char* ring = reinterpret_cast<char*>(smem);
+  SeqShared& sh = *reinterpret_cast<SeqShared*>(smem + (size_t)kSeqStages * kSeqStageBytes);
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int i = 0; i < kSeqStages; ++i) {
+      mbar_init(&sh.full[i], 1u);
+      mbar_init(&sh.empty[i], (uint32_t)kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (tid >= kConsumerThreads) {
+    if (tid == kConsumerThreads) seq_producer<E>(p, ring, sh);
+    return;
+  }
+  seq_consumer<E>(p, ring, sh, tid);
+}
+
+bool seq_mode_fits(int64_t K, int64_t V, int esz) {
+  const int64_t R = 2 * K + 1;
+  return R <= kSeqMaxRows && R * V * esz <= kSeqStageBytes && (V * esz) % 16 == 0;
+}
+
+template <typename E>
+static cudaError_t launch_seq_t(const Params& p, int grid, cudaStream_t stream) {
+  const size_t smem = seq_shared_bytes();
+  auto* k = verify_seq_kernel<E>;
+  static bool raised = false;
+  if (!raised) {
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    raised = true;
+  }
+  k<<<grid, kSeqThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_seq(const Params& p, int dtype, int grid, cudaStream_t stream) {
+  return dtype == 1 ? launch_seq_t<uint16_t>(p, grid, stream) : launch_seq_t<float>(p, grid, stream);
+}
+
 // ------------------------------------------------------------- launching ------
 
 template <typename E, int MODE>

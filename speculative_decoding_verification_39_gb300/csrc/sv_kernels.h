@@ -43,6 +43,12 @@ struct Params {
 
 size_t shared_bytes(int stages);
 cudaError_t launch(const Params& p, int dtype, int mode, int grid, cudaStream_t stream);
+
+// Sampling mode for short rows: one CTA per sequence, the whole sequence
+// staged in shared memory. seq_mode_fits() says whether a shape qualifies
+// (2K+1 <= 64 rows, the sequence within 48 KB, rows 16-byte aligned).
+bool seq_mode_fits(int64_t K, int64_t V, int esz);
+cudaError_t launch_seq(const Params& p, int dtype, int grid, cudaStream_t stream);
 int kernel_threads();
 
 }  // namespace sv

@@ -42,6 +42,10 @@ SAMPLE_CASES = {
     "topp_flat": C["cfg2_v32000_bf16"].with_(B=6, K=2, V=9000, target_sigma=0.05, draft_sigma=0.02, top_p=0.95,
                                              n_peaks=0),
     "hot_T2": C["cfg2_v32000_bf16"].with_(B=10, K=4, V=16384, temperature=2.0),
+    # whole sequences in one CTA (2K+1 rows within 48 KB, rows 16-byte aligned)
+    "seqmode_bf16_v2048_k3": C["cfg2_v32000_bf16"].with_(B=50, K=3, V=2048),
+    "seqmode_f32_v8_k2": C["cfg1_v1000_f32"].with_(B=400, K=2, V=8),
+    "seqmode_bf16_v512_k15": C["cfg2_v32000_bf16"].with_(B=40, K=15, V=512, temperature=0.6),
 }
 
 
@@ -136,6 +140,20 @@ def test_bad_inputs_flag_only_their_sequence():
     g["logits"][2, 0, 0, 3] = 0x7FC0
     compare_greedy(g)
     assert svpkg.get_status() == -4
+
+
+def test_bad_inputs_in_sequence_mode():
+    cfg = C["cfg2_v32000_bf16"].with_(B=8, K=3, V=1024)
+    d = sg.sample_inputs(cfg)
+    d["draft_tokens"][0, 1] = cfg.V
+    d["uniforms"][2, 3] = 1.0
+    d["target"][3, 2, 17] = 0x7FC0   # NaN
+    d["draft"][4, 1, 9] = 0x7F80     # +inf
+    d["target"][5, 0, :] = 0xFF80    # all -inf
+    gt, ga = run_sample(d, cfg.temperature)
+    assert svpkg.get_status() == -4
+    assert (ga[[0, 2, 3, 4, 5]] == -1).all() and (ga[[1, 6, 7]] >= 0).all()
+    compare_sample(d, cfg.temperature, gpu=(gt, ga))
 
 
 def test_empty_batch_is_a_noop():
