@@ -106,9 +106,31 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   p.NC = (p.NT + ct - 1) / ct;
   p.CT = (p.NT + p.NC - 1) / p.NC;
   p.W = rows_total * p.NC;
-  const size_t cnt_words = (size_t)rows_total + 2 * (size_t)p.B;
+  // Sampling draws over more cells than one ring half holds are split over
+  // CTAs: into at most one chunk per half-ring of cells, and into no more
+  // chunks than it takes for the call's draws to cover the CTAs once.
+  const int64_t CE = sv::cell_elems(p.V);
+  const int64_t ncells = (p.V + CE - 1) / CE;
+  p.DC = 0;
+  p.CPC = 0;
+  if (mode == sv::kSample) {
+    const int64_t half = sv::draw_cells_per_chunk(p.stages, esz, p.V);
+    int64_t dc = half > 0 ? (ncells + half - 1) / half : 0;
+    // Only long draws (six ring halves or more) in calls that leave most CTAs
+    // idle at the end gain from the split: short ones lose more to the hand-off.
+    const int64_t cover = (slots + p.B - 1) / p.B;
+    if (dc < 6 || p.B * 2 > slots) dc = 0;
+    if (dc > cover) dc = cover;
+    if (dc >= 2 && p.B * (1 + dc) < (int64_t(1) << 30)) {
+      p.DC = (int)dc;
+      p.CPC = (int)((ncells + dc - 1) / dc);
+    }
+  }
+  const size_t cnt_words = (size_t)rows_total + (size_t)p.B * (3 + (size_t)p.DC);
   const size_t part_bytes = align256((size_t)p.W * 8);
-  const size_t data_bytes = part_bytes + (size_t)rows_total * 16;
+  const size_t rowstat_bytes = align256((size_t)rows_total * 16);
+  const size_t dcells_bytes = p.DC ? align256((size_t)p.B * (size_t)ncells * 4) : 0;
+  const size_t data_bytes = part_bytes + rowstat_bytes + dcells_bytes + (p.DC ? (size_t)p.B * sizeof(sv::DrawJob) : 0);
   Scratch sc;
   int dev = 0;
   int rc = get_scratch(stream, cnt_words, data_bytes, &sc, &dev);
@@ -118,8 +140,11 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   p.row_cnt = reinterpret_cast<uint32_t*>(b + counter_offset());
   p.seq_cnt = p.row_cnt + rows_total;
   p.tail_q = p.seq_cnt + p.B;
+  p.dcnt = p.tail_q + p.B * (1 + p.DC);
   p.part = reinterpret_cast<float2*>(b + data_offset(sc));
   p.rowstat = reinterpret_cast<float4*>(b + data_offset(sc) + part_bytes);
+  p.dcells = reinterpret_cast<float*>(b + data_offset(sc) + part_bytes + rowstat_bytes);
+  p.djob = reinterpret_cast<sv::DrawJob*>(b + data_offset(sc) + part_bytes + rowstat_bytes + dcells_bytes);
   // Short rows: one CTA per sequence, the whole sequence staged in shared memory.
   const bool seq_mode = mode == sv::kSample && !p.topp && sv::seq_mode_fits(p.K, p.V, esz) &&
                         aligned_to(p.a, 16) && aligned_to(p.d, 16);

@@ -389,6 +389,14 @@ __device__ __forceinline__ void load8(const char* row, int64_t e, int64_t V, boo
   }
 }
 
+// The smallest stored value whose key is >= k (keys at or below key(-inf)
+// hold no value but NaN, which valid rows do not contain): x >= key_floor(k)
+// exactly when key(x) >= k.
+template <typename E>
+__device__ __forceinline__ float key_floor(uint32_t k) {
+  return k <= ET<E>::key(-INFINITY) ? -INFINITY : ET<E>::val(k);
+}
+
 // Eight consecutive elements of a row piece staged in shared memory (the
 // piece starts at element e0 of the row; -inf past V).
 template <typename E>
@@ -415,15 +423,15 @@ __device__ __forceinline__ void load8_smem(const char* piece, int64_t e_in_piece
 
 // The sampler's weights over one row: w_v = p'(v) up to a constant, or, with
 // two rows, w_v = max(0, p'(v) - q'(v)).
-template <typename E, bool kResidual>
+template <typename E, bool kResidual, bool kTopp>
 struct Weights {
   const char* rp;
   const char* rq;
   int64_t V;
   float c, nMcp, nMcq, ip, iq;
-  uint32_t taup, tauq;
-  int topp;
+  float tp, tq;  // the nucleus: elements below tp (tq) weigh nothing in p' (q'); -inf without top-p
   bool aligned;
+  static constexpr bool kRes = kResidual;
   __device__ __forceinline__ void w8(int64_t e, float w[8]) const {
     float lp[8], lq[8];
     load8<E>(rp, e, V, aligned, lp);
@@ -444,51 +452,92 @@ struct Weights {
       for (int k = 0; k < 8; ++k) {
         float ep = ex2(fmaf(lp[k], c, nMcp));
         float eq = ex2(fmaf(lq[k], c, nMcq));
-        if (topp) {
-          if (ET<E>::key(lp[k]) < taup) ep = 0.f;
-          if (ET<E>::key(lq[k]) < tauq) eq = 0.f;
+        if (kTopp) {
+          ep = lp[k] >= tp ? ep : 0.f;
+          eq = lq[k] >= tq ? eq : 0.f;
         }
         w[k] = fmaxf(0.f, fmaf(ep, ip, -eq * iq));
       }
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
-        float ep = ex2(fmaf(lp[k], c, nMcp));
-        if (topp && ET<E>::key(lp[k]) < taup) ep = 0.f;
-        w[k] = ep;
+        const float ep = ex2(fmaf(lp[k], c, nMcp));
+        w[k] = (!kTopp || lp[k] >= tp) ? ep : 0.f;
       }
     }
   }
 };
 
+// Cell sums of one piece staged in shared memory (row p at sp, row q at sq,
+// elements e0 .. of the row) for cells [cfirst, clast), written to dst[cell]:
+// a warp takes four of its cells at a time, all their weights first, then the
+// four warp reductions interleaved. Lane l sums elements l*8m .. of a cell.
+template <typename E, class WF>
+__device__ __forceinline__ void cells_piece(const WF& wf, const char* sp, const char* sq, int cfirst, int clast,
+                                            int64_t e0, int64_t CE, float* dst, int warp, int lane) {
+  const int64_t m = CE / 256;
+  constexpr int UC = 4;
+  for (int cb = cfirst + warp; cb < clast; cb += kConsumerWarps * UC) {
+    float acc[UC];
+#pragma unroll
+    for (int k = 0; k < UC; ++k) {
+      const int cc = cb + k * kConsumerWarps;
+      float a = 0.f;
+      if (cc < clast) {
+        for (int64_t q = 0; q < m; ++q) {
+          const int64_t e = (int64_t)cc * CE + (lane * m + q) * 8;
+          float w[8];
+          wf.w8_staged(sp, sq, e - e0, e, w);
+          a += ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+        }
+      }
+      acc[k] = a;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int k = 0; k < UC; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int k = 0; k < UC; ++k) {
+        const int cc = cb + k * kConsumerWarps;
+        if (cc < clast) dst[cc] = acc[k];
+      }
+    }
+  }
+}
+
 // Inverse-CDF draw by the 256 consumer threads: the smallest t with
 // sum_{v<=t} w_v > u * sum_v w_v. Returns -1 when every weight is zero.
-// The row is cut into cells of 256*m elements (at most kMaxCells cells); a
-// first pass sums each cell, one warp scans the cell sums to find the cell
-// holding the crossing, and rescans that cell alone.
-// Pass A from shared memory: the row (or the two rows) is moved in pieces of
-// whole cells into the two halves of the idle tile ring by bulk copies, the
-// next piece landing while the current one is summed. Returns false (having
-// touched nothing) when it cannot run: unaligned rows, or a ring too small for
-// one cell per row.
+// The row is cut into cells of CE = 256*m elements (at most kMaxCells cells);
+// pass A sums each cell, then one warp scans the cell sums to find the cell
+// holding the crossing and rescans that cell alone (cdf_cross). Pass A may
+// be split over CTAs by ranges of cells (draw_chunk).
+// Pass A over cells [cbeg, cend) from shared memory, sums to dst[cell]: the
+// row (or the two rows) is moved in pieces of whole cells into the two halves
+// of the idle tile ring by bulk copies, the next piece landing while the
+// current one is summed. Returns false (having touched nothing) when it cannot
+// run: unaligned rows, or a ring too small for one cell per row.
 template <typename E, class WF>
-__device__ bool cells_staged(const WF& wf, int64_t V, int64_t CE, int ncells, char* ring, size_t ring_bytes,
-                             Shared& sh, int tid, const uint32_t* ctl_status) {
+__device__ bool cells_staged(const WF& wf, int64_t V, int64_t CE, int cbeg, int cend, float* dst, char* ring,
+                             size_t ring_bytes, Shared& sh, int tid, const uint32_t* ctl_status) {
   constexpr int S = ET<E>::kSize;
-  const int nrows = wf.rq ? 2 : 1;
+  constexpr int nrows = WF::kRes ? 2 : 1;
   if (!wf.aligned || ring_bytes == 0) return false;
   const size_t half = (ring_bytes / 2) & ~size_t(15);
   int64_t cells_per_piece = (int64_t)(half / nrows / S) / CE;
   if (cells_per_piece < 1) return false;
   const int64_t P = cells_per_piece * CE;  // elements per row per piece
-  const int64_t npieces = (V + P - 1) / P;
+  const int64_t ebeg = (int64_t)cbeg * CE, eend = min(V, (int64_t)cend * CE);
+  const int64_t npieces = (eend - ebeg + P - 1) / P;
   const int warp = tid >> 5, lane = tid & 31;
   cbar();  // everyone has read dcount, and nothing reads the ring any more
   const uint32_t c0 = sh.dcount[0], c1 = sh.dcount[1];
   auto issue = [&](int64_t k) {  // thread 0 only
     const int buf = (int)(k & 1);
-    const int64_t e0 = k * P;
-    const int64_t n = min(P, V - e0);
+    const int64_t e0 = ebeg + k * P;
+    const int64_t n = min(P, eend - e0);
     const uint32_t bytes = (uint32_t)(n * S);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     mbar_arrive_expect_tx(&sh.dbar[buf], bytes * (uint32_t)nrows);
@@ -511,42 +560,10 @@ __device__ bool cells_staged(const WF& wf, int64_t V, int64_t CE, int ncells, ch
     }
     const char* sp = ring + (size_t)buf * half;
     const char* sq = sp + (size_t)P * S;
-    const int64_t e0 = k * P;
+    const int64_t e0 = ebeg + k * P;
     const int cfirst = (int)(e0 / CE);
-    const int clast = (int)min((int64_t)ncells, (e0 + P) / CE + ((e0 + P) % CE ? 1 : 0));
-    const int64_t m = CE / 256;
-    // A warp's cells of the piece, four at a time: all their weights first,
-    // then the four warp reductions interleaved.
-    constexpr int UC = 4;
-    for (int cb = cfirst + warp; cb < clast; cb += kConsumerWarps * UC) {
-      float acc[UC];
-#pragma unroll
-      for (int k = 0; k < UC; ++k) {
-        const int cc = cb + k * kConsumerWarps;
-        float a = 0.f;
-        if (cc < clast) {
-          for (int64_t q = 0; q < m; ++q) {
-            const int64_t e = (int64_t)cc * CE + (lane * m + q) * 8;
-            float w[8];
-            wf.w8_staged(sp, sq, e - e0, e, w);
-            a += ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
-          }
-        }
-        acc[k] = a;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-#pragma unroll
-        for (int k = 0; k < UC; ++k) acc[k] += __shfl_xor_sync(0xffffffffu, acc[k], o);
-      }
-      if (lane == 0) {
-#pragma unroll
-        for (int k = 0; k < UC; ++k) {
-          const int cc = cb + k * kConsumerWarps;
-          if (cc < clast) sh.cells[cc] = acc[k];
-        }
-      }
-    }
+    const int clast = (int)min((int64_t)cend, (e0 + P) / CE);
+    cells_piece<E>(wf, sp, sq, cfirst, clast, e0, CE, dst, warp, lane);
     cbar();  // the half is free again
     if (tid == 0 && k + 2 < npieces) issue(k + 2);
   }
@@ -564,24 +581,20 @@ __device__ bool cells_staged(const WF& wf, int64_t V, int64_t CE, int ncells, ch
   return ok;
 }
 
+// Pass A over cells [cbeg, cend) from global memory, sums to dst[cell]: four
+// cells per warp at a time so that their loads are in flight together.
 template <typename E, class WF>
-__device__ int64_t cdf_draw(const WF& wf, int64_t V, float u, Shared& sh, int tid, char* ring, size_t ring_bytes,
-                            const uint32_t* ctl_status) {
+__device__ void cells_global(const WF& wf, int64_t CE, int cbeg, int cend, float* dst, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
-  const int64_t m = (V + 256LL * kMaxCells - 1) / (256LL * kMaxCells) > 1 ? (V + 256LL * kMaxCells - 1) / (256LL * kMaxCells) : 1;
-  const int64_t CE = 256 * m;
-  const int ncells = (int)((V + CE - 1) / CE);
-  const bool staged = cells_staged<E>(wf, V, CE, ncells, ring, ring_bytes, sh, tid, ctl_status);
-  // Pass A without staging: cell sums from global memory, four cells per warp
-  // at a time so that their loads are in flight together.
+  const int64_t m = CE / 256;
   constexpr int U = 4;
-  for (int c0 = staged ? ncells : warp; c0 < ncells; c0 += kConsumerWarps * U) {
+  for (int c0 = cbeg + warp; c0 < cend; c0 += kConsumerWarps * U) {
     float sum[U];
 #pragma unroll
     for (int k = 0; k < U; ++k) {
       const int cc = c0 + k * kConsumerWarps;
       float acc = 0.f;
-      if (cc < ncells) {
+      if (cc < cend) {
         for (int64_t q = 0; q < m; ++q) {
           float w[8];
           wf.w8(cc * CE + (lane * m + q) * 8, w);
@@ -594,10 +607,20 @@ __device__ int64_t cdf_draw(const WF& wf, int64_t V, float u, Shared& sh, int ti
     for (int k = 0; k < U; ++k) {
       const float t = warp_sum(sum[k]);
       const int cc = c0 + k * kConsumerWarps;
-      if (lane == 0 && cc < ncells) sh.cells[cc] = t;
+      if (lane == 0 && cc < cend) dst[cc] = t;
     }
   }
-  cbar();
+}
+
+// The crossing, from the cell sums in sh.cells[0, ncells): one warp scans
+// them, finds the cell holding u * Z and walks it. Returns the token to every
+// consumer thread (-1 when every weight is zero).
+template <typename E, class WF>
+__device__ int64_t cdf_cross(const WF& wf, int64_t V, float u, Shared& sh, int tid) {
+  const int warp = tid >> 5, lane = tid & 31;
+  const int64_t CE = cell_elems(V);
+  const int64_t m = CE / 256;
+  const int ncells = (int)((V + CE - 1) / CE);
   if (warp == 0) {
     const int cpl = (ncells + 31) / 32;
     const int c0 = min(ncells, lane * cpl), c1 = min(ncells, c0 + cpl);
@@ -703,6 +726,18 @@ __device__ int64_t cdf_draw(const WF& wf, int64_t V, float u, Shared& sh, int ti
   const int64_t t = sh.bl[0];
   cbar();
   return t;
+}
+
+// The whole draw in this CTA.
+template <typename E, class WF>
+__device__ int64_t cdf_draw(const WF& wf, int64_t V, float u, Shared& sh, int tid, char* ring, size_t ring_bytes,
+                            const uint32_t* ctl_status) {
+  const int64_t CE = cell_elems(V);
+  const int ncells = (int)((V + CE - 1) / CE);
+  if (!cells_staged<E>(wf, V, CE, 0, ncells, sh.cells, ring, ring_bytes, sh, tid, ctl_status))
+    cells_global<E>(wf, CE, 0, ncells, sh.cells, tid);
+  cbar();
+  return cdf_cross<E>(wf, V, u, sh, tid);
 }
 
 // ------------------------------------------------ block-wide helpers ---------
@@ -859,6 +894,53 @@ __device__ void topp_cut(const Params& p, Shared& sh, const char* row, float M, 
 
 // ------------------------------------------------------ sequence tails -------
 
+__device__ __forceinline__ bool rows_aligned(const Params& p, int esz) {
+  return (p.V * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.a) & 15) == 0 &&
+         (reinterpret_cast<uintptr_t>(p.d) & 15) == 0;
+}
+
+template <typename E, bool kTopp>
+__device__ __forceinline__ Weights<E, true, kTopp> residual_weights(const Params& p, int64_t b, const DrawJob& jb) {
+  return Weights<E, true, kTopp>{row_ptr<E, kSample>(p, b, jb.j), row_ptr<E, kSample>(p, b, p.K + 1 + jb.j), p.V,
+                                 p.c, jb.nMcp, jb.nMcq, jb.ip, jb.iq, jb.tp, jb.tq, rows_aligned(p, ET<E>::kSize)};
+}
+template <typename E, bool kTopp>
+__device__ __forceinline__ Weights<E, false, kTopp> target_weights(const Params& p, int64_t b, const DrawJob& jb) {
+  return Weights<E, false, kTopp>{row_ptr<E, kSample>(p, b, jb.j), nullptr, p.V, p.c, jb.nMcp, 0.f, 1.f, 0.f, jb.tp,
+                                  -INFINITY, rows_aligned(p, ET<E>::kSize)};
+}
+
+// The draw of sequence b in this CTA alone: the residual at a rejection
+// (p'_j itself if that is all zero), or p'_K for the bonus token.
+template <typename E, bool kTopp>
+__device__ int64_t draw_whole(const Params& p, Shared& sh, int64_t b, const DrawJob& jb, int tid, char* ring,
+                              size_t ring_bytes) {
+  int64_t t = -1;
+  if (jb.j < p.K)
+    t = cdf_draw<E>(residual_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid, ring, ring_bytes, p.ctl + 3);
+  if (t < 0) t = cdf_draw<E>(target_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid, ring, ring_bytes, p.ctl + 3);
+  return t;
+}
+
+// Hand sequence b's draw to the CTAs draining the queue: its job record, then
+// p.DC chunk entries (thread 0).
+constexpr uint32_t kTailClaimed = 0x80000000u;
+constexpr uint32_t kTailChunk = 0x40000000u;
+__device__ void draw_publish(const Params& p, int64_t b, const DrawJob& jb) {
+  DrawJob* d = p.djob + b;
+  d->uK = jb.uK;
+  d->nMcp = jb.nMcp;
+  d->nMcq = jb.nMcq;
+  d->ip = jb.ip;
+  d->iq = jb.iq;
+  d->tp = jb.tp;
+  d->tq = jb.tq;
+  d->j = jb.j;
+  __threadfence();
+  const uint32_t k0 = atomicAdd(p.ctl + 4, (uint32_t)p.DC);
+  for (int c = 0; c < p.DC; ++c) st_release_gpu(p.tail_q + k0 + c, kTailChunk | (uint32_t)(b * p.DC + c + 1));
+}
+
 template <typename E>
 __device__ void seq_sample(const Params& p, Shared& sh, int64_t b, int tid) {
   const int K = p.K;
@@ -904,32 +986,40 @@ __device__ void seq_sample(const Params& p, Shared& sh, int64_t b, int tid) {
     if (tid == 0) {
       p.out_accept_len[b] = -1;
       atomicOr(p.ctl + 3, kStatusInput);
+      if (p.DC > 0) {  // the sequence's draw chunks still count: they do nothing
+        DrawJob jb{};
+        jb.j = -1;
+        draw_publish(p, b, jb);
+      }
     }
     return;
   }
   const float uK = p.uniforms[b * (K + 1) + K];
   const RowStat rp = rs_load(p, b * p.RS + j);
-  const bool aligned = (p.V * ET<E>::kSize) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.a) & 15) == 0 &&
-                       (reinterpret_cast<uintptr_t>(p.d) & 15) == 0;
+  const RowStat rq = rs_load(p, b * p.RS + K + 1 + (j < K ? j : 0));
+  DrawJob jb;
+  jb.uK = uK;
+  jb.j = j;
+  jb.nMcp = -mref(rp.M, c);
+  jb.ip = 1.f / rp.cum;
+  jb.tp = p.topp ? key_floor<E>(rp.tau) : -INFINITY;
+  jb.nMcq = -mref(rq.M, c);
+  jb.iq = 1.f / rq.cum;
+  jb.tq = p.topp ? key_floor<E>(rq.tau) : -INFINITY;
+  for (int i = tid; i <= K; i += kConsumerThreads)
+    if (i != j) out[i] = i < j ? p.tokens[b * K + i] : -1;
+  if (tid == 0) p.out_accept_len[b] = j;
+  if (p.DC > 0) {  // other CTAs sum the cells; the last of them finishes the draw
+    if (tid == 0) draw_publish(p, b, jb);
+    return;
+  }
   // The tile ring is idle while sequence tails run (they run only after the
   // CTA's streaming is over), so the draw stages its rows there.
   char* ring = reinterpret_cast<char*>(&sh) - (size_t)p.stages * kTileBytes;
   const size_t ring_bytes = (size_t)p.stages * kTileBytes;
-  int64_t t = -1;
-  if (j < K) {
-    const RowStat rq = rs_load(p, b * p.RS + K + 1 + j);
-    Weights<E, true> wf{row_ptr<E, kSample>(p, b, j), row_ptr<E, kSample>(p, b, K + 1 + j), p.V, c, -mref(rp.M, c),
-                        -mref(rq.M, c), 1.f / rp.cum, 1.f / rq.cum, rp.tau, rq.tau, p.topp, aligned};
-    t = cdf_draw<E>(wf, p.V, uK, sh, tid, ring, ring_bytes, p.ctl + 3);
-  }
-  if (t < 0) {  // bonus row, or a residual that is all zero: draw from p'_j
-    Weights<E, false> wf{row_ptr<E, kSample>(p, b, j), nullptr, p.V, c, -mref(rp.M, c), 0.f, 1.f, 0.f, rp.tau, 0u,
-                         p.topp, aligned};
-    t = cdf_draw<E>(wf, p.V, uK, sh, tid, ring, ring_bytes, p.ctl + 3);
-  }
-  for (int i = tid; i <= K; i += kConsumerThreads)
-    out[i] = i < j ? p.tokens[b * K + i] : (i == j ? (int32_t)t : -1);
-  if (tid == 0) p.out_accept_len[b] = j;
+  const int64_t t = p.topp ? draw_whole<E, true>(p, sh, b, jb, tid, ring, ring_bytes)
+                           : draw_whole<E, false>(p, sh, b, jb, tid, ring, ring_bytes);
+  if (tid == 0) out[j] = (int32_t)t;
 }
 
 template <typename E>
@@ -1071,7 +1161,6 @@ __device__ __forceinline__ void tail_enqueue(const Params& p, int64_t b) {
 // A tail that this CTA runs itself (its streaming is over, so running it here
 // holds up nothing): the queue entry is only marked as claimed, which keeps
 // the count of entries equal to the number of sequences.
-constexpr uint32_t kTailClaimed = 0x80000000u;
 __device__ __forceinline__ void tail_claim(const Params& p, int64_t b) {
   const uint32_t k = atomicAdd(p.ctl + 4, 1u);
   st_release_gpu(p.tail_q + k, kTailClaimed | (uint32_t)(b + 1));
@@ -1199,35 +1288,103 @@ __device__ void run_task(const Params& p, Shared& sh, int64_t task, float m, flo
   }
 }
 
+// One chunk of a split draw (sampling mode): the cell sums of cells
+// [c*CPC, (c+1)*CPC) of sequence b's draw, written to p.dcells. The CTA that
+// completes the last chunk scans all the cells and writes the token.
+template <typename E, bool kTopp>
+__device__ void draw_chunk(const Params& p, Shared& sh, int64_t b, int c, int tid) {
+  DrawJob jb;
+  {
+    const DrawJob* d = p.djob + b;
+    jb.uK = __ldcg(&d->uK);
+    jb.nMcp = __ldcg(&d->nMcp);
+    jb.nMcq = __ldcg(&d->nMcq);
+    jb.ip = __ldcg(&d->ip);
+    jb.iq = __ldcg(&d->iq);
+    jb.tp = __ldcg(&d->tp);
+    jb.tq = __ldcg(&d->tq);
+    jb.j = __ldcg(&d->j);
+  }
+  const int64_t CE = cell_elems(p.V);
+  const int ncells = (int)((p.V + CE - 1) / CE);
+  float* cells = p.dcells + b * ncells;
+  char* ring = reinterpret_cast<char*>(&sh) - (size_t)p.stages * kTileBytes;
+  const size_t ring_bytes = (size_t)p.stages * kTileBytes;
+  const int cbeg = min(ncells, c * p.CPC), cend = min(ncells, (c + 1) * p.CPC);
+  if (jb.j >= 0 && cbeg < cend) {
+    if (jb.j < p.K) {
+      const Weights<E, true, kTopp> wf = residual_weights<E, kTopp>(p, b, jb);
+      if (!cells_staged<E>(wf, p.V, CE, cbeg, cend, cells, ring, ring_bytes, sh, tid, p.ctl + 3))
+        cells_global<E>(wf, CE, cbeg, cend, cells, tid);
+    } else {
+      const Weights<E, false, kTopp> wf = target_weights<E, kTopp>(p, b, jb);
+      if (!cells_staged<E>(wf, p.V, CE, cbeg, cend, cells, ring, ring_bytes, sh, tid, p.ctl + 3))
+        cells_global<E>(wf, CE, cbeg, cend, cells, tid);
+    }
+  }
+  __threadfence();
+  cbar();
+  if (tid == 0) {
+    const uint32_t old = atom_add_acq_rel(p.dcnt + b, 1u);
+    const int last = old == (uint32_t)p.DC - 1u;
+    if (last) p.dcnt[b] = 0u;
+    sh.flag = last;
+  }
+  cbar();
+  const int last = sh.flag;
+  cbar();
+  if (!last || jb.j < 0) return;
+  for (int i = tid; i < ncells; i += kConsumerThreads) sh.cells[i] = __ldcg(cells + i);
+  cbar();
+  int64_t t = -1;
+  if (jb.j < p.K) t = cdf_cross<E>(residual_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid);
+  if (t < 0)  // the bonus draw, or a residual that is all zero: p'_j
+    t = jb.j < p.K
+            ? cdf_draw<E>(target_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid, ring, ring_bytes, p.ctl + 3)
+            : cdf_cross<E>(target_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid);
+  if (tid == 0) p.out_tokens[b * (p.K + 1) + jb.j] = (int32_t)t;
+}
+
 // Consumer side, after the CTA's streaming is done: take tickets for queued
-// sequence tails until every sequence of the call has one. Ticket k is the
-// k-th tail queued; it may not be written yet, but whoever will write it holds
-// the rows it waits for and needs nothing from this CTA, so the wait ends.
+// sequence tails and draw chunks until every entry of the call has been
+// taken. Ticket k is the k-th entry queued; it may not be written yet, but
+// whoever will write it holds what it waits for and needs nothing from this
+// CTA, so the wait ends.
 template <typename E, int MODE>
 __device__ void drain_tails(const Params& p, Shared& sh, int tid) {
+  const int64_t entries = p.B * (1 + (MODE == kSample ? (int64_t)p.DC : 0));
   for (;;) {
     if (tid == 0) {
       const uint32_t k = atomicAdd(p.ctl + 5, 1u);
-      int64_t b = -1;
-      if ((int64_t)k < p.B) {
+      int64_t e = -1;  // -1: none left; -2: skip; >= 0: b, or kTailChunk | (b*DC + c)
+      if ((int64_t)k < entries) {
         uint32_t v = ld_acquire_gpu(p.tail_q + k);
         if (v == 0u) {
           const uint64_t t0 = globaltimer_ns();
           while (v == 0u && globaltimer_ns() - t0 < kWaitLimitNs) v = ld_acquire_gpu(p.tail_q + k);
         }
         if (v == 0u) atomicOr(p.ctl + 3, kStatusTimeout);
-        else if (v & kTailClaimed) b = -2;  // run by the CTA that completed it
-        else b = (int64_t)v - 1;
+        else if (v & kTailClaimed) e = -2;  // run by the CTA that completed it
+        else if (v & kTailChunk) e = (int64_t)kTailChunk | (int64_t)((v & ~kTailChunk) - 1u);
+        else e = (int64_t)v - 1;
         p.tail_q[k] = 0u;
       }
-      sh.bl[1] = b;
+      sh.bl[1] = e;
     }
     cbar();
-    const int64_t b = sh.bl[1];
+    const int64_t e = sh.bl[1];
     cbar();
-    if (b == -2) continue;
-    if (b < 0) return;
-    seq_tail<E, MODE>(p, sh, b, tid);
+    if (e == -2) continue;
+    if (e < 0) return;
+    if (MODE == kSample && (e & kTailChunk)) {
+      const int64_t bc = e & ~(int64_t)kTailChunk;
+      if (p.topp)
+        draw_chunk<E, true>(p, sh, bc / p.DC, (int)(bc % p.DC), tid);
+      else
+        draw_chunk<E, false>(p, sh, bc / p.DC, (int)(bc % p.DC), tid);
+    } else {
+      seq_tail<E, MODE>(p, sh, e, tid);
+    }
   }
 }
 
@@ -1380,7 +1537,7 @@ __device__ void publisher_loop(const Params& p, Shared& sh) {
 // carries the abort vote of the bounded waits) lets all consumers see the
 // same task-queue snapshot.
 template <typename E, int MODE>
-__device__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int tid) {
+__device__ __forceinline__ void consumer_loop(const Params& p, const char* ring, Shared& sh, int tid) {
   constexpr int PV = ET<E>::kPerVec;
   const int warp = tid >> 5, lane = tid & 31;
   float m = -INFINITY;                      // sampling: online (max, sum)

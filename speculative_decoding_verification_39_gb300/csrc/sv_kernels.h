@@ -10,6 +10,31 @@ enum Mode { kSample = 0, kArgmaxLimit = 1, kGreedy = 2 };
 constexpr int kMaxStages = 6;  // 6 x 32 KB + control stays under the 227 KB a CTA may use
 constexpr int kTileBytes = 32768;  // one ring stage holds one tile
 
+constexpr int kMaxCells = 1024;    // inverse-CDF cells per row
+
+// Elements per inverse-CDF cell: 256 * m, the fewest that keep a row of V
+// elements within kMaxCells cells.
+__host__ __device__ inline int64_t cell_elems(int64_t V) {
+  const int64_t m = (V + 256LL * kMaxCells - 1) / (256LL * kMaxCells);
+  return 256 * (m > 1 ? m : 1);
+}
+
+// Cells of a residual draw (two rows) that fit one half of a ring of
+// `stages` tiles: the unit of work of a draw split over CTAs.
+inline int64_t draw_cells_per_chunk(int stages, int esz, int64_t V) {
+  const int64_t half = ((int64_t)stages * kTileBytes / 2) & ~int64_t(15);
+  return half / 2 / esz / cell_elems(V);
+}
+
+// A sampling draw handed to other CTAs: what the sequence's tail decided.
+struct DrawJob {
+  float uK;                 // the draw's uniform
+  float nMcp, nMcq;         // -M c of the p and q rows
+  float ip, iq;             // 1 / nucleus mass of the p and q rows
+  float tp, tq;             // nucleus thresholds (-inf without top-p)
+  int32_t j;                // the rejected position (K: bonus draw; -1: bad input, no draw)
+};
+
 struct Params {
   const char* a;           // target logits [B,K+1,V] (sampling) or logits [B,G,N,V] (greedy)
   const char* d;           // draft logits [B,K,V] (sampling, T > 0)
@@ -35,10 +60,17 @@ struct Params {
                            // [4] tails queued, [5] tails taken, [6] finished CTAs
   uint32_t* row_cnt;       // [B*RS] chunks published per row
   uint32_t* seq_cnt;       // [B] rows finished per sequence
-  uint32_t* tail_q;        // [B] queued sequence tails (b + 1; 0 = empty)
+  uint32_t* tail_q;        // [B * (1 + DC)] queued sequence tails and draw chunks (0 = empty)
   float2* part;            // [W] per-chunk partials
   float4* rowstat;         // [B*RS] per-row results
   int stages;
+  // Draws split over CTAs (sampling mode, T > 0): DC chunks of CPC cells per
+  // sequence; 0 = each sequence's tail draws alone.
+  int DC;
+  int CPC;
+  float* dcells;           // [B][kMaxCells] cell sums
+  uint32_t* dcnt;          // [B] chunks done
+  DrawJob* djob;           // [B]
 };
 
 size_t shared_bytes(int stages);

@@ -122,19 +122,43 @@ extern "C" int sv_verify_sample_noalloc(const void* target_logits, const void* d
   p.NC = (p.NT + ct - 1) / ct;
   p.CT = (p.NT + p.NC - 1) / p.NC;
   p.W = rows * p.NC;
+  // Draw splitting as sv_verify_sample chooses it.
+  const int64_t CE = sv::cell_elems(V);
+  const int64_t ncells = (V + CE - 1) / CE;
+  p.DC = 0;
+  p.CPC = 0;
+  if (!limit) {
+    const int64_t half = sv::draw_cells_per_chunk(kStages, (int)esz, V);
+    int64_t dc = half > 0 ? (ncells + half - 1) / half : 0;
+    // Only long draws (six ring halves or more) in calls that leave most CTAs
+    // idle at the end gain from the split: short ones lose more to the hand-off.
+    const int64_t cover = (slots + B - 1) / B;
+    if (dc < 6 || B * 2 > slots) dc = 0;
+    if (dc > cover) dc = cover;
+    if (dc >= 2 && B * (1 + dc) < (int64_t(1) << 30)) {
+      p.DC = (int)dc;
+      p.CPC = (int)((ncells + dc - 1) / dc);
+    }
+  }
 
   // Layout inside the fixed array: control block, counters, data.
-  const size_t cnt_bytes = up256((size_t)(rows + 2 * B) * 4);
+  const size_t cnt_bytes = up256((size_t)(rows + B * (3 + (int64_t)p.DC)) * 4);
   const size_t part_bytes = up256((size_t)p.W * 8);
-  const size_t need = kCtl + cnt_bytes + part_bytes + (size_t)rows * 16;
+  const size_t rowstat_bytes = up256((size_t)rows * 16);
+  const size_t dcells_bytes = p.DC ? up256((size_t)B * (size_t)ncells * 4) : 0;
+  const size_t need = kCtl + cnt_bytes + part_bytes + rowstat_bytes + dcells_bytes +
+                      (p.DC ? (size_t)B * sizeof(sv::DrawJob) : 0);
   if (need > kNoAllocScratchBytes) return SV_ERR_SCRATCH_LIMIT;
   char* s = static_cast<char*>(base);
   p.ctl = reinterpret_cast<uint32_t*>(s);
   p.row_cnt = reinterpret_cast<uint32_t*>(s + kCtl);
   p.seq_cnt = p.row_cnt + rows;
   p.tail_q = p.seq_cnt + B;
+  p.dcnt = p.tail_q + B * (1 + p.DC);
   p.part = reinterpret_cast<float2*>(s + kCtl + cnt_bytes);
   p.rowstat = reinterpret_cast<float4*>(s + kCtl + cnt_bytes + part_bytes);
+  p.dcells = reinterpret_cast<float*>(s + kCtl + cnt_bytes + part_bytes + rowstat_bytes);
+  p.djob = reinterpret_cast<sv::DrawJob*>(s + kCtl + cnt_bytes + part_bytes + rowstat_bytes + dcells_bytes);
 
   // The array keeps whatever the last call left: the control block and the
   // counters must start at zero, so clear them on the caller's stream (a
