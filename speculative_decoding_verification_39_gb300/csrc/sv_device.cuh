@@ -20,27 +20,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t addr) {
-  uint4 v;
-  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-  return v;
-}
-
-// Shared-memory reductions that only lanes with `pred` perform: one predicated
-// instruction, no branch (so no divergence when few lanes take part).
-__device__ __forceinline__ void red_shared_add_if(bool pred, uint32_t addr, uint32_t v) {
-  asm volatile(
-      "{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n @q red.shared.add.u32 [%1], %2;\n}" ::"r"((uint32_t)pred),
-      "r"(addr), "r"(v)
-      : "memory");
-}
-__device__ __forceinline__ void red_shared_add_if(bool pred, uint32_t addr, float v) {
-  asm volatile(
-      "{\n .reg .pred q;\n setp.ne.u32 q, %0, 0;\n @q red.shared.add.f32 [%1], %2;\n}" ::"r"((uint32_t)pred),
-      "r"(addr), "f"(v)
-      : "memory");
-}
-
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
