@@ -145,14 +145,19 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   p.rowstat = reinterpret_cast<float4*>(b + data_offset(sc) + part_bytes);
   p.dcells = reinterpret_cast<float*>(b + data_offset(sc) + part_bytes + rowstat_bytes);
   p.djob = reinterpret_cast<sv::DrawJob*>(b + data_offset(sc) + part_bytes + rowstat_bytes + dcells_bytes);
-  // Short rows: one CTA per sequence, the whole sequence staged in shared memory.
-  const bool seq_mode = mode == sv::kSample && !p.topp && sv::seq_mode_fits(p.K, p.V, esz) &&
-                        aligned_to(p.a, 16) && aligned_to(p.d, 16);
+  // Short rows: one warp per sequence (rows of at most 1024 elements), else
+  // one CTA per sequence with the whole sequence staged in shared memory.
+  const bool short_ok = mode == sv::kSample && !p.topp && aligned_to(p.a, 16) && aligned_to(p.d, 16);
+  const bool warp_mode = short_ok && sv::warp_mode_fits(p.K, p.V, esz);
+  const bool seq_mode = short_ok && !warp_mode && sv::seq_mode_fits(p.K, p.V, esz);
   int64_t grid = (int64_t)sm_count(dev) * g_ctas_per_sm.load();
-  const int64_t items = seq_mode ? p.B : p.W;
+  const int64_t items = warp_mode ? (p.B + sv::warp_mode_seqs_per_cta() - 1) / sv::warp_mode_seqs_per_cta()
+                                  : (seq_mode ? p.B : p.W);
   if (grid > items) grid = items;
   if (grid < 1) grid = 1;
-  cudaError_t e = seq_mode ? sv::launch_seq(p, dtype, (int)grid, stream) : sv::launch(p, dtype, mode, (int)grid, stream);
+  cudaError_t e = warp_mode  ? sv::launch_warp(p, dtype, (int)grid, stream)
+                  : seq_mode ? sv::launch_seq(p, dtype, (int)grid, stream)
+                             : sv::launch(p, dtype, mode, (int)grid, stream);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   g_launches.fetch_add(1);
   return SV_OK;

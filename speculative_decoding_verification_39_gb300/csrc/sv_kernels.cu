@@ -2085,6 +2085,281 @@ cudaError_t launch_seq(const Params& p, int dtype, int grid, cudaStream_t stream
   return dtype == 1 ? launch_seq_t<uint16_t>(p, grid, stream) : launch_seq_t<float>(p, grid, stream);
 }
 
+// ------------------------------------------------- warp-per-sequence mode ---
+// Sampling without top-p for short rows (V <= 1024 and the whole sequence
+// within 64 KB, rows 16-byte aligned): each warp verifies whole sequences on
+// its own, straight from global memory, with warp shuffles only — no shared
+// ring, no block barrier, no cross-CTA hand-off. Many sequences are in flight
+// per SM at once, which is what short rows need: their per-sequence work is a
+// chain of short dependent steps.
+
+constexpr int kWarpThreads = 256;
+constexpr int kWarpSeqWarps = kWarpThreads / 32;
+constexpr int kWarpMaxRows = 64;
+constexpr int64_t kWarpMaxV = 1024;
+
+// Online (max, sum 2^(x c - M c)) of NR rows at once (their loads in flight
+// together), every lane ending with the row's totals.
+template <typename E, int NR>
+__device__ __forceinline__ void warp_rows_ms(const char* row0, const char* row1, int nvec, float c, int lane,
+                                             float* m_out, float* s_out) {
+  const char* rows[2] = {row0, row1};
+  float m[NR], sa[NR][4];
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    m[r] = -INFINITY;
+    sa[r][0] = sa[r][1] = sa[r][2] = sa[r][3] = 0.f;
+  }
+  constexpr int kB = 8;  // vectors per lane per row per batch (a whole fp32 row of 1024)
+  for (int v0 = lane; v0 < nvec; v0 += 32 * kB) {
+    uint4 q[NR][kB];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+#pragma unroll
+      for (int k = 0; k < kB; ++k) {
+        const int v = v0 + 32 * k;
+        q[r][k] = v < nvec ? __ldg(reinterpret_cast<const uint4*>(rows[r]) + v) : neg_inf_vec(E());
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+      float vmax = vec_max(q[r][0], E());
+#pragma unroll
+      for (int k = 1; k < kB; ++k) vmax = fmax_nan(vmax, vec_max(q[r][k], E()));
+      const float nm = fmax_nan(m[r], vmax);
+      if (nm != m[r]) {
+        const float f = rescale(m[r], nm, c);
+        sa[r][0] *= f; sa[r][1] *= f; sa[r][2] *= f; sa[r][3] *= f;
+        m[r] = nm;
+      }
+      if (m[r] == -INFINITY) continue;
+      const float nmc = -mref(m[r], c);
+#pragma unroll
+      for (int k = 0; k < kB; ++k) vec_exp_add(q[r][k], c, nmc, sa[r], E());
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < NR; ++r) {
+    float mm = m[r], sum = (sa[r][0] + sa[r][1]) + (sa[r][2] + sa[r][3]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float m2 = __shfl_xor_sync(0xffffffffu, mm, o), s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+      ms_combine(mm, sum, m2, s2, c);
+    }
+    m_out[r] = mm;
+    s_out[r] = sum;
+  }
+}
+
+// The draw by one warp over rows of at most kWarpMaxV elements: the smallest
+// t with sum_{v<=t} w_v > u * Z (-1 when every weight is zero), w the residual
+// max(0, p' - q') (kRes) or p' up to a constant. A group is one 16-byte vector
+// of each row; lane l owns groups l, l+32, ... and keeps their sums, so the
+// scan that finds the crossing needs no second read; only the crossing
+// group's elements are read again.
+template <typename E, bool kRes>
+__device__ int64_t warp_draw(const char* rp, const char* rq, int64_t V, float c, float nMcp, float nMcq, float ip,
+                             float iq, float u, int lane) {
+  constexpr int PV = ET<E>::kPerVec;
+  constexpr int kMaxG = (int)(kWarpMaxV / 4 / 32);  // groups per lane
+  const int ng = (int)(V / PV);
+  auto weights = [&](const uint4 a, const uint4 bq, float w[PV]) {
+    float lp[PV], lq[PV];
+    if constexpr (PV == 8) {
+      lp[0] = bf_lo(a.x); lp[1] = bf_hi(a.x); lp[2] = bf_lo(a.y); lp[3] = bf_hi(a.y);
+      lp[4] = bf_lo(a.z); lp[5] = bf_hi(a.z); lp[6] = bf_lo(a.w); lp[7] = bf_hi(a.w);
+      lq[0] = bf_lo(bq.x); lq[1] = bf_hi(bq.x); lq[2] = bf_lo(bq.y); lq[3] = bf_hi(bq.y);
+      lq[4] = bf_lo(bq.z); lq[5] = bf_hi(bq.z); lq[6] = bf_lo(bq.w); lq[7] = bf_hi(bq.w);
+    } else {
+      lp[0] = __uint_as_float(a.x); lp[1] = __uint_as_float(a.y); lp[2] = __uint_as_float(a.z); lp[3] = __uint_as_float(a.w);
+      lq[0] = __uint_as_float(bq.x); lq[1] = __uint_as_float(bq.y); lq[2] = __uint_as_float(bq.z); lq[3] = __uint_as_float(bq.w);
+    }
+#pragma unroll
+    for (int k = 0; k < PV; ++k) {
+      const float ep = ex2(fmaf(lp[k], c, nMcp));
+      w[k] = kRes ? fmaxf(0.f, fmaf(ep, ip, -ex2(fmaf(lq[k], c, nMcq)) * iq)) : ep;
+    }
+  };
+  auto gsum = [&](const float w[PV]) {
+    float a = 0.f;
+#pragma unroll
+    for (int k = 0; k < PV; ++k) a += w[k];
+    return a;
+  };
+  const uint4* pv = reinterpret_cast<const uint4*>(rp);
+  const uint4* qv = reinterpret_cast<const uint4*>(rq);
+  uint4 a[kMaxG], bq[kMaxG];
+#pragma unroll
+  for (int i = 0; i < kMaxG; ++i) {
+    const int g = i * 32 + lane;
+    a[i] = g < ng ? __ldg(pv + g) : neg_inf_vec(E());
+    bq[i] = (kRes && g < ng) ? __ldg(qv + g) : neg_inf_vec(E());
+  }
+  float part[kMaxG];
+  float zl = 0.f;
+  int64_t lastpos = -1;
+#pragma unroll
+  for (int i = 0; i < kMaxG; ++i) {
+    float w[PV];
+    weights(a[i], bq[i], w);
+    part[i] = gsum(w);
+    zl += part[i];
+#pragma unroll
+    for (int k = 0; k < PV; ++k)
+      if (w[k] > 0.f) lastpos = (int64_t)(i * 32 + lane) * PV + k;
+  }
+  const float Z = warp_sum(zl);
+  if (!(Z > 0.f)) return -1;
+  const float Tg = u * Z;
+  float run = 0.f, before = 0.f;
+  int gstar = -1;  // the group holding the crossing, and the sum before it
+#pragma unroll
+  for (int i = 0; i < kMaxG; ++i) {
+    const float incl = warp_incl_scan(part[i], lane);
+    const float tot = __shfl_sync(0xffffffffu, incl, 31);
+    if (gstar < 0 && run + tot > Tg) {
+      const unsigned bal = __ballot_sync(0xffffffffu, run + incl > Tg);
+      const int fl = __ffs(bal) - 1;
+      gstar = i * 32 + fl;
+      before = __shfl_sync(0xffffffffu, run + incl - part[i], fl);
+    }
+    run += tot;
+  }
+  if (gstar >= 0) {  // one lane walks the crossing group, read again
+    int64_t t = -1;
+    if (lane == 0) {
+      float w[PV];
+      weights(__ldg(pv + gstar), kRes ? __ldg(qv + gstar) : neg_inf_vec(E()), w);
+      float acc = before;
+      int64_t lp = -1;
+#pragma unroll
+      for (int k = 0; k < PV; ++k) {
+        if (t < 0) {
+          acc += w[k];
+          if (w[k] > 0.f) lp = (int64_t)gstar * PV + k;
+          if (acc > Tg) t = (int64_t)gstar * PV + k;
+        }
+      }
+      if (t < 0) t = lp;  // rounding inside the group
+    }
+    return __shfl_sync(0xffffffffu, (long long)t, 0);
+  }
+  // u*Z at or past the total after rounding: the last positive weight
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) lastpos = max((long long)lastpos, __shfl_xor_sync(0xffffffffu, (long long)lastpos, o));
+  return lastpos;
+}
+
+template <typename E>
+__global__ void __launch_bounds__(kWarpThreads, 2) verify_warp_kernel(const Params p) {
+  __shared__ float s_m[kWarpSeqWarps][kWarpMaxRows], s_s[kWarpSeqWarps][kWarpMaxRows];
+  constexpr int S = ET<E>::kSize;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = p.K, R = p.RS;
+  const int64_t V = p.V;
+  const float c = p.c;
+  const int nvec = (int)(V / ET<E>::kPerVec);
+  float* rm = s_m[warp];
+  float* rsum = s_s[warp];
+  for (int64_t b = (int64_t)blockIdx.x * kWarpSeqWarps + warp; b < p.B; b += (int64_t)gridDim.x * kWarpSeqWarps) {
+    auto rowp = [&](int r) {
+      return r <= K ? p.a + ((b * (K + 1) + r) * V) * S : p.d + ((b * K + (r - K - 1)) * V) * S;
+    };
+    // this lane's first position's token and uniform, read while the rows stream
+    const int32_t x0 = lane < K ? __ldg(p.tokens + b * K + lane) : 0;
+    const float u0 = lane < K ? __ldg(p.uniforms + b * (K + 1) + lane) : 0.f;
+    const float uK = __ldg(p.uniforms + b * (K + 1) + K);
+    // ---- per-row (max, sum), two rows' loads in flight together
+    for (int r = 0; r < R; r += 2) {
+      float m2[2], s2[2];
+      if (r + 1 < R)
+        warp_rows_ms<E, 2>(rowp(r), rowp(r + 1), nvec, c, lane, m2, s2);
+      else
+        warp_rows_ms<E, 1>(rowp(r), nullptr, nvec, c, lane, m2, s2);
+      if (lane == 0) {
+        rm[r] = m2[0];
+        rsum[r] = s2[0];
+        if (r + 1 < R) {
+          rm[r + 1] = m2[1];
+          rsum[r + 1] = s2[1];
+        }
+      }
+    }
+    __syncwarp();
+    // ---- row stats out, validity, accept scan
+    int bad = 0;
+    for (int r = lane; r < R; r += 32) {
+      const float M = rm[r], sm = rsum[r];
+      const bool valid = (M > -INFINITY) && (M < INFINITY);
+      if (!valid) bad = 1;
+      if (p.out_row_stats) {
+        float4 o;
+        o.x = valid ? __fdiv_rn(M, p.T) : __int_as_float(0x7fc00000);
+        o.y = valid ? (mref(M, c) + lg2(sm)) * 0.69314718055994531f : __int_as_float(0x7fc00000);
+        o.z = valid ? 1.f : __int_as_float(0x7fc00000);
+        o.w = -INFINITY;
+        reinterpret_cast<float4*>(p.out_row_stats)[b * R + r] = o;
+      }
+    }
+    int jl = K;
+    for (int i = lane; i < K; i += 32) {
+      const int32_t x = i == lane ? x0 : p.tokens[b * K + i];
+      const float u = i == lane ? u0 : p.uniforms[b * (K + 1) + i];
+      if (x < 0 || (int64_t)x >= V || !(u >= 0.f && u < 1.f)) {
+        bad = 1;
+        continue;
+      }
+      const float Mp = rm[i], Mq = rm[K + 1 + i];
+      if (!(Mp > -INFINITY && Mp < INFINITY && Mq > -INFINITY && Mq < INFINITY)) continue;  // counted above
+      const float lp = ET<E>::load(rowp(i), x), lq = ET<E>::load(rowp(K + 1 + i), x);
+      float alpha;
+      if (lp == -INFINITY) alpha = 0.f;
+      else if (lq == -INFINITY) alpha = 1.f;
+      else alpha = fminf(1.f, ex2(fmaf(lp, c, -mref(Mp, c)) - fmaf(lq, c, -mref(Mq, c))) * (rsum[K + 1 + i] / rsum[i]));
+      if (!(u < alpha) && i < jl) jl = i;
+    }
+    if (lane == 0 && !(uK >= 0.f && uK < 1.f)) bad = 1;
+    const int j = (int)__reduce_min_sync(0xffffffffu, (unsigned)jl);
+    int32_t* out = p.out_tokens + b * (K + 1);
+    if (__any_sync(0xffffffffu, bad)) {
+      for (int i = lane; i <= K; i += 32) out[i] = -1;
+      if (lane == 0) {
+        p.out_accept_len[b] = -1;
+        atomicOr(p.ctl + 3, kStatusInput);
+      }
+      continue;
+    }
+    // ---- the draw
+    const float nMp = -mref(rm[j], c), ip = 1.f / rsum[j];
+    int64_t t = -1;
+    if (j < K) {
+      const float nMq = -mref(rm[K + 1 + j], c), iq = 1.f / rsum[K + 1 + j];
+      t = warp_draw<E, true>(rowp(j), rowp(K + 1 + j), V, c, nMp, nMq, ip, iq, uK, lane);
+    }
+    if (t < 0) t = warp_draw<E, false>(rowp(j), nullptr, V, c, nMp, 0.f, 1.f, 0.f, uK, lane);
+    for (int i = lane; i <= K; i += 32) out[i] = i < j ? p.tokens[b * K + i] : (i == j ? (int32_t)t : -1);
+    if (lane == 0) p.out_accept_len[b] = j;
+    __syncwarp();
+  }
+}
+
+bool warp_mode_fits(int64_t K, int64_t V, int esz) {
+  const int64_t R = 2 * K + 1;
+  return R <= kWarpMaxRows && V <= kWarpMaxV && (V * esz) % 16 == 0 && R * V * esz <= 65536;
+}
+
+template <typename E>
+static cudaError_t launch_warp_t(const Params& p, int grid, cudaStream_t stream) {
+  verify_warp_kernel<E><<<grid, kWarpThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_warp(const Params& p, int dtype, int grid, cudaStream_t stream) {
+  return dtype == 1 ? launch_warp_t<uint16_t>(p, grid, stream) : launch_warp_t<float>(p, grid, stream);
+}
+
+int warp_mode_seqs_per_cta() { return kWarpSeqWarps; }
+
 // ------------------------------------------------------------- launching ------
 
 template <typename E, int MODE>

@@ -80,6 +80,12 @@ cudaError_t launch(const Params& p, int dtype, int mode, int grid, cudaStream_t 
 // staged in shared memory. seq_mode_fits() says whether a shape qualifies
 // (2K+1 <= 64 rows, the sequence within 48 KB, rows 16-byte aligned).
 bool seq_mode_fits(int64_t K, int64_t V, int esz);
+// Sampling mode for rows of at most 1024 elements: one warp per sequence,
+// from global memory (2K+1 <= 64 rows, the sequence within 64 KB, rows
+// 16-byte aligned).
+bool warp_mode_fits(int64_t K, int64_t V, int esz);
+cudaError_t launch_warp(const Params& p, int dtype, int grid, cudaStream_t stream);
+int warp_mode_seqs_per_cta();
 cudaError_t launch_seq(const Params& p, int dtype, int grid, cudaStream_t stream);
 int kernel_threads();
 
