@@ -20,6 +20,15 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch: let the next kernel on the stream be
+// scheduled now (trigger), then wait until the previous one has completed and
+// its writes are visible (a no-op when the kernel was launched without the
+// attribute).
+__device__ __forceinline__ void grid_dependency_sync(bool trigger = true) {
+  if (trigger) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -1727,6 +1727,7 @@ __global__ void __launch_bounds__(kAllThreads, 2) verify_kernel(const Params p) 
     fence_mbar_init();
   }
   __syncthreads();
+  grid_dependency_sync();
   const int warp = tid >> 5;
   if (warp == kProducerWarp) {
     if ((tid & 31) == 0) producer_loop<E, MODE>(p, ring, sh);
@@ -2055,6 +2056,7 @@ __global__ void __launch_bounds__(kSeqThreads, 2) verify_seq_kernel(const Params
     fence_mbar_init();
   }
   __syncthreads();
+  grid_dependency_sync();
   if (tid >= kConsumerThreads) {
     if (tid == kConsumerThreads) seq_producer<E>(p, ring, sh);
     return;
@@ -2067,6 +2069,25 @@ bool seq_mode_fits(int64_t K, int64_t V, int esz) {
   return R <= kSeqMaxRows && R * V * esz <= kSeqStageBytes && (V * esz) % 16 == 0;
 }
 
+// Every kernel is launched with programmatic stream serialization: it may be
+// scheduled while the kernel before it on the stream is still finishing, and
+// waits for that kernel (grid_dependency_sync) before it touches global
+// memory, so only its launch and shared-memory set-up overlap.
+template <typename Kern>
+static cudaError_t launch_pdl(Kern* k, int grid, int threads, size_t smem, cudaStream_t stream, const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, k, p);
+}
+
 template <typename E>
 static cudaError_t launch_seq_t(const Params& p, int grid, cudaStream_t stream) {
   const size_t smem = seq_shared_bytes();
@@ -2077,8 +2098,7 @@ static cudaError_t launch_seq_t(const Params& p, int grid, cudaStream_t stream) 
     if (e != cudaSuccess) return e;
     raised = true;
   }
-  k<<<grid, kSeqThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k, grid, kSeqThreads, smem, stream, p);
 }
 
 cudaError_t launch_seq(const Params& p, int dtype, int grid, cudaStream_t stream) {
@@ -2261,6 +2281,9 @@ __global__ void __launch_bounds__(kWarpThreads, 2) verify_warp_kernel(const Para
   const int nvec = (int)(V / ET<E>::kPerVec);
   float* rm = s_m[warp];
   float* rsum = s_s[warp];
+  // No early trigger: this grid may leave SMs empty, and the next one should
+  // spread over all of them rather than fill the free slots of this one.
+  grid_dependency_sync(false);
   for (int64_t b = (int64_t)blockIdx.x * kWarpSeqWarps + warp; b < p.B; b += (int64_t)gridDim.x * kWarpSeqWarps) {
     auto rowp = [&](int r) {
       return r <= K ? p.a + ((b * (K + 1) + r) * V) * S : p.d + ((b * K + (r - K - 1)) * V) * S;
@@ -2350,8 +2373,7 @@ bool warp_mode_fits(int64_t K, int64_t V, int esz) {
 
 template <typename E>
 static cudaError_t launch_warp_t(const Params& p, int grid, cudaStream_t stream) {
-  verify_warp_kernel<E><<<grid, kWarpThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(verify_warp_kernel<E>, grid, kWarpThreads, 0, stream, p);
 }
 
 cudaError_t launch_warp(const Params& p, int dtype, int grid, cudaStream_t stream) {
@@ -2374,8 +2396,7 @@ static cudaError_t launch_t(const Params& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     raised = shared_bytes(kMaxStages);
   }
-  k<<<grid, kAllThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k, grid, kAllThreads, smem, stream, p);
 }
 
 int kernel_threads() { return kAllThreads; }
