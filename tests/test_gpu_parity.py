@@ -42,10 +42,13 @@ SAMPLE_CASES = {
     "topp_flat": C["cfg2_v32000_bf16"].with_(B=6, K=2, V=9000, target_sigma=0.05, draft_sigma=0.02, top_p=0.95,
                                              n_peaks=0),
     "hot_T2": C["cfg2_v32000_bf16"].with_(B=10, K=4, V=16384, temperature=2.0),
-    # whole sequences in one CTA (2K+1 rows within 48 KB, rows 16-byte aligned)
+    # whole sequences in one CTA (2K+1 rows within 48 KB, rows 16-byte aligned);
+    # rows of at most 1024 elements: one warp per sequence
     "seqmode_bf16_v2048_k3": C["cfg2_v32000_bf16"].with_(B=50, K=3, V=2048),
     "seqmode_f32_v8_k2": C["cfg1_v1000_f32"].with_(B=400, K=2, V=8),
     "seqmode_bf16_v512_k15": C["cfg2_v32000_bf16"].with_(B=40, K=15, V=512, temperature=0.6),
+    "warpmode_f32_v1024_k7": C["cfg1_v1000_f32"].with_(B=700, K=7, V=1024),
+    "warpmode_bf16_v16_k31": C["cfg2_v32000_bf16"].with_(B=90, K=31, V=16, temperature=1.3),
 }
 
 
@@ -142,8 +145,9 @@ def test_bad_inputs_flag_only_their_sequence():
     assert svpkg.get_status() == -4
 
 
-def test_bad_inputs_in_sequence_mode():
-    cfg = C["cfg2_v32000_bf16"].with_(B=8, K=3, V=1024)
+@pytest.mark.parametrize("V", [1024, 2048])  # one warp per sequence / one CTA per sequence
+def test_bad_inputs_in_sequence_mode(V):
+    cfg = C["cfg2_v32000_bf16"].with_(B=8, K=3, V=V)
     d = sg.sample_inputs(cfg)
     d["draft_tokens"][0, 1] = cfg.V
     d["uniforms"][2, 3] = 1.0
