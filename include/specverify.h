@@ -142,7 +142,7 @@ int sv_verify_greedy(const void* logits, const int32_t* cand, int64_t B, int32_t
  *   - A call whose scratch would exceed 4 MiB returns SV_ERR_SCRATCH_LIMIT and
  *     enqueues nothing. The scratch needed is about
  *     256 + 4*(B*R + B*(3+D)) + 8*B*R*ceil(NT/CT) + 16*B*R bytes (R = 2K+1
- *     rows per sequence), plus 4*B*ceil(V/256) + 32*B when the draws are split
+ *     rows per sequence), plus 4*B*ceil(V/256) when the draws are split
  *     over D > 0 chunks, e.g. about 0.2 MiB for B=256, K=8, V=128256.
  *   - The first call on a device looks up the array's device address on that
  *     device (cudaGetSymbolAddress, with the device current) and caches it;

@@ -116,10 +116,9 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   if (mode == sv::kSample) {
     const int64_t half = sv::draw_cells_per_chunk(p.stages, esz, p.V);
     int64_t dc = half > 0 ? (ncells + half - 1) / half : 0;
-    // Only long draws (six ring halves or more) in calls that leave most CTAs
-    // idle at the end gain from the split: short ones lose more to the hand-off.
+    // Only calls that leave most CTAs idle at their end gain from the split.
     const int64_t cover = (slots + p.B - 1) / p.B;
-    if (dc < 6 || p.B * 2 > slots) dc = 0;
+    if (p.B * 2 > slots) dc = 0;
     if (dc > cover) dc = cover;
     if (dc >= 2 && p.B * (1 + dc) < (int64_t(1) << 30)) {
       p.DC = (int)dc;
@@ -130,7 +129,7 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   const size_t part_bytes = align256((size_t)p.W * 8);
   const size_t rowstat_bytes = align256((size_t)rows_total * 16);
   const size_t dcells_bytes = p.DC ? align256((size_t)p.B * (size_t)ncells * 4) : 0;
-  const size_t data_bytes = part_bytes + rowstat_bytes + dcells_bytes + (p.DC ? (size_t)p.B * sizeof(sv::DrawJob) : 0);
+  const size_t data_bytes = part_bytes + rowstat_bytes + dcells_bytes;
   Scratch sc;
   int dev = 0;
   int rc = get_scratch(stream, cnt_words, data_bytes, &sc, &dev);
@@ -144,7 +143,6 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   p.part = reinterpret_cast<float2*>(b + data_offset(sc));
   p.rowstat = reinterpret_cast<float4*>(b + data_offset(sc) + part_bytes);
   p.dcells = reinterpret_cast<float*>(b + data_offset(sc) + part_bytes + rowstat_bytes);
-  p.djob = reinterpret_cast<sv::DrawJob*>(b + data_offset(sc) + part_bytes + rowstat_bytes + dcells_bytes);
   // Short rows: one warp per sequence (rows of at most 1024 elements), else
   // one CTA per sequence with the whole sequence staged in shared memory.
   const bool short_ok = mode == sv::kSample && !p.topp && aligned_to(p.a, 16) && aligned_to(p.d, 16);

@@ -894,6 +894,15 @@ __device__ void topp_cut(const Params& p, Shared& sh, const char* row, float M, 
 
 // ------------------------------------------------------ sequence tails -------
 
+// What a sequence's accept scan decided, for its draw.
+struct DrawJob {
+  float uK;          // the draw's uniform
+  float nMcp, nMcq;  // -M c of the p and q rows
+  float ip, iq;      // 1 / nucleus mass of the p and q rows
+  float tp, tq;      // nucleus thresholds (-inf without top-p)
+  int j;             // the rejected position (K: bonus draw)
+};
+
 __device__ __forceinline__ bool rows_aligned(const Params& p, int esz) {
   return (p.V * esz) % 16 == 0 && (reinterpret_cast<uintptr_t>(p.a) & 15) == 0 &&
          (reinterpret_cast<uintptr_t>(p.d) & 15) == 0;
@@ -922,27 +931,11 @@ __device__ int64_t draw_whole(const Params& p, Shared& sh, int64_t b, const Draw
   return t;
 }
 
-// Hand sequence b's draw to the CTAs draining the queue: its job record, then
-// p.DC chunk entries (thread 0).
 constexpr uint32_t kTailClaimed = 0x80000000u;
 constexpr uint32_t kTailChunk = 0x40000000u;
-__device__ void draw_publish(const Params& p, int64_t b, const DrawJob& jb) {
-  DrawJob* d = p.djob + b;
-  d->uK = jb.uK;
-  d->nMcp = jb.nMcp;
-  d->nMcq = jb.nMcq;
-  d->ip = jb.ip;
-  d->iq = jb.iq;
-  d->tp = jb.tp;
-  d->tq = jb.tq;
-  d->j = jb.j;
-  __threadfence();
-  const uint32_t k0 = atomicAdd(p.ctl + 4, (uint32_t)p.DC);
-  for (int c = 0; c < p.DC; ++c) st_release_gpu(p.tail_q + k0 + c, kTailChunk | (uint32_t)(b * p.DC + c + 1));
-}
 
 template <typename E>
-__device__ void seq_sample(const Params& p, Shared& sh, int64_t b, int tid) {
+__device__ __forceinline__ bool seq_decide(const Params& p, Shared& sh, int64_t b, int tid, DrawJob& jb) {
   const int K = p.K;
   const float c = p.c;
   if (tid == 0) sh.bi[1] = K;
@@ -980,25 +973,11 @@ __device__ void seq_sample(const Params& p, Shared& sh, int64_t b, int tid) {
   }
   bad = cbar_or(bad);
   const int j = sh.bi[1];
-  int32_t* out = p.out_tokens + b * (K + 1);
-  if (bad) {
-    for (int i = tid; i <= K; i += kConsumerThreads) out[i] = -1;
-    if (tid == 0) {
-      p.out_accept_len[b] = -1;
-      atomicOr(p.ctl + 3, kStatusInput);
-      if (p.DC > 0) {  // the sequence's draw chunks still count: they do nothing
-        DrawJob jb{};
-        jb.j = -1;
-        draw_publish(p, b, jb);
-      }
-    }
-    return;
-  }
-  const float uK = p.uniforms[b * (K + 1) + K];
+  cbar();
+  if (bad) return false;
   const RowStat rp = rs_load(p, b * p.RS + j);
   const RowStat rq = rs_load(p, b * p.RS + K + 1 + (j < K ? j : 0));
-  DrawJob jb;
-  jb.uK = uK;
+  jb.uK = p.uniforms[b * (K + 1) + K];
   jb.j = j;
   jb.nMcp = -mref(rp.M, c);
   jb.ip = 1.f / rp.cum;
@@ -1006,20 +985,41 @@ __device__ void seq_sample(const Params& p, Shared& sh, int64_t b, int tid) {
   jb.nMcq = -mref(rq.M, c);
   jb.iq = 1.f / rq.cum;
   jb.tq = p.topp ? key_floor<E>(rq.tau) : -INFINITY;
+  return true;
+}
+
+// Sequence b's outputs other than the drawn token (all -1 for bad input).
+__device__ __forceinline__ void seq_write_prefix(const Params& p, int64_t b, bool ok, int j, int tid) {
+  const int K = p.K;
+  int32_t* out = p.out_tokens + b * (K + 1);
+  if (!ok) {
+    for (int i = tid; i <= K; i += kConsumerThreads) out[i] = -1;
+    if (tid == 0) {
+      p.out_accept_len[b] = -1;
+      atomicOr(p.ctl + 3, kStatusInput);
+    }
+    return;
+  }
   for (int i = tid; i <= K; i += kConsumerThreads)
     if (i != j) out[i] = i < j ? p.tokens[b * K + i] : -1;
   if (tid == 0) p.out_accept_len[b] = j;
-  if (p.DC > 0) {  // other CTAs sum the cells; the last of them finishes the draw
-    if (tid == 0) draw_publish(p, b, jb);
-    return;
-  }
+}
+
+// Sequence b's tail when its draw is not split (p.DC == 0): the accept scan
+// and the whole draw in this CTA.
+template <typename E>
+__device__ void seq_sample(const Params& p, Shared& sh, int64_t b, int tid) {
+  DrawJob jb;
+  const bool ok = seq_decide<E>(p, sh, b, tid, jb);
+  seq_write_prefix(p, b, ok, jb.j, tid);
+  if (!ok) return;
   // The tile ring is idle while sequence tails run (they run only after the
   // CTA's streaming is over), so the draw stages its rows there.
   char* ring = reinterpret_cast<char*>(&sh) - (size_t)p.stages * kTileBytes;
   const size_t ring_bytes = (size_t)p.stages * kTileBytes;
   const int64_t t = p.topp ? draw_whole<E, true>(p, sh, b, jb, tid, ring, ring_bytes)
                            : draw_whole<E, false>(p, sh, b, jb, tid, ring, ring_bytes);
-  if (tid == 0) out[j] = (int32_t)t;
+  if (tid == 0) p.out_tokens[b * (p.K + 1) + jb.j] = (int32_t)t;
 }
 
 template <typename E>
@@ -1153,7 +1153,15 @@ __device__ void enqueue_task(const Params& p, Shared& sh, int64_t task, float m,
 // written, ctl[5] the entries taken, tq_global[k] holds b+1 (0 = not yet
 // written). CTAs take entries only once their own streaming work is done, so
 // a tail never holds up tiles that other sequences are waiting for.
+// A sequence whose draw is split over p.DC CTAs queues p.DC chunk entries
+// instead (kTailChunk | b*DC + c + 1), each running the accept scan and one
+// range of the draw's cells.
 __device__ __forceinline__ void tail_enqueue(const Params& p, int64_t b) {
+  if (p.DC > 0) {
+    const uint32_t k = atomicAdd(p.ctl + 4, (uint32_t)p.DC);
+    for (int c = 0; c < p.DC; ++c) st_release_gpu(p.tail_q + k + c, kTailChunk | (uint32_t)(b * p.DC + c + 1));
+    return;
+  }
   const uint32_t k = atomicAdd(p.ctl + 4, 1u);
   st_release_gpu(p.tail_q + k, (uint32_t)(b + 1));
 }
@@ -1180,7 +1188,7 @@ __device__ __forceinline__ bool seq_row_final(const Params& p, int64_t b) {
 // this CTA still streams, locally once it does not.
 __device__ __forceinline__ void seq_arrive(const Params& p, Shared& sh, int64_t b, bool local) {
   if (!seq_row_final(p, b)) return;
-  if (local) {
+  if (local && p.DC == 0) {
     enqueue_task(p, sh, -(b + 1), 0.f, 0.f);
     tail_claim(p, b);
   } else {
@@ -1272,7 +1280,7 @@ __device__ void run_task(const Params& p, Shared& sh, int64_t task, float m, flo
       store_sample_row<E>(p, task, m, s, cum, tau);
       int run_here = 0;
       if (seq_row_final(p, b)) {
-        if (local) {
+        if (local && p.DC == 0) {
           tail_claim(p, b);
           run_here = 1;
         } else {
@@ -1288,30 +1296,24 @@ __device__ void run_task(const Params& p, Shared& sh, int64_t task, float m, flo
   }
 }
 
-// One chunk of a split draw (sampling mode): the cell sums of cells
-// [c*CPC, (c+1)*CPC) of sequence b's draw, written to p.dcells. The CTA that
-// completes the last chunk scans all the cells and writes the token.
+// One chunk of sequence b's split draw (sampling mode, p.DC > 0). Every chunk
+// CTA runs the short accept scan itself, so no decision is handed over;
+// chunk 0 writes the outputs other than the drawn token. Each sums the cells
+// [c*CPC, (c+1)*CPC) of the draw into p.dcells; the CTA that completes the last
+// chunk scans all the cells and writes the drawn token.
 template <typename E, bool kTopp>
 __device__ void draw_chunk(const Params& p, Shared& sh, int64_t b, int c, int tid) {
   DrawJob jb;
-  {
-    const DrawJob* d = p.djob + b;
-    jb.uK = __ldcg(&d->uK);
-    jb.nMcp = __ldcg(&d->nMcp);
-    jb.nMcq = __ldcg(&d->nMcq);
-    jb.ip = __ldcg(&d->ip);
-    jb.iq = __ldcg(&d->iq);
-    jb.tp = __ldcg(&d->tp);
-    jb.tq = __ldcg(&d->tq);
-    jb.j = __ldcg(&d->j);
-  }
+  const bool ok = seq_decide<E>(p, sh, b, tid, jb);
+  if (c == 0) seq_write_prefix(p, b, ok, jb.j, tid);
+  if (!ok) jb.j = -1;
   const int64_t CE = cell_elems(p.V);
   const int ncells = (int)((p.V + CE - 1) / CE);
   float* cells = p.dcells + b * ncells;
   char* ring = reinterpret_cast<char*>(&sh) - (size_t)p.stages * kTileBytes;
   const size_t ring_bytes = (size_t)p.stages * kTileBytes;
   const int cbeg = min(ncells, c * p.CPC), cend = min(ncells, (c + 1) * p.CPC);
-  if (jb.j >= 0 && cbeg < cend) {
+  if (ok && cbeg < cend) {
     if (jb.j < p.K) {
       const Weights<E, true, kTopp> wf = residual_weights<E, kTopp>(p, b, jb);
       if (!cells_staged<E>(wf, p.V, CE, cbeg, cend, cells, ring, ring_bytes, sh, tid, p.ctl + 3))
@@ -1333,7 +1335,7 @@ __device__ void draw_chunk(const Params& p, Shared& sh, int64_t b, int c, int ti
   cbar();
   const int last = sh.flag;
   cbar();
-  if (!last || jb.j < 0) return;
+  if (!last || !ok) return;
   for (int i = tid; i < ncells; i += kConsumerThreads) sh.cells[i] = __ldcg(cells + i);
   cbar();
   int64_t t = -1;
@@ -1352,7 +1354,7 @@ __device__ void draw_chunk(const Params& p, Shared& sh, int64_t b, int c, int ti
 // CTA, so the wait ends.
 template <typename E, int MODE>
 __device__ void drain_tails(const Params& p, Shared& sh, int tid) {
-  const int64_t entries = p.B * (1 + (MODE == kSample ? (int64_t)p.DC : 0));
+  const int64_t entries = p.B * (MODE == kSample && p.DC > 0 ? (int64_t)p.DC : 1);
   for (;;) {
     if (tid == 0) {
       const uint32_t k = atomicAdd(p.ctl + 5, 1u);

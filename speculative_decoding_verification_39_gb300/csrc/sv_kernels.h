@@ -26,15 +26,6 @@ inline int64_t draw_cells_per_chunk(int stages, int esz, int64_t V) {
   return half / 2 / esz / cell_elems(V);
 }
 
-// A sampling draw handed to other CTAs: what the sequence's tail decided.
-struct DrawJob {
-  float uK;                 // the draw's uniform
-  float nMcp, nMcq;         // -M c of the p and q rows
-  float ip, iq;             // 1 / nucleus mass of the p and q rows
-  float tp, tq;             // nucleus thresholds (-inf without top-p)
-  int32_t j;                // the rejected position (K: bonus draw; -1: bad input, no draw)
-};
-
 struct Params {
   const char* a;           // target logits [B,K+1,V] (sampling) or logits [B,G,N,V] (greedy)
   const char* d;           // draft logits [B,K,V] (sampling, T > 0)
@@ -60,7 +51,7 @@ struct Params {
                            // [4] tails queued, [5] tails taken, [6] finished CTAs
   uint32_t* row_cnt;       // [B*RS] chunks published per row
   uint32_t* seq_cnt;       // [B] rows finished per sequence
-  uint32_t* tail_q;        // [B * (1 + DC)] queued sequence tails and draw chunks (0 = empty)
+  uint32_t* tail_q;        // [B * max(1, DC)] queued sequence tails or draw chunks (0 = empty)
   float2* part;            // [W] per-chunk partials
   float4* rowstat;         // [B*RS] per-row results
   int stages;
@@ -70,7 +61,6 @@ struct Params {
   int CPC;
   float* dcells;           // [B][kMaxCells] cell sums
   uint32_t* dcnt;          // [B] chunks done
-  DrawJob* djob;           // [B]
 };
 
 size_t shared_bytes(int stages);

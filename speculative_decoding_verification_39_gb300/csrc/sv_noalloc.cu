@@ -130,10 +130,9 @@ extern "C" int sv_verify_sample_noalloc(const void* target_logits, const void* d
   if (!limit) {
     const int64_t half = sv::draw_cells_per_chunk(kStages, (int)esz, V);
     int64_t dc = half > 0 ? (ncells + half - 1) / half : 0;
-    // Only long draws (six ring halves or more) in calls that leave most CTAs
-    // idle at the end gain from the split: short ones lose more to the hand-off.
+    // Only calls that leave most CTAs idle at their end gain from the split.
     const int64_t cover = (slots + B - 1) / B;
-    if (dc < 6 || B * 2 > slots) dc = 0;
+    if (B * 2 > slots) dc = 0;
     if (dc > cover) dc = cover;
     if (dc >= 2 && B * (1 + dc) < (int64_t(1) << 30)) {
       p.DC = (int)dc;
@@ -146,8 +145,7 @@ extern "C" int sv_verify_sample_noalloc(const void* target_logits, const void* d
   const size_t part_bytes = up256((size_t)p.W * 8);
   const size_t rowstat_bytes = up256((size_t)rows * 16);
   const size_t dcells_bytes = p.DC ? up256((size_t)B * (size_t)ncells * 4) : 0;
-  const size_t need = kCtl + cnt_bytes + part_bytes + rowstat_bytes + dcells_bytes +
-                      (p.DC ? (size_t)B * sizeof(sv::DrawJob) : 0);
+  const size_t need = kCtl + cnt_bytes + part_bytes + rowstat_bytes + dcells_bytes;
   if (need > kNoAllocScratchBytes) return SV_ERR_SCRATCH_LIMIT;
   char* s = static_cast<char*>(base);
   p.ctl = reinterpret_cast<uint32_t*>(s);
@@ -158,7 +156,6 @@ extern "C" int sv_verify_sample_noalloc(const void* target_logits, const void* d
   p.part = reinterpret_cast<float2*>(s + kCtl + cnt_bytes);
   p.rowstat = reinterpret_cast<float4*>(s + kCtl + cnt_bytes + part_bytes);
   p.dcells = reinterpret_cast<float*>(s + kCtl + cnt_bytes + part_bytes + rowstat_bytes);
-  p.djob = reinterpret_cast<sv::DrawJob*>(s + kCtl + cnt_bytes + part_bytes + rowstat_bytes + dcells_bytes);
 
   // The array keeps whatever the last call left: the control block and the
   // counters must start at zero, so clear them on the caller's stream (a
