@@ -2115,7 +2115,7 @@ cudaError_t launch_seq(const Params& p, int dtype, int grid, cudaStream_t stream
 // per SM at once, which is what short rows need: their per-sequence work is a
 // chain of short dependent steps.
 
-constexpr int kWarpThreads = 256;
+constexpr int kWarpThreads = 128;
 constexpr int kWarpSeqWarps = kWarpThreads / 32;
 constexpr int kWarpMaxRows = 64;
 constexpr int64_t kWarpMaxV = 1024;
@@ -2273,7 +2273,7 @@ __device__ int64_t warp_draw(const char* rp, const char* rq, int64_t V, float c,
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kWarpThreads, 2) verify_warp_kernel(const Params p) {
+__global__ void __launch_bounds__(kWarpThreads, 4) verify_warp_kernel(const Params p) {
   __shared__ float s_m[kWarpSeqWarps][kWarpMaxRows], s_s[kWarpSeqWarps][kWarpMaxRows];
   constexpr int S = ET<E>::kSize;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
