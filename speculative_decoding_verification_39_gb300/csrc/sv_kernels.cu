@@ -1157,9 +1157,10 @@ __device__ void enqueue_task(const Params& p, Shared& sh, int64_t task, float m,
 // instead (kTailChunk | b*DC + c + 1), each running the accept scan and one
 // range of the draw's cells.
 __device__ __forceinline__ void tail_enqueue(const Params& p, int64_t b) {
-  if (p.DC > 0) {
+  if (p.DC > 0) {  // one fence for all the entries, then plain stores
     const uint32_t k = atomicAdd(p.ctl + 4, (uint32_t)p.DC);
-    for (int c = 0; c < p.DC; ++c) st_release_gpu(p.tail_q + k + c, kTailChunk | (uint32_t)(b * p.DC + c + 1));
+    fence_acq_rel_gpu();
+    for (int c = 0; c < p.DC; ++c) st_relaxed_gpu(p.tail_q + k + c, kTailChunk | (uint32_t)(b * p.DC + c + 1));
     return;
   }
   const uint32_t k = atomicAdd(p.ctl + 4, 1u);
