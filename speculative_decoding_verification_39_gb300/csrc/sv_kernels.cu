@@ -1,18 +1,25 @@
 // sv_kernels.cu — the verify-step kernels of libspecverify (sm_103a).
 //
-// One persistent kernel per call. Each CTA has one producer warp and eight
-// consumer warps around a ring of shared-memory stages. The producer takes
-// the next tile of the call from a global work counter and moves it from HBM
-// into a stage with a 1-D bulk copy (TMA) that completes on the stage's
-// mbarrier; the consumers reduce the tile and hand the stage back. A tile is
-// up to 16 KB of one logit row; tiles are numbered sequence-major, so the
-// rows of one sequence are read close together in time and stay in L2 for
-// the second look the sampler needs.
+// verify_kernel: one persistent kernel per call. Each CTA has one producer
+// warp, eight consumer warps and one publisher warp around a ring of
+// shared-memory stages. The producer takes the next chunk of the call (up to
+// eight 32 KB tiles of one logit row) from a global work counter and moves
+// each tile from HBM into a stage with a 1-D bulk copy that completes on the
+// stage's mbarrier; the consumers reduce the tile and hand the stage back; the
+// publisher combines the warps' partials per chunk and finishes rows. Chunks
+// are numbered sequence-major, so the rows of one sequence are read close
+// together in time and stay in L2 for the second look the draw needs.
 //
-// Cross-CTA hand-off is "the last arriver does the work", never a wait: the
-// CTA that publishes the last tile partial of a row finalises the row (its
-// normaliser, its top-p cut or its argmax), and the CTA that finalises the
-// last row of a sequence runs the sequence's decision and draw.
+// Cross-CTA hand-off is "the last arriver does the work", never a wait on
+// another CTA's progress: the publisher that counts the last chunk of a row
+// finalises the row (its normaliser, its top-p cut or its argmax), and the one
+// that counts the last row of a sequence queues the sequence's tail (or the
+// chunks of its split draw) on a global ticket queue, which CTAs drain once
+// their own streaming is over. A split draw's last chunk finishes the draw.
+//
+// verify_seq_kernel (one CTA per sequence, the sequence staged in shared
+// memory) and verify_warp_kernel (one warp per sequence, from global memory)
+// serve sampling calls whose rows are short.
 //
 // Per-row quantities (sampling mode), with c = log2(e)/T:
 //   M   = max_v l_v                       (raw stored logit)
