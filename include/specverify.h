@@ -169,6 +169,18 @@ int sv_verify_sample_noalloc(const void* target_logits, const void* draft_logits
  */
 int sv_get_status(void* stream);
 
+/*
+ * Self-test of the failure path (the pages have no counterpart; it exists so
+ * that the timeout handling can be tested without any fault): enqueues on
+ * `stream` a one-thread kernel that waits for a control word nothing ever
+ * sets, gives up after limit_ns nanoseconds (0..2e9) exactly as every
+ * internal wait does, and records SV_ERR_TIMEOUT in the stream's status. A
+ * following sv_get_status(stream) returns SV_ERR_TIMEOUT and resets the
+ * stream's scratch; later calls work as before. Returns SV_ERR_ARG for a
+ * limit outside the range, SV_ERR_NOMEM / SV_ERR_CUDA as the other calls.
+ */
+int sv_selftest_wait_timeout(int64_t limit_ns, void* stream);
+
 /* A static, human-readable name for an sv_status value. */
 const char* sv_status_string(int status);
 

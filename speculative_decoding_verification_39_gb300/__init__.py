@@ -108,13 +108,15 @@ def lib():
         h.sv_launch_count.restype = ctypes.c_uint64
         h.sv_verify_sample_noalloc.argtypes = [vp, vp, vp, vp, i64, i32, i64, i32, f32, f32, vp, vp, vp, vp]
         h.sv_verify_sample_noalloc.restype = ctypes.c_int
+        h.sv_selftest_wait_timeout.argtypes = [i64, vp]
+        h.sv_selftest_wait_timeout.restype = ctypes.c_int
         _lib_handle = h
     return _lib_handle
 
 
 def exported_symbols() -> list:
     return ["sv_verify_sample", "sv_verify_greedy", "sv_get_status", "sv_status_string", "sv_release",
-            "sv_set_launch_shape", "sv_launch_count", "sv_verify_sample_noalloc"]
+            "sv_set_launch_shape", "sv_launch_count", "sv_verify_sample_noalloc", "sv_selftest_wait_timeout"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -238,6 +240,16 @@ def get_status(device=None) -> int:
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     with torch.cuda.device(dev):
         return lib().sv_get_status(_stream_handle(dev))
+
+
+def selftest_wait_timeout(limit_ns: int = 10_000_000, device=None) -> None:
+    """Enqueue the bounded-wait self-test on the current stream: a following
+    get_status() reports SV_ERR_TIMEOUT (-5)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        rc = lib().sv_selftest_wait_timeout(int(limit_ns), _stream_handle(dev))
+    if rc != 0:
+        raise SpecVerifyError(rc, "sv_selftest_wait_timeout")
 
 
 def set_launch_shape(stages: int = 0, ctas_per_sm: int = 0) -> None:

@@ -263,6 +263,18 @@ extern "C" int sv_get_status(void* stream) {
   return SV_ERR_INPUT;
 }
 
+extern "C" int sv_selftest_wait_timeout(int64_t limit_ns, void* stream) {
+  if (limit_ns < 0 || limit_ns > 2000000000LL) return SV_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Scratch sc;
+  int dev = 0;
+  const int rc = get_scratch(st, 1, 1, &sc, &dev);
+  if (rc != SV_OK) return rc;
+  if (sv::launch_wait_selftest(static_cast<uint32_t*>(sc.base), (uint64_t)limit_ns, st) != cudaSuccess)
+    return SV_ERR_CUDA;
+  return SV_OK;
+}
+
 extern "C" const char* sv_status_string(int status) {
   switch (status) {
     case SV_OK: return "ok";

@@ -2392,6 +2392,24 @@ cudaError_t launch_warp(const Params& p, int dtype, int grid, cudaStream_t strea
 
 int warp_mode_seqs_per_cta() { return kWarpSeqWarps; }
 
+// ------------------------------------------------------------ self-test ------
+// The bounded-wait path, made to run out on purpose without any fault: one
+// thread waits for a control word that nothing ever sets, gives up after
+// limit_ns like every wait in the kernels, and records a timeout in the
+// status word the host reads.
+__global__ void wait_selftest_kernel(uint32_t* ctl, uint64_t limit_ns) {
+  if (threadIdx.x != 0) return;
+  const uint64_t t0 = globaltimer_ns();
+  uint32_t v = ld_acquire_gpu(ctl + kCtlNeverSet);
+  while (v == 0u && globaltimer_ns() - t0 < limit_ns) v = ld_acquire_gpu(ctl + kCtlNeverSet);
+  if (v == 0u) atomicOr(ctl + 3, kStatusTimeout);
+}
+
+cudaError_t launch_wait_selftest(uint32_t* ctl, uint64_t limit_ns, cudaStream_t stream) {
+  wait_selftest_kernel<<<1, 32, 0, stream>>>(ctl, limit_ns);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------- launching ------
 
 template <typename E, int MODE>

@@ -48,7 +48,7 @@ struct Params {
   float top_p;
   int topp;                // top_p < 1
   uint32_t* ctl;           // [0..1] work counter (u64), [2] finished producers, [3] status bits,
-                           // [4] tails queued, [5] tails taken, [6] finished CTAs
+                           // [4] tails queued, [5] tails taken, [6] finished CTAs, [8] never set
   uint32_t* row_cnt;       // [B*RS] chunks published per row
   uint32_t* seq_cnt;       // [B] rows finished per sequence
   uint32_t* tail_q;        // [B * max(1, DC)] queued sequence tails or draw chunks (0 = empty)
@@ -76,6 +76,12 @@ bool seq_mode_fits(int64_t K, int64_t V, int esz);
 bool warp_mode_fits(int64_t K, int64_t V, int esz);
 cudaError_t launch_warp(const Params& p, int dtype, int grid, cudaStream_t stream);
 int warp_mode_seqs_per_cta();
+
+// A control word no kernel ever writes (the self-test waits for it).
+constexpr int kCtlNeverSet = 8;
+// Self-test of the bounded waits: a one-thread kernel that waits limit_ns for
+// ctl[kCtlNeverSet] and then records a timeout in ctl[3].
+cudaError_t launch_wait_selftest(uint32_t* ctl, uint64_t limit_ns, cudaStream_t stream);
 cudaError_t launch_seq(const Params& p, int dtype, int grid, cudaStream_t stream);
 int kernel_threads();
 

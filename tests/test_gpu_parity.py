@@ -160,6 +160,19 @@ def test_bad_inputs_in_sequence_mode(V):
     compare_sample(d, cfg.temperature, gpu=(gt, ga))
 
 
+def test_bounded_wait_reports_timeout_and_recovers():
+    # A wait that nothing ends gives up after its limit (10 ms here) and
+    # reports SV_ERR_TIMEOUT; the stream's scratch is reset and later calls work.
+    assert svpkg.get_status() == 0
+    svpkg.selftest_wait_timeout(10_000_000)
+    assert svpkg.get_status() == -5
+    assert svpkg.get_status() == 0
+    cfg = C["cfg2_v32000_bf16"].with_(B=6, V=9000)
+    d = sg.sample_inputs(cfg)
+    compare_sample(d, cfg.temperature, max_mismatch=1)
+    assert svpkg.get_status() == 0
+
+
 def test_empty_batch_is_a_noop():
     e = torch.empty((0, 5, 100), dtype=torch.bfloat16, device="cuda")
     ot, oa = svpkg.verify_sample(e, torch.empty((0, 4, 100), dtype=torch.bfloat16, device="cuda"),

@@ -76,6 +76,9 @@ def test_host_argument_checks(lib):
     assert g(None, None, 0, 7, 5, 100, 1, None, None, None, None) == 0
     assert lib.sv_set_launch_shape(7, 1) == -1
     assert lib.sv_set_launch_shape(0, 0) == 0
+    # the wait self-test checks its limit before touching the device
+    assert lib.sv_selftest_wait_timeout(-1, None) == -1
+    assert lib.sv_selftest_wait_timeout(3_000_000_000, None) == -1
 
 
 def test_binding_refuses_without_library(monkeypatch, tmp_path):
