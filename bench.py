@@ -71,6 +71,24 @@ def workload(name: str, batch: int | None = None):
     return cfg, greedy, positions, logit_bytes, small_in, out_bytes
 
 
+def kernel_for(cfg, greedy) -> str:
+    """Which kernel the library launches for this workload (the library's own
+    selection rule, restated for the report): one warp per sequence for rows of
+    at most 1024 elements, one CTA per sequence when a whole sequence fits
+    48 KB, else the streaming kernel. Inputs here are always 16-byte aligned."""
+    if greedy or cfg.temperature == 0.0 or cfg.top_p < 1.0:
+        return KERNEL
+    esz = 2 if cfg.dtype == sg.BF16 else 4
+    rows = 2 * cfg.K + 1
+    if (cfg.V * esz) % 16 != 0 or rows > 64:
+        return KERNEL
+    if cfg.V <= 1024 and rows * cfg.V * esz <= 65536:
+        return "verify_warp_kernel"
+    if rows * cfg.V * esz <= 49152:
+        return "verify_seq_kernel"
+    return KERNEL
+
+
 def config_json(cfg, greedy, rotation):
     c = {"workload": cfg.name if cfg.B == sg.CONFIGS[cfg.name].B else f"{cfg.name}_b{cfg.B}", "B": cfg.B, "V": cfg.V, "logits": "bf16" if cfg.dtype == sg.BF16 else "f32"}
     if greedy:
@@ -345,7 +363,8 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "traffic": profiled_traffic(name), "algorithmic_bytes_per_launch": logit_bytes,
-                     "kernel": KERNEL, "timing": "CUDA events over graph replays of the timed calls"},
+                     "kernel": kernel_for(cfg, greedy),
+                     "timing": "CUDA events over graph replays of the timed calls"},
         "clocks": clk.summary(),
         "e2e": {"value": positions * world / e2e_s, "unit": "positions/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": out_bytes},
