@@ -43,6 +43,9 @@ def _bind(lib):
     lib.oracle_row_stats.restype = ctypes.c_int
     lib.oracle_verify_greedy.argtypes = [vp, ctypes.c_int, vp, i64, i32, i32, i64, vp, vp, vp]
     lib.oracle_verify_greedy.restype = ctypes.c_int
+    lib.oracle_verify_lookahead_sample.argtypes = [vp, ctypes.c_int, vp, vp, i64, i32, i32, i64, f32, vp, vp, vp,
+                                                   vp]
+    lib.oracle_verify_lookahead_sample.restype = ctypes.c_int
     return lib
 
 
@@ -120,3 +123,24 @@ def verify_greedy(logits, cand, lib=None):
     if rc != 0:
         raise ValueError("oracle_verify_greedy: argument error")
     return out, acc, best
+
+
+def verify_lookahead_sample(logits, cand, uniforms, temperature: float, lib=None):
+    """Lookahead sampling-mode verify of greedily produced candidates.
+    Returns (tokens[B,N], accept_len[B], best[B], margin[B])."""
+    lib = lib or _lib()
+    logits = np.ascontiguousarray(logits)
+    B, G, N, V = logits.shape
+    cand = np.ascontiguousarray(cand, dtype=np.int32)
+    assert cand.shape == (B, G, N - 1)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32)
+    assert u.shape == (B, (N - 1) * G + 1)
+    out = np.empty((B, N), dtype=np.int32)
+    acc = np.empty(B, dtype=np.int32)
+    best = np.empty(B, dtype=np.int32)
+    margin = np.empty(B, dtype=np.float64)
+    rc = lib.oracle_verify_lookahead_sample(_p(logits), _dtype_code(logits), _p(cand), _p(u), B, G, N, V,
+                                            float(temperature), _p(out), _p(acc), _p(best), _p(margin))
+    if rc != 0:
+        raise ValueError("oracle_verify_lookahead_sample: argument error")
+    return out, acc, best, margin

@@ -19,13 +19,15 @@
  *        sides; resample only inside the truncated set).
  *   [P4] "Lookahead Decoding 完全拆解", section "验证分支" (greedy verify:
  *        candidate token i must equal the argmax at position i; longest
- *        matched prefix wins, plus one bonus token).
+ *        matched prefix wins, plus one bonus token) and section
+ *        "采样模式的验证" (sampling-mode verify of greedily produced
+ *        candidates: the draft distribution is one-hot on the token).
  *
  * Dtype codes: 0 = fp32, 1 = bf16 (raw 16-bit patterns).
  * Return value of every function: 0 on success, -1 on an argument error.
  * Per-sequence input errors (token id outside [0,V), uniform outside [0,1),
- * NaN logit, +inf logit or an all -inf row in sampling mode, NaN in greedy
- * mode) give out_accept_len[b] = -1 and out_tokens[b,:] = -1.
+ * NaN logit, +inf logit or an all -inf row in the sampling modes, NaN in
+ * greedy mode) give out_accept_len[b] = -1 and out_tokens[b,:] = -1.
  */
 #ifndef SPECVERIFY_ORACLE_H
 #define SPECVERIFY_ORACLE_H
@@ -65,6 +67,28 @@ int oracle_row_stats(const void* rows, int dtype, int64_t nrows, int64_t V, floa
  * [0,N-1]. out_best [B] (nullable): the winning candidate, lowest g on ties. */
 int oracle_verify_greedy(const void* logits, int dtype, const int32_t* cand, int64_t B, int32_t G, int32_t N,
                          int64_t V, int32_t* out_tokens, int32_t* out_accept_len, int32_t* out_best);
+
+/* Lookahead sampling-mode verify ([P4] section "采样模式的验证"): the
+ * candidates were produced greedily, so each one's draft distribution is
+ * one-hot on its token and only the token id is kept. logits [B,G,N,V]: row
+ * (g, n) is the target distribution at position n of candidate g's branch;
+ * cand [B,G,N-1]; uniforms [B,(N-1)*G+1]: u[n*G+g] is the accept test of
+ * candidate g at position n, u[(N-1)*G] drives the one draw; temperature > 0.
+ * At each position the still-matching candidates are tested in order of g
+ * against the current distribution, which starts as softmax(row/T) of the
+ * candidate that owns the accepted prefix (g = 0 at position 0). Candidate x
+ * is accepted when u < p(x) (alpha = min(1, p(x)/q(x)) with q one-hot); a
+ * rejection replaces p by norm(max(0, p - onehot(x))), i.e. p with x removed.
+ * When no candidate is accepted at position n, the token is drawn from the
+ * current p and the round ends; when all N-1 positions are accepted the bonus
+ * is drawn from row N-1 of the owning candidate.
+ * out_tokens [B,N] (accepted prefix, drawn token, -1 tail); out_accept_len
+ * [B] in [0,N-1]; out_best [B] (nullable): the candidate that owns the
+ * accepted prefix; out_margin [B] (nullable): as in oracle_verify_sample. */
+int oracle_verify_lookahead_sample(const void* logits, int dtype, const int32_t* cand, const float* uniforms,
+                                   int64_t B, int32_t G, int32_t N, int64_t V, float temperature,
+                                   int32_t* out_tokens, int32_t* out_accept_len, int32_t* out_best,
+                                   double* out_margin);
 
 #ifdef __cplusplus
 }

@@ -187,6 +187,34 @@ class GreedyConfig:
         return replace(self, **kw)
 
 
+@dataclass(frozen=True)
+class LookaheadSampleConfig:
+    """A Lookahead sampling-mode verify workload: logits [B,G,N,V] and cand
+    [B,G,N-1] made as for the greedy workload (candidates are produced
+    greedily), uniforms [B,(N-1)*G+1], temperature > 0."""
+    name: str
+    B: int
+    G: int
+    N: int
+    V: int
+    dtype: int
+    sigma: float
+    match_prob: float
+    temperature: float
+    seed: int = 0
+
+    @property
+    def rows(self) -> int:
+        return self.B * self.G * self.N
+
+    @property
+    def logit_bytes(self) -> int:
+        return self.rows * self.V * (2 if self.dtype == BF16 else 4)
+
+    def with_(self, **kw) -> "LookaheadSampleConfig":
+        return replace(self, **kw)
+
+
 # The five measured workloads. The first one's "1000 rounds of B=1" are 1000
 # independent sequences, verified as one batch of 1000.
 CONFIGS = {
@@ -201,6 +229,14 @@ CONFIGS = {
     "cfg5_topp_v151936_bf16": SampleConfig("cfg5_topp_v151936_bf16", B=128, K=6, V=151936, dtype=BF16,
                                            temperature=0.7, top_p=0.9, target_sigma=2.5, peak_height=5.0,
                                            n_peaks=10, draft_sigma=0.8),
+}
+
+
+# The Lookahead sampling-mode verify on the greedy workload's shape, at the
+# temperature the Lookahead page's sampling experiments use (1.0).
+LOOKAHEAD_CONFIGS = {
+    "la_sample_v32000_bf16": LookaheadSampleConfig("la_sample_v32000_bf16", B=32, G=7, N=5, V=32000, dtype=BF16,
+                                                   sigma=3.0, match_prob=0.5, temperature=1.0),
 }
 
 
@@ -239,4 +275,16 @@ def greedy_inputs(cfg: GreedyConfig, seq_offset: int = 0, B: int | None = None, 
     rc = _lib().sg_gen_greedy(_ptr(logits), _ptr(cand), cfg.dtype, B, cfg.G, cfg.N, cfg.V, cfg.sigma,
                               cfg.match_prob, cfg.seed, seq_offset, nthreads)
     assert rc == 0
+    return out
+
+
+def lookahead_sample_inputs(cfg: LookaheadSampleConfig, seq_offset: int = 0, B: int | None = None,
+                            nthreads: int = 0, out: dict | None = None) -> dict:
+    """Generate logits [B,G,N,V], cand [B,G,N-1] and uniforms [B,(N-1)*G+1] for ``cfg``."""
+    B = cfg.B if B is None else B
+    out = greedy_inputs(GreedyConfig(cfg.name, B=B, G=cfg.G, N=cfg.N, V=cfg.V, dtype=cfg.dtype, sigma=cfg.sigma,
+                                     match_prob=cfg.match_prob, seed=cfg.seed),
+                        seq_offset=seq_offset, B=B, nthreads=nthreads, out=out)
+    u = out.setdefault("uniforms", np.empty((B, (cfg.N - 1) * cfg.G + 1), dtype=np.float32))
+    assert _lib().sg_uniforms(B, (cfg.N - 1) * cfg.G, cfg.seed, seq_offset, _ptr(u)) == 0
     return out

@@ -9,7 +9,10 @@ Sources (page title, section):
       follows p; §2.4: E[accept] = 1 - TV(p, q); §3.1: tokens per round
       (1 - a^(K+1)) / (1 - a).
   "Lookahead Decoding 完全拆解" (pinghaoyang.com.cn), scaling-law section,
-      eq. (5): E[#tokens] = (g+1) - sum_{i=1..g} (1 - a^i)^b for b drafts.
+      eq. (5): E[#tokens] = (g+1) - sum_{i=1..g} (1 - a^i)^b for b drafts;
+      section "采样模式的验证": greedily produced candidates have a one-hot
+      draft distribution, and the sampling-mode verify keeps the target's
+      output distribution.
 """
 from __future__ import annotations
 
@@ -224,3 +227,177 @@ def check_greedy_multi_draft(lib, V=512, B=12_000):
     tokens = acc + 1.0
     expect = multi_draft_expected_tokens(cfg.N - 1, cfg.G, cfg.match_prob, 1.0 / V)
     assert abs(tokens.mean() - expect) < 4 * tokens.std() / math.sqrt(B), (tokens.mean(), expect)
+
+
+# ---------------------------------------------------------------------------
+# Lookahead sampling-mode verify ("Lookahead Decoding 完全拆解", section
+# "采样模式的验证"): candidates come from greedy decoding, so each one's draft
+# distribution is one-hot on its token; the verify only decides acceptance and
+# leaves the target distribution intact.
+
+def lookahead_law(P, cand):
+    """Law of the verify's output, from the page's invariance claim alone.
+
+    P[g][n] is the target distribution at position n of candidate g's branch,
+    cand[g][n] its token (n < N-1). Every emitted token follows the target:
+    position n's token t is drawn from P[lead][n], where lead owns the accepted
+    prefix (candidate 0 at n = 0). t extends the prefix when a candidate still
+    matching the prefix holds t at n (the new owner is the lowest such
+    candidate); otherwise the round ends with t. Row N-1 gives the bonus.
+    Returns {(accept_len, t_0, .., t_j): probability}."""
+    G, N = len(P), len(P[0])
+    V = len(P[0][0])
+    law = {}
+
+    def walk(n, alive, lead, prefix, mass):
+        p = P[lead][n]
+        if n == N - 1:
+            for t in range(V):
+                if p[t]:
+                    law[(n,) + prefix + (t,)] = law.get((n,) + prefix + (t,), 0) + mass * p[t]
+            return
+        held = {cand[g][n] for g in alive}
+        for t in range(V):
+            if not p[t]:
+                continue
+            if t in held:
+                nxt = [g for g in alive if cand[g][n] == t]
+                walk(n + 1, nxt, min(nxt), prefix + (t,), mass * p[t])
+            else:
+                law[(n,) + prefix + (t,)] = law.get((n,) + prefix + (t,), 0) + mass * p[t]
+
+    walk(0, list(range(G)), 0, (), 1)
+    return law
+
+
+def lookahead_outcomes(out, acc):
+    """Tally (accept_len, t_0..t_j) keys of a batch of verify outputs."""
+    keys = np.concatenate([acc[:, None], out], 1)
+    uniq, counts = np.unique(keys, axis=0, return_counts=True)
+    res = {}
+    for k, c in zip(uniq, counts):
+        res[(int(k[0]),) + tuple(int(v) for v in k[1: 2 + k[0]])] = int(c)
+    return res
+
+
+F = __import__("fractions").Fraction
+# Two shapes with G = 2, N = 3, V = 4 whose probabilities are multiples of
+# 1/12 and are picked so that every accept threshold and every CDF edge the
+# walk can meet (after removing rejected tokens and renormalising) is again a
+# multiple of 1/12: a midpoint grid of 12 values per uniform then integrates
+# the oracle's decisions exactly. Shape "shared": both candidates start with
+# the same token. Shape "split": they differ from the first token on.
+LA_EXACT = {
+    "shared": ([[[F(6, 12), F(3, 12), F(2, 12), F(1, 12)], [F(6, 12), F(2, 12), F(3, 12), F(1, 12)],
+                 [F(3, 12)] * 4],
+                [[F(1, 12), F(2, 12), F(3, 12), F(6, 12)], [F(2, 12), F(4, 12), F(3, 12), F(3, 12)],
+                 [F(6, 12), F(2, 12), F(2, 12), F(2, 12)]]],
+               [[0, 0], [0, 2]]),
+    "split": ([[[F(6, 12), F(3, 12), F(2, 12), F(1, 12)], [F(6, 12), F(2, 12), F(3, 12), F(1, 12)],
+                [F(3, 12)] * 4],
+               [[F(1, 12), F(2, 12), F(3, 12), F(6, 12)], [F(2, 12), F(6, 12), F(2, 12), F(2, 12)],
+                [F(6, 12), F(2, 12), F(2, 12), F(2, 12)]]],
+              [[0, 0], [1, 1]]),
+}
+
+
+def check_lookahead_exact(lib, shape, dtype=sg.F32, n=12):
+    """Every output's mass, integrated over the n^5 midpoint grid of uniforms,
+    equals lookahead_law exactly (up to the rounding of ln p in storage)."""
+    P, cand = LA_EXACT[shape]
+    G, N, V = len(P), len(P[0]), len(P[0][0])
+    logits = np.log(np.array([[[float(x) for x in row] for row in rows] for rows in P]))
+    grid = (np.arange(n) + 0.5) / n
+    U = np.array(list(itertools.product(grid, repeat=(N - 1) * G + 1)), np.float32)
+    B = U.shape[0]
+    L = np.broadcast_to(sg.from_float(logits, dtype), (B, G, N, V)).copy()
+    C = np.broadcast_to(np.array(cand, np.int32), (B, G, N - 1)).copy()
+    out, acc, best, _ = oracle.verify_lookahead_sample(L, C, U, 1.0, lib=lib)
+    assert (acc >= 0).all()
+    got = lookahead_outcomes(out, acc)
+    law = lookahead_law(P, cand)
+    assert sum(law.values()) == 1
+    for key in set(got) | set(law):
+        assert abs(got.get(key, 0) / B - float(law.get(key, 0))) < 1e-9, (shape, key, got.get(key, 0) / B,
+                                                                          law.get(key, 0))
+
+
+LA_CAND = [[2, 0], [2, 3], [4, 0]]  # G = 3, N = 3: a shared first token, a split, a repeat
+
+
+def check_lookahead_chisquare(lib, T=0.8, n=400_000, seed=21):
+    """The output law of random rows (V = 5, G = 3, N = 3) against
+    lookahead_law by chi-square over every outcome (small ones pooled)."""
+    G, N, V = 3, 3, 5
+    rows = np.random.default_rng(seed).normal(0, 1.2, size=(G, N, V)).astype(np.float32)
+    P = [[softmax(rows[g, k], T).tolist() for k in range(N)] for g in range(G)]
+    law = lookahead_law(P, LA_CAND)
+    L = np.broadcast_to(rows, (n, G, N, V)).copy()
+    C = np.broadcast_to(np.array(LA_CAND, np.int32), (n, G, N - 1)).copy()
+    U = sg.uniforms(n, (N - 1) * G, seed=seed)
+    out, acc, _, _ = oracle.verify_lookahead_sample(L, C, U, T, lib=lib)
+    got = lookahead_outcomes(out, acc)
+    assert set(got) <= set(law), "an outcome the law gives probability zero"
+    keys = sorted(law, key=lambda k: -law[k])
+    exp = np.array([law[k] * n for k in keys])
+    obs = np.array([got.get(k, 0) for k in keys], float)
+    big = exp >= 20
+    exp = np.append(exp[big], exp[~big].sum())
+    obs = np.append(obs[big], obs[~big].sum())
+    _, pval = stats.chisquare(obs, exp)
+    assert pval > 1e-3, f"chi-square p-value {pval:.3g}"
+
+
+def check_lookahead_single_candidate(lib, seed=22):
+    """G = 1 is the sampling-mode verify with a one-hot draft row (logit 0 on
+    the candidate, -inf elsewhere); candidates all equal to candidate 0 give
+    the same result as candidate 0 alone (a repeated token is already removed)."""
+    B, N, V, T = 3000, 5, 16, 0.9
+    rng = np.random.default_rng(seed)
+    rows = sg.from_float(rng.normal(0, 1.5, size=(B, 1, N, V)), sg.F32)
+    cand = rng.integers(0, V, size=(B, 1, N - 1)).astype(np.int32)
+    U = sg.uniforms(B, N - 1, seed=seed)
+    draft = np.full((B, N - 1, V), -np.inf, np.float32)
+    np.put_along_axis(draft, cand[:, 0, :, None], 0.0, axis=2)
+    out_s, acc_s, _ = oracle.verify_sample(rows[:, 0], draft, cand[:, 0], U, T, lib=lib)
+    out_l, acc_l, best, _ = oracle.verify_lookahead_sample(rows, cand, U, T, lib=lib)
+    assert (acc_s >= 0).all() and (best == 0).all()
+    np.testing.assert_array_equal(acc_l, acc_s)
+    np.testing.assert_array_equal(out_l, out_s)
+    G = 3
+    rows3 = np.repeat(rows, G, axis=1)
+    cand3 = np.repeat(cand, G, axis=1)
+    U3 = np.zeros((B, (N - 1) * G + 1), np.float32)
+    for k in range(N - 1):
+        U3[:, k * G] = U[:, k]
+        U3[:, k * G + 1: (k + 1) * G] = sg.uniforms(B, G - 2, seed=seed + 1 + k)
+    U3[:, -1] = U[:, -1]
+    out3, acc3, best3, _ = oracle.verify_lookahead_sample(rows3, cand3, U3, T, lib=lib)
+    np.testing.assert_array_equal(acc3, acc_s)
+    np.testing.assert_array_equal(out3, out_s)
+    assert (best3 == 0).all()
+
+
+def load_lookahead_golden():
+    lines = [l.strip() for l in open(os.path.join(GOLDEN, "lookahead_sample_hand.txt"))
+             if l.strip() and l[0] != "#"]
+    cases, i = [], 0
+    while i < len(lines):
+        _, G, N, V, T = lines[i].split()
+        G, N, V, T = int(G), int(N), int(V), float(T)
+        rows = [[float(x) for x in lines[i + 1 + r].split()] for r in range(G * N)]
+        cand = [[int(x) for x in lines[i + 1 + G * N + g].split()] for g in range(G)]
+        u = [float(x) for x in lines[i + 1 + G * N + G].split()[1:]]
+        exp = lines[i + 2 + G * N + G]
+        toks, acc, best = [s.strip() for s in exp[len("expect"):].split(";")]
+        cases.append((np.array(rows, np.float32).reshape(1, G, N, V), np.array(cand, np.int32).reshape(1, G, N - 1),
+                      np.array(u, np.float32).reshape(1, -1), T, [int(t) for t in toks.split()], int(acc),
+                      int(best)))
+        i += 3 + G * N + G
+    return cases
+
+
+def check_lookahead_golden(lib):
+    for logits, cand, u, T, toks, acc, best in load_lookahead_golden():
+        out, a, b, _ = oracle.verify_lookahead_sample(logits, cand, u, T, lib=lib)
+        assert out[0].tolist() == toks and a[0] == acc and b[0] == best, (out, a, b, toks, acc, best)

@@ -8,7 +8,8 @@ import pytest
 
 import oracle
 from pins import (check_acceptance_is_one_minus_tv, check_brute_force, check_greedy_golden,
-                  check_output_is_target_distribution, check_tokens_per_round)
+                  check_lookahead_exact, check_lookahead_golden, check_output_is_target_distribution,
+                  check_tokens_per_round)
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -46,6 +47,30 @@ MUTATIONS = {
                              check_greedy_golden),
     # equal prefix lengths: the lowest candidate wins
     "greedy_last_candidate": ("if (L > best_L) {", "if (L >= best_L) {", check_greedy_golden),
+    # Lookahead sampling: a rejected candidate token leaves the distribution
+    "lookahead_keeps_rejected": ("w[v] = fmax(0.0, p[v] - (v == x ? 1.0 : 0.0));", "w[v] = p[v];",
+                                 lambda lib: check_lookahead_exact(lib, "shared")),
+    # the distribution at position n is the row of the prefix's owner
+    "lookahead_row_of_candidate_0": ("load_row(logits, dtype, (b * G + lead) * N + n, V, l);",
+                                     "load_row(logits, dtype, (b * G + 0) * N + n, V, l);",
+                                     lambda lib: check_lookahead_exact(lib, "split")),
+    # so is the bonus row
+    "lookahead_bonus_of_candidate_0": ("load_row(logits, dtype, (b * G + lead) * N + (N - 1), V, l);",
+                                       "load_row(logits, dtype, (b * G + 0) * N + (N - 1), V, l);",
+                                       lambda lib: check_lookahead_exact(lib, "shared")),
+    # only candidates that still match the accepted prefix are tested
+    "lookahead_no_prefix_filter": ("alive[g] = alive[g] && (c[g * (N - 1) + n] == x);", "alive[g] = alive[g];",
+                                   lambda lib: check_lookahead_exact(lib, "split")),
+    # u[n*G + g] tests candidate g at position n
+    "lookahead_uniform_layout": ("if ((double)u[n * G + g] < alpha) {",
+                                 "if ((double)u[g * (N - 1) + n] < alpha) {", check_lookahead_golden),
+    # u = alpha rejects
+    "lookahead_accept_on_equal": ("if ((double)u[n * G + g] < alpha) {", "if ((double)u[n * G + g] <= alpha) {",
+                                  check_lookahead_golden),
+    # the draw after a rejection uses the last uniform
+    "lookahead_draw_uniform": ("out[n] = (int32_t)inverse_cdf(p, V, (double)u[(N - 1) * G], &margin);",
+                               "out[n] = (int32_t)inverse_cdf(p, V, (double)u[0], &margin);",
+                               check_lookahead_golden),
 }
 
 
