@@ -124,6 +124,43 @@ int sv_verify_greedy(const void* logits, const int32_t* cand, int64_t B, int32_t
                      void* stream);
 
 /*
+ * Sampling-mode verify of Lookahead n-gram candidates ("Lookahead Decoding
+ * 完全拆解", section "采样模式的验证"). The candidates were produced greedily,
+ * so only their token ids exist: each one's draft distribution is one-hot.
+ *
+ *   logits   [B, G, N, V] dtype: row (g, n) is the target's distribution
+ *            (as logits) at position n of candidate g's branch, i.e. after
+ *            cand[b,g,0..n-1]; row N-1 is the bonus position.
+ *   cand     [B, G, N-1] int32: the candidate n-grams.
+ *   uniforms [B, (N-1)*G + 1] fp32 in [0,1): u[n*G + g] is the accept test of
+ *            candidate g at position n (read only if that test happens); the
+ *            last one drives the one draw.
+ *   B >= 0, 1 <= G <= 32, N >= 2, G*N <= 1024, G*G*(N-1) <= 4096, V >= 2;
+ *   B*G*N < 2^31; temperature > 0 (finite).
+ * Each position n starts from p = softmax(logits[b, owner, n] / T), where the
+ * owner is the candidate whose token was accepted at n-1 (candidate 0 at
+ * n = 0). The candidates whose first n tokens equal the accepted prefix are
+ * tested in order of g: candidate g's token x is accepted when
+ * u[n*G + g] < p(x) (min(1, p(x)/q(x)) with q one-hot; a repeated token has
+ * p(x) = 0 by then); a rejection replaces p by p with x removed,
+ * renormalised. When none is accepted, the token at n is drawn from the
+ * current p and the round ends; after N-1 accepted positions the bonus is
+ * drawn from the owner's row N-1. A draw is the smallest t with
+ * sum_{v<=t} w_v > u * sum_v w_v (ascending vocabulary order).
+ * Outputs:
+ *   out_tokens     [B, N] int32: the accepted prefix, the drawn token, -1.
+ *   out_accept_len [B] int32: in [0, N-1] (-1 for bad input: a token id
+ *                  outside [0,V), a uniform outside [0,1), or a NaN, +inf or
+ *                  all -inf row anywhere in the sequence).
+ *   out_best_cand  nullable [B] int32: the owner of the accepted prefix.
+ *   out_row_lse    nullable [B, G, N] fp32: log sum_v exp(l_v/T) of every row.
+ * Two kernels are enqueued on the stream.
+ */
+int sv_verify_lookahead_sample(const void* logits, const int32_t* cand, const float* uniforms, int64_t B, int32_t G,
+                               int32_t N, int64_t V, int32_t dtype, float temperature, int32_t* out_tokens,
+                               int32_t* out_accept_len, int32_t* out_best_cand, float* out_row_lse, void* stream);
+
+/*
  * sv_verify_sample_noalloc: sv_verify_sample for callers that cannot allocate
  * device memory. The pages have no counterpart to this entry point; it exists
  * for deployment constraints, not for the method.

@@ -9,6 +9,7 @@ missing or cannot be loaded, every call raises.
 Entry points (same names as the C ABI):
   verify_sample(target, draft, draft_tokens, uniforms, temperature, top_p)
   verify_greedy(logits, cand)
+  verify_lookahead_sample(logits, cand, uniforms, temperature)
   get_status()
 """
 from __future__ import annotations
@@ -24,8 +25,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _SO = os.path.join(_HERE, "libspecverify.so")
-_SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_noalloc.cu"]
-_DEPS = _SOURCES + ["sv_kernels.h", "sv_device.cuh"]
+_SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_noalloc.cu", "sv_lookahead.cu"]
+_DEPS = _SOURCES + ["sv_kernels.h", "sv_device.cuh", "sv_lookahead.h"]
 
 SV_F32, SV_BF16 = 0, 1
 STATUS = {0: "SV_OK", -1: "SV_ERR_ARG", -2: "SV_ERR_DTYPE", -3: "SV_ERR_CUDA", -4: "SV_ERR_INPUT",
@@ -110,13 +111,16 @@ def lib():
         h.sv_verify_sample_noalloc.restype = ctypes.c_int
         h.sv_selftest_wait_timeout.argtypes = [i64, vp]
         h.sv_selftest_wait_timeout.restype = ctypes.c_int
+        h.sv_verify_lookahead_sample.argtypes = [vp, vp, vp, i64, i32, i32, i64, i32, f32, vp, vp, vp, vp, vp]
+        h.sv_verify_lookahead_sample.restype = ctypes.c_int
         _lib_handle = h
     return _lib_handle
 
 
 def exported_symbols() -> list:
     return ["sv_verify_sample", "sv_verify_greedy", "sv_get_status", "sv_status_string", "sv_release",
-            "sv_set_launch_shape", "sv_launch_count", "sv_verify_sample_noalloc", "sv_selftest_wait_timeout"]
+            "sv_set_launch_shape", "sv_launch_count", "sv_verify_sample_noalloc", "sv_selftest_wait_timeout",
+            "sv_verify_lookahead_sample"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -230,6 +234,47 @@ def verify_greedy(logits, cand, out_tokens=None, out_accept_len=None, best=False
     if host:
         outs = [r.to("cpu", non_blocking=True) if out is None else out.copy_(r, non_blocking=True)
                 for r, out in zip(res, [out_tokens, out_accept_len, None])]
+        torch.cuda.current_stream(dev).synchronize()
+        res = outs
+    return tuple(res)
+
+
+def verify_lookahead_sample(logits, cand, uniforms, temperature: float, out_tokens=None, out_accept_len=None,
+                            best=False, row_lse=False, device=None):
+    """Sampling-mode Lookahead verify of greedily produced candidates
+    (sv_verify_lookahead_sample).
+
+    logits [B,G,N,V] (bf16 or fp32), cand [B,G,N-1] int32, uniforms
+    [B,(N-1)*G+1] fp32. Returns (out_tokens [B,N], out_accept_len [B]), then
+    the owner of the accepted prefix [B] with ``best`` and the per-row
+    log-normalisers [B,G,N] with ``row_lse``. CPU tensors are handled as in
+    verify_sample.
+    """
+    host = logits.device.type == "cpu"
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if not host:
+        dev = logits.device
+    B, G, N, V = logits.shape
+    lg = _on_device(logits, dev, "logits")
+    c = _on_device(cand, dev, "cand")
+    u = _on_device(uniforms, dev, "uniforms")
+    _check(lg, (B, G, N, V), None, "logits")
+    dt = _dtype_code(lg)
+    _check(c, (B, G, N - 1), torch.int32, "cand")
+    _check(u, (B, (N - 1) * G + 1), torch.float32, "uniforms")
+    ot = torch.empty((B, N), dtype=torch.int32, device=dev) if (out_tokens is None or host) else out_tokens
+    oa = torch.empty((B,), dtype=torch.int32, device=dev) if (out_accept_len is None or host) else out_accept_len
+    ob = torch.empty((B,), dtype=torch.int32, device=dev) if best else None
+    ol = torch.empty((B, G, N), dtype=torch.float32, device=dev) if row_lse else None
+    with torch.cuda.device(dev):
+        rc = lib().sv_verify_lookahead_sample(_ptr(lg), _ptr(c), _ptr(u), B, G, N, V, dt, float(temperature),
+                                              _ptr(ot), _ptr(oa), _ptr(ob), _ptr(ol), _stream_handle(dev))
+    if rc != 0:
+        raise SpecVerifyError(rc, "sv_verify_lookahead_sample")
+    res = [ot, oa] + ([ob] if best else []) + ([ol] if row_lse else [])
+    if host:
+        outs = [r.to("cpu", non_blocking=True) if out is None else out.copy_(r, non_blocking=True)
+                for r, out in zip(res, [out_tokens, out_accept_len, None, None])]
         torch.cuda.current_stream(dev).synchronize()
         res = outs
     return tuple(res)

@@ -11,6 +11,7 @@
 
 #include "../../include/specverify.h"
 #include "sv_kernels.h"
+#include "sv_lookahead.h"
 
 namespace {
 
@@ -237,6 +238,54 @@ extern "C" int sv_verify_greedy(const void* logits, const int32_t* cand, int64_t
   p.top_p = 1.f;
   p.topp = 0;
   return run(p, dtype, sv::kGreedy, B * (int64_t)p.RS, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int sv_verify_lookahead_sample(const void* logits, const int32_t* cand, const float* uniforms, int64_t B,
+                                          int32_t G, int32_t N, int64_t V, int32_t dtype, float temperature,
+                                          int32_t* out_tokens, int32_t* out_accept_len, int32_t* out_best_cand,
+                                          float* out_row_lse, void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (B < 0 || B >= kMaxV || V < 2 || V >= kMaxV || !sv::la::fits(G, N)) return SV_ERR_ARG;
+  if (B * (int64_t)G * N >= kMaxV) return SV_ERR_ARG;
+  if (!(temperature > 0.f) || std::isinf(temperature)) return SV_ERR_ARG;
+  if (B == 0) return SV_OK;
+  if (!logits || !cand || !uniforms || !out_tokens || !out_accept_len) return SV_ERR_ARG;
+  const size_t esz = dtype == SV_BF16 ? 2 : 4;
+  if (!aligned_to(logits, esz)) return SV_ERR_DTYPE;
+  if (!aligned_to(cand, 4) || !aligned_to(uniforms, 4) || !aligned_to(out_tokens, 4) ||
+      !aligned_to(out_accept_len, 4) || (out_best_cand && !aligned_to(out_best_cand, 4)) ||
+      (out_row_lse && !aligned_to(out_row_lse, 4)))
+    return SV_ERR_ARG;
+  const float c = (float)(1.4426950408889634 / (double)temperature);
+  if (!std::isfinite(c)) return SV_ERR_ARG;
+  const int64_t rows = B * G * N;
+  const size_t rowstat_bytes = align256((size_t)rows * 8);
+  const size_t gath_bytes = align256((size_t)B * G * (N - 1) * G * 4);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Scratch sc;
+  int dev = 0;
+  int rc = get_scratch(st, 0, rowstat_bytes + gath_bytes, &sc, &dev);
+  if (rc != SV_OK) return rc;
+  char* base = static_cast<char*>(sc.base);
+  sv::la::Params p{};
+  p.logits = logits;
+  p.cand = cand;
+  p.uniforms = uniforms;
+  p.B = B;
+  p.V = V;
+  p.G = G;
+  p.N = N;
+  p.c = c;
+  p.rowstat = reinterpret_cast<float2*>(base + data_offset(sc));
+  p.gath = reinterpret_cast<float*>(base + data_offset(sc) + rowstat_bytes);
+  p.ctl = reinterpret_cast<uint32_t*>(base);
+  p.out_tokens = out_tokens;
+  p.out_accept_len = out_accept_len;
+  p.out_best = out_best_cand;
+  p.out_row_lse = out_row_lse;
+  if (sv::la::launch(p, dtype, st) != cudaSuccess) return SV_ERR_CUDA;
+  g_launches.fetch_add(2);
+  return SV_OK;
 }
 
 extern "C" int sv_get_status(void* stream) {

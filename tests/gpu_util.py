@@ -100,3 +100,32 @@ def compare_greedy(d: dict):
     np.testing.assert_array_equal(gt, rt)
     np.testing.assert_array_equal(gb, rb)
     return {"sequences": len(ra), "accept_mean": float(ra[ra >= 0].mean()) if (ra >= 0).any() else 0.0}
+
+
+def run_lookahead(d: dict, temperature: float, row_lse: bool = False):
+    res = svpkg.verify_lookahead_sample(to_dev(d["logits"]), to_dev(d["cand"]), to_dev(d["uniforms"]), temperature,
+                                        best=True, row_lse=row_lse)
+    torch.cuda.synchronize()
+    return tuple(r.cpu().numpy() for r in res)
+
+
+def compare_lookahead(d: dict, temperature: float, gpu=None, max_mismatch: int | None = 0):
+    """Lookahead sampling verify: tokens, accept lengths and owners equal the
+    oracle's except in sequences whose smallest decision margin (|u - alpha|
+    of a test, CDF gap / Z of the draw) is below NEAR_TIE; at most
+    ``max_mismatch`` such sequences differ. Returns counts."""
+    if gpu is None:
+        gpu = run_lookahead(d, temperature)
+    gt, ga, gb = gpu[0], gpu[1], gpu[2]
+    rt, ra, rb, margin = oracle.verify_lookahead_sample(d["logits"], d["cand"], d["uniforms"], temperature)
+    diff = (ga != ra) | (gb != rb) | (gt != rt).any(1)
+    near = margin < NEAR_TIE
+    bad = diff & ~near
+    i = int(np.argmax(bad))
+    assert not bad.any(), (
+        f"{int(bad.sum())} sequences differ from the oracle away from a near-tie; first: b={i} "
+        f"gpu {gt[i]} / {ga[i]} / {gb[i]} oracle {rt[i]} / {ra[i]} / {rb[i]} margin {margin[i]}")
+    if max_mismatch is not None:
+        assert diff.sum() <= max_mismatch, int(diff.sum())
+    return {"sequences": len(ra), "mismatch": int(diff.sum()), "near_ties": int(near.sum()),
+            "accept_hist": np.bincount(ra[ra >= 0], minlength=d["cand"].shape[2] + 1).tolist()}

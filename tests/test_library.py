@@ -74,6 +74,20 @@ def test_host_argument_checks(lib):
     assert g(p, p, 4, 7, 1, 100, 1, p, p, None, None) == -1
     assert g(p, p, 4, 7, 5, 100, 9, p, p, None, None) == -2
     assert g(None, None, 0, 7, 5, 100, 1, None, None, None, None) == 0
+    la = lib.sv_verify_lookahead_sample
+    assert la(p, p, p, 4, 7, 5, 100, 9, 1.0, p, p, None, None, None) == -2
+    assert la(p, p, p, 4, 0, 5, 100, 1, 1.0, p, p, None, None, None) == -1    # G < 1
+    assert la(p, p, p, 4, 33, 2, 100, 1, 1.0, p, p, None, None, None) == -1   # G > 32
+    assert la(p, p, p, 4, 7, 1, 100, 1, 1.0, p, p, None, None, None) == -1    # N < 2
+    assert la(p, p, p, 4, 16, 65, 100, 1, 1.0, p, p, None, None, None) == -1  # G*N > 1024
+    assert la(p, p, p, 4, 32, 6, 100, 1, 1.0, p, p, None, None, None) == -1   # G*G*(N-1) > 4096
+    assert la(p, p, p, 4, 7, 5, 1, 1, 1.0, p, p, None, None, None) == -1      # V < 2
+    assert la(p, p, p, 1 << 40, 7, 5, 100, 1, 1.0, p, p, None, None, None) == -1
+    assert la(p, p, p, 4, 7, 5, 100, 1, 0.0, p, p, None, None, None) == -1    # T = 0
+    assert la(p, p, p, 4, 7, 5, 100, 1, float("inf"), p, p, None, None, None) == -1
+    assert la(p, p, None, 4, 7, 5, 100, 1, 1.0, p, p, None, None, None) == -1  # no uniforms
+    assert la(q, p, p, 4, 7, 5, 100, 1, 1.0, p, p, None, None, None) == -2    # misaligned bf16 logits
+    assert la(None, None, None, 0, 7, 5, 100, 1, 1.0, None, None, None, None, None) == 0
     assert lib.sv_set_launch_shape(7, 1) == -1
     assert lib.sv_set_launch_shape(0, 0) == 0
     # the wait self-test checks its limit before touching the device
