@@ -10,6 +10,9 @@ bandwidth against the measured peak.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME|all] [--impl reference]
 
+NAME is one of the five verify workloads (specgen.CONFIGS) or the sampling-mode
+Lookahead verify on the greedy workload's shape (la_sample_v32000_bf16).
+
 Timing: inputs are resident in HBM before the timed region; the K timed calls
 are replayed from CUDA graphs, cycling through enough copies of the inputs
 that the working set exceeds the 129 MB L2 (so no call finds its inputs in
@@ -52,31 +55,44 @@ def log(*a):
 
 # ------------------------------------------------------------------ workload
 
+def find_config(name: str):
+    return sg.CONFIGS[name] if name in sg.CONFIGS else sg.LOOKAHEAD_CONFIGS[name]
+
+
 def workload(name: str, batch: int | None = None):
-    cfg = sg.CONFIGS[name]
+    """(cfg, mode, positions, logit bytes, small input bytes, output bytes) of
+    one call; mode is "sample", "greedy" or "lookahead" (the sampling-mode
+    Lookahead verify)."""
+    cfg = find_config(name)
     if batch:
         cfg = cfg.with_(B=batch)
-    greedy = isinstance(cfg, sg.GreedyConfig)
+    mode = ("greedy" if isinstance(cfg, sg.GreedyConfig) else
+            "lookahead" if isinstance(cfg, sg.LookaheadSampleConfig) else "sample")
     esz = 2 if cfg.dtype == sg.BF16 else 4
-    if greedy:
+    if mode != "sample":
         positions = cfg.B * cfg.G * cfg.N
         logit_bytes = cfg.B * cfg.G * cfg.N * cfg.V * esz
         small_in = cfg.B * cfg.G * (cfg.N - 1) * 4
+        if mode == "lookahead":
+            small_in += cfg.B * ((cfg.N - 1) * cfg.G + 1) * 4
         out_bytes = cfg.B * cfg.N * 4 + cfg.B * 4
     else:
         positions = cfg.B * (cfg.K + 1)
         logit_bytes = cfg.B * (2 * cfg.K + 1) * cfg.V * esz
         small_in = cfg.B * cfg.K * 4 + cfg.B * (cfg.K + 1) * 4
         out_bytes = cfg.B * (cfg.K + 1) * 4 + cfg.B * 4
-    return cfg, greedy, positions, logit_bytes, small_in, out_bytes
+    return cfg, mode, positions, logit_bytes, small_in, out_bytes
 
 
-def kernel_for(cfg, greedy) -> str:
+def kernel_for(cfg, mode) -> str:
     """Which kernel the library launches for this workload (the library's own
     selection rule, restated for the report): one warp per sequence for rows of
     at most 1024 elements, one CTA per sequence when a whole sequence fits
-    48 KB, else the streaming kernel. Inputs here are always 16-byte aligned."""
-    if greedy or cfg.temperature == 0.0 or cfg.top_p < 1.0:
+    48 KB, else the streaming kernel. Inputs here are always 16-byte aligned.
+    The Lookahead sampling verify streams its rows in la_rows_kernel."""
+    if mode == "lookahead":
+        return "la_rows_kernel"
+    if mode == "greedy" or cfg.temperature == 0.0 or cfg.top_p < 1.0:
         return KERNEL
     esz = 2 if cfg.dtype == sg.BF16 else 4
     rows = 2 * cfg.K + 1
@@ -89,10 +105,13 @@ def kernel_for(cfg, greedy) -> str:
     return KERNEL
 
 
-def config_json(cfg, greedy, rotation):
-    c = {"workload": cfg.name if cfg.B == sg.CONFIGS[cfg.name].B else f"{cfg.name}_b{cfg.B}", "B": cfg.B, "V": cfg.V, "logits": "bf16" if cfg.dtype == sg.BF16 else "f32"}
-    if greedy:
+def config_json(cfg, mode, rotation):
+    c = {"workload": cfg.name if cfg.B == find_config(cfg.name).B else f"{cfg.name}_b{cfg.B}", "B": cfg.B,
+         "V": cfg.V, "logits": "bf16" if cfg.dtype == sg.BF16 else "f32"}
+    if mode == "greedy":
         c.update({"mode": "greedy", "G": cfg.G, "N": cfg.N})
+    elif mode == "lookahead":
+        c.update({"mode": "lookahead_sample", "G": cfg.G, "N": cfg.N, "temperature": cfg.temperature})
     else:
         c.update({"mode": "sample", "K": cfg.K, "temperature": cfg.temperature, "top_p": cfg.top_p})
     c["l2"] = (f"inputs larger than L2: {rotation} rotating input sets" if rotation > 1
@@ -213,24 +232,35 @@ def max_over_ranks(value: float, device=None) -> float:
     return float(t.item())
 
 
-def oracle_cpu_rate(cfg, greedy, budget_s: float, nthreads: int):
+def host_inputs(cfg, mode, seq_offset: int = 0, B: int | None = None) -> dict:
+    if mode == "greedy":
+        return sg.greedy_inputs(cfg, seq_offset=seq_offset, B=B)
+    if mode == "lookahead":
+        return sg.lookahead_sample_inputs(cfg, seq_offset=seq_offset, B=B)
+    return sg.sample_inputs(cfg, seq_offset=seq_offset, B=B)
+
+
+def oracle_cpu_rate(cfg, mode, budget_s: float, nthreads: int):
     """Positions per second of the CPU oracle over a bounded sample of the
     workload, fanned out over sequences on ``nthreads`` host threads."""
     import oracle
     chunk = max(1, min(cfg.B, 8 if cfg.V > 50000 else 32))
-    inputs = (sg.greedy_inputs(cfg, B=chunk * nthreads) if greedy else sg.sample_inputs(cfg, B=chunk * nthreads))
+    inputs = host_inputs(cfg, mode, B=chunk * nthreads)
     oracle._lib()
 
     def one(i):
         sl = slice(i * chunk, (i + 1) * chunk)
-        if greedy:
+        if mode == "greedy":
             oracle.verify_greedy(inputs["logits"][sl], inputs["cand"][sl])
+        elif mode == "lookahead":
+            oracle.verify_lookahead_sample(inputs["logits"][sl], inputs["cand"][sl], inputs["uniforms"][sl],
+                                           cfg.temperature)
         else:
             oracle.verify_sample(inputs["target"][sl], inputs["draft"][sl], inputs["draft_tokens"][sl],
                                  inputs["uniforms"][sl], cfg.temperature, cfg.top_p)
         return chunk
 
-    per_seq = cfg.G * cfg.N if greedy else cfg.K + 1
+    per_seq = cfg.K + 1 if mode == "sample" else cfg.G * cfg.N
     done, t0 = 0, time.perf_counter()
     with ThreadPoolExecutor(nthreads) as ex:
         while True:
@@ -251,26 +281,34 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     svpkg.build()
-    cfg, greedy, positions, logit_bytes, small_in, out_bytes = workload(name, args.batch)
+    cfg, mode, positions, logit_bytes, small_in, out_bytes = workload(name, args.batch)
     rotation = 1 if logit_bytes > L2_BYTES else int(math.ceil(3 * L2_BYTES / logit_bytes)) + 1
     log(f"[bench] {name}: {logit_bytes / 1e6:.1f} MB of logits per call, {rotation} input set(s)")
     t0 = time.perf_counter()
     off = shard_offset(rank, cfg.B)
-    host = sg.greedy_inputs(cfg, seq_offset=off) if greedy else sg.sample_inputs(cfg, seq_offset=off)
+    host = host_inputs(cfg, mode, seq_offset=off)
     log(f"[bench] inputs generated in {time.perf_counter() - t0:.1f} s")
-    keys = ("logits", "cand") if greedy else ("target", "draft", "draft_tokens", "uniforms")
+    keys = {"greedy": ("logits", "cand"), "lookahead": ("logits", "cand", "uniforms"),
+            "sample": ("target", "draft", "draft_tokens", "uniforms")}[mode]
     pinned = {k: to_torch(host[k], torch, pin=True) for k in keys}
     sets = []
     for r in range(rotation):
         sets.append({k: pinned[k].to(dev, non_blocking=True) for k in keys})
     torch.cuda.synchronize()
-    outs = [(torch.empty((cfg.B, cfg.N if greedy else cfg.K + 1), dtype=torch.int32, device=dev),
+    outs = [(torch.empty((cfg.B, cfg.K + 1 if mode == "sample" else cfg.N), dtype=torch.int32, device=dev),
              torch.empty((cfg.B,), dtype=torch.int32, device=dev)) for _ in range(rotation)]
+
+    def public_call(*args, **kw):
+        if mode == "greedy":
+            return svpkg.verify_greedy(*args, **kw)
+        if mode == "lookahead":
+            return svpkg.verify_lookahead_sample(*args, cfg.temperature, **kw)
+        return svpkg.verify_sample(*args, cfg.temperature, cfg.top_p, **kw)
 
     def call(i):
         s, (ot, oa) = sets[i % rotation], outs[i % rotation]
-        if greedy:
-            svpkg.verify_greedy(s["logits"], s["cand"], out_tokens=ot, out_accept_len=oa)
+        if mode != "sample":
+            public_call(*(s[k] for k in keys), out_tokens=ot, out_accept_len=oa)
         else:
             svpkg.verify_sample(s["target"], s["draft"], s["draft_tokens"], s["uniforms"], cfg.temperature,
                                 cfg.top_p, out_tokens=ot, out_accept_len=oa)
@@ -334,13 +372,11 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
     host_args = [pinned[k] for k in keys]
     with torch.cuda.stream(stream):
         for _ in range(2):
-            (svpkg.verify_greedy(*host_args) if greedy else
-             svpkg.verify_sample(*host_args, cfg.temperature, cfg.top_p))
+            public_call(*host_args)
         torch.cuda.synchronize()
         t1 = time.perf_counter()
         for _ in range(e2e_steps):
-            (svpkg.verify_greedy(*host_args) if greedy else
-             svpkg.verify_sample(*host_args, cfg.temperature, cfg.top_p))
+            public_call(*host_args)
         e2e_s = (time.perf_counter() - t1) / e2e_steps
     h2d = logit_bytes + small_in
 
@@ -357,13 +393,13 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded Philox inputs of the workload's shapes)",
-        "config": config_json(cfg, greedy, rotation),
+        "config": config_json(cfg, mode, rotation),
         "rounds_per_s": cfg.B * world / (ms_per_step / 1e3),
         "achieved_gbs": achieved_gbs,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "traffic": profiled_traffic(name), "algorithmic_bytes_per_launch": logit_bytes,
-                     "kernel": kernel_for(cfg, greedy),
+                     "kernel": kernel_for(cfg, mode),
                      "timing": "CUDA events over graph replays of the timed calls"},
         "clocks": clk.summary(),
         "e2e": {"value": positions * world / e2e_s, "unit": "positions/s", "h2d_bytes_per_step": h2d,
@@ -372,7 +408,7 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nth = os.cpu_count() or 1
-        rate, n, el = oracle_cpu_rate(cfg, greedy, args.cpu_budget, nth)
+        rate, n, el = oracle_cpu_rate(cfg, mode, args.cpu_budget, nth)
         line["cpu_baseline"] = {"value": rate, "unit": "positions/s", "cores": nth, "kind": "oracle",
                                 "sample": f"{n} sequences of the workload in {el:.1f} s, "
                                           f"one oracle call per thread per batch"}
@@ -388,12 +424,12 @@ def run_reference(args, name: str):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if rank != 0:
         return
-    cfg, greedy, positions, logit_bytes, _, _ = workload(name, args.batch)
+    cfg, mode, positions, logit_bytes, _, _ = workload(name, args.batch)
     nth = os.cpu_count() or 1
     per_step = max(5.0, 60.0 / max(1, args.steps + args.warmup))
     rates = []
     for i in range(args.warmup + args.steps):
-        rate, n, el = oracle_cpu_rate(cfg, greedy, min(per_step, 20.0), nth)
+        rate, n, el = oracle_cpu_rate(cfg, mode, min(per_step, 20.0), nth)
         if i >= args.warmup:
             rates.append(rate)
     value = float(np.mean(rates))
@@ -411,7 +447,7 @@ def run_reference(args, name: str):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic (seeded Philox inputs of the workload's shapes)",
-        "config": config_json(cfg, greedy, 1),
+        "config": config_json(cfg, mode, 1),
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": nth, "kind": "oracle",
                          "sample": f"per step: a bounded sample of the workload's sequences, about "
                                    f"{min(per_step, 20.0):.0f} s of CPU work"},
@@ -432,7 +468,7 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size (profiling)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    names = list(sg.CONFIGS) if args.config == "all" else [args.config]
+    names = list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) if args.config == "all" else [args.config]
     if args.impl == "reference":
         for n in names:
             run_reference(args, n)
