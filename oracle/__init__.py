@@ -46,6 +46,9 @@ def _bind(lib):
     lib.oracle_verify_lookahead_sample.argtypes = [vp, ctypes.c_int, vp, vp, i64, i32, i32, i64, f32, vp, vp, vp,
                                                    vp]
     lib.oracle_verify_lookahead_sample.restype = ctypes.c_int
+    lib.oracle_verify_multidraft_sample.argtypes = [vp, vp, ctypes.c_int, vp, vp, i64, i32, i32, i64, f32, vp, vp,
+                                                    vp, vp]
+    lib.oracle_verify_multidraft_sample.restype = ctypes.c_int
     return lib
 
 
@@ -143,4 +146,28 @@ def verify_lookahead_sample(logits, cand, uniforms, temperature: float, lib=None
                                             float(temperature), _p(out), _p(acc), _p(best), _p(margin))
     if rc != 0:
         raise ValueError("oracle_verify_lookahead_sample: argument error")
+    return out, acc, best, margin
+
+
+def verify_multidraft_sample(target, draft, draft_tokens, uniforms, temperature: float, lib=None):
+    """Multi-draft sampling verify: target [B,G,N,V], draft [B,G,N-1,V],
+    draft_tokens [B,G,N-1], uniforms [B,(N-1)*G+1].
+    Returns (tokens[B,N], accept_len[B], best[B], margin[B])."""
+    lib = lib or _lib()
+    target = np.ascontiguousarray(target)
+    B, G, N, V = target.shape
+    draft = np.ascontiguousarray(draft)
+    assert draft.shape == (B, G, N - 1, V) and draft.dtype == target.dtype
+    toks = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    assert toks.shape == (B, G, N - 1)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32)
+    assert u.shape == (B, (N - 1) * G + 1)
+    out = np.empty((B, N), dtype=np.int32)
+    acc = np.empty(B, dtype=np.int32)
+    best = np.empty(B, dtype=np.int32)
+    margin = np.empty(B, dtype=np.float64)
+    rc = lib.oracle_verify_multidraft_sample(_p(target), _p(draft), _dtype_code(target), _p(toks), _p(u), B, G, N,
+                                             V, float(temperature), _p(out), _p(acc), _p(best), _p(margin))
+    if rc != 0:
+        raise ValueError("oracle_verify_multidraft_sample: argument error")
     return out, acc, best, margin

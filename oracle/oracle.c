@@ -456,3 +456,107 @@ int oracle_verify_lookahead_sample(const void* logits, int dtype, const int32_t*
   free(l); free(p); free(w); free(alive);
   return 0;
 }
+
+/* ------------------------------------------------ multi-draft sampling */
+
+int oracle_verify_multidraft_sample(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                                    const float* uniforms, int64_t B, int32_t G, int32_t N, int64_t V,
+                                    float temperature, int32_t* out_tokens, int32_t* out_accept_len,
+                                    int32_t* out_best, double* out_margin) {
+  if (!target || !draft || !draft_tokens || !uniforms || !out_tokens || !out_accept_len) return -1;
+  if (B < 0 || G < 1 || N < 2 || V < 2 || (dtype != 0 && dtype != 1)) return -1;
+  if (!(temperature > 0.0f)) return -1;
+  const double T = (double)temperature;
+  const int64_t NU = (int64_t)(N - 1) * G + 1;
+  double* l = (double*)malloc(sizeof(double) * (size_t)V);
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* q = (double*)malloc(sizeof(double) * (size_t)V);
+  double* w = (double*)malloc(sizeof(double) * (size_t)V);
+  int* alive = (int*)malloc(sizeof(int) * (size_t)G);
+  if (!l || !p || !q || !w || !alive) {
+    free(l); free(p); free(q); free(w); free(alive);
+    return -1;
+  }
+  for (int64_t b = 0; b < B; ++b) {
+    int32_t* out = out_tokens + b * N;
+    const int32_t* x = draft_tokens + b * G * (N - 1); /* x[g*(N-1) + n] */
+    const float* u = uniforms + b * NU;
+    double margin = INFINITY;
+    for (int n = 0; n < N; ++n) out[n] = -1;
+
+    int ok = 1;
+    for (int64_t k = 0; k < (int64_t)G * (N - 1); ++k) ok &= (x[k] >= 0 && (int64_t)x[k] < V);
+    for (int64_t k = 0; k < NU; ++k) ok &= (u[k] >= 0.0f && u[k] < 1.0f);
+    for (int64_t r = 0; ok && r < (int64_t)G * N; ++r) {
+      load_row(target, dtype, b * G * N + r, V, l);
+      ok = row_ok_sampling(l, V);
+    }
+    for (int64_t r = 0; ok && r < (int64_t)G * (N - 1); ++r) {
+      load_row(draft, dtype, b * G * (N - 1) + r, V, l);
+      ok = row_ok_sampling(l, V);
+    }
+    if (!ok) {
+      out_accept_len[b] = -1;
+      if (out_best) out_best[b] = -1;
+      if (out_margin) out_margin[b] = INFINITY;
+      continue;
+    }
+
+    for (int g = 0; g < G; ++g) alive[g] = 1;
+    int lead = 0, j = N - 1;
+    for (int n = 0; n < N - 1; ++n) {
+      load_row(target, dtype, (b * G + lead) * N + n, V, l);
+      softmax_T(l, V, T, p, NULL, NULL);
+      int accepted = -1;
+      for (int g = 0; g < G; ++g) {
+        if (!alive[g]) continue;
+        const int32_t xg = x[g * (N - 1) + n];
+        load_row(draft, dtype, (b * G + g) * (N - 1) + n, V, l);
+        softmax_T(l, V, T, q, NULL, NULL); /* q_g, the distribution x_g came from */
+        const double px = p[xg], qx = q[xg];
+        double alpha;
+        if (px == 0.0)
+          alpha = 0.0;
+        else if (qx == 0.0)
+          alpha = 1.0;
+        else
+          alpha = fmin(1.0, px / qx);
+        if (alpha > 0.0) {
+          double du = fabs((double)u[n * G + g] - alpha);
+          if (du < margin) margin = du;
+        }
+        if ((double)u[n * G + g] < alpha) {
+          accepted = g;
+          break;
+        }
+        /* Rejected: p <- norm(max(0, p - q_g)), or p itself if that is all zero. */
+        double Z = 0.0;
+        for (int64_t v = 0; v < V; ++v) {
+          w[v] = fmax(0.0, p[v] - q[v]);
+          Z += w[v];
+        }
+        if (Z > 0.0)
+          for (int64_t v = 0; v < V; ++v) p[v] = w[v] / Z;
+      }
+      if (accepted < 0) {
+        out[n] = (int32_t)inverse_cdf(p, V, (double)u[(N - 1) * G], &margin);
+        j = n;
+        break;
+      }
+      const int32_t xa = x[accepted * (N - 1) + n];
+      out[n] = xa;
+      for (int g = 0; g < G; ++g) alive[g] = alive[g] && (x[g * (N - 1) + n] == xa);
+      lead = accepted;
+    }
+    if (j == N - 1) {
+      load_row(target, dtype, (b * G + lead) * N + (N - 1), V, l);
+      softmax_T(l, V, T, p, NULL, NULL);
+      out[N - 1] = (int32_t)inverse_cdf(p, V, (double)u[(N - 1) * G], &margin);
+    }
+    out_accept_len[b] = j;
+    if (out_best) out_best[b] = lead;
+    if (out_margin) out_margin[b] = margin;
+  }
+  free(l); free(p); free(q); free(w); free(alive);
+  return 0;
+}

@@ -90,6 +90,21 @@ int oracle_verify_lookahead_sample(const void* logits, int dtype, const int32_t*
                                    int32_t* out_tokens, int32_t* out_accept_len, int32_t* out_best,
                                    double* out_margin);
 
+/* Multi-draft sampling verify: the same walk with G drafts that were sampled
+ * from full draft distributions. draft [B,G,N-1,V]: row (g, n) is the draft
+ * distribution (as logits) that draft g's token at position n was drawn from;
+ * draft_tokens [B,G,N-1]. Draft g is tested against the current p with
+ * alpha = min(1, p(x)/q_g(x)) (q_g(x) = 0 < p(x) gives 1, p(x) = 0 gives 0);
+ * a rejection replaces p by norm(max(0, p - q_g)) ([P1] §2.1 applied once per
+ * rejected draft; if that is all zero, p is kept, [P1] §4). Temperature
+ * applies to both sides ([P2] §3.4). Everything else — the owner's rows, the
+ * prefix filter, the uniform layout, the draw, the outputs and the input
+ * checks (every draft row too) — is as in oracle_verify_lookahead_sample. */
+int oracle_verify_multidraft_sample(const void* target, const void* draft, int dtype, const int32_t* draft_tokens,
+                                    const float* uniforms, int64_t B, int32_t G, int32_t N, int64_t V,
+                                    float temperature, int32_t* out_tokens, int32_t* out_accept_len,
+                                    int32_t* out_best, double* out_margin);
+
 #ifdef __cplusplus
 }
 #endif

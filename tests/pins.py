@@ -401,3 +401,119 @@ def check_lookahead_golden(lib):
     for logits, cand, u, T, toks, acc, best in load_lookahead_golden():
         out, a, b, _ = oracle.verify_lookahead_sample(logits, cand, u, T, lib=lib)
         assert out[0].tolist() == toks and a[0] == acc and b[0] == best, (out, a, b, toks, acc, best)
+
+
+# ---------------------------------------------------------------------------
+# Multi-draft sampling verify: G drafts, each drawn from its own draft
+# distribution, verified by the walk above with alpha = min(1, p(x)/q_g(x)) and
+# the residual norm(max(0, p - q_g)) after each rejection ("Speculative
+# Decoding —— LLM推理优化技术（一）" §2.1-2.2, applied once per rejected draft).
+
+def one_hot_rows(tokens, V):
+    """Draft logits that put all mass on the given tokens: 0 there, -inf elsewhere."""
+    rows = np.full(tokens.shape + (V,), -np.inf, np.float32)
+    np.put_along_axis(rows, tokens[..., None], 0.0, axis=-1)
+    return rows
+
+
+def check_multidraft_one_hot_is_lookahead(lib, seed=31):
+    """One-hot draft rows make the multi-draft verify the Lookahead one."""
+    B, G, N, V, T = 2000, 4, 4, 12, 0.8
+    rng = np.random.default_rng(seed)
+    target = rng.normal(0, 1.5, size=(B, G, N, V)).astype(np.float32)
+    cand = rng.integers(0, 3, size=(B, G, N - 1)).astype(np.int32)  # few distinct tokens: shared prefixes
+    U = sg.uniforms(B, (N - 1) * G, seed=seed)
+    m = oracle.verify_multidraft_sample(target, one_hot_rows(cand, V), cand, U, T, lib=lib)
+    la = oracle.verify_lookahead_sample(target, cand, U, T)
+    for a, b in zip(m[:3], la[:3]):
+        np.testing.assert_array_equal(a, b)
+
+
+def check_multidraft_single_draft_is_sampling(lib, seed=32):
+    """One draft makes it the sampling-mode verify with K = N-1."""
+    B, N, V, T = 3000, 5, 10, 0.9
+    rng = np.random.default_rng(seed)
+    target = rng.normal(0, 1.5, size=(B, 1, N, V)).astype(np.float32)
+    draft = (target[:, :, : N - 1] + rng.normal(0, 1.0, size=(B, 1, N - 1, V))).astype(np.float32)
+    toks = sg.draft_tokens(draft[:, 0], sg.F32, T, 1.0, seed=seed)
+    U = sg.uniforms(B, N - 1, seed=seed)
+    out, acc, best, _ = oracle.verify_multidraft_sample(target, draft, toks[:, None, :], U, T, lib=lib)
+    rt, ra, margin = oracle.verify_sample(target[:, 0], draft[:, 0], toks, U, T)
+    assert (best == 0).all() and (ra >= 0).all()
+    firm = margin > 1e-9  # the two normalise the residual in a different order
+    np.testing.assert_array_equal(acc[firm], ra[firm])
+    np.testing.assert_array_equal(out[firm], rt[firm])
+
+
+MD_G, MD_N, MD_V = 3, 3, 6
+
+
+def multidraft_case(n, T, seed):
+    """Fixed target and draft rows (draft g's rows near the target's, so that
+    drafts are often accepted), drafts sampled from their own rows."""
+    rng = np.random.default_rng(seed)
+    lt = rng.normal(0, 1.0, size=(MD_G, MD_N, MD_V)).astype(np.float32)
+    ld = (lt[:, : MD_N - 1] + rng.normal(0, 0.8, size=(MD_G, MD_N - 1, MD_V))).astype(np.float32)
+    target = np.broadcast_to(lt, (n,) + lt.shape).copy()
+    draft = np.broadcast_to(ld, (n,) + ld.shape).copy()
+    toks = sg.draft_tokens(draft.reshape(n * MD_G, MD_N - 1, MD_V), sg.F32, T, 1.0, seed=seed)
+    toks = toks.reshape(n, MD_G, MD_N - 1)
+    U = sg.uniforms(n, (MD_N - 1) * MD_G, seed=seed + 1)
+    return lt, target, draft, toks, U
+
+
+def check_multidraft_marginal(lib, T=0.9, n=300_000, seed=33):
+    """Over drafts drawn from their rows, the first token follows the target
+    row of candidate 0; given an accepted first token t_0, the next token
+    follows the target row of the lowest draft starting with t_0 (chi-square).
+    The accepted prefix is the reported owner's, and no lower draft has it."""
+    lt, target, draft, toks, U = multidraft_case(n, T, seed)
+    out, acc, best, _ = oracle.verify_multidraft_sample(target, draft, toks, U, T, lib=lib)
+    assert (acc >= 0).all()
+    for b in np.nonzero(acc >= 1)[0][:20000]:
+        j, g = acc[b], best[b]
+        assert (out[b, :j] == toks[b, g, :j]).all()
+        assert not any((toks[b, h, :j] == out[b, :j]).all() for h in range(g))
+    p0 = softmax(lt[0, 0], T)
+    _, pval = stats.chisquare(np.bincount(out[:, 0], minlength=MD_V), p0 * n)
+    assert pval > 1e-3, f"position 0: chi-square p-value {pval:.3g}"
+    ext = acc >= 1
+    owner = np.argmax(toks[:, :, 0] == out[:, 0:1], axis=1)  # lowest draft holding t_0
+    for a in range(MD_G):
+        rows = ext & (owner == a)
+        if rows.sum() < 2000:
+            continue
+        p1 = softmax(lt[a, 1], T)
+        _, pval = stats.chisquare(np.bincount(out[rows, 1], minlength=MD_V), p1 * rows.sum())
+        assert pval > 1e-3, f"position 1 after owner {a}: chi-square p-value {pval:.3g}"
+
+
+def load_multidraft_golden():
+    lines = [l.strip() for l in open(os.path.join(GOLDEN, "multidraft_sample_hand.txt"))
+             if l.strip() and l[0] != "#"]
+    cases, i = [], 0
+    while i < len(lines):
+        _, G, N, V, T = lines[i].split()
+        G, N, V, T = int(G), int(N), int(V), float(T)
+        k = i + 1
+        tgt = [[float(x) for x in lines[k + r].split()] for r in range(G * N)]
+        k += G * N
+        dft = [[float(x) for x in lines[k + r].split()] for r in range(G * (N - 1))]
+        k += G * (N - 1)
+        toks = [[int(x) for x in lines[k + g].split()] for g in range(G)]
+        k += G
+        u = [float(x) for x in lines[k].split()[1:]]
+        exp = lines[k + 1]
+        out, acc, best = [s.strip() for s in exp[len("expect"):].split(";")]
+        cases.append((np.array(tgt, np.float32).reshape(1, G, N, V), np.array(dft, np.float32).reshape(1, G, N - 1, V),
+                      np.array(toks, np.int32).reshape(1, G, N - 1), np.array(u, np.float32).reshape(1, -1), T,
+                      [int(t) for t in out.split()], int(acc), int(best)))
+        i = k + 2
+    return cases
+
+
+def check_multidraft_golden(lib):
+    for tgt, dft, toks, u, T, out_e, acc_e, best_e in load_multidraft_golden():
+        out, acc, best, _ = oracle.verify_multidraft_sample(tgt, dft, toks, u, T, lib=lib)
+        assert out[0].tolist() == out_e and acc[0] == acc_e and best[0] == best_e, (out, acc, best, out_e, acc_e,
+                                                                                   best_e)

@@ -8,8 +8,8 @@ import pytest
 
 import oracle
 from pins import (check_acceptance_is_one_minus_tv, check_brute_force, check_greedy_golden,
-                  check_lookahead_exact, check_lookahead_golden, check_output_is_target_distribution,
-                  check_tokens_per_round)
+                  check_lookahead_exact, check_lookahead_golden, check_multidraft_golden,
+                  check_multidraft_marginal, check_output_is_target_distribution, check_tokens_per_round)
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -71,6 +71,23 @@ MUTATIONS = {
     "lookahead_draw_uniform": ("out[n] = (int32_t)inverse_cdf(p, V, (double)u[(N - 1) * G], &margin);",
                                "out[n] = (int32_t)inverse_cdf(p, V, (double)u[0], &margin);",
                                check_lookahead_golden),
+    # multi-draft: the residual is max(0, p - q_g)
+    "multidraft_residual_sign": ("w[v] = fmax(0.0, p[v] - q[v]);", "w[v] = fmax(0.0, q[v] - p[v]);",
+                                 check_multidraft_marginal),
+    # alpha = min(1, p/q_g)
+    "multidraft_ratio_inverted": ("alpha = fmin(1.0, px / qx);", "alpha = fmin(1.0, qx / px);",
+                                  check_multidraft_marginal),
+    # the residual is renormalised before the next draft's test
+    "multidraft_no_renormalise": ("p[v] = w[v] / Z;", "p[v] = w[v];", check_multidraft_marginal),
+    # each draft is tested against the distribution it was drawn from
+    "multidraft_q_of_draft_0": ("load_row(draft, dtype, (b * G + g) * (N - 1) + n, V, l);",
+                                "load_row(draft, dtype, (b * G + 0) * (N - 1) + n, V, l);", check_multidraft_golden),
+    # only drafts that still match the accepted prefix are tested
+    "multidraft_no_prefix_filter": ("alive[g] = alive[g] && (x[g * (N - 1) + n] == xa);", "alive[g] = alive[g];",
+                                    check_multidraft_marginal),
+    # the target row at position n is the owner's
+    "multidraft_row_of_draft_0": ("load_row(target, dtype, (b * G + lead) * N + n, V, l);",
+                                  "load_row(target, dtype, (b * G + 0) * N + n, V, l);", check_multidraft_marginal),
 }
 
 
@@ -80,14 +97,44 @@ def tmpdir_mod():
         yield d
 
 
+# The oracle function each mutation is planted in; the anchor must occur
+# exactly once within that function's body.
+FUNCTIONS = ("oracle_verify_sample", "oracle_row_stats", "oracle_verify_greedy", "oracle_verify_lookahead_sample",
+             "oracle_verify_multidraft_sample")
+
+
+def function_span(src: str, fn: str):
+    """[start, end) of the definition of ``fn`` in the oracle source."""
+    start = src.index(f"\nint {fn}(")
+    ends = [src.find(f"\nint {g}(", start + 1) for g in FUNCTIONS]
+    ends = [e for e in ends if e > start]
+    return start, min(ends) if ends else len(src)
+
+
+def function_of(name: str) -> str:
+    if name.startswith("lookahead_"):
+        return "oracle_verify_lookahead_sample"
+    if name.startswith("multidraft_"):
+        return "oracle_verify_multidraft_sample"
+    if name.startswith(("argmax_", "greedy_")):
+        return "oracle_verify_greedy"
+    return "oracle_verify_sample"
+
+
 @pytest.mark.parametrize("name", sorted(MUTATIONS))
 def test_pin_rejects_planted_mistake(name, tmpdir_mod):
     old, new, check = MUTATIONS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutation anchor for {name} must occur exactly once"
+    fn = function_of(name)
+    if name in ("argmax_highest_index", "no_renormalise"):  # helpers (argmax, inverse CDF) shared by the modes
+        a, b = 0, len(src)
+    else:
+        a, b = function_span(src, fn)
+    body = src[a:b]
+    assert body.count(old) == 1, f"mutation anchor for {name} must occur exactly once in {fn}"
     path = os.path.join(tmpdir_mod, f"oracle_{name}.c")
     with open(path, "w") as f:
-        f.write(src.replace(old, new))
+        f.write(src[:a] + body.replace(old, new) + src[b:])
     lib = oracle.load_library(oracle.compile_oracle(path, os.path.join(tmpdir_mod, f"lib_{name}.so")))
     with pytest.raises(AssertionError):
         check(lib)
