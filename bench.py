@@ -105,7 +105,7 @@ def kernel_for(cfg, mode) -> str:
     return KERNEL
 
 
-def config_json(cfg, mode, rotation):
+def config_json(cfg, mode, rotation, l2_resident=False):
     c = {"workload": cfg.name if cfg.B == find_config(cfg.name).B else f"{cfg.name}_b{cfg.B}", "B": cfg.B,
          "V": cfg.V, "logits": "bf16" if cfg.dtype == sg.BF16 else "f32"}
     if mode == "greedy":
@@ -114,8 +114,13 @@ def config_json(cfg, mode, rotation):
         c.update({"mode": "lookahead_sample", "G": cfg.G, "N": cfg.N, "temperature": cfg.temperature})
     else:
         c.update({"mode": "sample", "K": cfg.K, "temperature": cfg.temperature, "top_p": cfg.top_p})
-    c["l2"] = (f"inputs larger than L2: {rotation} rotating input sets" if rotation > 1
-               else "inputs larger than L2 (one set)")
+    esz = 2 if cfg.dtype == sg.BF16 else 4
+    fits = cfg.B * cfg.V * esz * ((2 * cfg.K + 1) if hasattr(cfg, "K") else cfg.G * cfg.N) <= L2_BYTES
+    if l2_resident and fits:
+        c["l2"] = "L2-resident: one input set replayed (not an HBM figure)"
+    else:
+        c["l2"] = (f"inputs larger than L2: {rotation} rotating input sets" if rotation > 1
+                   else "inputs larger than L2 (one set)")
     return c
 
 
@@ -283,6 +288,8 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
     svpkg.build()
     cfg, mode, positions, logit_bytes, small_in, out_bytes = workload(name, args.batch)
     rotation = 1 if logit_bytes > L2_BYTES else int(math.ceil(3 * L2_BYTES / logit_bytes)) + 1
+    if args.l2_resident:
+        rotation = 1  # one input set, replayed: it stays in L2 when it fits
     log(f"[bench] {name}: {logit_bytes / 1e6:.1f} MB of logits per call, {rotation} input set(s)")
     t0 = time.perf_counter()
     off = shard_offset(rank, cfg.B)
@@ -393,7 +400,7 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
         "vs_baseline": None,
         "dtype": "f32",
         "data": "synthetic (seeded Philox inputs of the workload's shapes)",
-        "config": config_json(cfg, mode, rotation),
+        "config": config_json(cfg, mode, rotation, args.l2_resident),
         "rounds_per_s": cfg.B * world / (ms_per_step / 1e3),
         "achieved_gbs": achieved_gbs,
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
@@ -409,9 +416,12 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nth = os.cpu_count() or 1
         rate, n, el = oracle_cpu_rate(cfg, mode, args.cpu_budget, nth)
+        rate1, n1, el1 = oracle_cpu_rate(cfg, mode, args.cpu_budget / 2, 1)
         line["cpu_baseline"] = {"value": rate, "unit": "positions/s", "cores": nth, "kind": "oracle",
                                 "sample": f"{n} sequences of the workload in {el:.1f} s, "
-                                          f"one oracle call per thread per batch"}
+                                          f"one oracle call per thread per batch",
+                                "single_thread": {"value": rate1, "unit": "positions/s", "cores": 1,
+                                                  "sample": f"{n1} sequences in {el1:.1f} s"}}
     if print_line and rank == 0:
         print(json.dumps(line), flush=True)
     return line
@@ -465,7 +475,11 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size (profiling)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (--batch 1: per-call latency of one sequence)")
+    ap.add_argument("--l2-resident", action="store_true",
+                    help="replay one input set, so that inputs that fit stay in L2 (reported as such; not an "
+                         "HBM figure)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     names = list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) if args.config == "all" else [args.config]
