@@ -1,0 +1,54 @@
+"""The benchmark's host side, without a GPU: the algorithmic bytes and
+positions it credits per call, and the JSON line of its reference arm (the
+CPU oracle on a bounded sample)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+import bench
+import specgen as sg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.mark.parametrize("name", list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS))
+def test_algorithmic_bytes_are_one_read_of_every_logit(name):
+    cfg, mode, positions, logit_bytes, small_in, out_bytes = bench.workload(name)
+    s = 2 if cfg.dtype == sg.BF16 else 4
+    if mode == "sample":
+        assert positions == cfg.B * (cfg.K + 1)
+        assert logit_bytes == cfg.B * (2 * cfg.K + 1) * cfg.V * s
+        assert out_bytes == cfg.B * (cfg.K + 1) * 4 + cfg.B * 4
+    else:
+        assert positions == cfg.B * cfg.G * cfg.N
+        assert logit_bytes == cfg.B * cfg.G * cfg.N * cfg.V * s
+        assert out_bytes == cfg.B * cfg.N * 4 + cfg.B * 4
+    assert mode == {"cfg4_greedy_v32000_bf16": "greedy", "la_sample_v32000_bf16": "lookahead"}.get(name, "sample")
+    c = bench.config_json(cfg, mode, 3)
+    assert c["workload"] == name and c["B"] == cfg.B and c["V"] == cfg.V
+
+
+def test_batch_override_names_the_workload():
+    cfg, mode, *_ = bench.workload("cfg1_v1000_f32", batch=1)
+    assert cfg.B == 1 and bench.config_json(cfg, mode, 1)["workload"] == "cfg1_v1000_f32_b1"
+
+
+def test_reference_arm_prints_one_contract_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config",
+                        "cfg1_v1000_f32", "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                       timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["higher_is_better"] is True
+    assert line["steps"] == 1 and line["warmup"] == 3 and line["config"]["workload"] == "cfg1_v1000_f32"
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}

@@ -32,9 +32,12 @@ def _rank_main(rank, world, port, B, out_q):
         g = sg.CONFIGS["cfg4_greedy_v32000_bf16"].with_(B=B, V=300)
         gd = sg.greedy_inputs(g, seq_offset=bench.shard_offset(rank, B))
         gt, ga, _ = oracle.verify_greedy(gd["logits"], gd["cand"])
+        la = sg.LOOKAHEAD_CONFIGS["la_sample_v32000_bf16"].with_(B=B, V=400, temperature=0.5)
+        ld = sg.lookahead_sample_inputs(la, seq_offset=bench.shard_offset(rank, B))
+        lt, lacc, _, _ = oracle.verify_lookahead_sample(ld["logits"], ld["cand"], ld["uniforms"], la.temperature)
         slowest = bench.max_over_ranks(10.0 + rank)
         parts = [None] * world
-        dist.all_gather_object(parts, (rank, toks, acc, gt, ga, slowest))
+        dist.all_gather_object(parts, (rank, toks, acc, gt, ga, slowest, lt, lacc))
         if rank == 0:
             out_q.put(parts)
     finally:
@@ -66,3 +69,8 @@ def test_two_rank_shards_equal_the_global_batch():
     gt, ga, _ = oracle.verify_greedy(gd["logits"], gd["cand"])
     np.testing.assert_array_equal(np.concatenate([x[3] for x in parts]), gt)
     np.testing.assert_array_equal(np.concatenate([x[4] for x in parts]), ga)
+    la = sg.LOOKAHEAD_CONFIGS["la_sample_v32000_bf16"].with_(B=world * B, V=400, temperature=0.5)
+    ld = sg.lookahead_sample_inputs(la)
+    lt, lacc, _, _ = oracle.verify_lookahead_sample(ld["logits"], ld["cand"], ld["uniforms"], la.temperature)
+    np.testing.assert_array_equal(np.concatenate([x[6] for x in parts]), lt)
+    np.testing.assert_array_equal(np.concatenate([x[7] for x in parts]), lacc)
