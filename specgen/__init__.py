@@ -232,6 +232,45 @@ CONFIGS = {
 }
 
 
+@dataclass(frozen=True)
+class MultiDraftConfig:
+    """A multi-draft sampling verify workload: target [B,G,N,V], draft
+    [B,G,N-1,V], draft_tokens [B,G,N-1] drawn from the draft rows, uniforms
+    [B,(N-1)*G+1]. Each (sequence, draft) pair is made like one sampling-mode
+    sequence with K = N-1: target rows sigma*N(0,1) with n_peaks raised by
+    peak_height, draft rows = target + draft_sigma*N(0,1)."""
+    name: str
+    B: int
+    G: int
+    N: int
+    V: int
+    dtype: int
+    temperature: float
+    target_sigma: float
+    peak_height: float
+    n_peaks: int
+    draft_sigma: float
+    seed: int = 0
+
+    @property
+    def rows(self) -> int:
+        return self.B * self.G * (2 * self.N - 1)
+
+    @property
+    def logit_bytes(self) -> int:
+        return self.rows * self.V * (2 if self.dtype == BF16 else 4)
+
+    def with_(self, **kw) -> "MultiDraftConfig":
+        return replace(self, **kw)
+
+
+MULTIDRAFT_CONFIGS = {
+    "md_sample_v32000_bf16": MultiDraftConfig("md_sample_v32000_bf16", B=32, G=7, N=5, V=32000, dtype=BF16,
+                                              temperature=1.0, target_sigma=3.0, peak_height=6.0, n_peaks=5,
+                                              draft_sigma=0.7),
+}
+
+
 # The Lookahead sampling-mode verify on the greedy workload's shape, at the
 # temperature the Lookahead page's sampling experiments use (1.0).
 LOOKAHEAD_CONFIGS = {
@@ -288,3 +327,24 @@ def lookahead_sample_inputs(cfg: LookaheadSampleConfig, seq_offset: int = 0, B: 
     u = out.setdefault("uniforms", np.empty((B, (cfg.N - 1) * cfg.G + 1), dtype=np.float32))
     assert _lib().sg_uniforms(B, (cfg.N - 1) * cfg.G, cfg.seed, seq_offset, _ptr(u)) == 0
     return out
+
+
+def multidraft_inputs(cfg: MultiDraftConfig, seq_offset: int = 0, B: int | None = None, nthreads: int = 0) -> dict:
+    """Generate target, draft, draft_tokens and uniforms for ``cfg``; shards
+    (``seq_offset``) equal the same batch generated whole."""
+    B = cfg.B if B is None else B
+    G, N = cfg.G, cfg.N
+    dt = np_dtype(cfg.dtype)
+    target = np.empty((B * G, N, cfg.V), dtype=dt)
+    draft = np.empty((B * G, N - 1, cfg.V), dtype=dt)
+    rc = _lib().sg_gen_logits(_ptr(target), _ptr(draft), cfg.dtype, B * G, N - 1, cfg.V, cfg.target_sigma,
+                              cfg.peak_height, cfg.n_peaks, cfg.draft_sigma, cfg.seed, seq_offset * G, nthreads)
+    assert rc == 0
+    toks = np.empty((B * G, N - 1), dtype=np.int32)
+    rc = _lib().sg_draft_tokens(_ptr(draft), cfg.dtype, B * G, N - 1, cfg.V, float(cfg.temperature), 1.0, cfg.seed,
+                                seq_offset * G, _ptr(toks), nthreads)
+    assert rc == 0
+    u = np.empty((B, (N - 1) * G + 1), dtype=np.float32)
+    assert _lib().sg_uniforms(B, (N - 1) * G, cfg.seed, seq_offset, _ptr(u)) == 0
+    return {"target": target.reshape(B, G, N, cfg.V), "draft": draft.reshape(B, G, N - 1, cfg.V),
+            "draft_tokens": toks.reshape(B, G, N - 1), "uniforms": u}

@@ -59,3 +59,26 @@ def test_input_errors_flag_the_sequence(lib):
     assert acc[4] >= 0
     with pytest.raises(ValueError):
         oracle.verify_multidraft_sample(target, draft, toks, U, 0.0, lib=lib)
+
+
+def test_workload_layout_and_shards(lib):
+    cfg = sg.MULTIDRAFT_CONFIGS["md_sample_v32000_bf16"].with_(B=80, V=500)
+    d = sg.multidraft_inputs(cfg)
+    part = sg.multidraft_inputs(cfg, seq_offset=30, B=25)
+    for k in d:
+        np.testing.assert_array_equal(d[k][30:55], part[k])
+    out, acc, best, _ = oracle.verify_multidraft_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                                                        cfg.temperature, lib=lib)
+    assert (acc >= 0).all()
+    x = d["draft_tokens"]
+    for b in range(cfg.B):
+        j, g = acc[b], best[b]
+        assert (out[b, :j] == x[b, g, :j]).all()
+        assert not any((x[b, h, :j] == out[b, :j]).all() for h in range(g))
+        assert 0 <= out[b, j] < cfg.V and (out[b, j + 1:] == -1).all()
+        if j < cfg.N - 1:
+            # after every still-matching draft is rejected, the residual is zero
+            # at each of their tokens, so the drawn token is none of them
+            held = {int(x[b, h, j]) for h in range(cfg.G) if (x[b, h, :j] == out[b, :j]).all()}
+            assert int(out[b, j]) not in held
+    assert len(set(acc.tolist())) >= 3
