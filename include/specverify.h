@@ -25,8 +25,9 @@
  *     library never frees or retains it past the call's completion on the
  *     stream. Arrays are dense, row-major, with the vocabulary innermost.
  *   - Calls are asynchronous: they validate arguments on the host, enqueue
- *     one kernel on `stream` (a cudaStream_t; NULL = the legacy default
- *     stream) and return. Results are valid once the stream reaches them.
+ *     their kernels on `stream` (one; two for sv_verify_lookahead_sample) (a
+ *     cudaStream_t; NULL = the legacy default stream) and return. Results are
+ *     valid once the stream reaches them.
  *   - The library keeps a small scratch area per (device, stream), allocated
  *     on the first call that needs it (or a larger one) and reused after.
  *     Calls on the same stream are ordered; calls on different streams use
