@@ -418,9 +418,11 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
         rate, n, el = oracle_cpu_rate(cfg, mode, args.cpu_budget, nth)
         rate1, n1, el1 = oracle_cpu_rate(cfg, mode, args.cpu_budget / 2, 1)
         line["cpu_baseline"] = {"value": rate, "unit": "positions/s", "cores": nth, "kind": "oracle",
+                                "rounds_per_s": n / el,
                                 "sample": f"{n} sequences of the workload in {el:.1f} s, "
                                           f"one oracle call per thread per batch",
                                 "single_thread": {"value": rate1, "unit": "positions/s", "cores": 1,
+                                                  "rounds_per_s": n1 / el1,
                                                   "sample": f"{n1} sequences in {el1:.1f} s"}}
     if print_line and rank == 0:
         print(json.dumps(line), flush=True)
@@ -437,11 +439,12 @@ def run_reference(args, name: str):
     cfg, mode, positions, logit_bytes, _, _ = workload(name, args.batch)
     nth = os.cpu_count() or 1
     per_step = max(5.0, 60.0 / max(1, args.steps + args.warmup))
-    rates = []
+    rates, rounds = [], []
     for i in range(args.warmup + args.steps):
         rate, n, el = oracle_cpu_rate(cfg, mode, min(per_step, 20.0), nth)
         if i >= args.warmup:
             rates.append(rate)
+            rounds.append(n / el)
     value = float(np.mean(rates))
     line = {
         "impl": "reference",
@@ -458,6 +461,7 @@ def run_reference(args, name: str):
         "dtype": "f64",
         "data": "synthetic (seeded Philox inputs of the workload's shapes)",
         "config": config_json(cfg, mode, 1),
+        "rounds_per_s": float(np.mean(rounds)),
         "cpu_baseline": {"value": value, "unit": "positions/s", "cores": nth, "kind": "oracle",
                          "sample": f"per step: a bounded sample of the workload's sequences, about "
                                    f"{min(per_step, 20.0):.0f} s of CPU work"},
