@@ -49,6 +49,9 @@ def _bind(lib):
     lib.oracle_verify_multidraft_sample.argtypes = [vp, vp, ctypes.c_int, vp, vp, i64, i32, i32, i64, f32, vp, vp,
                                                     vp, vp]
     lib.oracle_verify_multidraft_sample.restype = ctypes.c_int
+    lib.oracle_verify_sample_lmhead.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp, i64, i32, i64, i64, f32, f32,
+                                                vp, vp, vp]
+    lib.oracle_verify_sample_lmhead.restype = ctypes.c_int
     return lib
 
 
@@ -171,3 +174,28 @@ def verify_multidraft_sample(target, draft, draft_tokens, uniforms, temperature:
     if rc != 0:
         raise ValueError("oracle_verify_multidraft_sample: argument error")
     return out, acc, best, margin
+
+
+def verify_sample_lmhead(h_target, h_draft, w_target, w_draft, draft_tokens, uniforms, temperature: float,
+                         top_p: float = 1.0, lib=None):
+    """Sampling verify on logits h · W^T computed in fp64 from hidden states
+    h_target [B,K+1,D], h_draft [B,K,D] and LM heads w_target, w_draft [V,D].
+    Returns (tokens[B,K+1], accept_len[B], margin[B])."""
+    lib = lib or _lib()
+    ht, hd = np.ascontiguousarray(h_target), np.ascontiguousarray(h_draft)
+    wt, wd = np.ascontiguousarray(w_target), np.ascontiguousarray(w_draft)
+    B, K1, D = ht.shape
+    K = K1 - 1
+    V = wt.shape[0]
+    assert hd.shape == (B, K, D) and wt.shape == (V, D) and wd.shape == (V, D)
+    assert ht.dtype == hd.dtype == wt.dtype == wd.dtype
+    toks = np.ascontiguousarray(draft_tokens, dtype=np.int32)
+    u = np.ascontiguousarray(uniforms, dtype=np.float32)
+    out = np.empty((B, K1), dtype=np.int32)
+    acc = np.empty(B, dtype=np.int32)
+    margin = np.empty(B, dtype=np.float64)
+    rc = lib.oracle_verify_sample_lmhead(_p(ht), _p(hd), _p(wt), _p(wd), _dtype_code(ht), _p(toks), _p(u), B, K, D, V,
+                                         float(temperature), float(top_p), _p(out), _p(acc), _p(margin))
+    if rc != 0:
+        raise ValueError("oracle_verify_sample_lmhead: argument error")
+    return out, acc, margin

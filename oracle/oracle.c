@@ -15,6 +15,7 @@
 /* ------------------------------------------------------------ storage */
 
 static double load_logit(const void* base, int dtype, int64_t i) {
+  if (dtype == 2) return ((const double*)base)[i];
   if (dtype == 1) {
     uint32_t u = (uint32_t)((const uint16_t*)base)[i] << 16;
     float f;
@@ -162,7 +163,7 @@ int oracle_verify_sample(const void* target, const void* draft, int dtype, const
                          const float* uniforms, int64_t B, int32_t K, int64_t V, float temperature, float top_p,
                          int32_t* out_tokens, int32_t* out_accept_len, double* out_margin) {
   if (!target || !draft_tokens || !out_tokens || !out_accept_len) return -1;
-  if (B < 0 || K < 1 || V < 2 || (dtype != 0 && dtype != 1)) return -1;
+  if (B < 0 || K < 1 || V < 2 || dtype < 0 || dtype > 2) return -1;
   if (!(temperature >= 0.0f) || !(top_p > 0.0f && top_p <= 1.0f)) return -1;
   const int greedy_limit = (temperature == 0.0f);
   if (!greedy_limit && (!draft || !uniforms)) return -1;
@@ -559,4 +560,38 @@ int oracle_verify_multidraft_sample(const void* target, const void* draft, int d
   }
   free(l); free(p); free(q); free(w); free(alive);
   return 0;
+}
+
+/* ------------------------------------------------- LM head + verify */
+
+int oracle_verify_sample_lmhead(const void* h_target, const void* h_draft, const void* w_target, const void* w_draft,
+                                int dtype, const int32_t* draft_tokens, const float* uniforms, int64_t B, int32_t K,
+                                int64_t D, int64_t V, float temperature, float top_p, int32_t* out_tokens,
+                                int32_t* out_accept_len, double* out_margin) {
+  if (!h_target || !h_draft || !w_target || !w_draft) return -1;
+  if (B < 0 || K < 1 || D < 1 || V < 2 || (dtype != 0 && dtype != 1)) return -1;
+  double* lt = (double*)malloc(sizeof(double) * (size_t)(B * (K + 1) * V + 1));
+  double* ld = (double*)malloc(sizeof(double) * (size_t)(B * K * V + 1));
+  if (!lt || !ld) {
+    free(lt); free(ld);
+    return -1;
+  }
+  /* logits[r, v] = sum_d h[r, d] * W[v, d], each product and sum in fp64. */
+  for (int64_t r = 0; r < B * (K + 1); ++r)
+    for (int64_t v = 0; v < V; ++v) {
+      double s = 0.0;
+      for (int64_t d = 0; d < D; ++d) s += load_logit(h_target, dtype, r * D + d) * load_logit(w_target, dtype, v * D + d);
+      lt[r * V + v] = s;
+    }
+  for (int64_t r = 0; r < B * K; ++r)
+    for (int64_t v = 0; v < V; ++v) {
+      double s = 0.0;
+      for (int64_t d = 0; d < D; ++d) s += load_logit(h_draft, dtype, r * D + d) * load_logit(w_draft, dtype, v * D + d);
+      ld[r * V + v] = s;
+    }
+  const int rc = oracle_verify_sample(lt, ld, 2, draft_tokens, uniforms, B, K, V, temperature, top_p, out_tokens,
+                                      out_accept_len, out_margin);
+  free(lt);
+  free(ld);
+  return rc;
 }

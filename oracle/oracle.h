@@ -23,7 +23,8 @@
  *        "采样模式的验证" (sampling-mode verify of greedily produced
  *        candidates: the draft distribution is one-hot on the token).
  *
- * Dtype codes: 0 = fp32, 1 = bf16 (raw 16-bit patterns).
+ * Dtype codes: 0 = fp32, 1 = bf16 (raw 16-bit patterns); the sampling verify
+ * also takes 2 = fp64, for logits the oracle computes itself.
  * Return value of every function: 0 on success, -1 on an argument error.
  * Per-sequence input errors (token id outside [0,V), uniform outside [0,1),
  * NaN logit, +inf logit or an all -inf row in the sampling modes, NaN in
@@ -104,6 +105,18 @@ int oracle_verify_multidraft_sample(const void* target, const void* draft, int d
                                     const float* uniforms, int64_t B, int32_t G, int32_t N, int64_t V,
                                     float temperature, int32_t* out_tokens, int32_t* out_accept_len,
                                     int32_t* out_best, double* out_margin);
+
+/* The sampling verify on logits computed from hidden states by the LM heads:
+ * target logits [B,K+1,V] = h_target [B,K+1,D] · w_target[V,D]^T, draft
+ * logits [B,K,V] = h_draft [B,K,D] · w_draft[V,D]^T, every product and sum in
+ * fp64 (no rounding to a stored logit type), then oracle_verify_sample on
+ * them. This is the computation a fused LM-head GEMM with a verify epilogue
+ * must reproduce; the pages' verify takes the logits as given. dtype 0 or 1
+ * for h and w. */
+int oracle_verify_sample_lmhead(const void* h_target, const void* h_draft, const void* w_target, const void* w_draft,
+                                int dtype, const int32_t* draft_tokens, const float* uniforms, int64_t B, int32_t K,
+                                int64_t D, int64_t V, float temperature, float top_p, int32_t* out_tokens,
+                                int32_t* out_accept_len, double* out_margin);
 
 #ifdef __cplusplus
 }

@@ -517,3 +517,46 @@ def check_multidraft_golden(lib):
         out, acc, best, _ = oracle.verify_multidraft_sample(tgt, dft, toks, u, T, lib=lib)
         assert out[0].tolist() == out_e and acc[0] == acc_e and best[0] == best_e, (out, acc, best, out_e, acc_e,
                                                                                    best_e)
+
+
+# ---------------------------------------------------------------------------
+# The sampling verify on logits computed by the LM heads, h · W^T (the
+# computation a fused LM-head GEMM with a verify epilogue reproduces).
+
+def check_lmhead_identity(lib, seed=41):
+    """Identity heads (D = V, W = I) leave the hidden states as the logits."""
+    B, K, V, T = 400, 3, 24, 0.8
+    rng = np.random.default_rng(seed)
+    ht = rng.normal(0, 1.5, size=(B, K + 1, V)).astype(np.float32)
+    hd = (ht[:, :K] + rng.normal(0, 0.7, size=(B, K, V))).astype(np.float32)
+    toks = sg.draft_tokens(hd, sg.F32, T, 1.0, seed=seed)
+    U = sg.uniforms(B, K, seed=seed)
+    eye = np.eye(V, dtype=np.float32)
+    out, acc, _ = oracle.verify_sample_lmhead(ht, hd, eye, eye, toks, U, T, lib=lib)
+    rt, ra, _ = oracle.verify_sample(ht, hd, toks, U, T)
+    np.testing.assert_array_equal(acc, ra)
+    np.testing.assert_array_equal(out, rt)
+
+
+def check_lmhead_integer_products(lib, dtype=sg.F32, seed=42):
+    """With small integers in h and W every product and sum is exact, so the
+    verify must see exactly numpy's h @ W.T (target head for the target rows,
+    draft head for the draft rows). Square heads (D = V) so that a transposed
+    head is a different, in-bounds matrix."""
+    B, K, V, T = 300, 2, 12, 2.5
+    D = V
+    rng = np.random.default_rng(seed)
+    ht = rng.integers(-3, 4, size=(B, K + 1, D)).astype(np.float32)
+    hd = rng.integers(-3, 4, size=(B, K, D)).astype(np.float32)
+    wt = rng.integers(-2, 3, size=(V, D)).astype(np.float32)
+    wd = rng.integers(-2, 3, size=(V, D)).astype(np.float32)
+    lt = (ht.astype(np.float64) @ wt.T.astype(np.float64)).astype(np.float32)
+    ld = (hd.astype(np.float64) @ wd.T.astype(np.float64)).astype(np.float32)
+    toks = sg.draft_tokens(ld, sg.F32, T, 1.0, seed=seed)
+    U = sg.uniforms(B, K, seed=seed)
+    conv = (lambda a: sg.from_float(a, sg.BF16)) if dtype == sg.BF16 else (lambda a: a)
+    out, acc, _ = oracle.verify_sample_lmhead(conv(ht), conv(hd), conv(wt), conv(wd), toks, U, T, lib=lib)
+    rt, ra, _ = oracle.verify_sample(lt, ld, toks, U, T)
+    assert (ra >= 0).all()
+    np.testing.assert_array_equal(acc, ra)
+    np.testing.assert_array_equal(out, rt)

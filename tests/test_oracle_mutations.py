@@ -8,7 +8,8 @@ import pytest
 
 import oracle
 from pins import (check_acceptance_is_one_minus_tv, check_brute_force, check_greedy_golden,
-                  check_lookahead_exact, check_lookahead_golden, check_multidraft_golden,
+                  check_lmhead_integer_products, check_lookahead_exact, check_lookahead_golden,
+                  check_multidraft_golden,
                   check_multidraft_marginal, check_output_is_target_distribution, check_tokens_per_round)
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
@@ -86,6 +87,12 @@ MUTATIONS = {
     "multidraft_no_prefix_filter": ("alive[g] = alive[g] && (x[g * (N - 1) + n] == xa);", "alive[g] = alive[g];",
                                     check_multidraft_marginal),
     # the target row at position n is the owner's
+    # the LM head is applied as h · W^T (W stored [V, D])
+    "lmhead_transposed": ("load_logit(w_target, dtype, v * D + d)", "load_logit(w_target, dtype, d * V + v)",
+                          check_lmhead_integer_products),
+    # the draft rows use the draft model's head
+    "lmhead_draft_uses_target_head": ("load_logit(w_draft, dtype, v * D + d)", "load_logit(w_target, dtype, v * D + d)",
+                                      check_lmhead_integer_products),
     "multidraft_row_of_draft_0": ("load_row(target, dtype, (b * G + lead) * N + n, V, l);",
                                   "load_row(target, dtype, (b * G + 0) * N + n, V, l);", check_multidraft_marginal),
 }
@@ -100,7 +107,7 @@ def tmpdir_mod():
 # The oracle function each mutation is planted in; the anchor must occur
 # exactly once within that function's body.
 FUNCTIONS = ("oracle_verify_sample", "oracle_row_stats", "oracle_verify_greedy", "oracle_verify_lookahead_sample",
-             "oracle_verify_multidraft_sample")
+             "oracle_verify_multidraft_sample", "oracle_verify_sample_lmhead")
 
 
 def function_span(src: str, fn: str):
@@ -116,6 +123,8 @@ def function_of(name: str) -> str:
         return "oracle_verify_lookahead_sample"
     if name.startswith("multidraft_"):
         return "oracle_verify_multidraft_sample"
+    if name.startswith("lmhead_"):
+        return "oracle_verify_sample_lmhead"
     if name.startswith(("argmax_", "greedy_")):
         return "oracle_verify_greedy"
     return "oracle_verify_sample"
