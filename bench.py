@@ -470,12 +470,22 @@ def run_reference(args, name: str):
     print(json.dumps(line), flush=True)
 
 
+def config_names(spec: str) -> list:
+    """'all', one workload name, or several separated by commas."""
+    if spec == "all":
+        return list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS)
+    names = [n.strip() for n in spec.split(",") if n.strip()]
+    for n in names:
+        find_config(n)  # KeyError for an unknown name, before any work
+    return names
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default=DEFAULT_CONFIG, help="workload name, or 'all'")
+    ap.add_argument("--config", default=DEFAULT_CONFIG, help="workload name, several joined by commas, or 'all'")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -486,7 +496,7 @@ def main():
                          "HBM figure)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
-    names = list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) if args.config == "all" else [args.config]
+    names = config_names(args.config)
     if args.impl == "reference":
         for n in names:
             run_reference(args, n)

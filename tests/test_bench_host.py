@@ -52,3 +52,11 @@ def test_reference_arm_prints_one_contract_line():
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
+
+
+def test_config_names():
+    assert bench.config_names("cfg2_v32000_bf16") == ["cfg2_v32000_bf16"]
+    assert bench.config_names("cfg1_v1000_f32, la_sample_v32000_bf16") == ["cfg1_v1000_f32", "la_sample_v32000_bf16"]
+    assert bench.config_names("all")[:5] == list(sg.CONFIGS)
+    with pytest.raises(KeyError):
+        bench.config_names("cfg2_v32000_bf16,nope")
