@@ -56,7 +56,10 @@ def log(*a):
 # ------------------------------------------------------------------ workload
 
 def find_config(name: str):
-    return sg.CONFIGS[name] if name in sg.CONFIGS else sg.LOOKAHEAD_CONFIGS[name]
+    for table in (sg.CONFIGS, sg.LOOKAHEAD_CONFIGS, sg.MULTIDRAFT_CONFIGS):
+        if name in table:
+            return table[name]
+    raise KeyError(name)
 
 
 def workload(name: str, batch: int | None = None):
@@ -67,9 +70,15 @@ def workload(name: str, batch: int | None = None):
     if batch:
         cfg = cfg.with_(B=batch)
     mode = ("greedy" if isinstance(cfg, sg.GreedyConfig) else
-            "lookahead" if isinstance(cfg, sg.LookaheadSampleConfig) else "sample")
+            "lookahead" if isinstance(cfg, sg.LookaheadSampleConfig) else
+            "multidraft" if isinstance(cfg, sg.MultiDraftConfig) else "sample")
     esz = 2 if cfg.dtype == sg.BF16 else 4
-    if mode != "sample":
+    if mode == "multidraft":
+        positions = cfg.B * cfg.G * cfg.N
+        logit_bytes = cfg.B * cfg.G * (2 * cfg.N - 1) * cfg.V * esz
+        small_in = cfg.B * cfg.G * (cfg.N - 1) * 4 + cfg.B * ((cfg.N - 1) * cfg.G + 1) * 4
+        out_bytes = cfg.B * cfg.N * 4 + cfg.B * 4
+    elif mode != "sample":
         positions = cfg.B * cfg.G * cfg.N
         logit_bytes = cfg.B * cfg.G * cfg.N * cfg.V * esz
         small_in = cfg.B * cfg.G * (cfg.N - 1) * 4
@@ -92,6 +101,8 @@ def kernel_for(cfg, mode) -> str:
     The Lookahead sampling verify streams its rows in la_rows_kernel."""
     if mode == "lookahead":
         return "la_rows_kernel"
+    if mode == "multidraft":
+        return "md_rows_kernel"
     if mode == "greedy" or cfg.temperature == 0.0 or cfg.top_p < 1.0:
         return KERNEL
     esz = 2 if cfg.dtype == sg.BF16 else 4
@@ -112,10 +123,12 @@ def config_json(cfg, mode, rotation, l2_resident=False):
         c.update({"mode": "greedy", "G": cfg.G, "N": cfg.N})
     elif mode == "lookahead":
         c.update({"mode": "lookahead_sample", "G": cfg.G, "N": cfg.N, "temperature": cfg.temperature})
+    elif mode == "multidraft":
+        c.update({"mode": "multidraft_sample", "G": cfg.G, "N": cfg.N, "temperature": cfg.temperature})
     else:
         c.update({"mode": "sample", "K": cfg.K, "temperature": cfg.temperature, "top_p": cfg.top_p})
     esz = 2 if cfg.dtype == sg.BF16 else 4
-    fits = cfg.B * cfg.V * esz * ((2 * cfg.K + 1) if hasattr(cfg, "K") else cfg.G * cfg.N) <= L2_BYTES
+    fits = workload(cfg.name, cfg.B)[3] <= L2_BYTES
     if l2_resident and fits:
         c["l2"] = "L2-resident: one input set replayed (not an HBM figure)"
     else:
@@ -242,6 +255,8 @@ def host_inputs(cfg, mode, seq_offset: int = 0, B: int | None = None) -> dict:
         return sg.greedy_inputs(cfg, seq_offset=seq_offset, B=B)
     if mode == "lookahead":
         return sg.lookahead_sample_inputs(cfg, seq_offset=seq_offset, B=B)
+    if mode == "multidraft":
+        return sg.multidraft_inputs(cfg, seq_offset=seq_offset, B=B)
     return sg.sample_inputs(cfg, seq_offset=seq_offset, B=B)
 
 
@@ -260,6 +275,9 @@ def oracle_cpu_rate(cfg, mode, budget_s: float, nthreads: int):
         elif mode == "lookahead":
             oracle.verify_lookahead_sample(inputs["logits"][sl], inputs["cand"][sl], inputs["uniforms"][sl],
                                            cfg.temperature)
+        elif mode == "multidraft":
+            oracle.verify_multidraft_sample(inputs["target"][sl], inputs["draft"][sl], inputs["draft_tokens"][sl],
+                                            inputs["uniforms"][sl], cfg.temperature)
         else:
             oracle.verify_sample(inputs["target"][sl], inputs["draft"][sl], inputs["draft_tokens"][sl],
                                  inputs["uniforms"][sl], cfg.temperature, cfg.top_p)
@@ -296,6 +314,7 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
     host = host_inputs(cfg, mode, seq_offset=off)
     log(f"[bench] inputs generated in {time.perf_counter() - t0:.1f} s")
     keys = {"greedy": ("logits", "cand"), "lookahead": ("logits", "cand", "uniforms"),
+            "multidraft": ("target", "draft", "draft_tokens", "uniforms"),
             "sample": ("target", "draft", "draft_tokens", "uniforms")}[mode]
     pinned = {k: to_torch(host[k], torch, pin=True) for k in keys}
     sets = []
@@ -310,6 +329,8 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
             return svpkg.verify_greedy(*args, **kw)
         if mode == "lookahead":
             return svpkg.verify_lookahead_sample(*args, cfg.temperature, **kw)
+        if mode == "multidraft":
+            return svpkg.verify_multidraft_sample(*args, cfg.temperature, **kw)
         return svpkg.verify_sample(*args, cfg.temperature, cfg.top_p, **kw)
 
     def call(i):
@@ -473,7 +494,7 @@ def run_reference(args, name: str):
 def config_names(spec: str) -> list:
     """'all', one workload name, or several separated by commas."""
     if spec == "all":
-        return list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS)
+        return list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS)
     names = [n.strip() for n in spec.split(",") if n.strip()]
     for n in names:
         find_config(n)  # KeyError for an unknown name, before any work

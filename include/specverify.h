@@ -162,6 +162,32 @@ int sv_verify_lookahead_sample(const void* logits, const int32_t* cand, const fl
                                int32_t* out_accept_len, int32_t* out_best_cand, float* out_row_lse, void* stream);
 
 /*
+ * Multi-draft sampling verify: G drafts drawn from full draft distributions,
+ * verified by the walk of sv_verify_lookahead_sample with the single-draft
+ * rule of "Speculative Decoding —— LLM推理优化技术（一）" §2.1 for each draft.
+ *
+ *   target       [B, G, N, V] dtype: row (g, n) is the target's distribution
+ *                at position n of draft g's branch; row N-1 the bonus.
+ *   draft        [B, G, N-1, V] dtype: row (g, n) is the distribution draft
+ *                g's token at position n was drawn from.
+ *   draft_tokens [B, G, N-1] int32.
+ *   uniforms     [B, (N-1)*G + 1] fp32 in [0,1), laid out as for
+ *                sv_verify_lookahead_sample.
+ *   B >= 0, 1 <= G <= 32, N >= 2, G*N <= 1024, G*G*(N-1) <= 2048, V >= 2;
+ *   B*G*(2N-1) < 2^31; temperature > 0 (finite), on both sides.
+ * Draft g's token x is accepted when u < min(1, p(x)/q_g(x)) (q_g(x) = 0 <
+ * p(x) accepts, p(x) = 0 rejects), p the current distribution; a rejection
+ * replaces p by norm(max(0, p - q_g)) (p itself if that is all zero).
+ * Outputs as for sv_verify_lookahead_sample; out_row_lse, if given, holds
+ * B*G*N target rows then B*G*(N-1) draft rows. Bad input also covers every
+ * draft row.
+ */
+int sv_verify_multidraft_sample(const void* target, const void* draft, const int32_t* draft_tokens,
+                                const float* uniforms, int64_t B, int32_t G, int32_t N, int64_t V, int32_t dtype,
+                                float temperature, int32_t* out_tokens, int32_t* out_accept_len,
+                                int32_t* out_best_cand, float* out_row_lse, void* stream);
+
+/*
  * sv_verify_sample_noalloc: sv_verify_sample for callers that cannot allocate
  * device memory. The pages have no counterpart to this entry point; it exists
  * for deployment constraints, not for the method.

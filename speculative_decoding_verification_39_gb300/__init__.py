@@ -10,6 +10,7 @@ Entry points (same names as the C ABI):
   verify_sample(target, draft, draft_tokens, uniforms, temperature, top_p)
   verify_greedy(logits, cand)
   verify_lookahead_sample(logits, cand, uniforms, temperature)
+  verify_multidraft_sample(target, draft, draft_tokens, uniforms, temperature)
   get_status()
 """
 from __future__ import annotations
@@ -25,8 +26,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _SO = os.path.join(_HERE, "libspecverify.so")
-_SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_noalloc.cu", "sv_lookahead.cu"]
-_DEPS = _SOURCES + ["sv_kernels.h", "sv_device.cuh", "sv_lookahead.h"]
+_SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_noalloc.cu", "sv_lookahead.cu", "sv_multidraft.cu"]
+_DEPS = _SOURCES + ["sv_kernels.h", "sv_device.cuh", "sv_lookahead.h", "sv_multidraft.h", "sv_rowstat.cuh"]
 
 SV_F32, SV_BF16 = 0, 1
 STATUS = {0: "SV_OK", -1: "SV_ERR_ARG", -2: "SV_ERR_DTYPE", -3: "SV_ERR_CUDA", -4: "SV_ERR_INPUT",
@@ -113,6 +114,8 @@ def lib():
         h.sv_selftest_wait_timeout.restype = ctypes.c_int
         h.sv_verify_lookahead_sample.argtypes = [vp, vp, vp, i64, i32, i32, i64, i32, f32, vp, vp, vp, vp, vp]
         h.sv_verify_lookahead_sample.restype = ctypes.c_int
+        h.sv_verify_multidraft_sample.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i32, f32, vp, vp, vp, vp, vp]
+        h.sv_verify_multidraft_sample.restype = ctypes.c_int
         _lib_handle = h
     return _lib_handle
 
@@ -120,7 +123,7 @@ def lib():
 def exported_symbols() -> list:
     return ["sv_verify_sample", "sv_verify_greedy", "sv_get_status", "sv_status_string", "sv_release",
             "sv_set_launch_shape", "sv_launch_count", "sv_verify_sample_noalloc", "sv_selftest_wait_timeout",
-            "sv_verify_lookahead_sample"]
+            "sv_verify_lookahead_sample", "sv_verify_multidraft_sample"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -271,6 +274,49 @@ def verify_lookahead_sample(logits, cand, uniforms, temperature: float, out_toke
                                               _ptr(ot), _ptr(oa), _ptr(ob), _ptr(ol), _stream_handle(dev))
     if rc != 0:
         raise SpecVerifyError(rc, "sv_verify_lookahead_sample")
+    res = [ot, oa] + ([ob] if best else []) + ([ol] if row_lse else [])
+    if host:
+        outs = [r.to("cpu", non_blocking=True) if out is None else out.copy_(r, non_blocking=True)
+                for r, out in zip(res, [out_tokens, out_accept_len, None, None])]
+        torch.cuda.current_stream(dev).synchronize()
+        res = outs
+    return tuple(res)
+
+
+def verify_multidraft_sample(target, draft, draft_tokens, uniforms, temperature: float, out_tokens=None,
+                             out_accept_len=None, best=False, row_lse=False, device=None):
+    """Multi-draft sampling verify (sv_verify_multidraft_sample).
+
+    target [B,G,N,V] and draft [B,G,N-1,V] logits (bf16 or fp32), draft_tokens
+    [B,G,N-1] int32, uniforms [B,(N-1)*G+1] fp32. Returns (out_tokens [B,N],
+    out_accept_len [B]), then the owner [B] with ``best`` and the row
+    log-normalisers [B*G*(2N-1)] (target rows, then draft rows) with
+    ``row_lse``. CPU tensors are handled as in verify_sample.
+    """
+    host = target.device.type == "cpu"
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if not host:
+        dev = target.device
+    B, G, N, V = target.shape
+    t = _on_device(target, dev, "target")
+    d = _on_device(draft, dev, "draft")
+    x = _on_device(draft_tokens, dev, "draft_tokens")
+    u = _on_device(uniforms, dev, "uniforms")
+    _check(t, (B, G, N, V), None, "target")
+    dt = _dtype_code(t)
+    _check(d, (B, G, N - 1, V), t.dtype, "draft")
+    _check(x, (B, G, N - 1), torch.int32, "draft_tokens")
+    _check(u, (B, (N - 1) * G + 1), torch.float32, "uniforms")
+    ot = torch.empty((B, N), dtype=torch.int32, device=dev) if (out_tokens is None or host) else out_tokens
+    oa = torch.empty((B,), dtype=torch.int32, device=dev) if (out_accept_len is None or host) else out_accept_len
+    ob = torch.empty((B,), dtype=torch.int32, device=dev) if best else None
+    ol = torch.empty((B * G * (2 * N - 1),), dtype=torch.float32, device=dev) if row_lse else None
+    with torch.cuda.device(dev):
+        rc = lib().sv_verify_multidraft_sample(_ptr(t), _ptr(d), _ptr(x), _ptr(u), B, G, N, V, dt,
+                                               float(temperature), _ptr(ot), _ptr(oa), _ptr(ob), _ptr(ol),
+                                               _stream_handle(dev))
+    if rc != 0:
+        raise SpecVerifyError(rc, "sv_verify_multidraft_sample")
     res = [ot, oa] + ([ob] if best else []) + ([ol] if row_lse else [])
     if host:
         outs = [r.to("cpu", non_blocking=True) if out is None else out.copy_(r, non_blocking=True)

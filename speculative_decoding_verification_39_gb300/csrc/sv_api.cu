@@ -12,6 +12,7 @@
 #include "../../include/specverify.h"
 #include "sv_kernels.h"
 #include "sv_lookahead.h"
+#include "sv_multidraft.h"
 
 namespace {
 
@@ -284,6 +285,57 @@ extern "C" int sv_verify_lookahead_sample(const void* logits, const int32_t* can
   p.out_best = out_best_cand;
   p.out_row_lse = out_row_lse;
   if (sv::la::launch(p, dtype, st) != cudaSuccess) return SV_ERR_CUDA;
+  g_launches.fetch_add(2);
+  return SV_OK;
+}
+
+extern "C" int sv_verify_multidraft_sample(const void* target, const void* draft, const int32_t* draft_tokens,
+                                           const float* uniforms, int64_t B, int32_t G, int32_t N, int64_t V,
+                                           int32_t dtype, float temperature, int32_t* out_tokens,
+                                           int32_t* out_accept_len, int32_t* out_best_cand, float* out_row_lse,
+                                           void* stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (B < 0 || B >= kMaxV || V < 2 || V >= kMaxV || !sv::md::fits(G, N)) return SV_ERR_ARG;
+  if (B * (int64_t)G * (2 * N - 1) >= kMaxV) return SV_ERR_ARG;
+  if (!(temperature > 0.f) || std::isinf(temperature)) return SV_ERR_ARG;
+  if (B == 0) return SV_OK;
+  if (!target || !draft || !draft_tokens || !uniforms || !out_tokens || !out_accept_len) return SV_ERR_ARG;
+  const size_t esz = dtype == SV_BF16 ? 2 : 4;
+  if (!aligned_to(target, esz) || !aligned_to(draft, esz)) return SV_ERR_DTYPE;
+  if (!aligned_to(draft_tokens, 4) || !aligned_to(uniforms, 4) || !aligned_to(out_tokens, 4) ||
+      !aligned_to(out_accept_len, 4) || (out_best_cand && !aligned_to(out_best_cand, 4)) ||
+      (out_row_lse && !aligned_to(out_row_lse, 4)))
+    return SV_ERR_ARG;
+  const float c = (float)(1.4426950408889634 / (double)temperature);
+  if (!std::isfinite(c)) return SV_ERR_ARG;
+  const int64_t rows = B * G * (2 * N - 1);
+  const size_t rowstat_bytes = align256((size_t)rows * 8);
+  const size_t gath_bytes = align256((size_t)B * G * (N - 1) * G * 4);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Scratch sc;
+  int dev = 0;
+  int rc = get_scratch(st, 0, rowstat_bytes + 2 * gath_bytes, &sc, &dev);
+  if (rc != SV_OK) return rc;
+  char* base = static_cast<char*>(sc.base);
+  sv::md::Params p{};
+  p.target = target;
+  p.draft = draft;
+  p.tokens = draft_tokens;
+  p.uniforms = uniforms;
+  p.B = B;
+  p.V = V;
+  p.G = G;
+  p.N = N;
+  p.c = c;
+  p.rowstat = reinterpret_cast<float2*>(base + data_offset(sc));
+  p.gp = reinterpret_cast<float*>(base + data_offset(sc) + rowstat_bytes);
+  p.gq = reinterpret_cast<float*>(base + data_offset(sc) + rowstat_bytes + gath_bytes);
+  p.ctl = reinterpret_cast<uint32_t*>(base);
+  p.out_tokens = out_tokens;
+  p.out_accept_len = out_accept_len;
+  p.out_best = out_best_cand;
+  p.out_row_lse = out_row_lse;
+  if (sv::md::launch(p, dtype, st) != cudaSuccess) return SV_ERR_CUDA;
   g_launches.fetch_add(2);
   return SV_OK;
 }

@@ -129,3 +129,30 @@ def compare_lookahead(d: dict, temperature: float, gpu=None, max_mismatch: int |
         assert diff.sum() <= max_mismatch, int(diff.sum())
     return {"sequences": len(ra), "mismatch": int(diff.sum()), "near_ties": int(near.sum()),
             "accept_hist": np.bincount(ra[ra >= 0], minlength=d["cand"].shape[2] + 1).tolist()}
+
+
+def run_multidraft(d: dict, temperature: float, row_lse: bool = False):
+    res = svpkg.verify_multidraft_sample(to_dev(d["target"]), to_dev(d["draft"]), to_dev(d["draft_tokens"]),
+                                         to_dev(d["uniforms"]), temperature, best=True, row_lse=row_lse)
+    torch.cuda.synchronize()
+    return tuple(r.cpu().numpy() for r in res)
+
+
+def compare_multidraft(d: dict, temperature: float, gpu=None, max_mismatch: int | None = 0):
+    """Multi-draft sampling verify against the oracle, with the same near-tie
+    rule as compare_lookahead."""
+    if gpu is None:
+        gpu = run_multidraft(d, temperature)
+    gt, ga, gb = gpu[0], gpu[1], gpu[2]
+    rt, ra, rb, margin = oracle.verify_multidraft_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"],
+                                                         temperature)
+    diff = (ga != ra) | (gb != rb) | (gt != rt).any(1)
+    near = margin < NEAR_TIE
+    bad = diff & ~near
+    i = int(np.argmax(bad))
+    assert not bad.any(), (
+        f"{int(bad.sum())} sequences differ from the oracle away from a near-tie; first: b={i} "
+        f"gpu {gt[i]} / {ga[i]} / {gb[i]} oracle {rt[i]} / {ra[i]} / {rb[i]} margin {margin[i]}")
+    if max_mismatch is not None:
+        assert diff.sum() <= max_mismatch, int(diff.sum())
+    return {"sequences": len(ra), "mismatch": int(diff.sum()), "near_ties": int(near.sum())}

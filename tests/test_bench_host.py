@@ -14,11 +14,14 @@ import specgen as sg
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-@pytest.mark.parametrize("name", list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS))
+@pytest.mark.parametrize("name", list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS))
 def test_algorithmic_bytes_are_one_read_of_every_logit(name):
     cfg, mode, positions, logit_bytes, small_in, out_bytes = bench.workload(name)
     s = 2 if cfg.dtype == sg.BF16 else 4
-    if mode == "sample":
+    if mode == "multidraft":
+        assert positions == cfg.B * cfg.G * cfg.N
+        assert logit_bytes == cfg.B * cfg.G * (2 * cfg.N - 1) * cfg.V * s
+    elif mode == "sample":
         assert positions == cfg.B * (cfg.K + 1)
         assert logit_bytes == cfg.B * (2 * cfg.K + 1) * cfg.V * s
         assert out_bytes == cfg.B * (cfg.K + 1) * 4 + cfg.B * 4
@@ -26,7 +29,8 @@ def test_algorithmic_bytes_are_one_read_of_every_logit(name):
         assert positions == cfg.B * cfg.G * cfg.N
         assert logit_bytes == cfg.B * cfg.G * cfg.N * cfg.V * s
         assert out_bytes == cfg.B * cfg.N * 4 + cfg.B * 4
-    assert mode == {"cfg4_greedy_v32000_bf16": "greedy", "la_sample_v32000_bf16": "lookahead"}.get(name, "sample")
+    assert mode == {"cfg4_greedy_v32000_bf16": "greedy", "la_sample_v32000_bf16": "lookahead",
+                    "md_sample_v32000_bf16": "multidraft"}.get(name, "sample")
     c = bench.config_json(cfg, mode, 3)
     assert c["workload"] == name and c["B"] == cfg.B and c["V"] == cfg.V
 

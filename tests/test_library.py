@@ -88,6 +88,15 @@ def test_host_argument_checks(lib):
     assert la(p, p, None, 4, 7, 5, 100, 1, 1.0, p, p, None, None, None) == -1  # no uniforms
     assert la(q, p, p, 4, 7, 5, 100, 1, 1.0, p, p, None, None, None) == -2    # misaligned bf16 logits
     assert la(None, None, None, 0, 7, 5, 100, 1, 1.0, None, None, None, None, None) == 0
+    md = lib.sv_verify_multidraft_sample
+    assert md(p, p, p, p, 4, 7, 5, 100, 9, 1.0, p, p, None, None, None) == -2
+    assert md(p, p, p, p, 4, 33, 2, 100, 1, 1.0, p, p, None, None, None) == -1   # G > 32
+    assert md(p, p, p, p, 4, 16, 10, 100, 1, 1.0, p, p, None, None, None) == -1  # G*G*(N-1) > 2048
+    assert md(p, p, p, p, 4, 7, 1, 100, 1, 1.0, p, p, None, None, None) == -1    # N < 2
+    assert md(p, p, p, p, 4, 7, 5, 100, 1, 0.0, p, p, None, None, None) == -1    # T = 0
+    assert md(p, None, p, p, 4, 7, 5, 100, 1, 1.0, p, p, None, None, None) == -1  # no draft
+    assert md(p, q, p, p, 4, 7, 5, 100, 1, 1.0, p, p, None, None, None) == -2    # misaligned draft
+    assert md(None, None, None, None, 0, 7, 5, 100, 1, 1.0, None, None, None, None, None) == 0
     assert lib.sv_set_launch_shape(7, 1) == -1
     assert lib.sv_set_launch_shape(0, 0) == 0
     # the wait self-test checks its limit before touching the device
