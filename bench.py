@@ -304,6 +304,7 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     svpkg.build()
+    svpkg.set_greedy_path(args.greedy_path)
     cfg, mode, positions, logit_bytes, small_in, out_bytes = workload(name, args.batch)
     rotation = 1 if logit_bytes > L2_BYTES else int(math.ceil(3 * L2_BYTES / logit_bytes)) + 1
     if args.l2_resident:
@@ -427,7 +428,8 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
                      "traffic": profiled_traffic(name), "algorithmic_bytes_per_launch": logit_bytes,
-                     "kernel": kernel_for(cfg, mode),
+                     "kernel": ("gr_rows_kernel" if mode == "greedy" and args.greedy_path == 1
+                                else kernel_for(cfg, mode)),
                      "timing": "CUDA events over graph replays of the timed calls"},
         "clocks": clk.summary(),
         "e2e": {"value": positions * world / e2e_s, "unit": "positions/s", "h2d_bytes_per_step": h2d,
@@ -512,6 +514,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (--batch 1: per-call latency of one sequence)")
+    ap.add_argument("--greedy-path", type=int, default=0, choices=[0, 1],
+                    help="greedy verify kernels: 0 the streaming kernel, 1 row argmax + match kernels")
     ap.add_argument("--l2-resident", action="store_true",
                     help="replay one input set, so that inputs that fit stay in L2 (reported as such; not an "
                          "HBM figure)")

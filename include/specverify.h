@@ -259,6 +259,11 @@ int sv_set_launch_shape(int32_t stages, int32_t ctas_per_sm);
 /* How many kernel launches the library has enqueued since it was loaded. */
 uint64_t sv_launch_count(void);
 
+/* Which kernels sv_verify_greedy uses, for comparing them: 0 (default) the
+ * streaming kernel; 1 one CTA per row for the argmax, then one warp per
+ * sequence for the match. Applies to calls made after it. */
+int sv_set_greedy_path(int32_t path);
+
 #ifdef __cplusplus
 }
 #endif

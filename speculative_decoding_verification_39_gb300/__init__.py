@@ -26,8 +26,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _SO = os.path.join(_HERE, "libspecverify.so")
-_SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_noalloc.cu", "sv_lookahead.cu", "sv_multidraft.cu"]
-_DEPS = _SOURCES + ["sv_kernels.h", "sv_device.cuh", "sv_lookahead.h", "sv_multidraft.h", "sv_rowstat.cuh"]
+_SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_noalloc.cu", "sv_lookahead.cu", "sv_multidraft.cu",
+            "sv_greedy_rows.cu"]
+_DEPS = _SOURCES + ["sv_kernels.h", "sv_device.cuh", "sv_lookahead.h", "sv_multidraft.h", "sv_rowstat.cuh",
+                    "sv_greedy_rows.h"]
 
 SV_F32, SV_BF16 = 0, 1
 STATUS = {0: "SV_OK", -1: "SV_ERR_ARG", -2: "SV_ERR_DTYPE", -3: "SV_ERR_CUDA", -4: "SV_ERR_INPUT",
@@ -116,6 +118,8 @@ def lib():
         h.sv_verify_lookahead_sample.restype = ctypes.c_int
         h.sv_verify_multidraft_sample.argtypes = [vp, vp, vp, vp, i64, i32, i32, i64, i32, f32, vp, vp, vp, vp, vp]
         h.sv_verify_multidraft_sample.restype = ctypes.c_int
+        h.sv_set_greedy_path.argtypes = [i32]
+        h.sv_set_greedy_path.restype = ctypes.c_int
         _lib_handle = h
     return _lib_handle
 
@@ -123,7 +127,7 @@ def lib():
 def exported_symbols() -> list:
     return ["sv_verify_sample", "sv_verify_greedy", "sv_get_status", "sv_status_string", "sv_release",
             "sv_set_launch_shape", "sv_launch_count", "sv_verify_sample_noalloc", "sv_selftest_wait_timeout",
-            "sv_verify_lookahead_sample", "sv_verify_multidraft_sample"]
+            "sv_verify_lookahead_sample", "sv_verify_multidraft_sample", "sv_set_greedy_path"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -347,6 +351,13 @@ def set_launch_shape(stages: int = 0, ctas_per_sm: int = 0) -> None:
     rc = lib().sv_set_launch_shape(stages, ctas_per_sm)
     if rc != 0:
         raise SpecVerifyError(rc, "sv_set_launch_shape")
+
+
+def set_greedy_path(path: int) -> None:
+    """0: the streaming kernel (default); 1: row argmax then match kernels."""
+    rc = lib().sv_set_greedy_path(int(path))
+    if rc != 0:
+        raise SpecVerifyError(rc, "sv_set_greedy_path")
 
 
 def launch_count() -> int:

@@ -11,6 +11,7 @@
 
 #include "../../include/specverify.h"
 #include "sv_kernels.h"
+#include "sv_greedy_rows.h"
 #include "sv_lookahead.h"
 #include "sv_multidraft.h"
 
@@ -23,6 +24,7 @@ constexpr int64_t kMaxV = (int64_t)1 << 31;
 std::atomic<int> g_stages{kDefaultStages};
 std::atomic<int> g_ctas_per_sm{kDefaultCtasPerSm};
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_greedy_path{0};  // 0: the streaming kernel; 1: row argmax + match kernels
 
 // A scratch area has three parts at fixed places: the control block, a
 // counter region and a data region. Every counter is back at zero when a call
@@ -219,6 +221,29 @@ extern "C" int sv_verify_greedy(const void* logits, const int32_t* cand, int64_t
   if (!aligned_to(cand, 4) || !aligned_to(out_tokens, 4) || !aligned_to(out_accept_len, 4) ||
       (out_best_cand && !aligned_to(out_best_cand, 4)))
     return SV_ERR_ARG;
+  if (g_greedy_path.load() == 1 && B * (int64_t)G * N < kMaxV) {
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    Scratch sc;
+    int dev = 0;
+    const int rc = get_scratch(st, 0, (size_t)B * G * N * 4, &sc, &dev);
+    if (rc != SV_OK) return rc;
+    char* base = static_cast<char*>(sc.base);
+    sv::gr::Params q{};
+    q.logits = logits;
+    q.cand = cand;
+    q.B = B;
+    q.V = V;
+    q.G = G;
+    q.N = N;
+    q.am = reinterpret_cast<int32_t*>(base + data_offset(sc));
+    q.ctl = reinterpret_cast<uint32_t*>(base);
+    q.out_tokens = out_tokens;
+    q.out_accept_len = out_accept_len;
+    q.out_best = out_best_cand;
+    if (sv::gr::launch(q, dtype, st) != cudaSuccess) return SV_ERR_CUDA;
+    g_launches.fetch_add(2);
+    return SV_OK;
+  }
   sv::Params p{};
   p.a = static_cast<const char*>(logits);
   p.d = p.a;
@@ -414,3 +439,9 @@ extern "C" int sv_set_launch_shape(int32_t stages, int32_t ctas_per_sm) {
 }
 
 extern "C" uint64_t sv_launch_count(void) { return g_launches.load(); }
+
+extern "C" int sv_set_greedy_path(int32_t path) {
+  if (path < 0 || path > 1) return SV_ERR_ARG;
+  g_greedy_path.store(path);
+  return SV_OK;
+}

@@ -301,3 +301,20 @@ def test_near_tie_mismatch_rate_target():
     """The target bar: mismatches at or below 1e-4 of decisions."""
     totals = _TOTALS or _mismatch_totals()
     assert totals["mismatch"] <= max(1, 1e-4 * totals["decisions"]), totals
+
+
+@pytest.mark.parametrize("path", [0, 1])
+def test_greedy_paths_agree(path):
+    # the streaming kernel and the row-argmax + match kernels, bit-exact
+    svpkg.set_greedy_path(path)
+    try:
+        for cfg in (C["cfg4_greedy_v32000_bf16"], C["cfg4_greedy_v32000_bf16"].with_(B=9, V=1001, dtype=sg.F32),
+                    C["cfg4_greedy_v32000_bf16"].with_(B=5, G=40, N=3, V=333)):
+            compare_greedy(sg.greedy_inputs(cfg))
+        g = sg.greedy_inputs(C["cfg4_greedy_v32000_bf16"].with_(B=3, V=500))
+        g["cand"][1, 2, 1] = 500
+        g["logits"][2, 0, 0, 3] = 0x7FC0
+        compare_greedy(g)
+        assert svpkg.get_status() == -4
+    finally:
+        svpkg.set_greedy_path(0)

@@ -97,6 +97,7 @@ def test_host_argument_checks(lib):
     assert md(p, None, p, p, 4, 7, 5, 100, 1, 1.0, p, p, None, None, None) == -1  # no draft
     assert md(p, q, p, p, 4, 7, 5, 100, 1, 1.0, p, p, None, None, None) == -2    # misaligned draft
     assert md(None, None, None, None, 0, 7, 5, 100, 1, 1.0, None, None, None, None, None) == 0
+    assert lib.sv_set_greedy_path(2) == -1 and lib.sv_set_greedy_path(-1) == -1
     assert lib.sv_set_launch_shape(7, 1) == -1
     assert lib.sv_set_launch_shape(0, 0) == 0
     # the wait self-test checks its limit before touching the device
