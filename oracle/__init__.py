@@ -52,6 +52,10 @@ def _bind(lib):
     lib.oracle_verify_sample_lmhead.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp, i64, i32, i64, i64, f32, f32,
                                                 vp, vp, vp]
     lib.oracle_verify_sample_lmhead.restype = ctypes.c_int
+    lib.oracle_inverse_cdf.argtypes = [vp, i64, ctypes.c_double, vp]
+    lib.oracle_inverse_cdf.restype = ctypes.c_int
+    lib.oracle_residual_draw.argtypes = [vp, vp, i64, ctypes.c_double, vp]
+    lib.oracle_residual_draw.restype = ctypes.c_int
     return lib
 
 
@@ -199,3 +203,25 @@ def verify_sample_lmhead(h_target, h_draft, w_target, w_draft, draft_tokens, uni
     if rc != 0:
         raise ValueError("oracle_verify_sample_lmhead: argument error")
     return out, acc, margin
+
+
+def inverse_cdf(w, u: float, lib=None) -> int:
+    """The oracle's inverse-CDF draw from unnormalised weights (test-only entry)."""
+    lib = lib or _lib()
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    out = np.zeros(1, dtype=np.int64)
+    if lib.oracle_inverse_cdf(_p(w), w.size, float(u), _p(out)) != 0:
+        raise ValueError("oracle_inverse_cdf: argument error")
+    return int(out[0])
+
+
+def residual_draw(p, q, u: float, lib=None) -> int:
+    """The oracle's draw after a rejection: max(0, p - q), or p if that is all zero."""
+    lib = lib or _lib()
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    q = np.ascontiguousarray(q, dtype=np.float64)
+    assert p.shape == q.shape
+    out = np.zeros(1, dtype=np.int64)
+    if lib.oracle_residual_draw(_p(p), _p(q), p.size, float(u), _p(out)) != 0:
+        raise ValueError("oracle_residual_draw: argument error")
+    return int(out[0])

@@ -148,6 +148,19 @@ static int64_t inverse_cdf(const double* w, int64_t V, double u, double* margin)
   return V - 1;
 }
 
+/* The draw after a rejection ([P1] §2.1-2.2): from norm(max(0, p - q)); if
+ * that residual is all zero, from p itself ([P1] §4 fallback). w is V doubles
+ * of scratch. */
+static int64_t residual_draw(const double* p, const double* q, double* w, int64_t V, double u, double* margin) {
+  double Z = 0.0;
+  for (int64_t v = 0; v < V; ++v) {
+    const double d = p[v] - q[v];
+    w[v] = d > 0.0 ? d : 0.0;
+    Z += w[v];
+  }
+  return inverse_cdf(Z > 0.0 ? w : p, V, u, margin);
+}
+
 /* Argmax with the lowest index among equal maxima (numeric order, so -0 and
  * +0 tie). */
 static int64_t argmax_lowest(const double* l, int64_t V) {
@@ -258,12 +271,7 @@ int oracle_verify_sample(const void* target, const void* draft, int dtype, const
       }
       /* Rejected at i: draw from norm(max(0, p - q)) ([P1] §2.1-2.2); if that
        * residual is all zero, draw from p instead ([P1] §4). */
-      double Z = 0.0;
-      for (int64_t v = 0; v < V; ++v) {
-        w[v] = fmax(0.0, p[v] - q[v]);
-        Z += w[v];
-      }
-      out[i] = (int32_t)inverse_cdf(Z > 0.0 ? w : p, V, (double)u[K], &margin);
+      out[i] = (int32_t)residual_draw(p, q, w, V, (double)u[K], &margin);
       j = i;
       break;
     }
@@ -594,4 +602,21 @@ int oracle_verify_sample_lmhead(const void* h_target, const void* h_draft, const
   free(lt);
   free(ld);
   return rc;
+}
+
+/* ------------------------------------------------- test-only entry points */
+
+int oracle_inverse_cdf(const double* w, int64_t V, double u, int64_t* out_token) {
+  if (!w || !out_token || V < 1) return -1;
+  *out_token = inverse_cdf(w, V, u, NULL);
+  return 0;
+}
+
+int oracle_residual_draw(const double* p, const double* q, int64_t V, double u, int64_t* out_token) {
+  if (!p || !q || !out_token || V < 1) return -1;
+  double* w = (double*)malloc(sizeof(double) * (size_t)V);
+  if (!w) return -1;
+  *out_token = residual_draw(p, q, w, V, u, NULL);
+  free(w);
+  return 0;
 }

@@ -118,6 +118,16 @@ int oracle_verify_sample_lmhead(const void* h_target, const void* h_draft, const
                                 int64_t D, int64_t V, float temperature, float top_p, int32_t* out_tokens,
                                 int32_t* out_accept_len, double* out_margin);
 
+/* Test-only entry points to the draw's two edge rules, so that tests can pin
+ * them directly (valid verify inputs do not reach them in exact arithmetic).
+ * oracle_inverse_cdf: the inverse-CDF draw from unnormalised weights w[V]:
+ *   the smallest t with sum_{v<=t} w_v > u * sum_v w_v; if u * Z is at or past
+ *   the last partial sum, the largest t with w_t > 0.
+ * oracle_residual_draw: the draw after a rejection, from max(0, p - q), or
+ *   from p when that residual is all zero ([P1] §4). */
+int oracle_inverse_cdf(const double* w, int64_t V, double u, int64_t* out_token);
+int oracle_residual_draw(const double* p, const double* q, int64_t V, double u, int64_t* out_token);
+
 #ifdef __cplusplus
 }
 #endif

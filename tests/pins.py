@@ -164,6 +164,36 @@ def check_brute_force(lib, K=2, n=16):
     assert abs(sum(mass.values()) - 1.0) < 1e-9
 
 
+def check_draw_edge_rules(lib):
+    """The draw's two edge rules, on hand-made weights (readings c5 and c7).
+
+    c5 ("Speculative Decoding" §2.1 inverse CDF, ascending vocabulary order,
+    strict comparison): the smallest t with C_t > u*Z; when u*Z is at or past
+    the last partial sum (here u = 1, which a valid uniform never is), the
+    largest t with positive weight. c7 ("Speculative Decoding" §4, the
+    fallback when the residual sums to zero): with p <= q everywhere the
+    residual max(0, p - q) is all zero and the token is drawn from p itself.
+    Expected tokens are worked out by hand in the comments."""
+    w = np.array([0.5, 0.25, 0.25, 0.0, 0.0])
+    # u*Z = 0.5: C_0 = 0.5 is not > 0.5, C_1 = 0.75 is -> token 1
+    assert oracle.inverse_cdf(w, 0.5, lib) == 1
+    # u = 0: the first token with positive weight
+    assert oracle.inverse_cdf(np.array([0.0, 0.0, 1.0, 0.0]), 0.0, lib) == 2
+    # u*Z = Z: no partial sum exceeds it -> the largest t with w_t > 0 (2, not V-1)
+    assert oracle.inverse_cdf(w, 1.0, lib) == 2
+    assert oracle.inverse_cdf(np.array([0.0, 0.0, 1.0, 0.0]), 1.0, lib) == 2
+    # residual max(0, p - q) = [0, 0.4, 0]: every u draws token 1
+    p, q = np.array([0.1, 0.6, 0.3]), np.array([0.4, 0.2, 0.4])
+    for u in (0.0, 0.3, 0.99):
+        assert oracle.residual_draw(p, q, u, lib) == 1
+    # p <= q everywhere: the residual is zero, the draw is from p: u*Z = 0.5 < C_0 = 0.6 -> 0
+    # (from q it would be 0.9 -> 1; from max(0, q - p) = [0, .4, .4] it would be 2)
+    p, q = np.array([0.6, 0.2, 0.2]), np.array([0.6, 0.6, 0.6])
+    assert oracle.residual_draw(p, q, 0.5, lib) == 0
+    # from p, u*Z = 0.85: C = 0.6, 0.8, 1.0 -> 2
+    assert oracle.residual_draw(p, q, 0.85, lib) == 2
+
+
 def load_topp_golden():
     cases = []
     for line in open(os.path.join(GOLDEN, "topp_ties.txt")):

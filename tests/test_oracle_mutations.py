@@ -7,7 +7,8 @@ import tempfile
 import pytest
 
 import oracle
-from pins import (check_acceptance_is_one_minus_tv, check_brute_force, check_greedy_golden,
+from pins import (check_acceptance_is_one_minus_tv, check_brute_force, check_draw_edge_rules,
+                  check_greedy_golden,
                   check_lmhead_integer_products, check_lookahead_exact, check_lookahead_golden,
                   check_multidraft_golden,
                   check_multidraft_marginal, check_output_is_target_distribution, check_tokens_per_round)
@@ -16,8 +17,18 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
 MUTATIONS = {
     # the residual is max(0, p - q), not max(0, q - p)
-    "residual_sign": ("w[v] = fmax(0.0, p[v] - q[v]);", "w[v] = fmax(0.0, q[v] - p[v]);",
+    "residual_sign": ("const double d = p[v] - q[v];", "const double d = q[v] - p[v];",
                       lambda lib: check_brute_force(lib, K=2)),
+    # a residual that sums to zero falls back to p, not to q
+    "zero_residual_from_q": ("return inverse_cdf(Z > 0.0 ? w : p, V, u, margin);",
+                             "return inverse_cdf(Z > 0.0 ? w : q, V, u, margin);", check_draw_edge_rules),
+    # past the last partial sum: the largest t with positive weight, not V - 1
+    "past_end_last_index": ("    if (w[t] > 0.0) return t;\n  return V - 1;", "  return V - 1;",
+                            check_draw_edge_rules),
+    # ... and not the first positive one
+    "past_end_first_positive": ("for (int64_t t = V - 1; t >= 0; --t)\n    if (w[t] > 0.0) return t;",
+                                "for (int64_t t = 0; t < V; ++t)\n    if (w[t] > 0.0) return t;",
+                                check_draw_edge_rules),
     # alpha = min(1, p/q), not min(1, q/p)
     "ratio_inverted": ("alpha = fmin(1.0, px / qx);", "alpha = fmin(1.0, qx / px);",
                        check_acceptance_is_one_minus_tv),
@@ -135,7 +146,8 @@ def test_pin_rejects_planted_mistake(name, tmpdir_mod):
     old, new, check = MUTATIONS[name]
     src = open(SRC).read()
     fn = function_of(name)
-    if name in ("argmax_highest_index", "no_renormalise"):  # helpers (argmax, inverse CDF) shared by the modes
+    if name in ("argmax_highest_index", "no_renormalise", "residual_sign", "zero_residual_from_q",
+                "past_end_last_index", "past_end_first_positive"):  # helpers shared by the modes
         a, b = 0, len(src)
     else:
         a, b = function_span(src, fn)

@@ -7,7 +7,8 @@ import pytest
 import oracle
 import specgen as sg
 
-from pins import (LD, LT, check_acceptance_is_one_minus_tv, check_brute_force, check_greedy_golden,
+from pins import (LD, LT, check_acceptance_is_one_minus_tv, check_brute_force, check_draw_edge_rules,
+                  check_greedy_golden,
                   check_greedy_multi_draft, check_output_is_target_distribution, check_tokens_per_round,
                   check_topp_golden, multi_draft_expected_tokens, nucleus_bruteforce, replicate, softmax)
 
@@ -34,6 +35,10 @@ def test_tokens_per_round(lib, K):
 @pytest.mark.parametrize("K", [1, 2])
 def test_brute_force_joint_mass(lib, K):
     check_brute_force(lib, K=K)
+
+
+def test_draw_edge_rules(lib):
+    check_draw_edge_rules(lib)
 
 
 def test_topp_golden(lib):
