@@ -52,6 +52,14 @@ def _bind(lib):
     lib.oracle_verify_sample_lmhead.argtypes = [vp, vp, vp, vp, ctypes.c_int, vp, vp, i64, i32, i64, i64, f32, f32,
                                                 vp, vp, vp]
     lib.oracle_verify_sample_lmhead.restype = ctypes.c_int
+    lib.oracle_ngram_pool_create.argtypes = [i64, i64, i32, i32]
+    lib.oracle_ngram_pool_create.restype = vp
+    lib.oracle_ngram_pool_destroy.argtypes = [vp]
+    lib.oracle_ngram_pool_destroy.restype = None
+    lib.oracle_ngram_pool_insert.argtypes = [vp, vp, i32]
+    lib.oracle_ngram_pool_insert.restype = ctypes.c_int
+    lib.oracle_ngram_pool_lookup.argtypes = [vp, vp, i32, vp, vp]
+    lib.oracle_ngram_pool_lookup.restype = ctypes.c_int
     lib.oracle_inverse_cdf.argtypes = [vp, i64, ctypes.c_double, vp]
     lib.oracle_inverse_cdf.restype = ctypes.c_int
     lib.oracle_residual_draw.argtypes = [vp, vp, i64, ctypes.c_double, vp]
@@ -225,3 +233,36 @@ def residual_draw(p, q, u: float, lib=None) -> int:
     if lib.oracle_residual_draw(_p(p), _p(q), p.size, float(u), _p(out)) != 0:
         raise ValueError("oracle_residual_draw: argument error")
     return int(out[0])
+
+
+class NgramPool:
+    """The oracle's n-gram pool (one per sequence, keyed by first token)."""
+
+    def __init__(self, B: int, V: int, N: int, cap: int, lib=None):
+        self.lib = lib or _lib()
+        self.B, self.V, self.N, self.cap = B, V, N, cap
+        self.h = self.lib.oracle_ngram_pool_create(B, V, N, cap)
+        if not self.h:
+            raise ValueError("oracle_ngram_pool_create: argument error")
+
+    def insert(self, ngrams):
+        g = np.ascontiguousarray(ngrams, dtype=np.int32)
+        assert g.ndim == 3 and g.shape[0] == self.B and g.shape[2] == self.N
+        if self.lib.oracle_ngram_pool_insert(self.h, _p(g), g.shape[1]) != 0:
+            raise ValueError("oracle_ngram_pool_insert: argument error")
+
+    def lookup(self, last, G: int):
+        last = np.ascontiguousarray(last, dtype=np.int32)
+        cand = np.empty((self.B, G, self.N - 1), dtype=np.int32)
+        count = np.empty(self.B, dtype=np.int32)
+        if self.lib.oracle_ngram_pool_lookup(self.h, _p(last), G, _p(cand), _p(count)) != 0:
+            raise ValueError("oracle_ngram_pool_lookup: argument error")
+        return cand, count
+
+    def close(self):
+        if self.h:
+            self.lib.oracle_ngram_pool_destroy(self.h)
+            self.h = None
+
+    def __del__(self):
+        self.close()

@@ -9,6 +9,7 @@
 #include "oracle.h"
 
 #include <math.h>
+#include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -618,5 +619,140 @@ int oracle_residual_draw(const double* p, const double* q, int64_t V, double u, 
   if (!w) return -1;
   *out_token = residual_draw(p, q, w, V, u, NULL);
   free(w);
+  return 0;
+}
+
+/* ------------------------------------------------------------ n-gram pool */
+/* [P4] section "N-gram 池与身份判定": a pool caches the n-grams the lookahead
+ * branch collects (W new n-grams of N tokens per step, section "Lookahead
+ * 分支:用 2D 窗口制造 n-gram"); only n-grams whose first token equals the
+ * last generated token are verified, at most G of them (the "GUESS_SET_SIZE"
+ * of the engineering section), and n-grams that are not adopted stay in the
+ * pool. The page leaves open how much the pool holds and what it drops; the
+ * readings taken: each sequence has its own pool; each first token keeps at
+ * most `cap` n-grams; the n-grams of a step are inserted in order; an n-gram
+ * already held is not inserted again and keeps its place; inserting into a
+ * full key drops that key's oldest n-gram; the candidates are the newest
+ * first; an n-gram holding a token outside [0, V) is ignored. The pool here is
+ * a plain list per sequence, searched linearly. */
+
+typedef struct {
+  int32_t key;
+  int32_t* toks; /* the N-1 tokens after the first */
+  int64_t stamp; /* insertion order */
+} og_entry;
+
+typedef struct {
+  og_entry* e;
+  int64_t n, cap_alloc;
+} og_list;
+
+struct oracle_ngram_pool {
+  int64_t B, V;
+  int32_t N, cap;
+  int64_t next_stamp;
+  og_list* seq;
+};
+
+oracle_ngram_pool* oracle_ngram_pool_create(int64_t B, int64_t V, int32_t N, int32_t cap) {
+  if (B < 0 || V < 1 || N < 2 || cap < 1) return NULL;
+  oracle_ngram_pool* p = (oracle_ngram_pool*)calloc(1, sizeof(oracle_ngram_pool));
+  if (!p) return NULL;
+  p->B = B;
+  p->V = V;
+  p->N = N;
+  p->cap = cap;
+  p->seq = (og_list*)calloc((size_t)(B > 0 ? B : 1), sizeof(og_list));
+  return p;
+}
+
+void oracle_ngram_pool_destroy(oracle_ngram_pool* p) {
+  if (!p) return;
+  for (int64_t b = 0; b < p->B; ++b) {
+    for (int64_t i = 0; i < p->seq[b].n; ++i) free(p->seq[b].e[i].toks);
+    free(p->seq[b].e);
+  }
+  free(p->seq);
+  free(p);
+}
+
+/* Removes entry i of list l. */
+static void og_remove(og_list* l, int64_t i) {
+  free(l->e[i].toks);
+  for (int64_t k = i + 1; k < l->n; ++k) l->e[k - 1] = l->e[k];
+  l->n -= 1;
+}
+
+int oracle_ngram_pool_insert(oracle_ngram_pool* p, const int32_t* ngrams, int32_t W) {
+  if (!p || (W > 0 && !ngrams) || W < 0) return -1;
+  const int32_t N = p->N;
+  for (int64_t b = 0; b < p->B; ++b) {
+    og_list* l = &p->seq[b];
+    for (int32_t w = 0; w < W; ++w) {
+      const int32_t* g = ngrams + (b * W + w) * N;
+      int ok = 1;
+      for (int32_t t = 0; t < N; ++t)
+        if (g[t] < 0 || (int64_t)g[t] >= p->V) ok = 0;
+      if (!ok) continue; /* a token outside [0, V): ignored */
+      /* already held under its first token? */
+      int dup = 0;
+      int64_t held = 0, oldest = -1;
+      for (int64_t i = 0; i < l->n; ++i) {
+        if (l->e[i].key != g[0]) continue;
+        held += 1;
+        if (oldest < 0 || l->e[i].stamp < l->e[oldest].stamp) oldest = i;
+        if (memcmp(l->e[i].toks, g + 1, sizeof(int32_t) * (size_t)(N - 1)) == 0) dup = 1;
+      }
+      if (dup) continue;
+      if (held >= p->cap) og_remove(l, oldest); /* a full key drops its oldest n-gram */
+      if (l->n == l->cap_alloc) {
+        int64_t nc = l->cap_alloc ? 2 * l->cap_alloc : 16;
+        og_entry* ne = (og_entry*)realloc(l->e, sizeof(og_entry) * (size_t)nc);
+        if (!ne) return -1;
+        l->e = ne;
+        l->cap_alloc = nc;
+      }
+      og_entry* e = &l->e[l->n++];
+      e->key = g[0];
+      e->toks = (int32_t*)malloc(sizeof(int32_t) * (size_t)(N - 1));
+      memcpy(e->toks, g + 1, sizeof(int32_t) * (size_t)(N - 1));
+      e->stamp = p->next_stamp++;
+    }
+  }
+  return 0;
+}
+
+int oracle_ngram_pool_lookup(const oracle_ngram_pool* p, const int32_t* last, int32_t G, int32_t* cand,
+                             int32_t* count) {
+  if (!p || !last || !cand || !count || G < 1) return -1;
+  const int32_t N = p->N;
+  for (int64_t b = 0; b < p->B; ++b) {
+    int32_t* out = cand + b * (int64_t)G * (N - 1);
+    const int32_t key = last[b];
+    if (key < 0 || (int64_t)key >= p->V) {
+      for (int64_t k = 0; k < (int64_t)G * (N - 1); ++k) out[k] = -1;
+      count[b] = -1;
+      continue;
+    }
+    /* the first-token filter, newest first: repeatedly take the unused entry
+     * with the largest stamp */
+    const og_list* l = &p->seq[b];
+    int64_t prev = INT64_MAX;
+    int32_t c = 0;
+    while (c < G) {
+      int64_t best = -1;
+      for (int64_t i = 0; i < l->n; ++i)
+        if (l->e[i].key == key && l->e[i].stamp < prev && (best < 0 || l->e[i].stamp > l->e[best].stamp)) best = i;
+      if (best < 0) break;
+      memcpy(out + (int64_t)c * (N - 1), l->e[best].toks, sizeof(int32_t) * (size_t)(N - 1));
+      prev = l->e[best].stamp;
+      c += 1;
+    }
+    count[b] = c;
+    /* unused slots: a copy of the newest candidate, or, with none, the last
+     * token repeated (any guess keeps the greedy verify exact) */
+    for (int32_t g = c; g < G; ++g)
+      for (int32_t t = 0; t < N - 1; ++t) out[(int64_t)g * (N - 1) + t] = c > 0 ? out[t] : key;
+  }
   return 0;
 }

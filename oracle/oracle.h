@@ -118,6 +118,25 @@ int oracle_verify_sample_lmhead(const void* h_target, const void* h_draft, const
                                 int64_t D, int64_t V, float temperature, float top_p, int32_t* out_tokens,
                                 int32_t* out_accept_len, double* out_margin);
 
+/* N-gram pool ([P4] section "N-gram 池与身份判定"): one pool per sequence,
+ * keyed by an n-gram's first token, each key holding at most `cap` n-grams
+ * of N tokens.
+ *   create/destroy: an empty pool for B sequences over a vocabulary of V.
+ *   insert: ngrams [B, W, N]; sequence b's W n-grams go into its pool in
+ *     order. An n-gram already held is not inserted again; a full key drops
+ *     its oldest n-gram; an n-gram with a token outside [0, V) is ignored.
+ *   lookup: for each b, the n-grams whose first token equals last[b], newest
+ *     first, at most G: cand [B, G, N-1] holds their tokens after the first,
+ *     count [B] how many there are. Unused slots hold a copy of the newest
+ *     candidate, or last[b] repeated when there is none. A last token outside
+ *     [0, V) gives count -1 and -1 tokens. The pool is not changed. */
+typedef struct oracle_ngram_pool oracle_ngram_pool;
+oracle_ngram_pool* oracle_ngram_pool_create(int64_t B, int64_t V, int32_t N, int32_t cap);
+void oracle_ngram_pool_destroy(oracle_ngram_pool* p);
+int oracle_ngram_pool_insert(oracle_ngram_pool* p, const int32_t* ngrams, int32_t W);
+int oracle_ngram_pool_lookup(const oracle_ngram_pool* p, const int32_t* last, int32_t G, int32_t* cand,
+                             int32_t* count);
+
 /* Test-only entry points to the draw's two edge rules, so that tests can pin
  * them directly (valid verify inputs do not reach them in exact arithmetic).
  * oracle_inverse_cdf: the inverse-CDF draw from unnormalised weights w[V]:

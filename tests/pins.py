@@ -590,3 +590,79 @@ def check_lmhead_integer_products(lib, dtype=sg.F32, seed=42):
     assert (ra >= 0).all()
     np.testing.assert_array_equal(acc, ra)
     np.testing.assert_array_equal(out, rt)
+
+
+def load_ngram_golden():
+    """The hand-worked n-gram pool cases of tests/golden/ngram_pool_hand.txt:
+    a list of (V, N, cap, G, ops), ops ("insert", [[tokens]]) or
+    ("lookup", key, count, [[cand]])."""
+    path = os.path.join(os.path.dirname(__file__), "golden", "ngram_pool_hand.txt")
+    cases = []
+    for line in open(path):
+        line = line.split("#", 1)[0].strip()
+        if not line:
+            continue
+        word, rest = line.split(None, 1)
+        if word == "pool":
+            V, N, cap, G = (int(x) for x in rest.split())
+            cases.append((V, N, cap, G, []))
+        elif word == "insert":
+            cases[-1][4].append(("insert", [[int(x) for x in g.split()] for g in rest.split("|")]))
+        elif word == "lookup":
+            left, right = rest.split("->")
+            count, cands = right.split(":")
+            cases[-1][4].append(("lookup", int(left), int(count),
+                                 [[int(x) for x in g.split()] for g in cands.split("|")]))
+    return cases
+
+
+def check_ngram_golden(lib):
+    """Every hand-worked insert/lookup sequence gives the expected candidates."""
+    for V, N, cap, G, ops in load_ngram_golden():
+        pool = oracle.NgramPool(1, V, N, cap, lib=lib)
+        for op in ops:
+            if op[0] == "insert":
+                pool.insert(np.array([op[1]], dtype=np.int32))
+            else:
+                cand, count = pool.lookup(np.array([op[1]], dtype=np.int32), G)
+                assert count[0] == op[2], (op, count)
+                assert cand[0].tolist() == op[3], (op, cand[0].tolist())
+        pool.close()
+
+
+def check_ngram_properties(lib, seed=31, steps=60):
+    """Properties the page fixes, on random streams of several sequences:
+    every real candidate is an inserted n-gram whose first token is the key
+    (the first-token filter), at most G of them, none twice; a lookup leaves
+    the pool unchanged (n-grams that are not adopted stay); W new distinct
+    n-grams of one key, in an empty pool that holds them, all come back,
+    newest first."""
+    rng = np.random.default_rng(seed)
+    B, V, N, cap, G, W = 3, 12, 4, 3, 4, 5
+    pool = oracle.NgramPool(B, V, N, cap, lib=lib)
+    inserted = [set() for _ in range(B)]
+    for _ in range(steps):
+        g = rng.integers(0, V, size=(B, W, N)).astype(np.int32)
+        g[:, :, 0] = rng.integers(0, 3, size=(B, W))  # few keys, so keys fill and evict
+        pool.insert(g)
+        for b in range(B):
+            for w in range(W):
+                inserted[b].add(tuple(g[b, w]))
+        last = rng.integers(0, 3, size=B).astype(np.int32)
+        cand, count = pool.lookup(last, G)
+        cand2, count2 = pool.lookup(last, G)
+        assert np.array_equal(cand, cand2) and np.array_equal(count, count2)
+        for b in range(B):
+            assert 0 <= count[b] <= min(G, cap)
+            real = [tuple([int(last[b])] + cand[b, k].tolist()) for k in range(count[b])]
+            assert len(set(real)) == len(real)
+            for r in real:
+                assert r in inserted[b] and r[0] == last[b]
+    pool.close()
+    pool = oracle.NgramPool(1, 100, 3, 8, lib=lib)
+    grams = np.array([[[7, 10 + w, 20 + w] for w in range(6)]], dtype=np.int32)
+    pool.insert(grams)
+    cand, count = pool.lookup(np.array([7], dtype=np.int32), 8)
+    assert count[0] == 6
+    assert cand[0, :6].tolist() == [[10 + w, 20 + w] for w in reversed(range(6))]
+    pool.close()

@@ -11,7 +11,8 @@ from pins import (check_acceptance_is_one_minus_tv, check_brute_force, check_dra
                   check_greedy_golden,
                   check_lmhead_integer_products, check_lookahead_exact, check_lookahead_golden,
                   check_multidraft_golden,
-                  check_multidraft_marginal, check_output_is_target_distribution, check_tokens_per_round)
+                  check_multidraft_marginal, check_ngram_golden, check_ngram_properties,
+                  check_output_is_target_distribution, check_tokens_per_round)
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
 
@@ -104,6 +105,19 @@ MUTATIONS = {
     # the draft rows use the draft model's head
     "lmhead_draft_uses_target_head": ("load_logit(w_draft, dtype, v * D + d)", "load_logit(w_target, dtype, v * D + d)",
                                       check_lmhead_integer_products),
+    # n-gram pool: an n-gram already held is not inserted again
+    "ngram_no_dedup": ("if (dup) continue;", "if (0) continue;", check_ngram_golden),
+    # a full key drops its oldest n-gram, not its newest
+    "ngram_evict_newest": ("if (oldest < 0 || l->e[i].stamp < l->e[oldest].stamp) oldest = i;",
+                           "if (oldest < 0 || l->e[i].stamp > l->e[oldest].stamp) oldest = i;", check_ngram_golden),
+    # only n-grams whose first token is the last generated token are candidates
+    "ngram_no_first_token_filter": ("if (l->e[i].key == key && l->e[i].stamp < prev",
+                                    "if (l->e[i].stamp < prev", check_ngram_properties),
+    # candidates newest first
+    "ngram_oldest_first": ("(best < 0 || l->e[i].stamp > l->e[best].stamp)",
+                           "(best < 0 || l->e[i].stamp < l->e[best].stamp)", check_ngram_golden),
+    # unused slots copy the newest candidate (or repeat the key)
+    "ngram_pad_zeros": ("c > 0 ? out[t] : key;", "0;", check_ngram_golden),
     "multidraft_row_of_draft_0": ("load_row(target, dtype, (b * G + lead) * N + n, V, l);",
                                   "load_row(target, dtype, (b * G + 0) * N + n, V, l);", check_multidraft_marginal),
 }
@@ -118,7 +132,8 @@ def tmpdir_mod():
 # The oracle function each mutation is planted in; the anchor must occur
 # exactly once within that function's body.
 FUNCTIONS = ("oracle_verify_sample", "oracle_row_stats", "oracle_verify_greedy", "oracle_verify_lookahead_sample",
-             "oracle_verify_multidraft_sample", "oracle_verify_sample_lmhead")
+             "oracle_verify_multidraft_sample", "oracle_verify_sample_lmhead", "oracle_inverse_cdf",
+             "oracle_residual_draw", "oracle_ngram_pool_insert", "oracle_ngram_pool_lookup")
 
 
 def function_span(src: str, fn: str):
@@ -138,6 +153,10 @@ def function_of(name: str) -> str:
         return "oracle_verify_sample_lmhead"
     if name.startswith(("argmax_", "greedy_")):
         return "oracle_verify_greedy"
+    if name in ("ngram_no_dedup", "ngram_evict_newest"):
+        return "oracle_ngram_pool_insert"
+    if name.startswith("ngram_"):
+        return "oracle_ngram_pool_lookup"
     return "oracle_verify_sample"
 
 
