@@ -3,24 +3,30 @@
 
 One step = one verify call over one batch of the workload: every row of
 target and draft logits read once, the accept scan, and the residual or bonus
-draw. Default workload: B=64, K=5, V=32000 bf16, T=1 (the workload the
-headline metric is quoted on). Metric: verified positions per second
-(B*(K+1) target positions per call), with the achieved algorithmic HBM
-bandwidth against the measured peak.
+draw. Metric: verified positions per second (B*(K+1) target positions per
+sampling call, B*G*N per greedy call), with the achieved algorithmic HBM
+bandwidth (one read of every logit) against the measured peak.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME|all] [--impl reference]
+Headline workload: B=256, K=8, V=128256 bf16, T=0.8 — the largest of the five
+verify workloads and the largest that one GPU holds several copies of. The
+same JSON line carries a ``per_config`` record for every other workload (the
+four other verify workloads, the Lookahead sampling verify and the multi-draft
+verify), each with its own throughput, roofline, end-to-end figure, CPU
+baseline and GPU/oracle mismatch counts.
 
-NAME is one of the five verify workloads (specgen.CONFIGS) or the sampling-mode
-Lookahead verify on the greedy workload's shape (la_sample_v32000_bf16).
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME[,NAME..]|all] [--impl reference]
 
 Timing: inputs are resident in HBM before the timed region; the K timed calls
 are replayed from CUDA graphs, cycling through enough copies of the inputs
 that the working set exceeds the 129 MB L2 (so no call finds its inputs in
 L2); CUDA events on the launching stream bracket the timed replays, with a
-barrier and a device synchronise on both sides. ``e2e`` repeats the metric
-through the public API with pinned host buffers, copies included.
-``--impl reference`` times the CPU oracle (the baseline this project is
-checked against) on a bounded sample of the same workload.
+barrier and a device synchronise on both sides. That is the pipelined
+per-call time: consecutive calls on the stream may overlap their launch and
+ramp. ``isolated_us`` is the per-call time with every call followed by a
+one-element torch kernel that ends the overlap, minus that kernel's own time.
+``e2e`` repeats the metric through the public API with pinned host buffers,
+copies included. ``--impl reference`` times the CPU oracle (the baseline this
+project is checked against) on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -45,7 +51,7 @@ import specgen as sg  # noqa: E402
 
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
-DEFAULT_CONFIG = "cfg2_v32000_bf16"
+DEFAULT_CONFIG = "cfg3_v128256_bf16"
 KERNEL = "verify_kernel"
 
 
@@ -205,32 +211,58 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-KERNEL_SOURCES = ("sv_kernels.cu", "sv_device.cuh", "sv_kernels.h")
+# The sources each kernel is built from: a profiled traffic figure is only
+# reported while they are the ones that were profiled.
+KERNEL_SOURCES = {
+    "rows_kernel": ("sv_rows.cu", "sv_v2.h", "sv_device.cuh"),
+    "decide_kernel": ("sv_decide.cu", "sv_df.cuh", "sv_v2.h", "sv_device.cuh"),
+    "verify_kernel": ("sv_kernels.cu", "sv_device.cuh", "sv_kernels.h"),
+    "verify_warp_kernel": ("sv_kernels.cu", "sv_device.cuh", "sv_kernels.h"),
+    "verify_seq_kernel": ("sv_kernels.cu", "sv_device.cuh", "sv_kernels.h"),
+    "gr_rows_kernel": ("sv_greedy_rows.cu", "sv_greedy_rows.h", "sv_device.cuh"),
+    "la_rows_kernel": ("sv_lookahead.cu", "sv_lookahead.h", "sv_device.cuh"),
+    "md_rows_kernel": ("sv_multidraft.cu", "sv_multidraft.h", "sv_rowstat.cuh", "sv_device.cuh"),
+}
 
 
-def kernel_source_hash() -> str:
-    """Hash of the verify kernel's sources; a profiled traffic figure is only
-    reported while the kernel is the one that was profiled."""
+def kernel_source_hash(kernel: str = "verify_kernel") -> str:
+    """Hash of the sources of ``kernel``."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_verification_39_gb300", "csrc")
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[kernel]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload_name: str):
-    """DRAM bytes per launch from the committed ncu summary of this workload,
-    or None if there is none or the kernel sources changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"{KERNEL}_{workload_name}.md")
+def profiled_traffic(workload_name: str, kernel: str = "verify_kernel"):
+    """DRAM bytes per launch of ``kernel`` from the committed ncu summary of
+    this workload (profiles/<kernel>_<workload>.md), or None if there is none
+    or the kernel's sources changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload_name}.md")
     try:
         text = open(path).read()
     except OSError:
         return None
     m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", text)
     h = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", text)
-    if not m or not h or h.group(1) != kernel_source_hash():
+    if not m or not h or kernel not in KERNEL_SOURCES or h.group(1) != kernel_source_hash(kernel):
         return None
     return float(m.group(1))
+
+
+def launched_kernel(cfg, mode, args) -> str:
+    """The streaming kernel (the one that reads the logits) the library
+    launches for this workload, by the library's own selection rule."""
+    if mode == "greedy":
+        return "gr_rows_kernel" if args.greedy_path == 0 else "verify_kernel"
+    if mode == "lookahead":
+        return "la_rows_kernel"
+    if mode == "multidraft":
+        return "md_rows_kernel"
+    if (args.sample_path == 0 and cfg.temperature > 0 and cfg.top_p == 1.0 and cfg.K <= 1024
+            and cfg.V <= 1048576):
+        return "rows_kernel"
+    return kernel_for(cfg, mode)
 
 
 def shard_offset(rank: int, batch: int) -> int:
@@ -296,15 +328,56 @@ def oracle_cpu_rate(cfg, mode, budget_s: float, nthreads: int):
 
 # --------------------------------------------------------------- GPU arm
 
-def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
+def oracle_counts(host, cfg, mode, gpu_tokens, gpu_acc, nthreads: int):
+    """GPU/oracle comparison on one full input set: sequences whose tokens or
+    accept length differ, near-ties (the oracle's smallest decision margin
+    below 1e-6) and decisions (accept tests and draws; greedy: one per
+    sequence). The oracle runs over the sequences on host threads."""
+    import oracle
+    B = cfg.B
+    chunk = max(1, min(32, (B + nthreads - 1) // nthreads))
+    sl = [slice(i, min(B, i + chunk)) for i in range(0, B, chunk)]
+
+    def one(s):
+        if mode == "greedy":
+            t, a, _ = oracle.verify_greedy(host["logits"][s], host["cand"][s])
+            return t, a, np.full(len(a), np.inf)
+        if mode == "lookahead":
+            t, a, _, m = oracle.verify_lookahead_sample(host["logits"][s], host["cand"][s], host["uniforms"][s],
+                                                        cfg.temperature)
+            return t, a, m
+        if mode == "multidraft":
+            t, a, _, m = oracle.verify_multidraft_sample(host["target"][s], host["draft"][s],
+                                                         host["draft_tokens"][s], host["uniforms"][s],
+                                                         cfg.temperature)
+            return t, a, m
+        return oracle.verify_sample(host["target"][s], host["draft"][s], host["draft_tokens"][s],
+                                    host["uniforms"][s], cfg.temperature, cfg.top_p)
+
+    with ThreadPoolExecutor(nthreads) as ex:
+        parts = list(ex.map(one, sl))
+    rt = np.concatenate([x[0] for x in parts])
+    ra = np.concatenate([x[1] for x in parts])
+    margin = np.concatenate([x[2] for x in parts])
+    diff = (gpu_acc != ra) | (gpu_tokens != rt).any(1)
+    near = margin < 1e-6
+    if mode == "sample":
+        decisions = int(np.where(ra >= 0, np.minimum(ra + 1, cfg.K) + 1, 0).sum())
+    elif mode == "greedy":
+        decisions = int(B)
+    else:
+        decisions = int(np.where(ra >= 0, ra + 1, 0).sum())
+    return {"sequences": int(B), "decisions": decisions, "mismatch": int(diff.sum()),
+            "mismatch_away_from_near_tie": int((diff & ~near).sum()), "near_ties": int(near.sum())}
+
+
+def measure(args, name: str, rank: int, world: int, steps: int, cpu_budget: float, counts: bool):
+    """Times one workload on this rank's GPU; returns its record."""
     import torch
     import speculative_decoding_verification_39_gb300 as svpkg
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
     dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    svpkg.build()
-    svpkg.set_greedy_path(args.greedy_path)
     cfg, mode, positions, logit_bytes, small_in, out_bytes = workload(name, args.batch)
     rotation = 1 if logit_bytes > L2_BYTES else int(math.ceil(3 * L2_BYTES / logit_bytes)) + 1
     if args.l2_resident:
@@ -318,29 +391,24 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
             "multidraft": ("target", "draft", "draft_tokens", "uniforms"),
             "sample": ("target", "draft", "draft_tokens", "uniforms")}[mode]
     pinned = {k: to_torch(host[k], torch, pin=True) for k in keys}
-    sets = []
-    for r in range(rotation):
-        sets.append({k: pinned[k].to(dev, non_blocking=True) for k in keys})
+    sets = [{k: pinned[k].to(dev, non_blocking=True) for k in keys} for _ in range(rotation)]
     torch.cuda.synchronize()
-    outs = [(torch.empty((cfg.B, cfg.K + 1 if mode == "sample" else cfg.N), dtype=torch.int32, device=dev),
+    width = cfg.K + 1 if mode == "sample" else cfg.N
+    outs = [(torch.empty((cfg.B, width), dtype=torch.int32, device=dev),
              torch.empty((cfg.B,), dtype=torch.int32, device=dev)) for _ in range(rotation)]
 
-    def public_call(*args, **kw):
+    def public_call(*a, **kw):
         if mode == "greedy":
-            return svpkg.verify_greedy(*args, **kw)
+            return svpkg.verify_greedy(*a, **kw)
         if mode == "lookahead":
-            return svpkg.verify_lookahead_sample(*args, cfg.temperature, **kw)
+            return svpkg.verify_lookahead_sample(*a, cfg.temperature, **kw)
         if mode == "multidraft":
-            return svpkg.verify_multidraft_sample(*args, cfg.temperature, **kw)
-        return svpkg.verify_sample(*args, cfg.temperature, cfg.top_p, **kw)
+            return svpkg.verify_multidraft_sample(*a, cfg.temperature, **kw)
+        return svpkg.verify_sample(*a, cfg.temperature, cfg.top_p, **kw)
 
     def call(i):
         s, (ot, oa) = sets[i % rotation], outs[i % rotation]
-        if mode != "sample":
-            public_call(*(s[k] for k in keys), out_tokens=ot, out_accept_len=oa)
-        else:
-            svpkg.verify_sample(s["target"], s["draft"], s["draft_tokens"], s["uniforms"], cfg.temperature,
-                                cfg.top_p, out_tokens=ot, out_accept_len=oa)
+        public_call(*(s[k] for k in keys), out_tokens=ot, out_accept_len=oa)
 
     stream = torch.cuda.Stream(dev)
     with torch.cuda.stream(stream):
@@ -350,54 +418,70 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
     with torch.cuda.stream(stream):
         if svpkg.get_status() != 0:
             raise RuntimeError("device status set during warm-up")
-    # graphs of at most 1000 calls; the timed region replays exactly K calls
-    chunk = min(args.steps, 1000)
-    graphs = []
-    n_left = args.steps
-    launches_before = svpkg.launch_count()
-    idx = 0
-    while n_left > 0:
-        n = min(chunk, n_left)
+    breaker = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def capture(n, idx0, with_breaker=False, only_breaker=False):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            for _ in range(n):
-                call(idx)
-                idx += 1
-        graphs.append((g, n))
+            for k in range(n):
+                if not only_breaker:
+                    call(idx0 + k)
+                if with_breaker or only_breaker:
+                    breaker.add_(1)
+        return g
+
+    # graphs of at most 1000 calls; the timed region replays exactly `steps` calls
+    graphs, n_left, idx = [], steps, 0
+    launches_before = svpkg.launch_count()
+    while n_left > 0:
+        n = min(1000, n_left)
+        graphs.append(capture(n, idx))
+        idx += n
         n_left -= n
     captured = svpkg.launch_count() - launches_before
+    n_iso = 100
+    g_iso = capture(n_iso, 0, with_breaker=True)
+    g_brk = capture(n_iso, 0, only_breaker=True)
+
+    def timed(gs):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for g in gs:
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+
     # pre-roll: replay for ~1 s so that clocks settle and the sampler sees the load
     with ClockSampler(local) as clk:
         t_pre = time.perf_counter()
         with torch.cuda.stream(stream):
             while time.perf_counter() - t_pre < 1.0:
-                graphs[0][0].replay()
+                graphs[0].replay()
                 stream.synchronize()
         if world > 1:
             torch.distributed.barrier()
         torch.cuda.synchronize()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(stream):
-            e0.record(stream)
-            for g, _ in graphs:
-                g.replay()
-            e1.record(stream)
-        torch.cuda.synchronize()
+        ms = timed(graphs)
         if world > 1:
             torch.distributed.barrier()
-        ms = e0.elapsed_time(e1)
+        ms_iso = min(timed([g_iso]) for _ in range(3))
+        ms_brk = min(timed([g_brk]) for _ in range(3))
     with torch.cuda.stream(stream):
         status = svpkg.get_status()
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
     ms = max_over_ranks(ms, dev)
-    ms_per_step = ms / args.steps
-    value = positions * world * args.steps / (ms / 1e3)
+    ms_per_step = ms / steps
+    iso_us = max(0.0, (ms_iso - ms_brk) / n_iso * 1e3)
+    value = positions * world * steps / (ms / 1e3)
     achieved_gbs = logit_bytes / (ms_per_step / 1e3) / 1e9
     peak, peak_kind = measured_peak()
+    gt, ga = outs[0][0].cpu().numpy(), outs[0][1].cpu().numpy()
 
     # end to end through the public API with pinned host buffers
-    e2e_steps = max(3, min(20, args.steps))
+    e2e_steps = max(3, min(20, steps))
     host_args = [pinned[k] for k in keys]
     with torch.cuda.stream(stream):
         for _ in range(2):
@@ -408,46 +492,88 @@ def run_gpu(args, name: str, rank: int, world: int, print_line: bool):
             public_call(*host_args)
         e2e_s = (time.perf_counter() - t1) / e2e_steps
     h2d = logit_bytes + small_in
-
-    line = {
-        "metric": "verified positions/sec and achieved HBM GB/s (% of GB300 peak) per verify call",
+    kernel = launched_kernel(cfg, mode, args)
+    rec = {
+        "workload": config_json(cfg, mode, rotation, args.l2_resident),
         "value": value,
         "unit": "positions/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
         "ms_per_step": ms_per_step,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f32",
-        "data": "synthetic (seeded Philox inputs of the workload's shapes)",
-        "config": config_json(cfg, mode, rotation, args.l2_resident),
+        "steps": steps,
         "rounds_per_s": cfg.B * world / (ms_per_step / 1e3),
-        "achieved_gbs": achieved_gbs,
+        "isolated_us": iso_us,
+        "isolated_note": f"{n_iso} calls each followed by a one-element torch kernel that ends the launch "
+                         f"overlap, minus {n_iso} such kernels alone ({ms_brk * 1e3 / n_iso:.2f} us each)",
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": peak, "unit": "GB/s",
                      "frac": achieved_gbs / peak, "peak_source": f"{peak_kind} hbm_gbs",
-                     "traffic": profiled_traffic(name), "algorithmic_bytes_per_launch": logit_bytes,
-                     "kernel": ("gr_rows_kernel" if mode == "greedy" and args.greedy_path == 1
-                                else kernel_for(cfg, mode)),
+                     "traffic": profiled_traffic(name, kernel), "algorithmic_bytes_per_launch": logit_bytes,
+                     "kernel": kernel,
+                     "isolated_frac": (logit_bytes / (iso_us * 1e-6) / 1e9 / peak) if iso_us > 0 else None,
                      "timing": "CUDA events over graph replays of the timed calls"},
         "clocks": clk.summary(),
         "e2e": {"value": positions * world / e2e_s, "unit": "positions/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": out_bytes},
         "gpu_launches": int(captured),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        nth = os.cpu_count() or 1
-        rate, n, el = oracle_cpu_rate(cfg, mode, args.cpu_budget, nth)
+    nth = os.cpu_count() or 1
+    if counts and rank == 0:
+        t2 = time.perf_counter()
+        rec["parity"] = oracle_counts(host, cfg, mode, gt, ga, nth)
+        log(f"[bench] oracle comparison in {time.perf_counter() - t2:.1f} s: {rec['parity']}")
+    if cpu_budget > 0 and rank == 0 and world == 1:
+        rate, n, el = oracle_cpu_rate(cfg, mode, cpu_budget, nth)
+        rec["cpu_baseline"] = {"value": rate, "unit": "positions/s", "cores": nth, "kind": "oracle",
+                               "rounds_per_s": n / el,
+                               "sample": f"{n} sequences of the workload in {el:.1f} s, "
+                                         f"one oracle call per thread per batch"}
+    del sets, outs, graphs, g_iso, g_brk
+    torch.cuda.empty_cache()
+    return rec
+
+
+def run_gpu(args, names: list, rank: int, world: int):
+    import torch
+    import speculative_decoding_verification_39_gb300 as svpkg
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(torch.device("cuda", local))
+    svpkg.build()
+    svpkg.set_greedy_path(args.greedy_path)
+    svpkg.set_sample_path(args.sample_path)
+    head = names[0]
+    rec = measure(args, head, rank, world, args.steps, 0.0 if args.no_cpu_baseline else args.cpu_budget,
+                  counts=not args.no_counts)
+    cfg, mode = workload(head, args.batch)[:2]
+    line = {
+        "metric": "verified positions/sec and achieved HBM GB/s (% of GB300 peak) per verify call",
+        "value": rec["value"],
+        "unit": "positions/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": rec["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded Philox inputs of the workload's shapes)",
+        "config": rec["workload"],
+    }
+    for k in ("rounds_per_s", "isolated_us", "isolated_note", "roofline", "clocks", "e2e", "gpu_launches",
+              "parity", "cpu_baseline"):
+        if k in rec:
+            line[k] = rec[k]
+    if "cpu_baseline" in line and not args.no_cpu_baseline and rank == 0 and world == 1:
         rate1, n1, el1 = oracle_cpu_rate(cfg, mode, args.cpu_budget / 2, 1)
-        line["cpu_baseline"] = {"value": rate, "unit": "positions/s", "cores": nth, "kind": "oracle",
-                                "rounds_per_s": n / el,
-                                "sample": f"{n} sequences of the workload in {el:.1f} s, "
-                                          f"one oracle call per thread per batch",
-                                "single_thread": {"value": rate1, "unit": "positions/s", "cores": 1,
-                                                  "rounds_per_s": n1 / el1,
-                                                  "sample": f"{n1} sequences in {el1:.1f} s"}}
-    if print_line and rank == 0:
+        line["cpu_baseline"]["single_thread"] = {"value": rate1, "unit": "positions/s", "cores": 1,
+                                                 "rounds_per_s": n1 / el1, "sample": f"{n1} sequences in {el1:.1f} s"}
+    if len(names) > 1 and world == 1:
+        per = {}
+        for n in names[1:]:
+            r = measure(args, n, rank, world, max(args.steps, 100), 0.0 if args.no_cpu_baseline else 2.0,
+                        counts=not args.no_counts)
+            per[n] = r
+        line["per_config"] = per
+    if rank == 0:
         print(json.dumps(line), flush=True)
     return line
 
@@ -493,10 +619,16 @@ def run_reference(args, name: str):
     print(json.dumps(line), flush=True)
 
 
-def config_names(spec: str) -> list:
-    """'all', one workload name, or several separated by commas."""
-    if spec == "all":
-        return list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS)
+def all_names() -> list:
+    return list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS)
+
+
+def config_names(spec) -> list:
+    """None: the headline workload, then every other one (their per_config
+    records); 'all': the same; otherwise one workload name or several
+    separated by commas (the first is the line's own)."""
+    if spec is None or spec == "all":
+        return [DEFAULT_CONFIG] + [n for n in all_names() if n != DEFAULT_CONFIG]
     names = [n.strip() for n in spec.split(",") if n.strip()]
     for n in names:
         find_config(n)  # KeyError for an unknown name, before any work
@@ -506,16 +638,22 @@ def config_names(spec: str) -> list:
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", default=DEFAULT_CONFIG, help="workload name, several joined by commas, or 'all'")
+    ap.add_argument("--config", default=None,
+                    help="workload name, several joined by commas (the first is the line's own, the rest its "
+                         "per_config records), or 'all' (the default: the headline workload, then every other)")
+    ap.add_argument("--no-counts", action="store_true", help="skip the GPU/oracle mismatch counts")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (--batch 1: per-call latency of one sequence)")
     ap.add_argument("--greedy-path", type=int, default=0, choices=[0, 1],
-                    help="greedy verify kernels: 0 the streaming kernel, 1 row argmax + match kernels")
+                    help="greedy verify kernels: 0 row argmax + match kernels, 1 the streaming kernel")
+    ap.add_argument("--sample-path", type=int, default=0, choices=[0, 1],
+                    help="sampling verify kernels: 0 the row pass + cluster decide kernel where they fit, 1 the "
+                         "streaming kernel")
     ap.add_argument("--l2-resident", action="store_true",
                     help="replay one input set, so that inputs that fit stay in L2 (reported as such; not an "
                          "HBM figure)")
@@ -523,8 +661,7 @@ def main():
     args.warmup = max(3, args.warmup)
     names = config_names(args.config)
     if args.impl == "reference":
-        for n in names:
-            run_reference(args, n)
+        run_reference(args, names[0])
         return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -534,8 +671,7 @@ def main():
         import torch
         torch.distributed.init_process_group("nccl")
     try:
-        for n in names:
-            run_gpu(args, n, rank, world, print_line=True)
+        run_gpu(args, names, rank, world)
     finally:
         if world > 1:
             import torch

@@ -188,6 +188,44 @@ int sv_verify_multidraft_sample(const void* target, const void* draft, const int
                                 int32_t* out_best_cand, float* out_row_lse, void* stream);
 
 /*
+ * N-gram pool of Lookahead decoding ("Lookahead Decoding 完全拆解", section
+ * "N-gram 池与身份判定"; W new n-grams per step from the section on the 2D
+ * window; at most G candidates, GUESS_SET_SIZE, in the engineering section).
+ * The pool caches the n-grams the lookahead branch collects, one pool per
+ * sequence, keyed by an n-gram's first token; only the n-grams whose first
+ * token equals the sequence's last generated token are candidates for the
+ * verify branch, and a lookup leaves the pool as it was (n-grams that are not
+ * adopted stay). Where the page is silent this library reads: each first
+ * token holds at most `cap` n-grams; a step's n-grams are inserted in order;
+ * an n-gram already held is not inserted again and keeps its place;
+ * inserting into a full first token drops its oldest n-gram; candidates are
+ * the newest first; an n-gram with a token outside [0, V) is ignored.
+ *
+ * The pool lives in caller-owned device memory of sv_ngram_pool_bytes(B, V,
+ * N, cap) bytes (256-byte aligned); B, V, N and cap must be the same on every
+ * call that uses it. 1 <= N <= 4096 is the n-gram length (N >= 2), 1 <= cap <=
+ * 4096. Calls are asynchronous on `stream` like the verify calls.
+ *
+ *   sv_ngram_pool_bytes: the bytes a pool needs (-1 for a bad shape).
+ *   sv_ngram_pool_reset: empties the pool (a memset of its counters).
+ *   sv_ngram_pool_insert: ngrams [B, W, N] int32; sequence b's W n-grams go
+ *     into its pool in order.
+ *   sv_ngram_pool_lookup: last [B] int32, each sequence's last generated
+ *     token; writes cand [B, G, N-1] int32, the tokens after the first of the
+ *     matching n-grams, newest first (the layout sv_verify_greedy reads), and
+ *     count [B] int32, how many there are. Unused candidate slots hold a copy
+ *     of the newest candidate, or the last token repeated when there is none
+ *     (a guess that cannot change what the greedy verify outputs). A last
+ *     token outside [0, V) gives count -1 and -1 tokens.
+ */
+int64_t sv_ngram_pool_bytes(int64_t B, int64_t V, int32_t N, int32_t cap);
+int sv_ngram_pool_reset(void* pool, int64_t B, int64_t V, int32_t N, int32_t cap, void* stream);
+int sv_ngram_pool_insert(void* pool, int64_t B, int64_t V, int32_t N, int32_t cap, const int32_t* ngrams,
+                         int32_t W, void* stream);
+int sv_ngram_pool_lookup(const void* pool, int64_t B, int64_t V, int32_t N, int32_t cap, const int32_t* last,
+                         int32_t G, int32_t* cand, int32_t* count, void* stream);
+
+/*
  * sv_verify_sample_noalloc: sv_verify_sample for callers that cannot allocate
  * device memory. The pages have no counterpart to this entry point; it exists
  * for deployment constraints, not for the method.
@@ -201,13 +239,17 @@ int sv_verify_multidraft_sample(const void* target, const void* draft, const int
  * part of the library image and that every GPU which loads the library holds
  * until the process exits.
  *
- * Arguments, outputs and results are exactly those of sv_verify_sample (the
- * same kernel runs). Differences:
+ * Arguments, outputs and results are exactly those of sv_verify_sample: the
+ * same argument checks, the same choice of kernels and the same launch
+ * shapes; only the scratch differs. Differences:
  *   - A call whose scratch would exceed 4 MiB returns SV_ERR_SCRATCH_LIMIT and
- *     enqueues nothing. The scratch needed is about
- *     256 + 4*(B*R + B*(3+D)) + 8*B*R*ceil(NT/CT) + 16*B*R bytes (R = 2K+1
- *     rows per sequence), plus 4*B*ceil(V/256) when the draws are split
- *     over D > 0 chunks, e.g. about 0.2 MiB for B=256, K=8, V=128256.
+ *     enqueues nothing. Without top-p (T > 0, K <= 1024, V <= 1048576) the
+ *     scratch is 256 + 8*B*(2K+1)*ceil(V*s/32768) bytes (s = 2 for bf16, 4 for
+ *     fp32; one chunk per row when a row holds at most 16 KB), e.g. about
+ *     0.3 MiB for B=256, K=8, V=128256 bf16; with top-p or T = 0 it is about
+ *     256 + 4*(B*R + B*(3+D)) + 8*B*R*ceil(NT/CT) + 16*B*R bytes (R rows per
+ *     sequence), plus 4*B*ceil(V/256) when the draws are split over D > 0
+ *     chunks.
  *   - The first call on a device looks up the array's device address on that
  *     device (cudaGetSymbolAddress, with the device current) and caches it;
  *     make that first call before any stream capture.
@@ -259,10 +301,16 @@ int sv_set_launch_shape(int32_t stages, int32_t ctas_per_sm);
 /* How many kernel launches the library has enqueued since it was loaded. */
 uint64_t sv_launch_count(void);
 
-/* Which kernels sv_verify_greedy uses, for comparing them: 0 (default) the
- * streaming kernel; 1 one CTA per row for the argmax, then one warp per
- * sequence for the match. Applies to calls made after it. */
+/* Which kernels sv_verify_greedy uses, for comparing them: 0 (default) one
+ * CTA per row for the argmax, then one warp per sequence for the match; 1 the
+ * streaming kernel. Applies to calls made after it. */
 int sv_set_greedy_path(int32_t path);
+
+/* Which kernels sv_verify_sample uses, for comparing them: 0 (default) the
+ * row pass and the cluster decide kernel whenever T > 0, top_p = 1,
+ * K <= 1024 and V <= 1048576 (the streaming kernel otherwise); 1 always the
+ * streaming kernel. Applies to calls made after it. */
+int sv_set_sample_path(int32_t path);
 
 #ifdef __cplusplus
 }

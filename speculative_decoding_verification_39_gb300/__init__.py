@@ -27,9 +27,10 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _SO = os.path.join(_HERE, "libspecverify.so")
 _SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_noalloc.cu", "sv_lookahead.cu", "sv_multidraft.cu",
-            "sv_greedy_rows.cu"]
+            "sv_greedy_rows.cu", "sv_rows.cu", "sv_decide.cu", "sv_ngram.cu", "sv_refine.cu"]
 _DEPS = _SOURCES + ["sv_kernels.h", "sv_device.cuh", "sv_lookahead.h", "sv_multidraft.h", "sv_rowstat.cuh",
-                    "sv_greedy_rows.h"]
+                    "sv_greedy_rows.h", "sv_v2.h", "sv_df.cuh", "sv_sample_impl.h",
+                    "sv_refine.h"]
 
 SV_F32, SV_BF16 = 0, 1
 STATUS = {0: "SV_OK", -1: "SV_ERR_ARG", -2: "SV_ERR_DTYPE", -3: "SV_ERR_CUDA", -4: "SV_ERR_INPUT",
@@ -120,6 +121,16 @@ def lib():
         h.sv_verify_multidraft_sample.restype = ctypes.c_int
         h.sv_set_greedy_path.argtypes = [i32]
         h.sv_set_greedy_path.restype = ctypes.c_int
+        h.sv_set_sample_path.argtypes = [i32]
+        h.sv_set_sample_path.restype = ctypes.c_int
+        h.sv_ngram_pool_bytes.argtypes = [i64, i64, i32, i32]
+        h.sv_ngram_pool_bytes.restype = ctypes.c_int64
+        h.sv_ngram_pool_reset.argtypes = [vp, i64, i64, i32, i32, vp]
+        h.sv_ngram_pool_reset.restype = ctypes.c_int
+        h.sv_ngram_pool_insert.argtypes = [vp, i64, i64, i32, i32, vp, i32, vp]
+        h.sv_ngram_pool_insert.restype = ctypes.c_int
+        h.sv_ngram_pool_lookup.argtypes = [vp, i64, i64, i32, i32, vp, i32, vp, vp, vp]
+        h.sv_ngram_pool_lookup.restype = ctypes.c_int
         _lib_handle = h
     return _lib_handle
 
@@ -127,7 +138,9 @@ def lib():
 def exported_symbols() -> list:
     return ["sv_verify_sample", "sv_verify_greedy", "sv_get_status", "sv_status_string", "sv_release",
             "sv_set_launch_shape", "sv_launch_count", "sv_verify_sample_noalloc", "sv_selftest_wait_timeout",
-            "sv_verify_lookahead_sample", "sv_verify_multidraft_sample", "sv_set_greedy_path"]
+            "sv_verify_lookahead_sample", "sv_verify_multidraft_sample", "sv_set_greedy_path",
+            "sv_set_sample_path", "sv_ngram_pool_bytes", "sv_ngram_pool_reset", "sv_ngram_pool_insert",
+            "sv_ngram_pool_lookup"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -140,6 +153,14 @@ def _dtype_code(t: torch.Tensor) -> int:
 
 def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev_i32(a, device) -> torch.Tensor:
+    """An int32 contiguous tensor on ``device`` from a tensor or an array."""
+    t = a if isinstance(a, torch.Tensor) else torch.as_tensor(a)
+    if t.dtype != torch.int32:
+        raise TypeError(f"expected int32 token ids, got {t.dtype}")
+    return _on_device(t, device, "tokens").contiguous()
 
 
 def _stream_handle(device) -> ctypes.c_void_p:
@@ -354,10 +375,18 @@ def set_launch_shape(stages: int = 0, ctas_per_sm: int = 0) -> None:
 
 
 def set_greedy_path(path: int) -> None:
-    """0: the streaming kernel (default); 1: row argmax then match kernels."""
+    """0 (default): row argmax then match kernels; 1: the streaming kernel."""
     rc = lib().sv_set_greedy_path(int(path))
     if rc != 0:
         raise SpecVerifyError(rc, "sv_set_greedy_path")
+
+
+def set_sample_path(path: int) -> None:
+    """0 (default): the row pass and the cluster decide kernel where they fit;
+    1: the streaming kernel."""
+    rc = lib().sv_set_sample_path(int(path))
+    if rc != 0:
+        raise SpecVerifyError(rc, "sv_set_sample_path")
 
 
 def launch_count() -> int:
@@ -368,3 +397,46 @@ def release() -> None:
     rc = lib().sv_release()
     if rc != 0:
         raise SpecVerifyError(rc, "sv_release")
+
+
+class NgramPool:
+    """The Lookahead n-gram pool in device memory (sv_ngram_pool_*): one pool
+    per sequence, keyed by first token, at most ``cap`` n-grams of N tokens per
+    key. ``insert`` takes int32 n-grams [B, W, N]; ``lookup`` takes the last
+    generated token of each sequence [B] and returns (cand [B, G, N-1],
+    count [B]) on the device, in the layout ``verify_greedy`` reads."""
+
+    def __init__(self, B: int, V: int, N: int, cap: int, device=None):
+        self.B, self.V, self.N, self.cap = B, V, N, cap
+        nbytes = lib().sv_ngram_pool_bytes(B, V, N, cap)
+        if nbytes < 0:
+            raise SpecVerifyError(-1, "sv_ngram_pool_bytes")
+        self.device = device or torch.device("cuda", torch.cuda.current_device())
+        self.mem = torch.empty(max(1, int(nbytes)), dtype=torch.uint8, device=self.device)
+        self.reset()
+
+    def _stream(self):
+        return ctypes.c_void_p(torch.cuda.current_stream(self.device).cuda_stream)
+
+    def reset(self):
+        rc = lib().sv_ngram_pool_reset(_ptr(self.mem), self.B, self.V, self.N, self.cap, self._stream())
+        if rc != 0:
+            raise SpecVerifyError(rc, "sv_ngram_pool_reset")
+
+    def insert(self, ngrams):
+        g = _dev_i32(ngrams, self.device)
+        assert g.dim() == 3 and g.shape[0] == self.B and g.shape[2] == self.N
+        rc = lib().sv_ngram_pool_insert(_ptr(self.mem), self.B, self.V, self.N, self.cap, _ptr(g), g.shape[1],
+                                        self._stream())
+        if rc != 0:
+            raise SpecVerifyError(rc, "sv_ngram_pool_insert")
+
+    def lookup(self, last, G: int):
+        t = _dev_i32(last, self.device)
+        cand = torch.empty((self.B, G, self.N - 1), dtype=torch.int32, device=self.device)
+        count = torch.empty((self.B,), dtype=torch.int32, device=self.device)
+        rc = lib().sv_ngram_pool_lookup(_ptr(self.mem), self.B, self.V, self.N, self.cap, _ptr(t), G, _ptr(cand),
+                                        _ptr(count), self._stream())
+        if rc != 0:
+            raise SpecVerifyError(rc, "sv_ngram_pool_lookup")
+        return cand, count

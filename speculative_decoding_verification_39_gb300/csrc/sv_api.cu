@@ -14,6 +14,9 @@
 #include "sv_greedy_rows.h"
 #include "sv_lookahead.h"
 #include "sv_multidraft.h"
+#include "sv_refine.h"
+#include "sv_sample_impl.h"
+#include "sv_v2.h"
 
 namespace {
 
@@ -24,7 +27,8 @@ constexpr int64_t kMaxV = (int64_t)1 << 31;
 std::atomic<int> g_stages{kDefaultStages};
 std::atomic<int> g_ctas_per_sm{kDefaultCtasPerSm};
 std::atomic<uint64_t> g_launches{0};
-std::atomic<int> g_greedy_path{0};  // 0: the streaming kernel; 1: row argmax + match kernels
+std::atomic<int> g_greedy_path{0};  // 0: row argmax + match kernels; 1: the streaming kernel
+std::atomic<int> g_sample_path{0};  // 0: row pass + cluster decide where it fits; 1: the streaming kernel
 
 // A scratch area has three parts at fixed places: the control block, a
 // counter region and a data region. Every counter is back at zero when a call
@@ -91,7 +95,30 @@ int sm_count(int dev) {
 
 bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t stream) {
+// The refine kernel after a sampling call: it redoes, in double-float
+// arithmetic, the draws the call's fp32 walks could not settle.
+int launch_refine(const void* target, const void* draft, int64_t B, int K, int64_t V, int esz, float temperature,
+                  uint32_t* rf_ctl, sv::rf::Rec* recs, float* part, uint32_t* status, int32_t* out_tokens, int grid,
+                  cudaStream_t stream) {
+  sv::rf::Params r{};
+  r.target = static_cast<const char*>(target);
+  r.draft = static_cast<const char*>(draft);
+  r.B = B;
+  r.V = V;
+  r.K = K;
+  r.esz = esz;
+  sv::rf::fill_table(r, temperature);
+  r.ctl = rf_ctl;
+  r.status = status;
+  r.recs = recs;
+  r.part = part;
+  r.out_tokens = out_tokens;
+  if (sv::rf::launch(r, grid, stream) != cudaSuccess) return SV_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return SV_OK;
+}
+
+int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t stream, sv::ScratchGet get, void* ctx) {
   const int esz = dtype == SV_BF16 ? 2 : 4;
   p.TE = sv::kTileBytes / esz;
   p.NT = (p.V + p.TE - 1) / p.TE;
@@ -129,30 +156,38 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
       p.CPC = (int)((ncells + dc - 1) / dc);
     }
   }
-  const size_t cnt_words = (size_t)rows_total + (size_t)p.B * (3 + (size_t)p.DC);
+  const bool refine = mode == sv::kSample;
+  const int sms = sm_count(dev0);
+  const size_t cnt_words = (size_t)rows_total + (size_t)p.B * (3 + (size_t)p.DC) + (refine ? sv::rf::kCtlWords : 0);
   const size_t part_bytes = align256((size_t)p.W * 8);
   const size_t rowstat_bytes = align256((size_t)rows_total * 16);
   const size_t dcells_bytes = p.DC ? align256((size_t)p.B * (size_t)ncells * 4) : 0;
-  const size_t data_bytes = part_bytes + rowstat_bytes + dcells_bytes;
-  Scratch sc;
-  int dev = 0;
-  int rc = get_scratch(stream, cnt_words, data_bytes, &sc, &dev);
+  const size_t recs_bytes = refine ? align256((size_t)p.B * sizeof(sv::rf::Rec)) : 0;
+  const size_t rfpart_bytes = refine ? align256(sv::rf::part_bytes(sms)) : 0;
+  const size_t data_bytes = part_bytes + rowstat_bytes + dcells_bytes + recs_bytes + rfpart_bytes;
+  sv::ScratchArea sa;
+  int rc = get(ctx, stream, cnt_words, data_bytes, &sa);
   if (rc != SV_OK) return rc;
-  char* b = static_cast<char*>(sc.base);
+  char* b = sa.base;
+  if (sa.clear_counters && cudaMemsetAsync(b, 0, sa.data_off, stream) != cudaSuccess) return SV_ERR_CUDA;
   p.ctl = reinterpret_cast<uint32_t*>(b);
   p.row_cnt = reinterpret_cast<uint32_t*>(b + counter_offset());
   p.seq_cnt = p.row_cnt + rows_total;
   p.tail_q = p.seq_cnt + p.B;
   p.dcnt = p.tail_q + p.B * (1 + p.DC);
-  p.part = reinterpret_cast<float2*>(b + data_offset(sc));
-  p.rowstat = reinterpret_cast<float4*>(b + data_offset(sc) + part_bytes);
-  p.dcells = reinterpret_cast<float*>(b + data_offset(sc) + part_bytes + rowstat_bytes);
+  p.part = reinterpret_cast<float2*>(b + sa.data_off);
+  p.rowstat = reinterpret_cast<float4*>(b + sa.data_off + part_bytes);
+  p.dcells = reinterpret_cast<float*>(b + sa.data_off + part_bytes + rowstat_bytes);
+  p.rf_ctl = refine ? p.dcnt + p.B : nullptr;
+  p.rf_recs = refine ? reinterpret_cast<sv::rf::Rec*>(b + sa.data_off + part_bytes + rowstat_bytes + dcells_bytes)
+                     : nullptr;
+  float* rf_part = reinterpret_cast<float*>(b + sa.data_off + part_bytes + rowstat_bytes + dcells_bytes + recs_bytes);
   // Short rows: one warp per sequence (rows of at most 1024 elements), else
   // one CTA per sequence with the whole sequence staged in shared memory.
   const bool short_ok = mode == sv::kSample && !p.topp && aligned_to(p.a, 16) && aligned_to(p.d, 16);
   const bool warp_mode = short_ok && sv::warp_mode_fits(p.K, p.V, esz);
   const bool seq_mode = short_ok && !warp_mode && sv::seq_mode_fits(p.K, p.V, esz);
-  int64_t grid = (int64_t)sm_count(dev) * g_ctas_per_sm.load();
+  int64_t grid = slots;
   const int64_t items = warp_mode ? (p.B + sv::warp_mode_seqs_per_cta() - 1) / sv::warp_mode_seqs_per_cta()
                                   : (seq_mode ? p.B : p.W);
   if (grid > items) grid = items;
@@ -162,15 +197,30 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
                              : sv::launch(p, dtype, mode, (int)grid, stream);
   if (e != cudaSuccess) return SV_ERR_CUDA;
   g_launches.fetch_add(1);
+  if (refine)
+    return launch_refine(p.a, p.d, p.B, p.K, p.V, esz, p.T, p.rf_ctl, p.rf_recs, rf_part, p.ctl + 3, p.out_tokens,
+                         sms, stream);
+  return SV_OK;
+}
+
+// The allocating provider: the per-(device, stream) scratch area.
+int cached_scratch(void*, cudaStream_t stream, size_t cnt_words, size_t data_bytes, sv::ScratchArea* out) {
+  Scratch sc;
+  int dev = 0;
+  const int rc = get_scratch(stream, cnt_words, data_bytes, &sc, &dev);
+  if (rc != SV_OK) return rc;
+  out->base = static_cast<char*>(sc.base);
+  out->data_off = data_offset(sc);
+  out->clear_counters = false;  // zeroed when allocated; every kernel leaves its counters at zero
   return SV_OK;
 }
 
 }  // namespace
 
-extern "C" int sv_verify_sample(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
-                                const float* uniforms, int64_t B, int32_t K, int64_t V, int32_t dtype,
-                                float temperature, float top_p, int32_t* out_tokens, int32_t* out_accept_len,
-                                float* out_row_stats, void* stream) {
+int sv::verify_sample_impl(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                           const float* uniforms, int64_t B, int32_t K, int64_t V, int32_t dtype, float temperature,
+                           float top_p, int32_t* out_tokens, int32_t* out_accept_len, float* out_row_stats,
+                           cudaStream_t st, sv::ScratchGet get, void* ctx) {
   if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
   if (B < 0 || K < 1 || V < 2 || V >= kMaxV || K > (1 << 20)) return SV_ERR_ARG;
   if (!(temperature >= 0.f) || std::isinf(temperature)) return SV_ERR_ARG;
@@ -186,6 +236,44 @@ extern "C" int sv_verify_sample(const void* target_logits, const void* draft_log
     return SV_ERR_ARG;
   const float c = limit ? 0.f : (float)(1.4426950408889634 / (double)temperature);
   if (!limit && !std::isfinite(c)) return SV_ERR_ARG;
+  if (!limit && top_p == 1.f && g_sample_path.load() == 0 && sv::v2::fits(K, V)) {
+    sv::v2::Params q{};
+    q.target = static_cast<const char*>(target_logits);
+    q.draft = static_cast<const char*>(draft_logits);
+    q.tokens = draft_tokens;
+    q.uniforms = uniforms;
+    q.out_tokens = out_tokens;
+    q.out_accept_len = out_accept_len;
+    q.out_row_stats = out_row_stats;
+    q.B = B;
+    q.V = V;
+    q.K = K;
+    q.R = 2 * K + 1;
+    q.esz = (int)esz;
+    q.c = c;
+    q.T = temperature;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+    sv::v2::plan(q, sm_count(dev));
+    if (q.items >= (int64_t(1) << 31) || B * q.D >= (int64_t(1) << 31)) return SV_ERR_ARG;
+    const int sms = sm_count(dev);
+    const size_t v2_bytes = align256(sv::v2::scratch_bytes(q));
+    const size_t recs_bytes = align256((size_t)B * sizeof(sv::rf::Rec));
+    sv::ScratchArea sa;
+    const int rc = get(ctx, st, sv::rf::kCtlWords, v2_bytes + recs_bytes + sv::rf::part_bytes(sms), &sa);
+    if (rc != SV_OK) return rc;
+    if (sa.clear_counters && cudaMemsetAsync(sa.base, 0, sa.data_off, st) != cudaSuccess) return SV_ERR_CUDA;
+    q.ctl = reinterpret_cast<uint32_t*>(sa.base);
+    q.part = reinterpret_cast<float2*>(sa.base + sa.data_off);
+    q.gz = reinterpret_cast<float*>(sa.base + sa.data_off + sv::v2::part_bytes(q));
+    q.rf_ctl = reinterpret_cast<uint32_t*>(sa.base + counter_offset());
+    q.rf_recs = reinterpret_cast<sv::rf::Rec*>(sa.base + sa.data_off + v2_bytes);
+    float* rf_part = reinterpret_cast<float*>(sa.base + sa.data_off + v2_bytes + recs_bytes);
+    if (sv::v2::launch(q, dtype, st) != cudaSuccess) return SV_ERR_CUDA;
+    g_launches.fetch_add(2);
+    return launch_refine(target_logits, draft_logits, B, K, V, (int)esz, temperature, q.rf_ctl, q.rf_recs, rf_part,
+                         q.ctl + 3, out_tokens, sms, st);
+  }
   sv::Params p{};
   p.a = static_cast<const char*>(target_logits);
   p.d = static_cast<const char*>(limit ? target_logits : draft_logits);
@@ -205,7 +293,16 @@ extern "C" int sv_verify_sample(const void* target_logits, const void* draft_log
   p.T = temperature;
   p.top_p = top_p;
   p.topp = (!limit && top_p < 1.f) ? 1 : 0;
-  return run(p, dtype, limit ? sv::kArgmaxLimit : sv::kSample, B * (int64_t)p.RS, static_cast<cudaStream_t>(stream));
+  return run(p, dtype, limit ? sv::kArgmaxLimit : sv::kSample, B * (int64_t)p.RS, st, get, ctx);
+}
+
+extern "C" int sv_verify_sample(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                                const float* uniforms, int64_t B, int32_t K, int64_t V, int32_t dtype,
+                                float temperature, float top_p, int32_t* out_tokens, int32_t* out_accept_len,
+                                float* out_row_stats, void* stream) {
+  return sv::verify_sample_impl(target_logits, draft_logits, draft_tokens, uniforms, B, K, V, dtype, temperature,
+                                top_p, out_tokens, out_accept_len, out_row_stats, static_cast<cudaStream_t>(stream),
+                                cached_scratch, nullptr);
 }
 
 extern "C" int sv_verify_greedy(const void* logits, const int32_t* cand, int64_t B, int32_t G, int32_t N, int64_t V,
@@ -221,7 +318,7 @@ extern "C" int sv_verify_greedy(const void* logits, const int32_t* cand, int64_t
   if (!aligned_to(cand, 4) || !aligned_to(out_tokens, 4) || !aligned_to(out_accept_len, 4) ||
       (out_best_cand && !aligned_to(out_best_cand, 4)))
     return SV_ERR_ARG;
-  if (g_greedy_path.load() == 1 && B * (int64_t)G * N < kMaxV) {
+  if (g_greedy_path.load() == 0 && B * (int64_t)G * N < kMaxV) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     Scratch sc;
     int dev = 0;
@@ -263,7 +360,7 @@ extern "C" int sv_verify_greedy(const void* logits, const int32_t* cand, int64_t
   p.T = 0.f;
   p.top_p = 1.f;
   p.topp = 0;
-  return run(p, dtype, sv::kGreedy, B * (int64_t)p.RS, static_cast<cudaStream_t>(stream));
+  return run(p, dtype, sv::kGreedy, B * (int64_t)p.RS, static_cast<cudaStream_t>(stream), cached_scratch, nullptr);
 }
 
 extern "C" int sv_verify_lookahead_sample(const void* logits, const int32_t* cand, const float* uniforms, int64_t B,
@@ -443,5 +540,11 @@ extern "C" uint64_t sv_launch_count(void) { return g_launches.load(); }
 extern "C" int sv_set_greedy_path(int32_t path) {
   if (path < 0 || path > 1) return SV_ERR_ARG;
   g_greedy_path.store(path);
+  return SV_OK;
+}
+
+extern "C" int sv_set_sample_path(int32_t path) {
+  if (path < 0 || path > 1) return SV_ERR_ARG;
+  g_sample_path.store(path);
   return SV_OK;
 }

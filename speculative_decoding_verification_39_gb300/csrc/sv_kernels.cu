@@ -31,11 +31,32 @@
 //           = min(1, 2^(a_p - a_q) * cum_q / cum_p),  a = fma(l_x, c, -Mc).
 #include "sv_device.cuh"
 #include "sv_kernels.h"
+#include "sv_refine.h"
 
-#include <climits>
 #include <cfloat>
+#include <climits>
+#include <mutex>
+#include <set>
+#include <utility>
 
 namespace sv {
+
+// Raises a kernel's dynamic shared-memory limit to `bytes`, once per (kernel,
+// device): the attribute belongs to the current device's context, so a
+// process that calls on several devices raises it on each. Not a stream
+// operation; kept out of later calls so that those can be graph-captured.
+static cudaError_t raise_smem_limit(const void* kernel, size_t bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) done.insert({kernel, dev});
+  return e;
+}
 
 // ------------------------------------------------------------------ layout ---
 
@@ -636,6 +657,7 @@ __device__ int64_t cdf_cross(const WF& wf, int64_t V, float u, Shared& sh, int t
     const float incl = warp_incl_scan(ls, lane);
     const float Z = __shfl_sync(0xffffffffu, incl, 31);
     int64_t t = -1;
+    int settled = 0;  // the fp32 walk found the token clear of its interval's edges
     if (Z > 0.f) {
       const float Tg = u * Z;
       float run = incl - ls;
@@ -697,15 +719,22 @@ __device__ int64_t cdf_cross(const WF& wf, int64_t V, float u, Shared& sh, int t
 #pragma unroll
               for (int k = 0; k < 8; ++k) {
                 if (mine < 0) {
+                  const float prev = acc;
                   acc += w[k];
                   if (w[k] > 0.f) lastpos = base + q * 8 + k;
-                  if (acc > Tl) mine = base + q * 8 + k;
+                  if (acc > Tl) {
+                    mine = base + q * 8 + k;
+                    // u*Z within the refine margin of an edge of the token's
+                    // interval: too close for fp32 to be sure
+                    settled = fminf(acc - Tl, Tl - prev) >= rf::kRefineMargin * Z;
+                  }
                 }
               }
             }
             if (mine < 0) mine = lastpos;  // rounding inside the lane
           }
           mine = __shfl_sync(0xffffffffu, mine, fl2);
+          settled = __shfl_sync(0xffffffffu, settled, fl2);
         } else {
           last_positive = true;
         }
@@ -726,8 +755,12 @@ __device__ int64_t cdf_cross(const WF& wf, int64_t V, float u, Shared& sh, int t
         mine = lastpos;
       }
       t = mine;
+      if (last_positive) settled = 0;
     }
-    if (lane == 0) sh.bl[0] = t;
+    if (lane == 0) {
+      sh.bl[0] = t;
+      sh.bi[7] = settled;
+    }
   }
   cbar();
   const int64_t t = sh.bl[0];
@@ -928,13 +961,37 @@ __device__ __forceinline__ Weights<E, false, kTopp> target_weights(const Params&
 
 // The draw of sequence b in this CTA alone: the residual at a rejection
 // (p'_j itself if that is all zero), or p'_K for the bonus token.
+// Appends a draw the fp32 walk could not settle to the refine kernel's list
+// (the draw's rows, their largest raw logits and nucleus cuts, its uniform).
+template <typename E>
+__device__ __forceinline__ void flag_draw(const Params& p, int64_t b, const DrawJob& jb) {
+  if (!p.rf_ctl) return;
+  rf::Rec r{};
+  r.b = (int32_t)b;
+  r.j = jb.j;
+  r.resid = jb.j < p.K ? 1 : 0;
+  r.mp = rs_load(p, b * p.RS + jb.j).M;
+  r.mq = jb.j < p.K ? rs_load(p, b * p.RS + p.K + 1 + jb.j).M : 0.f;
+  r.taup = jb.tp;
+  r.tauq = jb.j < p.K ? jb.tq : -INFINITY;
+  r.u = jb.uK;
+  rf::flag(p.rf_ctl, p.rf_recs, p.B, r);
+}
+
 template <typename E, bool kTopp>
 __device__ int64_t draw_whole(const Params& p, Shared& sh, int64_t b, const DrawJob& jb, int tid, char* ring,
                               size_t ring_bytes) {
   int64_t t = -1;
-  if (jb.j < p.K)
+  int settled = 1;
+  if (jb.j < p.K) {
     t = cdf_draw<E>(residual_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid, ring, ring_bytes, p.ctl + 3);
-  if (t < 0) t = cdf_draw<E>(target_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid, ring, ring_bytes, p.ctl + 3);
+    settled = t >= 0 && sh.bi[7];  // a residual of zero mass in fp32 may not be zero exactly
+  }
+  if (t < 0) {
+    t = cdf_draw<E>(target_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid, ring, ring_bytes, p.ctl + 3);
+    if (jb.j == p.K) settled = sh.bi[7];
+  }
+  if (!settled && tid == 0) flag_draw<E>(p, b, jb);
   return t;
 }
 
@@ -1347,12 +1404,21 @@ __device__ void draw_chunk(const Params& p, Shared& sh, int64_t b, int c, int ti
   for (int i = tid; i < ncells; i += kConsumerThreads) sh.cells[i] = __ldcg(cells + i);
   cbar();
   int64_t t = -1;
-  if (jb.j < p.K) t = cdf_cross<E>(residual_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid);
-  if (t < 0)  // the bonus draw, or a residual that is all zero: p'_j
+  int settled = 1;
+  if (jb.j < p.K) {
+    t = cdf_cross<E>(residual_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid);
+    settled = t >= 0 && sh.bi[7];
+  }
+  if (t < 0) {  // the bonus draw, or a residual that is all zero: p'_j
     t = jb.j < p.K
             ? cdf_draw<E>(target_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid, ring, ring_bytes, p.ctl + 3)
             : cdf_cross<E>(target_weights<E, kTopp>(p, b, jb), p.V, jb.uK, sh, tid);
-  if (tid == 0) p.out_tokens[b * (p.K + 1) + jb.j] = (int32_t)t;
+    if (jb.j == p.K) settled = sh.bi[7];
+  }
+  if (tid == 0) {
+    p.out_tokens[b * (p.K + 1) + jb.j] = (int32_t)t;
+    if (!settled) flag_draw<E>(p, b, jb);
+  }
 }
 
 // Consumer side, after the CTA's streaming is done: take tickets for queued
@@ -2102,12 +2168,8 @@ template <typename E>
 static cudaError_t launch_seq_t(const Params& p, int grid, cudaStream_t stream) {
   const size_t smem = seq_shared_bytes();
   auto* k = verify_seq_kernel<E>;
-  static bool raised = false;
-  if (!raised) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    raised = true;
-  }
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k), smem);
+  if (e != cudaSuccess) return e;
   return launch_pdl(k, grid, kSeqThreads, smem, stream, p);
 }
 
@@ -2416,14 +2478,8 @@ template <typename E, int MODE>
 static cudaError_t launch_t(const Params& p, int grid, cudaStream_t stream) {
   const size_t smem = shared_bytes(p.stages);
   auto* k = verify_kernel<E, MODE>;
-  // Raise the dynamic shared-memory limit once per size (not a stream
-  // operation, but kept out of later calls so they can be graph-captured).
-  static size_t raised = 0;
-  if (smem > raised) {
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(shared_bytes(kMaxStages)));
-    if (e != cudaSuccess) return e;
-    raised = shared_bytes(kMaxStages);
-  }
+  cudaError_t e = raise_smem_limit(reinterpret_cast<const void*>(k), shared_bytes(kMaxStages));
+  if (e != cudaSuccess) return e;
   return launch_pdl(k, grid, kAllThreads, smem, stream, p);
 }
 

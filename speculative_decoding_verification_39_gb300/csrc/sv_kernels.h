@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "sv_refine.h"
+
 namespace sv {
 
 enum Mode { kSample = 0, kArgmaxLimit = 1, kGreedy = 2 };
@@ -61,6 +63,10 @@ struct Params {
   int CPC;
   float* dcells;           // [B][kMaxCells] cell sums
   uint32_t* dcnt;          // [B] chunks done
+  // Draws the fp32 walk cannot settle go to the refine kernel's list (null:
+  // the greedy modes, which draw nothing).
+  uint32_t* rf_ctl;
+  rf::Rec* rf_recs;
 };
 
 size_t shared_bytes(int stages);

@@ -1,0 +1,62 @@
+// sv_refine.h — the draws that fp32 cannot settle, redone in double-float
+// arithmetic over the whole GPU (sv_refine.cu). Not part of the public ABI.
+//
+// A sampling draw finds the smallest t with sum_{v<=t} w_v > u*Z in fp32.
+// When u*Z lands within kRefineMargin*Z of an edge of the chosen token's CDF
+// interval (or the weights sum to zero, or the walk meets rounding), the draw
+// kernel appends a record here; the refine kernel, launched after it on the
+// same stream, recomputes those draws with double-float weights and sums and
+// overwrites their tokens.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+namespace rf {
+
+// fp32 draws closer than this (times Z) to a CDF edge are redone.
+constexpr float kRefineMargin = 3e-8f;
+// Flagged draws handled together in one pass of the refine kernel.
+constexpr int kMaxBatch = 64;
+constexpr int kThreads = 256;
+
+// One flagged draw: sequence b drew position j from target row (b, j)
+// (minus draft row (b, j) after a rejection) with uniform u; M are the
+// rows' largest raw logits; tau the nucleus cut (stored logit value, -inf
+// without top-p).
+struct Rec {
+  int32_t b, j, resid, pad;
+  float mp, mq, taup, tauq, u;
+  float pad2[3];
+};
+
+// Control words of the refine kernel, zero between calls: [0] flagged
+// draws, [1] grid-barrier arrivals, [2] CTAs finished, [3] abort.
+constexpr int kCtlWords = 4;
+
+struct Params {
+  const char* target;  // [B,K+1,V]
+  const char* draft;   // [B,K,V]
+  int64_t B, V;
+  int K, esz;
+  float c_hi, c_lo;    // log2(e)/T as a double-float
+  float tab_hi[32], tab_lo[32];
+  uint32_t* ctl;       // kCtlWords words
+  uint32_t* status;    // sticky status word of the call's scratch
+  Rec* recs;           // [B]
+  float* part;         // [kMaxBatch][grid][8]
+  int32_t* out_tokens; // [B, K+1]
+};
+
+// Appends a flagged draw (device side; any thread).
+__device__ __forceinline__ void flag(uint32_t* ctl, Rec* recs, int64_t B, const Rec& r) {
+  const uint32_t slot = atomicAdd(ctl, 1u);
+  if (slot < (uint32_t)B) recs[slot] = r;
+}
+
+size_t part_bytes(int grid);
+void fill_table(Params& p, float temperature);
+cudaError_t launch(const Params& p, int grid, cudaStream_t stream);
+
+}  // namespace rf
+}  // namespace sv

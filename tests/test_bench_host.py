@@ -61,6 +61,26 @@ def test_reference_arm_prints_one_contract_line():
 def test_config_names():
     assert bench.config_names("cfg2_v32000_bf16") == ["cfg2_v32000_bf16"]
     assert bench.config_names("cfg1_v1000_f32, la_sample_v32000_bf16") == ["cfg1_v1000_f32", "la_sample_v32000_bf16"]
-    assert bench.config_names("all")[:5] == list(sg.CONFIGS)
+    every = list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS)
+    # the headline workload (the largest) first, then every other one, each once
+    for spec in ("all", None):
+        names = bench.config_names(spec)
+        assert names[0] == "cfg3_v128256_bf16" and sorted(names) == sorted(every)
     with pytest.raises(KeyError):
         bench.config_names("cfg2_v32000_bf16,nope")
+
+
+def test_launched_kernel_follows_the_library_rule():
+    class A:
+        sample_path = 0
+        greedy_path = 0
+    for name, kernel in (("cfg1_v1000_f32", "rows_kernel"), ("cfg3_v128256_bf16", "rows_kernel"),
+                         ("cfg5_topp_v151936_bf16", "verify_kernel"), ("cfg4_greedy_v32000_bf16", "gr_rows_kernel"),
+                         ("la_sample_v32000_bf16", "la_rows_kernel"), ("md_sample_v32000_bf16", "md_rows_kernel")):
+        cfg, mode = bench.workload(name)[:2]
+        assert bench.launched_kernel(cfg, mode, A) == kernel, name
+    A.sample_path = A.greedy_path = 1
+    cfg, mode = bench.workload("cfg1_v1000_f32")[:2]
+    assert bench.launched_kernel(cfg, mode, A) == "verify_warp_kernel"
+    cfg, mode = bench.workload("cfg4_greedy_v32000_bf16")[:2]
+    assert bench.launched_kernel(cfg, mode, A) == "verify_kernel"

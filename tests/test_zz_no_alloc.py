@@ -1,9 +1,10 @@
 """sv_verify_sample_noalloc: the sampling-mode verify for callers that cannot
 allocate device memory (code inside a memory pool or arena that accounts for
 every byte, allocator hooks that must not recurse into cudaMalloc, services
-that reserve all device memory at start-up). It runs the same kernel as
-sv_verify_sample on a fixed scratch array inside the library, so it must give
-the same results. Both entry points are called through the C ABI.
+that reserve all device memory at start-up). It runs the same kernels as
+sv_verify_sample, chosen by the same rule, on a fixed scratch array inside the
+library, so it must give the same results; it is also checked against the
+oracle directly. Both entry points are called through the C ABI.
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.
@@ -14,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import specgen as sg
 import speculative_decoding_verification_39_gb300 as svpkg
 
@@ -43,12 +45,24 @@ def _call(fn, d, cfg, stream):
     return tokens, acc, stats
 
 
-@pytest.mark.parametrize("name", ["cfg2_v32000_bf16", "cfg5_topp_v151936_bf16"])
+CASES = {
+    # the row pass + cluster decide kernels
+    "cfg2_v20011": sg.CONFIGS["cfg2_v32000_bf16"].with_(B=12, V=20011),
+    # short fp32 rows (a group of rows per CTA in the row pass)
+    "cfg1_v1000_f32": sg.CONFIGS["cfg1_v1000_f32"].with_(B=300),
+    # top-p: the streaming kernel
+    "cfg5_topp_v20011": sg.CONFIGS["cfg5_topp_v151936_bf16"].with_(B=12, V=20011),
+    # T = 0, the greedy limit: the streaming kernel's argmax mode
+    "cfg2_greedy_limit": sg.CONFIGS["cfg2_v32000_bf16"].with_(B=12, V=20011, temperature=0.0),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
 def test_noalloc_matches_sample_on_two_calls(name):
     svpkg.build()
     lib = svpkg.lib()
     torch.cuda.set_device(0)
-    cfg = sg.CONFIGS[name].with_(B=12, V=20011)
+    cfg = CASES[name]
     host = sg.sample_inputs(cfg)
     d = {k: _dev(v) for k, v in host.items()}
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
@@ -63,6 +77,13 @@ def test_noalloc_matches_sample_on_two_calls(name):
         np.testing.assert_array_equal(ga, ra)
         np.testing.assert_array_equal(gt, rt)
         np.testing.assert_allclose(gs, rs, rtol=1e-5, atol=1e-5)
+    # and against the oracle: identical except at near-ties (margin < 1e-6)
+    ot, oa, margin = oracle.verify_sample(host["target"], host["draft"], host["draft_tokens"], host["uniforms"],
+                                          cfg.temperature, cfg.top_p)
+    gt, ga = second[0].cpu().numpy(), second[1].cpu().numpy()
+    diff = (ga != oa) | (gt != ot).any(1)
+    assert not (diff & (margin >= 1e-6)).any(), np.nonzero(diff)[0]
+    assert diff.sum() <= 1
 
 
 def test_noalloc_rejects_a_call_beyond_its_scratch():
