@@ -259,9 +259,15 @@ def launched_kernel(cfg, mode, args) -> str:
         return "la_rows_kernel"
     if mode == "multidraft":
         return "md_rows_kernel"
-    if (args.sample_path == 0 and cfg.temperature > 0 and cfg.top_p == 1.0 and cfg.K <= 1024
-            and cfg.V <= 1048576):
+    esz = 2 if cfg.dtype == sg.BF16 else 4
+    small = cfg.B * (2 * cfg.K + 1) * cfg.V * esz <= 96 * 1024 * 1024
+    rows = 2 * cfg.K + 1
+    warp_rows = cfg.V <= 1024 and (cfg.V * esz) % 16 == 0 and rows <= 64 and rows * cfg.V * esz <= 65536
+    if (cfg.temperature > 0 and cfg.top_p == 1.0 and cfg.K <= 1024 and cfg.V <= 1048576
+            and (args.sample_path == 2 or (args.sample_path == 0 and small and not warp_rows))):
         return "rows_kernel"
+    if args.sample_path == 0 and cfg.temperature > 0 and cfg.top_p == 1.0 and not warp_rows:
+        return KERNEL
     return kernel_for(cfg, mode)
 
 
@@ -419,6 +425,8 @@ def measure(args, name: str, rank: int, world: int, steps: int, cpu_budget: floa
         if svpkg.get_status() != 0:
             raise RuntimeError("device status set during warm-up")
     breaker = torch.zeros(1, dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        refined0 = svpkg.refined_draws()
 
     def capture(n, idx0, with_breaker=False, only_breaker=False):
         g = torch.cuda.CUDAGraph()
@@ -470,6 +478,7 @@ def measure(args, name: str, rank: int, world: int, steps: int, cpu_budget: floa
         ms_brk = min(timed([g_brk]) for _ in range(3))
     with torch.cuda.stream(stream):
         status = svpkg.get_status()
+        refined = svpkg.refined_draws() - refined0
     if status != 0:
         raise RuntimeError(f"device status {status} after the timed region")
     ms = max_over_ranks(ms, dev)
@@ -513,6 +522,10 @@ def measure(args, name: str, rank: int, world: int, steps: int, cpu_budget: floa
         "e2e": {"value": positions * world / e2e_s, "unit": "positions/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": out_bytes},
         "gpu_launches": int(captured),
+        "refined_draws_per_call": refined / max(1, steps + 2 * n_iso + 50),
+        "refined_note": "draws redone in double-float because the fp32 walk landed within 1e-7*Z of a CDF edge, "
+                        "per call, over every call of the timed graphs and the isolated runs (the pre-roll "
+                        "replays are counted too, so this is an estimate)",
     }
     nth = os.cpu_count() or 1
     if counts and rank == 0:
@@ -651,9 +664,9 @@ def main():
                     help="override the workload's batch size (--batch 1: per-call latency of one sequence)")
     ap.add_argument("--greedy-path", type=int, default=0, choices=[0, 1],
                     help="greedy verify kernels: 0 row argmax + match kernels, 1 the streaming kernel")
-    ap.add_argument("--sample-path", type=int, default=0, choices=[0, 1],
-                    help="sampling verify kernels: 0 the row pass + cluster decide kernel where they fit, 1 the "
-                         "streaming kernel")
+    ap.add_argument("--sample-path", type=int, default=0, choices=[0, 1, 2],
+                    help="sampling verify kernels: 0 by the library's size rule, 1 the streaming kernel, 2 the row "
+                         "pass + cluster decide kernel wherever they fit")
     ap.add_argument("--l2-resident", action="store_true",
                     help="replay one input set, so that inputs that fit stay in L2 (reported as such; not an "
                          "HBM figure)")

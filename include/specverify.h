@@ -188,6 +188,33 @@ int sv_verify_multidraft_sample(const void* target, const void* draft, const int
                                 int32_t* out_best_cand, float* out_row_lse, void* stream);
 
 /*
+ * Sampling-mode verify on hidden states: the target's and the draft's logits
+ * are computed here from their last hidden states and LM heads, on the
+ * tensor cores, then verified exactly as sv_verify_sample verifies logits.
+ * The pages take the logits as given ("Speculative Decoding —— LLM推理优化技术
+ * （一）" §2.1-2.3, §4: p = softmax(target logits / T), q likewise); this entry
+ * point produces them as logits = h · Wᵀ.
+ *
+ *   h_target [B, K+1, D] bf16, h_draft [B, K, D] bf16: the hidden states at
+ *            the positions whose logits sv_verify_sample would take.
+ *   w_target, w_draft [V, D] bf16: the two LM heads (row v is vocabulary
+ *            entry v).
+ *   D a multiple of 64; the four arrays 16-byte aligned.
+ *   draft_tokens, uniforms, B, K, V, temperature (> 0), top_p, out_tokens,
+ *   out_accept_len: as for sv_verify_sample.
+ *   out_logits nullable [B*(K+1) + B*K, V] fp32: where to put the logits
+ *            (target rows, then draft rows); without it the library keeps a
+ *            workspace per (device, stream), freed by sv_release().
+ * The products of bf16 values are exact in fp32 and the sums are fp32: the
+ * logits equal h · Wᵀ up to fp32 summation rounding. Three kernels run on
+ * `stream`: the GEMM, then the verify's.
+ */
+int sv_verify_sample_lmhead(const void* h_target, const void* h_draft, const void* w_target, const void* w_draft,
+                            const int32_t* draft_tokens, const float* uniforms, int64_t B, int32_t K, int64_t D,
+                            int64_t V, float temperature, float top_p, int32_t* out_tokens, int32_t* out_accept_len,
+                            float* out_logits, void* stream);
+
+/*
  * N-gram pool of Lookahead decoding ("Lookahead Decoding 完全拆解", section
  * "N-gram 池与身份判定"; W new n-grams per step from the section on the 2D
  * window; at most G candidates, GUESS_SET_SIZE, in the engineering section).
@@ -287,6 +314,12 @@ int sv_get_status(void* stream);
  */
 int sv_selftest_wait_timeout(int64_t limit_ns, void* stream);
 
+/* Synchronises `stream` and returns how many sampling draws on that stream's
+ * scratch area were redone in double-float arithmetic so far (the fp32 walk
+ * found u*Z within 1e-7*Z of an edge of the token's CDF interval); -1 on a
+ * CUDA error. For monitoring; the pages have no counterpart. */
+int64_t sv_refined_draws(void* stream);
+
 /* A static, human-readable name for an sv_status value. */
 const char* sv_status_string(int status);
 
@@ -306,10 +339,16 @@ uint64_t sv_launch_count(void);
  * streaming kernel. Applies to calls made after it. */
 int sv_set_greedy_path(int32_t path);
 
-/* Which kernels sv_verify_sample uses, for comparing them: 0 (default) the
- * row pass and the cluster decide kernel whenever T > 0, top_p = 1,
- * K <= 1024 and V <= 1048576 (the streaming kernel otherwise); 1 always the
- * streaming kernel. Applies to calls made after it. */
+/* Which kernels sv_verify_sample uses, for comparing them. 0 (default):
+ * with T > 0 and top_p = 1, rows of at most 1024 elements go to the
+ * streaming kernel's one-warp-per-sequence mode; calls whose logits are at
+ * most 96 MiB (so that the second look at the draw rows hits L2) to the row
+ * pass and the cluster decide kernel; everything else (larger calls, top-p,
+ * T = 0) to the streaming kernel. 1: always the streaming kernel, including
+ * its sequence-in-shared-memory mode (whose draws are not handed to the
+ * refine kernel). 2: the row pass and decide kernel wherever they fit
+ * (T > 0, top_p = 1, K <= 1024, V <= 1048576). Applies to calls made after
+ * it. */
 int sv_set_sample_path(int32_t path);
 
 #ifdef __cplusplus

@@ -27,10 +27,10 @@ _CSRC = os.path.join(_HERE, "csrc")
 _INCLUDE = os.path.join(os.path.dirname(_HERE), "include")
 _SO = os.path.join(_HERE, "libspecverify.so")
 _SOURCES = ["sv_kernels.cu", "sv_api.cu", "sv_noalloc.cu", "sv_lookahead.cu", "sv_multidraft.cu",
-            "sv_greedy_rows.cu", "sv_rows.cu", "sv_decide.cu", "sv_ngram.cu", "sv_refine.cu"]
+            "sv_greedy_rows.cu", "sv_rows.cu", "sv_decide.cu", "sv_ngram.cu", "sv_refine.cu", "sv_lmhead.cu"]
 _DEPS = _SOURCES + ["sv_kernels.h", "sv_device.cuh", "sv_lookahead.h", "sv_multidraft.h", "sv_rowstat.cuh",
                     "sv_greedy_rows.h", "sv_v2.h", "sv_df.cuh", "sv_sample_impl.h",
-                    "sv_refine.h"]
+                    "sv_refine.h", "sv_lmhead.h"]
 
 SV_F32, SV_BF16 = 0, 1
 STATUS = {0: "SV_OK", -1: "SV_ERR_ARG", -2: "SV_ERR_DTYPE", -3: "SV_ERR_CUDA", -4: "SV_ERR_INPUT",
@@ -123,6 +123,10 @@ def lib():
         h.sv_set_greedy_path.restype = ctypes.c_int
         h.sv_set_sample_path.argtypes = [i32]
         h.sv_set_sample_path.restype = ctypes.c_int
+        h.sv_verify_sample_lmhead.argtypes = [vp, vp, vp, vp, vp, vp, i64, i32, i64, i64, f32, f32, vp, vp, vp, vp]
+        h.sv_verify_sample_lmhead.restype = ctypes.c_int
+        h.sv_refined_draws.argtypes = [vp]
+        h.sv_refined_draws.restype = ctypes.c_int64
         h.sv_ngram_pool_bytes.argtypes = [i64, i64, i32, i32]
         h.sv_ngram_pool_bytes.restype = ctypes.c_int64
         h.sv_ngram_pool_reset.argtypes = [vp, i64, i64, i32, i32, vp]
@@ -140,7 +144,7 @@ def exported_symbols() -> list:
             "sv_set_launch_shape", "sv_launch_count", "sv_verify_sample_noalloc", "sv_selftest_wait_timeout",
             "sv_verify_lookahead_sample", "sv_verify_multidraft_sample", "sv_set_greedy_path",
             "sv_set_sample_path", "sv_ngram_pool_bytes", "sv_ngram_pool_reset", "sv_ngram_pool_insert",
-            "sv_ngram_pool_lookup"]
+            "sv_ngram_pool_lookup", "sv_refined_draws", "sv_verify_sample_lmhead"]
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -440,3 +444,41 @@ class NgramPool:
         if rc != 0:
             raise SpecVerifyError(rc, "sv_ngram_pool_lookup")
         return cand, count
+
+
+def refined_draws(device=None) -> int:
+    """Draws redone in double-float so far on the current stream's scratch."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    n = lib().sv_refined_draws(_stream_handle(dev))
+    if n < 0:
+        raise SpecVerifyError(-3, "sv_refined_draws")
+    return int(n)
+
+
+def verify_sample_lmhead(h_target, h_draft, w_target, w_draft, draft_tokens, uniforms, temperature: float,
+                         top_p: float = 1.0, logits: bool = False):
+    """Sampling-mode verify on hidden states (sv_verify_sample_lmhead): the
+    logits h · Wᵀ of the target (h_target [B,K+1,D], w_target [V,D]) and the
+    draft (h_draft [B,K,D], w_draft [V,D]), all bf16 on one CUDA device, then
+    the verify. Returns (out_tokens [B,K+1], out_accept_len [B]) and, with
+    ``logits``, the fp32 logits [B*(K+1) + B*K, V] (target rows first)."""
+    dev = h_target.device
+    B, K1, D = h_target.shape
+    K = K1 - 1
+    V = w_target.shape[0]
+    for t, name in ((h_target, "h_target"), (h_draft, "h_draft"), (w_target, "w_target"), (w_draft, "w_draft")):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or t.device != dev:
+            raise TypeError(f"{name} must be a contiguous bfloat16 tensor on {dev}")
+    _check(h_draft, (B, K, D), None, "h_draft")
+    _check(w_draft, (V, D), None, "w_draft")
+    x = _on_device(draft_tokens, dev, "draft_tokens")
+    u = _on_device(uniforms, dev, "uniforms")
+    out_t = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    out_a = torch.empty((B,), dtype=torch.int32, device=dev)
+    lg = torch.empty((B * (K + 1) + B * K, V), dtype=torch.float32, device=dev) if logits else None
+    rc = lib().sv_verify_sample_lmhead(_ptr(h_target), _ptr(h_draft), _ptr(w_target), _ptr(w_draft), _ptr(x), _ptr(u),
+                                       B, K, D, V, float(temperature), float(top_p), _ptr(out_t), _ptr(out_a),
+                                       _ptr(lg), _stream_handle(dev))
+    if rc != 0:
+        raise SpecVerifyError(rc, "sv_verify_sample_lmhead")
+    return (out_t, out_a, lg) if logits else (out_t, out_a)

@@ -11,6 +11,7 @@
 
 #include "../../include/specverify.h"
 #include "sv_kernels.h"
+#include "sv_lmhead.h"
 #include "sv_greedy_rows.h"
 #include "sv_lookahead.h"
 #include "sv_multidraft.h"
@@ -28,7 +29,7 @@ std::atomic<int> g_stages{kDefaultStages};
 std::atomic<int> g_ctas_per_sm{kDefaultCtasPerSm};
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_greedy_path{0};  // 0: row argmax + match kernels; 1: the streaming kernel
-std::atomic<int> g_sample_path{0};  // 0: row pass + cluster decide where it fits; 1: the streaming kernel
+std::atomic<int> g_sample_path{0};  // 0: by size; 1: the streaming kernel; 2: row pass + cluster decide
 
 // A scratch area has three parts at fixed places: the control block, a
 // counter region and a data region. Every counter is back at zero when a call
@@ -45,9 +46,15 @@ struct Scratch {
 
 std::mutex g_mu;
 std::map<std::pair<int, uintptr_t>, Scratch> g_scratch;
+// The fp32 logits of sv_verify_sample_lmhead when the caller gives no buffer:
+// one workspace per (device, stream), grown on demand, freed by sv_release.
+std::map<std::pair<int, uintptr_t>, std::pair<void*, size_t>> g_lm_ws;
 std::map<int, int> g_sm_count;
 
 constexpr size_t kCtlBytes = 256;
+// Word of the control block that counts the draws the refine kernel redid
+// (cumulative per scratch area; word 3 is the sticky status).
+constexpr int kCtlRefined = 12;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -110,6 +117,7 @@ int launch_refine(const void* target, const void* draft, int64_t B, int K, int64
   sv::rf::fill_table(r, temperature);
   r.ctl = rf_ctl;
   r.status = status;
+  r.stats = status + (kCtlRefined - 3);
   r.recs = recs;
   r.part = part;
   r.out_tokens = out_tokens;
@@ -118,7 +126,8 @@ int launch_refine(const void* target, const void* draft, int64_t B, int K, int64
   return SV_OK;
 }
 
-int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t stream, sv::ScratchGet get, void* ctx) {
+int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t stream, sv::ScratchGet get, void* ctx,
+        bool allow_seq = true) {
   const int esz = dtype == SV_BF16 ? 2 : 4;
   p.TE = sv::kTileBytes / esz;
   p.NT = (p.V + p.TE - 1) / p.TE;
@@ -186,7 +195,7 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   // one CTA per sequence with the whole sequence staged in shared memory.
   const bool short_ok = mode == sv::kSample && !p.topp && aligned_to(p.a, 16) && aligned_to(p.d, 16);
   const bool warp_mode = short_ok && sv::warp_mode_fits(p.K, p.V, esz);
-  const bool seq_mode = short_ok && !warp_mode && sv::seq_mode_fits(p.K, p.V, esz);
+  const bool seq_mode = allow_seq && short_ok && !warp_mode && sv::seq_mode_fits(p.K, p.V, esz);
   int64_t grid = slots;
   const int64_t items = warp_mode ? (p.B + sv::warp_mode_seqs_per_cta() - 1) / sv::warp_mode_seqs_per_cta()
                                   : (seq_mode ? p.B : p.W);
@@ -236,7 +245,18 @@ int sv::verify_sample_impl(const void* target_logits, const void* draft_logits, 
     return SV_ERR_ARG;
   const float c = limit ? 0.f : (float)(1.4426950408889634 / (double)temperature);
   if (!limit && !std::isfinite(c)) return SV_ERR_ARG;
-  if (!limit && top_p == 1.f && g_sample_path.load() == 0 && sv::v2::fits(K, V)) {
+  // The row pass + cluster decide kernels re-read the draw rows after the
+  // whole call has streamed: cheap while the call's logits stay in L2 (the
+  // streaming kernel draws each sequence as soon as its rows are in, which
+  // wins for larger calls).
+  // Rows of at most 1024 elements go to the streaming kernel's one-warp-per-
+  // sequence mode, which reads a whole sequence with one round of loads.
+  const bool two_kernel_size = (double)B * (2.0 * K + 1.0) * (double)V * (double)esz <= 96.0 * 1024 * 1024;
+  const bool warp_rows = sv::warp_mode_fits(K, V, (int)esz) && aligned_to(target_logits, 16) &&
+                         aligned_to(draft_logits, 16);
+  const int path = g_sample_path.load();
+  if (!limit && top_p == 1.f && sv::v2::fits(K, V) &&
+      (path == 2 || (path == 0 && two_kernel_size && !warp_rows))) {
     sv::v2::Params q{};
     q.target = static_cast<const char*>(target_logits);
     q.draft = static_cast<const char*>(draft_logits);
@@ -293,7 +313,8 @@ int sv::verify_sample_impl(const void* target_logits, const void* draft_logits, 
   p.T = temperature;
   p.top_p = top_p;
   p.topp = (!limit && top_p < 1.f) ? 1 : 0;
-  return run(p, dtype, limit ? sv::kArgmaxLimit : sv::kSample, B * (int64_t)p.RS, st, get, ctx);
+  // the sequence-in-shared-memory mode has no refine hand-off: only on request
+  return run(p, dtype, limit ? sv::kArgmaxLimit : sv::kSample, B * (int64_t)p.RS, st, get, ctx, path == 1);
 }
 
 extern "C" int sv_verify_sample(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
@@ -524,6 +545,13 @@ extern "C" int sv_release(void) {
     if (cudaFree(kv.second.base) != cudaSuccess) rc = SV_ERR_CUDA;
   }
   g_scratch.clear();
+  for (auto& kv : g_lm_ws) {
+    if (!kv.second.first) continue;
+    cudaSetDevice(kv.first.first);
+    cudaDeviceSynchronize();
+    if (cudaFree(kv.second.first) != cudaSuccess) rc = SV_ERR_CUDA;
+  }
+  g_lm_ws.clear();
   cudaSetDevice(cur);
   return rc;
 }
@@ -544,7 +572,99 @@ extern "C" int sv_set_greedy_path(int32_t path) {
 }
 
 extern "C" int sv_set_sample_path(int32_t path) {
-  if (path < 0 || path > 1) return SV_ERR_ARG;
+  if (path < 0 || path > 2) return SV_ERR_ARG;
   g_sample_path.store(path);
   return SV_OK;
+}
+
+extern "C" int64_t sv_refined_draws(void* stream) {
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return -1;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  Scratch sc;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_scratch.find({dev, reinterpret_cast<uintptr_t>(s)});
+    if (it == g_scratch.end()) return 0;
+    sc = it->second;
+  }
+  uint32_t n = 0;
+  if (cudaMemcpy(&n, static_cast<char*>(sc.base) + 4 * kCtlRefined, 4, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return -1;
+  return (int64_t)n;
+}
+
+namespace {
+
+
+int lm_workspace(cudaStream_t stream, size_t bytes, void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto& w = g_lm_ws[{dev, reinterpret_cast<uintptr_t>(stream)}];
+  if (w.second < bytes) {
+    if (w.first) {
+      cudaStreamSynchronize(stream);
+      cudaFree(w.first);
+      w = {nullptr, 0};
+    }
+    void* p = nullptr;
+    if (cudaMalloc(&p, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return SV_ERR_NOMEM;
+    }
+    w = {p, bytes};
+  }
+  *out = w.first;
+  return SV_OK;
+}
+
+}  // namespace
+
+extern "C" int sv_verify_sample_lmhead(const void* h_target, const void* h_draft, const void* w_target,
+                                       const void* w_draft, const int32_t* draft_tokens, const float* uniforms,
+                                       int64_t B, int32_t K, int64_t D, int64_t V, float temperature, float top_p,
+                                       int32_t* out_tokens, int32_t* out_accept_len, float* out_logits,
+                                       void* stream) {
+  if (B < 0 || K < 1 || V < 2 || V >= kMaxV || K > (1 << 20) || !sv::lm::fits(D)) return SV_ERR_ARG;
+  if (!(temperature > 0.f) || std::isinf(temperature)) return SV_ERR_ARG;
+  if (!(top_p > 0.f && top_p <= 1.f)) return SV_ERR_ARG;
+  if (B == 0) return SV_OK;
+  if (!h_target || !h_draft || !w_target || !w_draft || !draft_tokens || !uniforms || !out_tokens ||
+      !out_accept_len)
+    return SV_ERR_ARG;
+  if (!aligned_to(h_target, 16) || !aligned_to(h_draft, 16) || !aligned_to(w_target, 16) || !aligned_to(w_draft, 16))
+    return SV_ERR_DTYPE;
+  if (out_logits && !aligned_to(out_logits, 16)) return SV_ERR_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int64_t mt = B * (K + 1), md = B * (int64_t)K;
+  float* logits = out_logits;
+  if (!logits) {
+    void* w = nullptr;
+    const int rc = lm_workspace(st, (size_t)(mt + md) * (size_t)V * sizeof(float), &w);
+    if (rc != SV_OK) return rc;
+    logits = static_cast<float*>(w);
+  }
+  // the sticky status word of this stream's scratch
+  Scratch sc;
+  int dev = 0;
+  int rc = get_scratch(st, 1, 1, &sc, &dev);
+  if (rc != SV_OK) return rc;
+  sv::lm::Params q{};
+  q.h[0] = static_cast<const uint16_t*>(h_target);
+  q.h[1] = static_cast<const uint16_t*>(h_draft);
+  q.w[0] = static_cast<const uint16_t*>(w_target);
+  q.w[1] = static_cast<const uint16_t*>(w_draft);
+  q.out[0] = logits;
+  q.out[1] = logits + mt * V;
+  q.Mrows[0] = mt;
+  q.Mrows[1] = md;
+  q.V = V;
+  q.D = D;
+  q.status = static_cast<uint32_t*>(sc.base) + 3;
+  if (sv::lm::launch(q, st) != cudaSuccess) return SV_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return sv::verify_sample_impl(q.out[0], q.out[1], draft_tokens, uniforms, B, K, V, SV_F32, temperature, top_p,
+                                out_tokens, out_accept_len, nullptr, st, cached_scratch, nullptr);
 }

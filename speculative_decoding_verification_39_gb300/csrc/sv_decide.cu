@@ -13,7 +13,7 @@
 //    unnormalised p_K for the bonus; per-cell sums; the ranks' totals are
 //    exchanged through distributed shared memory; the rank whose run holds
 //    u_K * Z finds the crossing cell and walks it. The token stands when u_K*Z
-//    is at least 3e-8 * Z from both edges of the token's CDF interval;
+//    is at least 1e-7 * Z from both edges of the token's CDF interval;
 //    otherwise (and for a residual of zero mass, or a draw past the last
 //    partial sum) the draw is appended to the refine kernel's list, which
 //    redoes it in double-float arithmetic (sv_refine.cu).
@@ -28,6 +28,7 @@
 #include <utility>
 
 #include "sv_device.cuh"
+#include "sv_df.cuh"
 #include "sv_refine.h"
 #include "sv_v2.h"
 
@@ -177,12 +178,23 @@ struct FastW {
   }
 };
 
+__device__ __forceinline__ df warp_incl_scan_df(df v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    df t;
+    t.h = __shfl_up_sync(0xffffffffu, v.h, o);
+    t.l = __shfl_up_sync(0xffffffffu, v.l, o);
+    if (lane >= o) v = df_add(v, t);
+  }
+  return v;
+}
+
 // Per-CTA state of the decide kernel. The arrays sized by K and by the
 // cells per rank live in dynamic shared memory (see Layout); this part is
 // fixed.
 struct Smem {
   // exchanged through distributed shared memory
-  float x_tot;              // this rank's total weight
+  float x_tot_h, x_tot_l;   // this rank's total weight (double-float)
   int res_tok, res_precise; // on rank 0: the token and whether to redo the draw
   int bad, j;
   uint64_t slice_bar;       // the slice copies of the draw rows landed
@@ -411,47 +423,63 @@ __global__ void __launch_bounds__(kDecideThreads, 3) decide_kernel(const Params 
   fw.resid = x.resid;
   if (!bad) fast_cells<E>(fw, x, L, warp, lane);
   __syncthreads();
-  if (warp == 0) {  // inclusive prefix of this rank's cells; its total
-    float carry = 0.f;
+  if (warp == 0) {
+    // inclusive prefix of this rank's cells and its total, in double-float:
+    // the running sums reach the size of Z, where fp32 would round at ~6e-8*Z
+    df carry{0.f, 0.f};
     for (int c0 = 0; c0 < ce - cb; c0 += 32) {
-      const float v = c0 + lane < ce - cb ? L.cs_h[c0 + lane] : 0.f;
-      const float incl = carry + warp_incl_scan(v, lane);
-      if (c0 + lane < ce - cb) L.cp_h[c0 + lane] = incl;
-      carry = __shfl_sync(0xffffffffu, incl, 31);
+      const bool in = c0 + lane < ce - cb;
+      const df v{in ? L.cs_h[c0 + lane] : 0.f, 0.f};
+      const df incl = df_add(carry, warp_incl_scan_df(v, lane));
+      if (in) {
+        L.cp_h[c0 + lane] = incl.h;
+        L.cp_l[c0 + lane] = incl.l;
+      }
+      carry.h = __shfl_sync(0xffffffffu, incl.h, 31);
+      carry.l = __shfl_sync(0xffffffffu, incl.l, 31);
     }
-    if (lane == 0) sm.x_tot = carry;
+    if (lane == 0) {
+      sm.x_tot_h = carry.h;
+      sm.x_tot_l = carry.l;
+    }
   }
   __syncthreads();
   cluster_sync();  // (1) rank totals visible
   if (warp == 0 && !bad) {
     // The ranks' running sums, in rank order, identical in every CTA.
-    float P = 0.f, Pme = 0.f;
-    for (int q = 0; q < D; ++q) {
-      const float tq = dsmem_ld_f32(&sm.x_tot, q);
-      if (q == (int)rank) Pme = P;
-      P = P + tq;
-    }
-    const float Z = P;
-    const float target = x.u * Z;
+    df P{0.f, 0.f}, Pme{0.f, 0.f};
     int owner = -1;
-    P = 0.f;
+    df tots[kMaxCluster];
     for (int q = 0; q < D; ++q) {
-      P = P + dsmem_ld_f32(&sm.x_tot, q);
-      if (owner < 0 && P > target) owner = q;
+      tots[q] = df{dsmem_ld_f32(&sm.x_tot_h, q), dsmem_ld_f32(&sm.x_tot_l, q)};
+      P = df_add(P, tots[q]);
     }
-    const bool need_precise_all = !(Z > 0.f) || owner < 0;
+    const df Z = P;
+    const df target = df_mul_f(Z, x.u);
+    P = df{0.f, 0.f};
+    for (int q = 0; q < D; ++q) {
+      if (q == (int)rank) Pme = P;
+      P = df_add(P, tots[q]);
+      if (owner < 0 && df_gt(P, target)) owner = q;
+    }
+    const bool need_precise_all = !df_pos(Z) || owner < 0;
     if ((int)rank == owner && !need_precise_all) {
       // the crossing cell: the first whose inclusive sum exceeds the target
       int cc = -1;
       for (int c0 = 0; c0 < ce - cb && cc < 0; c0 += 32) {
-        const bool hit = c0 + lane < ce - cb && Pme + L.cp_h[c0 + lane] > target;
+        const bool hit =
+            c0 + lane < ce - cb && df_gt(df_add(Pme, df{L.cp_h[c0 + lane], L.cp_l[c0 + lane]}), target);
         const uint32_t m = __ballot_sync(0xffffffffu, hit);
         if (m) cc = c0 + __ffs(m) - 1;
       }
       int tok = -1;
       bool precise = true;
       if (cc >= 0) {
-        const float base = Pme + (cc > 0 ? L.cp_h[cc - 1] : 0.f);
+        // what is left of the target inside the crossing cell, exactly enough
+        // in fp32 (it is below the cell's sum)
+        const df base = cc > 0 ? df_add(Pme, df{L.cp_h[cc - 1], L.cp_l[cc - 1]}) : Pme;
+        const df rem = df_sub(target, base);
+        const float Rm = rem.h + rem.l;
         const int64_t e = (int64_t)(cb + cc) * kCellElems + lane * 8;
         float lp[8], lq[8], w[8];
         load8<E>(x.prow, e, V, lp);
@@ -460,17 +488,17 @@ __global__ void __launch_bounds__(kDecideThreads, 3) decide_kernel(const Params 
         for (int k = 0; k < 8; ++k) w[k] = fw.w(lp[k], fw.resid ? lq[k] : 0.f);
         const float s = ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
         const float incl = warp_incl_scan(s, lane);
-        const uint32_t m = __ballot_sync(0xffffffffu, base + incl > target);
+        const uint32_t m = __ballot_sync(0xffffffffu, incl > Rm);
         int found = 0;
         float margin = 0.f;
         if (m && lane == __ffs(m) - 1) {
-          float C = base + (incl - s);
+          float C = incl - s;
           for (int k = 0; k < 8; ++k) {
             const float prev = C;
             C = C + w[k];
-            if (C > target) {
+            if (C > Rm) {
               tok = (int)(e + k);
-              margin = fminf(C - target, target - prev);
+              margin = fminf(C - Rm, Rm - prev);
               found = 1;
               break;
             }
@@ -481,7 +509,7 @@ __global__ void __launch_bounds__(kDecideThreads, 3) decide_kernel(const Params 
           const int src = __ffs(fm) - 1;
           tok = __shfl_sync(0xffffffffu, tok, src);
           margin = __shfl_sync(0xffffffffu, margin, src);
-          precise = !(margin >= rf::kRefineMargin * Z);
+          precise = !(margin >= rf::kRefineMargin * Z.h);
         }
       }
       if (lane == 0) {

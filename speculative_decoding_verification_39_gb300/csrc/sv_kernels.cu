@@ -31,6 +31,7 @@
 //           = min(1, 2^(a_p - a_q) * cum_q / cum_p),  a = fma(l_x, c, -Mc).
 #include "sv_device.cuh"
 #include "sv_kernels.h"
+#include "sv_df.cuh"
 #include "sv_refine.h"
 
 #include <cfloat>
@@ -650,33 +651,50 @@ __device__ int64_t cdf_cross(const WF& wf, int64_t V, float u, Shared& sh, int t
   const int64_t m = CE / 256;
   const int ncells = (int)((V + CE - 1) / CE);
   if (warp == 0) {
+    // The running sums over the cells are carried in double-float: they reach
+    // the size of Z, where fp32 would round at ~6e-8*Z.
     const int cpl = (ncells + 31) / 32;
     const int c0 = min(ncells, lane * cpl), c1 = min(ncells, c0 + cpl);
-    float ls = 0.f;
-    for (int cc = c0; cc < c1; ++cc) ls += sh.cells[cc];
-    const float incl = warp_incl_scan(ls, lane);
-    const float Z = __shfl_sync(0xffffffffu, incl, 31);
+    df ls{0.f, 0.f};
+    for (int cc = c0; cc < c1; ++cc) ls = df_add(ls, df{sh.cells[cc], 0.f});
+    df incl = ls;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      df t2;
+      t2.h = __shfl_up_sync(0xffffffffu, incl.h, o);
+      t2.l = __shfl_up_sync(0xffffffffu, incl.l, o);
+      if (lane >= o) incl = df_add(incl, t2);
+    }
+    df Zd;
+    Zd.h = __shfl_sync(0xffffffffu, incl.h, 31);
+    Zd.l = __shfl_sync(0xffffffffu, incl.l, 31);
+    const float Z = Zd.h;
     int64_t t = -1;
     int settled = 0;  // the fp32 walk found the token clear of its interval's edges
     if (Z > 0.f) {
-      const float Tg = u * Z;
-      float run = incl - ls;
+      const df Tg = df_mul_f(Zd, u);
+      df run = df_sub(incl, ls);
       int hit = -1;
       for (int cc = c0; cc < c1; ++cc) {
-        if (run + sh.cells[cc] > Tg) {
+        const df nr = df_add(run, df{sh.cells[cc], 0.f});
+        if (df_gt(nr, Tg)) {
           hit = cc;
           break;
         }
-        run += sh.cells[cc];
+        run = nr;
       }
       const unsigned bal = __ballot_sync(0xffffffffu, hit >= 0);
       int cstar;
-      float Tl = 0.f;
+      float Tl = 0.f;  // what is left of the target inside the crossing cell
       bool last_positive = false;
       if (bal) {
         const int fl = __ffs(bal) - 1;
         cstar = __shfl_sync(0xffffffffu, hit, fl);
-        Tl = Tg - __shfl_sync(0xffffffffu, run, fl);
+        df rn;
+        rn.h = __shfl_sync(0xffffffffu, run.h, fl);
+        rn.l = __shfl_sync(0xffffffffu, run.l, fl);
+        const df rem = df_sub(Tg, rn);
+        Tl = rem.h + rem.l;
       } else {  // u*Z at or past the total after rounding: the last positive weight
         int last = -1;
         for (int cc = c0; cc < c1; ++cc)
@@ -2251,7 +2269,7 @@ __device__ __forceinline__ void warp_rows_ms(const char* row0, const char* row1,
 // group's elements are read again.
 template <typename E, bool kRes>
 __device__ int64_t warp_draw(const char* rp, const char* rq, int64_t V, float c, float nMcp, float nMcq, float ip,
-                             float iq, float u, int lane) {
+                             float iq, float u, int lane, int& settled) {
   constexpr int PV = ET<E>::kPerVec;
   constexpr int kMaxG = (int)(kWarpMaxV / 4 / 32);  // groups per lane
   const int ng = (int)(V / PV);
@@ -2300,40 +2318,70 @@ __device__ int64_t warp_draw(const char* rp, const char* rq, int64_t V, float c,
     for (int k = 0; k < PV; ++k)
       if (w[k] > 0.f) lastpos = (int64_t)(i * 32 + lane) * PV + k;
   }
-  const float Z = warp_sum(zl);
+  // the running sums in double-float: they reach the size of Z, where fp32
+  // would round at ~6e-8*Z
+  df Zd{zl, 0.f};
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    df t2;
+    t2.h = __shfl_xor_sync(0xffffffffu, Zd.h, o);
+    t2.l = __shfl_xor_sync(0xffffffffu, Zd.l, o);
+    Zd = df_add(Zd, t2);
+  }
+  const float Z = Zd.h;
+  settled = 0;
   if (!(Z > 0.f)) return -1;
-  const float Tg = u * Z;
-  float run = 0.f, before = 0.f;
+  const df Tg = df_mul_f(Zd, u);
+  df run{0.f, 0.f}, before{0.f, 0.f};
   int gstar = -1;  // the group holding the crossing, and the sum before it
 #pragma unroll
   for (int i = 0; i < kMaxG; ++i) {
-    const float incl = warp_incl_scan(part[i], lane);
-    const float tot = __shfl_sync(0xffffffffu, incl, 31);
-    if (gstar < 0 && run + tot > Tg) {
-      const unsigned bal = __ballot_sync(0xffffffffu, run + incl > Tg);
+    df incl{part[i], 0.f};
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      df t2;
+      t2.h = __shfl_up_sync(0xffffffffu, incl.h, o);
+      t2.l = __shfl_up_sync(0xffffffffu, incl.l, o);
+      if (lane >= o) incl = df_add(incl, t2);
+    }
+    df tot;
+    tot.h = __shfl_sync(0xffffffffu, incl.h, 31);
+    tot.l = __shfl_sync(0xffffffffu, incl.l, 31);
+    if (gstar < 0 && df_gt(df_add(run, tot), Tg)) {
+      const unsigned bal = __ballot_sync(0xffffffffu, df_gt(df_add(run, incl), Tg));
       const int fl = __ffs(bal) - 1;
       gstar = i * 32 + fl;
-      before = __shfl_sync(0xffffffffu, run + incl - part[i], fl);
+      const df bl = df_add(run, df_sub(incl, df{part[i], 0.f}));
+      before.h = __shfl_sync(0xffffffffu, bl.h, fl);
+      before.l = __shfl_sync(0xffffffffu, bl.l, fl);
     }
-    run += tot;
+    run = df_add(run, tot);
   }
   if (gstar >= 0) {  // one lane walks the crossing group, read again
     int64_t t = -1;
+    int ok = 0;
     if (lane == 0) {
       float w[PV];
       weights(__ldg(pv + gstar), kRes ? __ldg(qv + gstar) : neg_inf_vec(E()), w);
-      float acc = before;
+      const df rem = df_sub(Tg, before);
+      const float Tl = rem.h + rem.l;  // what is left of the target inside the group
+      float acc = 0.f;
       int64_t lp = -1;
 #pragma unroll
       for (int k = 0; k < PV; ++k) {
         if (t < 0) {
+          const float prev = acc;
           acc += w[k];
           if (w[k] > 0.f) lp = (int64_t)gstar * PV + k;
-          if (acc > Tg) t = (int64_t)gstar * PV + k;
+          if (acc > Tl) {
+            t = (int64_t)gstar * PV + k;
+            ok = fminf(acc - Tl, Tl - prev) >= rf::kRefineMargin * Z;
+          }
         }
       }
       if (t < 0) t = lp;  // rounding inside the group
     }
+    settled = __shfl_sync(0xffffffffu, ok, 0);
     return __shfl_sync(0xffffffffu, (long long)t, 0);
   }
   // u*Z at or past the total after rounding: the last positive weight
@@ -2427,13 +2475,30 @@ __global__ void __launch_bounds__(kWarpThreads, 4) verify_warp_kernel(const Para
     // ---- the draw
     const float nMp = -mref(rm[j], c), ip = 1.f / rsum[j];
     int64_t t = -1;
+    int settled = 1, st2 = 0;
     if (j < K) {
       const float nMq = -mref(rm[K + 1 + j], c), iq = 1.f / rsum[K + 1 + j];
-      t = warp_draw<E, true>(rowp(j), rowp(K + 1 + j), V, c, nMp, nMq, ip, iq, uK, lane);
+      t = warp_draw<E, true>(rowp(j), rowp(K + 1 + j), V, c, nMp, nMq, ip, iq, uK, lane, settled);
     }
-    if (t < 0) t = warp_draw<E, false>(rowp(j), nullptr, V, c, nMp, 0.f, 1.f, 0.f, uK, lane);
+    if (t < 0) {  // the bonus draw, or a residual that is all zero in fp32 (which stays unsettled)
+      t = warp_draw<E, false>(rowp(j), nullptr, V, c, nMp, 0.f, 1.f, 0.f, uK, lane, st2);
+      if (j == K) settled = st2;
+    }
     for (int i = lane; i <= K; i += 32) out[i] = i < j ? p.tokens[b * K + i] : (i == j ? (int32_t)t : -1);
-    if (lane == 0) p.out_accept_len[b] = j;
+    if (lane == 0) {
+      p.out_accept_len[b] = j;
+      if (!settled && p.rf_ctl) {  // the refine kernel redoes this draw
+        rf::Rec r{};
+        r.b = (int32_t)b;
+        r.j = j;
+        r.resid = j < K ? 1 : 0;
+        r.mp = rm[j];
+        r.mq = j < K ? rm[K + 1 + j] : 0.f;
+        r.taup = r.tauq = -INFINITY;
+        r.u = uK;
+        rf::flag(p.rf_ctl, p.rf_recs, p.B, r);
+      }
+    }
     __syncwarp();
   }
 }

@@ -14,8 +14,12 @@
 namespace sv {
 namespace rf {
 
-// fp32 draws closer than this (times Z) to a CDF edge are redone.
-constexpr float kRefineMargin = 3e-8f;
+// fp32 draws closer than this (times Z) to a CDF edge are redone. The fp32
+// weights carry ~6e-8 relative error each (rounding, ex2.approx) and
+// log2(e)/T rounded to fp32 (a relative error of up to 3e-8, the same in
+// every weight and normaliser) shifts the CDF by up to a few 1e-8 of Z;
+// with the running sums in double-float, 1e-7 of Z leaves room for both.
+constexpr float kRefineMargin = 1e-7f;
 // Flagged draws handled together in one pass of the refine kernel.
 constexpr int kMaxBatch = 64;
 constexpr int kThreads = 256;
@@ -43,6 +47,7 @@ struct Params {
   float tab_hi[32], tab_lo[32];
   uint32_t* ctl;       // kCtlWords words
   uint32_t* status;    // sticky status word of the call's scratch
+  uint32_t* stats;     // nullable: a running count of the draws refined
   Rec* recs;           // [B]
   float* part;         // [kMaxBatch][grid][8]
   int32_t* out_tokens; // [B, K+1]

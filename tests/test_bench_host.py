@@ -74,7 +74,8 @@ def test_launched_kernel_follows_the_library_rule():
     class A:
         sample_path = 0
         greedy_path = 0
-    for name, kernel in (("cfg1_v1000_f32", "rows_kernel"), ("cfg3_v128256_bf16", "rows_kernel"),
+    for name, kernel in (("cfg1_v1000_f32", "verify_warp_kernel"), ("cfg3_v128256_bf16", "verify_kernel"),
+                         ("cfg2_v32000_bf16", "rows_kernel"),
                          ("cfg5_topp_v151936_bf16", "verify_kernel"), ("cfg4_greedy_v32000_bf16", "gr_rows_kernel"),
                          ("la_sample_v32000_bf16", "la_rows_kernel"), ("md_sample_v32000_bf16", "md_rows_kernel")):
         cfg, mode = bench.workload(name)[:2]
