@@ -61,6 +61,15 @@ def log(*a):
 
 # ------------------------------------------------------------------ workload
 
+# The Lookahead n-gram pool ("Lookahead Decoding 完全拆解", "N-gram 池与身份判定"):
+# per step, every sequence inserts the W n-grams of one Lookahead window step
+# and looks up G candidates for its last token (the greedy workload's shape:
+# B = 32, G = W = 7, N = 5, V = 32000; at most cap = 7 n-grams per first
+# token). First tokens and last tokens come from 64 ids, so that lookups find
+# n-grams; the other tokens are uniform over the vocabulary.
+POOL_WORKLOADS = {"ngram_pool_v32000": {"B": 32, "V": 32000, "N": 5, "cap": 7, "G": 7, "W": 7, "keys": 64}}
+
+
 def find_config(name: str):
     for table in (sg.CONFIGS, sg.LOOKAHEAD_CONFIGS, sg.MULTIDRAFT_CONFIGS):
         if name in table:
@@ -215,6 +224,8 @@ def measured_peak():
 # reported while they are the ones that were profiled.
 KERNEL_SOURCES = {
     "rows_kernel": ("sv_rows.cu", "sv_v2.h", "sv_device.cuh"),
+    "topp_rows_kernel": ("sv_rows.cu", "sv_v2.h", "sv_device.cuh"),
+    "refine_kernel": ("sv_refine.cu", "sv_refine.h", "sv_df.cuh", "sv_device.cuh"),
     "decide_kernel": ("sv_decide.cu", "sv_df.cuh", "sv_v2.h", "sv_device.cuh"),
     "verify_kernel": ("sv_kernels.cu", "sv_device.cuh", "sv_kernels.h"),
     "verify_warp_kernel": ("sv_kernels.cu", "sv_device.cuh", "sv_kernels.h"),
@@ -263,6 +274,9 @@ def launched_kernel(cfg, mode, args) -> str:
     small = cfg.B * (2 * cfg.K + 1) * cfg.V * esz <= 96 * 1024 * 1024
     rows = 2 * cfg.K + 1
     warp_rows = cfg.V <= 1024 and (cfg.V * esz) % 16 == 0 and rows <= 64 and rows * cfg.V * esz <= 65536
+    if (cfg.temperature > 0 and cfg.top_p < 1.0 and args.sample_path != 1 and esz == 2 and cfg.V % 8 == 0
+            and cfg.V <= 327680 and cfg.K <= 1024):
+        return "topp_rows_kernel"
     if (cfg.temperature > 0 and cfg.top_p == 1.0 and cfg.K <= 1024 and cfg.V <= 1048576
             and (args.sample_path == 2 or (args.sample_path == 0 and small and not warp_rows))):
         return "rows_kernel"
@@ -543,6 +557,114 @@ def measure(args, name: str, rank: int, world: int, steps: int, cpu_budget: floa
     return rec
 
 
+def pool_inputs(w: dict, nsets: int, seed: int = 0):
+    """Seeded n-gram steps: ngrams [nsets, B, W, N] and last tokens [nsets, B]."""
+    rng = np.random.default_rng(seed)
+    B, V, N, W, keys = w["B"], w["V"], w["N"], w["W"], w["keys"]
+    ng = rng.integers(0, V, size=(nsets, B, W, N)).astype(np.int32)
+    ng[..., 0] = rng.integers(0, keys, size=(nsets, B, W))
+    last = rng.integers(0, keys, size=(nsets, B)).astype(np.int32)
+    return ng, last
+
+
+def measure_pool(args, name: str, steps: int, cpu_budget: float, counts: bool):
+    """The n-gram pool: one insert of W n-grams per sequence and one lookup
+    of G candidates per sequence per step, timed over CUDA-graph replays of
+    exactly ``steps`` steps; bit-exact comparison with the oracle's pool over
+    the first steps after a reset."""
+    import torch
+    import speculative_decoding_verification_39_gb300 as svpkg
+    w = POOL_WORKLOADS[name]
+    B, V, N, cap, G, W = w["B"], w["V"], w["N"], w["cap"], w["G"], w["W"]
+    nsets = 64
+    ng_h, last_h = pool_inputs(w, nsets)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ng = torch.from_numpy(ng_h).to(dev)
+    last = torch.from_numpy(last_h).to(dev)
+    cand = torch.empty((B, G, N - 1), dtype=torch.int32, device=dev)
+    count = torch.empty((B,), dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(dev)
+    log(f"[bench] {name}: B={B} W={W} N={N} cap={cap} G={G}")
+    rec = {"workload": {"workload": name, "mode": "ngram_pool", "B": B, "V": V, "N": N, "cap": cap, "G": G, "W": W,
+                        "l2": "pool and inputs are L2-resident (a few MB); latency-bound"}}
+    with torch.cuda.stream(stream):
+        pool = svpkg.NgramPool(B, V, N, cap, device=dev)
+        if counts:
+            # parity: the first nsets steps after a reset, step by step
+            ora = __import__("oracle").NgramPool(B, V, N, cap)
+            bad = 0
+            for i in range(nsets):
+                pool.insert(ng[i])
+                c, n = pool.lookup(last[i], G, cand=cand, count=count)
+                ora.insert(ng_h[i])
+                rc, rn = ora.lookup(last_h[i], G)
+                bad += int((c.cpu().numpy() != rc).any(axis=(1, 2)).sum() + (n.cpu().numpy() != rn).sum())
+            ora.close()
+            rec["parity"] = {"steps": nsets, "sequences": B, "lookups": nsets * B, "mismatch": bad,
+                             "comparison": "bit-exact candidates and counts against the oracle's pool"}
+            log(f"[bench] pool parity: {rec['parity']}")
+        pool.reset()
+        for i in range(max(3, args.warmup)):
+            pool.insert(ng[i % nsets])
+            pool.lookup(last[i % nsets], G, cand=cand, count=count)
+    stream.synchronize()
+    launches_before = svpkg.launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for i in range(steps):
+            pool.insert(ng[i % nsets])
+            pool.lookup(last[i % nsets], G, cand=cand, count=count)
+    captured = svpkg.launch_count() - launches_before
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        t_pre = time.perf_counter()
+        with torch.cuda.stream(stream):
+            while time.perf_counter() - t_pre < 0.5:
+                graph.replay()
+                stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+    ms_per_step = ms / steps
+    peak, peak_kind = measured_peak()
+    # bytes a step must touch: per n-gram the key's directory word (read and
+    # write), its cap slots (compared) and one slot written; per lookup the
+    # directory word, G slots read and G candidates written
+    step_bytes = B * W * (8 + cap * (N - 1) * 4 + (N - 1) * 4) + B * (4 + 2 * G * (N - 1) * 4 + 4)
+    achieved = step_bytes / (ms_per_step / 1e3) / 1e9
+    rec.update({
+        "value": B * W * steps / (ms / 1e3),
+        "unit": "n-grams inserted/s",
+        "lookups_per_s": B * steps / (ms / 1e3),
+        "ms_per_step": ms_per_step,
+        "steps": steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": None,
+                     "algorithmic_bytes_per_launch": step_bytes, "kernel": "insert_kernel + lookup_kernel",
+                     "note": "a few KB per step: the pool is latency-bound (two dependent launches per step), "
+                             "not bandwidth-bound",
+                     "timing": "CUDA events over one graph of the timed steps"},
+        "clocks": clk.summary(),
+        "gpu_launches": int(captured),
+    })
+    if cpu_budget > 0:
+        ora = __import__("oracle").NgramPool(B, V, N, cap)
+        n, t0 = 0, time.perf_counter()
+        while time.perf_counter() - t0 < cpu_budget:
+            ora.insert(ng_h[n % nsets])
+            ora.lookup(last_h[n % nsets], G)
+            n += 1
+        el = time.perf_counter() - t0
+        ora.close()
+        rec["cpu_baseline"] = {"value": B * W * n / el, "unit": "n-grams inserted/s", "cores": 1, "kind": "oracle",
+                               "sample": f"{n} steps in {el:.1f} s on one host thread"}
+    del pool, graph
+    return rec
+
+
 def run_gpu(args, names: list, rank: int, world: int):
     import torch
     import speculative_decoding_verification_39_gb300 as svpkg
@@ -572,7 +694,7 @@ def run_gpu(args, names: list, rank: int, world: int):
         "config": rec["workload"],
     }
     for k in ("rounds_per_s", "isolated_us", "isolated_note", "roofline", "clocks", "e2e", "gpu_launches",
-              "parity", "cpu_baseline"):
+              "refined_draws_per_call", "refined_note", "parity", "cpu_baseline"):
         if k in rec:
             line[k] = rec[k]
     if "cpu_baseline" in line and not args.no_cpu_baseline and rank == 0 and world == 1:
@@ -582,8 +704,12 @@ def run_gpu(args, names: list, rank: int, world: int):
     if len(names) > 1 and world == 1:
         per = {}
         for n in names[1:]:
-            r = measure(args, n, rank, world, max(args.steps, 100), 0.0 if args.no_cpu_baseline else 2.0,
-                        counts=not args.no_counts)
+            if n in POOL_WORKLOADS:
+                r = measure_pool(args, n, max(args.steps, 100), 0.0 if args.no_cpu_baseline else 2.0,
+                                 counts=not args.no_counts)
+            else:
+                r = measure(args, n, rank, world, max(args.steps, 100), 0.0 if args.no_cpu_baseline else 2.0,
+                            counts=not args.no_counts)
             per[n] = r
         line["per_config"] = per
     if rank == 0:
@@ -633,7 +759,7 @@ def run_reference(args, name: str):
 
 
 def all_names() -> list:
-    return list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS)
+    return list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS) + list(POOL_WORKLOADS)
 
 
 def config_names(spec) -> list:
@@ -644,7 +770,10 @@ def config_names(spec) -> list:
         return [DEFAULT_CONFIG] + [n for n in all_names() if n != DEFAULT_CONFIG]
     names = [n.strip() for n in spec.split(",") if n.strip()]
     for n in names:
-        find_config(n)  # KeyError for an unknown name, before any work
+        if n not in POOL_WORKLOADS:
+            find_config(n)  # KeyError for an unknown name, before any work
+    if names[0] in POOL_WORKLOADS:
+        raise KeyError(f"{names[0]} cannot be the line's own workload (it is not a verify call)")
     return names
 
 

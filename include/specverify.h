@@ -270,13 +270,15 @@ int sv_ngram_pool_lookup(const void* pool, int64_t B, int64_t V, int32_t N, int3
  * same argument checks, the same choice of kernels and the same launch
  * shapes; only the scratch differs. Differences:
  *   - A call whose scratch would exceed 4 MiB returns SV_ERR_SCRATCH_LIMIT and
- *     enqueues nothing. Without top-p (T > 0, K <= 1024, V <= 1048576) the
- *     scratch is 256 + 8*B*(2K+1)*ceil(V*s/32768) bytes (s = 2 for bf16, 4 for
- *     fp32; one chunk per row when a row holds at most 16 KB), e.g. about
- *     0.3 MiB for B=256, K=8, V=128256 bf16; with top-p or T = 0 it is about
- *     256 + 4*(B*R + B*(3+D)) + 8*B*R*ceil(NT/CT) + 16*B*R bytes (R rows per
- *     sequence), plus 4*B*ceil(V/256) when the draws are split over D > 0
- *     chunks.
+ *     enqueues nothing. On the row pass + decide kernels (see
+ *     sv_set_sample_path) the scratch is 512 + 8*B*R*NCH + 8*B*K + 48*B bytes,
+ *     each term rounded up to 256, with R = 2K+1 rows per sequence and
+ *     NCH = ceil(V*s/32768) chunks per row (s = 2 for bf16, 4 for fp32; 1 when
+ *     a row holds at most 16 KB); with top-p the 8*B*R*NCH term is 16*B*R.
+ *     E.g. about 0.3 MiB for B=256, K=8, V=128256 bf16. On the streaming
+ *     kernel it is about 256 + 4*(B*R + B*(3+D)) + 8*B*R*ceil(NT/CT) +
+ *     16*B*R + 48*B bytes, plus 4*B*ceil(V/256) when the draws are split over
+ *     D > 0 chunks.
  *   - The first call on a device looks up the array's device address on that
  *     device (cudaGetSymbolAddress, with the device current) and caches it;
  *     make that first call before any stream capture.
@@ -343,12 +345,15 @@ int sv_set_greedy_path(int32_t path);
  * with T > 0 and top_p = 1, rows of at most 1024 elements go to the
  * streaming kernel's one-warp-per-sequence mode; calls whose logits are at
  * most 96 MiB (so that the second look at the draw rows hits L2) to the row
- * pass and the cluster decide kernel; everything else (larger calls, top-p,
- * T = 0) to the streaming kernel. 1: always the streaming kernel, including
- * its sequence-in-shared-memory mode (whose draws are not handed to the
- * refine kernel). 2: the row pass and decide kernel wherever they fit
- * (T > 0, top_p = 1, K <= 1024, V <= 1048576). Applies to calls made after
- * it. */
+ * pass and the cluster decide kernel; with top_p < 1, bf16 rows with V a
+ * multiple of 8 and V <= 327680 (16-byte aligned logits, K <= 1024) go to
+ * the row pass in its top-p form (one thread-block cluster per row) and the
+ * decide kernel at every size; everything else (larger calls, other top-p
+ * calls, T = 0) to the streaming kernel. 1: always the streaming kernel,
+ * including its sequence-in-shared-memory mode (whose draws are not handed
+ * to the refine kernel). 2: the row pass and decide kernel wherever they fit
+ * (top_p = 1: T > 0, K <= 1024, V <= 1048576; top_p < 1 as for 0). Applies
+ * to calls made after it. */
 int sv_set_sample_path(int32_t path);
 
 #ifdef __cplusplus

@@ -435,10 +435,18 @@ class NgramPool:
         if rc != 0:
             raise SpecVerifyError(rc, "sv_ngram_pool_insert")
 
-    def lookup(self, last, G: int):
+    def lookup(self, last, G: int, cand=None, count=None):
+        """(cand [B, G, N-1], count [B]); ``cand`` and ``count`` may be given
+        (int32, contiguous, on the pool's device) to be written in place."""
         t = _dev_i32(last, self.device)
-        cand = torch.empty((self.B, G, self.N - 1), dtype=torch.int32, device=self.device)
-        count = torch.empty((self.B,), dtype=torch.int32, device=self.device)
+        if cand is None:
+            cand = torch.empty((self.B, G, self.N - 1), dtype=torch.int32, device=self.device)
+        if count is None:
+            count = torch.empty((self.B,), dtype=torch.int32, device=self.device)
+        _check(cand, (self.B, G, self.N - 1), torch.int32, "cand")
+        _check(count, (self.B,), torch.int32, "count")
+        if cand.device != self.device or count.device != self.device:
+            raise ValueError(f"cand and count must be on {self.device}")
         rc = lib().sv_ngram_pool_lookup(_ptr(self.mem), self.B, self.V, self.N, self.cap, _ptr(t), G, _ptr(cand),
                                         _ptr(count), self._stream())
         if rc != 0:

@@ -105,8 +105,7 @@ bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p
 // The refine kernel after a sampling call: it redoes, in double-float
 // arithmetic, the draws the call's fp32 walks could not settle.
 int launch_refine(const void* target, const void* draft, int64_t B, int K, int64_t V, int esz, float temperature,
-                  uint32_t* rf_ctl, sv::rf::Rec* recs, float* part, uint32_t* status, int32_t* out_tokens, int grid,
-                  cudaStream_t stream) {
+                  uint32_t* rf_ctl, sv::rf::Rec* recs, uint32_t* status, int32_t* out_tokens, cudaStream_t stream) {
   sv::rf::Params r{};
   r.target = static_cast<const char*>(target);
   r.draft = static_cast<const char*>(draft);
@@ -116,12 +115,10 @@ int launch_refine(const void* target, const void* draft, int64_t B, int K, int64
   r.esz = esz;
   sv::rf::fill_table(r, temperature);
   r.ctl = rf_ctl;
-  r.status = status;
   r.stats = status + (kCtlRefined - 3);
   r.recs = recs;
-  r.part = part;
   r.out_tokens = out_tokens;
-  if (sv::rf::launch(r, grid, stream) != cudaSuccess) return SV_ERR_CUDA;
+  if (sv::rf::launch(r, stream) != cudaSuccess) return SV_ERR_CUDA;
   g_launches.fetch_add(1);
   return SV_OK;
 }
@@ -166,14 +163,12 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
     }
   }
   const bool refine = mode == sv::kSample;
-  const int sms = sm_count(dev0);
   const size_t cnt_words = (size_t)rows_total + (size_t)p.B * (3 + (size_t)p.DC) + (refine ? sv::rf::kCtlWords : 0);
   const size_t part_bytes = align256((size_t)p.W * 8);
   const size_t rowstat_bytes = align256((size_t)rows_total * 16);
   const size_t dcells_bytes = p.DC ? align256((size_t)p.B * (size_t)ncells * 4) : 0;
   const size_t recs_bytes = refine ? align256((size_t)p.B * sizeof(sv::rf::Rec)) : 0;
-  const size_t rfpart_bytes = refine ? align256(sv::rf::part_bytes(sms)) : 0;
-  const size_t data_bytes = part_bytes + rowstat_bytes + dcells_bytes + recs_bytes + rfpart_bytes;
+  const size_t data_bytes = part_bytes + rowstat_bytes + dcells_bytes + recs_bytes;
   sv::ScratchArea sa;
   int rc = get(ctx, stream, cnt_words, data_bytes, &sa);
   if (rc != SV_OK) return rc;
@@ -190,7 +185,6 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   p.rf_ctl = refine ? p.dcnt + p.B : nullptr;
   p.rf_recs = refine ? reinterpret_cast<sv::rf::Rec*>(b + sa.data_off + part_bytes + rowstat_bytes + dcells_bytes)
                      : nullptr;
-  float* rf_part = reinterpret_cast<float*>(b + sa.data_off + part_bytes + rowstat_bytes + dcells_bytes + recs_bytes);
   // Short rows: one warp per sequence (rows of at most 1024 elements), else
   // one CTA per sequence with the whole sequence staged in shared memory.
   const bool short_ok = mode == sv::kSample && !p.topp && aligned_to(p.a, 16) && aligned_to(p.d, 16);
@@ -207,8 +201,7 @@ int run(sv::Params& p, int dtype, int mode, int64_t rows_total, cudaStream_t str
   if (e != cudaSuccess) return SV_ERR_CUDA;
   g_launches.fetch_add(1);
   if (refine)
-    return launch_refine(p.a, p.d, p.B, p.K, p.V, esz, p.T, p.rf_ctl, p.rf_recs, rf_part, p.ctl + 3, p.out_tokens,
-                         sms, stream);
+    return launch_refine(p.a, p.d, p.B, p.K, p.V, esz, p.T, p.rf_ctl, p.rf_recs, p.ctl + 3, p.out_tokens, stream);
   return SV_OK;
 }
 
@@ -255,9 +248,16 @@ int sv::verify_sample_impl(const void* target_logits, const void* draft_logits, 
   const bool warp_rows = sv::warp_mode_fits(K, V, (int)esz) && aligned_to(target_logits, 16) &&
                          aligned_to(draft_logits, 16);
   const int path = g_sample_path.load();
-  if (!limit && top_p == 1.f && sv::v2::fits(K, V) &&
-      (path == 2 || (path == 0 && two_kernel_size && !warp_rows))) {
+  // Top-p: the row pass holds each row in one cluster's registers while it
+  // takes the nucleus cut, so the rows are read once at every size.
+  const bool topp = top_p < 1.f;
+  const bool v2_topp = !limit && topp && path != 1 && sv::v2::fits_topp(K, V, (int)esz) &&
+                       aligned_to(target_logits, 16) && aligned_to(draft_logits, 16);
+  if (v2_topp || (!limit && !topp && sv::v2::fits(K, V) &&
+                  (path == 2 || (path == 0 && two_kernel_size && !warp_rows)))) {
     sv::v2::Params q{};
+    q.topp = topp ? 1 : 0;
+    q.top_p = top_p;
     q.target = static_cast<const char*>(target_logits);
     q.draft = static_cast<const char*>(draft_logits);
     q.tokens = draft_tokens;
@@ -276,23 +276,22 @@ int sv::verify_sample_impl(const void* target_logits, const void* draft_logits, 
     if (cudaGetDevice(&dev) != cudaSuccess) return SV_ERR_CUDA;
     sv::v2::plan(q, sm_count(dev));
     if (q.items >= (int64_t(1) << 31) || B * q.D >= (int64_t(1) << 31)) return SV_ERR_ARG;
-    const int sms = sm_count(dev);
     const size_t v2_bytes = align256(sv::v2::scratch_bytes(q));
     const size_t recs_bytes = align256((size_t)B * sizeof(sv::rf::Rec));
     sv::ScratchArea sa;
-    const int rc = get(ctx, st, sv::rf::kCtlWords, v2_bytes + recs_bytes + sv::rf::part_bytes(sms), &sa);
+    const int rc = get(ctx, st, sv::rf::kCtlWords, v2_bytes + recs_bytes, &sa);
     if (rc != SV_OK) return rc;
     if (sa.clear_counters && cudaMemsetAsync(sa.base, 0, sa.data_off, st) != cudaSuccess) return SV_ERR_CUDA;
     q.ctl = reinterpret_cast<uint32_t*>(sa.base);
     q.part = reinterpret_cast<float2*>(sa.base + sa.data_off);
+    q.rstat = reinterpret_cast<float4*>(sa.base + sa.data_off);
     q.gz = reinterpret_cast<float*>(sa.base + sa.data_off + sv::v2::part_bytes(q));
     q.rf_ctl = reinterpret_cast<uint32_t*>(sa.base + counter_offset());
     q.rf_recs = reinterpret_cast<sv::rf::Rec*>(sa.base + sa.data_off + v2_bytes);
-    float* rf_part = reinterpret_cast<float*>(sa.base + sa.data_off + v2_bytes + recs_bytes);
     if (sv::v2::launch(q, dtype, st) != cudaSuccess) return SV_ERR_CUDA;
     g_launches.fetch_add(2);
-    return launch_refine(target_logits, draft_logits, B, K, V, (int)esz, temperature, q.rf_ctl, q.rf_recs, rf_part,
-                         q.ctl + 3, out_tokens, sms, st);
+    return launch_refine(target_logits, draft_logits, B, K, V, (int)esz, temperature, q.rf_ctl, q.rf_recs, q.ctl + 3,
+                         out_tokens, st);
   }
   sv::Params p{};
   p.a = static_cast<const char*>(target_logits);
@@ -564,6 +563,8 @@ extern "C" int sv_set_launch_shape(int32_t stages, int32_t ctas_per_sm) {
 }
 
 extern "C" uint64_t sv_launch_count(void) { return g_launches.load(); }
+
+void sv::note_launches(int n) { g_launches.fetch_add((uint64_t)n); }
 
 extern "C" int sv_set_greedy_path(int32_t path) {
   if (path < 0 || path > 1) return SV_ERR_ARG;

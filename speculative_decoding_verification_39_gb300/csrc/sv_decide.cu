@@ -41,36 +41,6 @@ constexpr float kLn2 = 0.693147180559945309f;
 
 __device__ __forceinline__ int nwarps() { return (int)(blockDim.x >> 5); }
 
-// ---------------------------------------------------------------- cluster ---
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// All threads of every CTA of the cluster; orders shared-memory writes before
-// the barrier with reads after it, across the cluster.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float dsmem_ld_f32(const void* p, uint32_t rank) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(dsmem_addr(p, rank)) : "memory");
-  return v;
-}
-__device__ __forceinline__ int dsmem_ld_s32(const void* p, uint32_t rank) {
-  int v;
-  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(dsmem_addr(p, rank)) : "memory");
-  return v;
-}
-__device__ __forceinline__ void dsmem_st_s32(void* p, uint32_t rank, int v) {
-  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(dsmem_addr(p, rank)), "r"(v) : "memory");
-}
-
 // -------------------------------------------------------------- elements ---
 template <typename E>
 struct Elem;
@@ -167,13 +137,15 @@ __device__ __forceinline__ void load8(const RowView& r, int64_t e, int64_t V, fl
 // ---------------------------------------------------------------- weights ---
 // fp32 weights of the fast draw. Residual: max(0, 2^(l_p c - Mc_p)/s_p -
 // 2^(l_q c - Mc_q)/s_q); bonus (or a residual of zero mass): 2^(l_p c - Mc_p).
+// With top-p, an element outside a row's nucleus (l < tp, resp. tq) has
+// weight 0 in that row.
 struct FastW {
-  float c, mcp, ip, mcq, iq;
+  float c, mcp, ip, mcq, iq, tp, tq;
   bool resid;
   __device__ __forceinline__ float w(float lp, float lq) const {
-    const float ep = ex2(fmaf(lp, c, -mcp));
+    const float ep = lp >= tp ? ex2(fmaf(lp, c, -mcp)) : 0.f;
     if (!resid) return ep;
-    const float eq = ex2(fmaf(lq, c, -mcq));
+    const float eq = lq >= tq ? ex2(fmaf(lq, c, -mcq)) : 0.f;
     return fmaxf(0.f, fmaf(ep, ip, -eq * iq));
   }
 };
@@ -200,18 +172,20 @@ struct Smem {
   uint64_t slice_bar;       // the slice copies of the draw rows landed
 };
 
-// Dynamic shared memory, in floats: rM[R] rS[R] gz[2K] us[K+1] xs[K]
+// Dynamic shared memory, in floats: rM[R] rS[R] rT[R] gz[2K] us[K+1] xs[K]
 // cs_h cs_l cp_h cp_l [cpr each], then (16-byte aligned) the copies of this
-// CTA's slice of the two draw rows.
+// CTA's slice of the two draw rows. rS is the nucleus mass (the whole row's
+// sum without top-p), rT the smallest logit in the nucleus (-inf: all).
 struct Layout {
-  float *rM, *rS, *gz, *us;
+  float *rM, *rS, *rT, *gz, *us;
   int32_t* xs;
   float *cs_h, *cs_l, *cp_h, *cp_l;
   char* slice;
   __device__ Layout(float* d, int K, int R, int cpr) {
     rM = d;
     rS = rM + R;
-    gz = rS + R;
+    rT = rS + R;
+    gz = rT + R;
     us = gz + 2 * K;
     xs = reinterpret_cast<int32_t*>(us + K + 1);
     cs_h = reinterpret_cast<float*>(xs + K);
@@ -224,7 +198,7 @@ struct Layout {
 
 // Floats of the Layout arrays (the slice area follows them).
 __host__ __device__ inline size_t layout_floats(int K, int R, int cpr) {
-  return (size_t)2 * R + 2 * (size_t)K + (K + 1) + K + 4 * (size_t)cpr;
+  return (size_t)3 * R + 2 * (size_t)K + (K + 1) + K + 4 * (size_t)cpr;
 }
 
 // What the draw works on: the rows, this rank's cells, the uniform.
@@ -285,7 +259,16 @@ __global__ void __launch_bounds__(kDecideThreads, 3) decide_kernel(const Params 
     L.us[i] = u;
     bad |= !(u >= 0.f && u < 1.f);
   }
-  for (int i = tid; i < R; i += (int)blockDim.x) {
+  for (int i = tid; i < R && p.topp; i += (int)blockDim.x) {
+    const float4 r = p.rstat[b * R + i];
+    const uint32_t tau = __float_as_uint(r.w);
+    L.rM[i] = r.x;
+    L.rS[i] = r.z;
+    // the smallest bf16 value whose key is >= tau (tau = 0: every value)
+    L.rT[i] = tau <= key_bf16(-INFINITY) ? -INFINITY : val_bf16(tau);
+    bad |= !(r.x > -INFINITY && r.x < INFINITY && r.z > 0.f);
+  }
+  for (int i = tid; i < R && !p.topp; i += (int)blockDim.x) {
     const float2* pp = p.part + (b * R + i) * p.NCH;
     float m = pp[0].x, s = pp[0].y;
     for (int k = 1; k < p.NCH; ++k) {
@@ -302,6 +285,7 @@ __global__ void __launch_bounds__(kDecideThreads, 3) decide_kernel(const Params 
     }
     L.rM[i] = m;
     L.rS[i] = s;
+    L.rT[i] = -INFINITY;
     bad |= !(m > -INFINITY && m < INFINITY && s > 0.f);
   }
   // the logits of the draft tokens, recorded by the row pass
@@ -321,9 +305,9 @@ __global__ void __launch_bounds__(kDecideThreads, 3) decide_kernel(const Params 
           // underflow fp32 are taken in the log2 domain instead.
           const float lp = L.gz[i], lq = L.gz[K + i];
           float alpha;
-          if (lp == -INFINITY) {
+          if (!(lp > -INFINITY && lp >= L.rT[i])) {  // p(x) = 0
             alpha = 0.f;
-          } else if (lq == -INFINITY) {
+          } else if (!(lq > -INFINITY && lq >= L.rT[K + 1 + i])) {  // q(x) = 0
             alpha = 1.f;
           } else {
             const float xp = fmaf(lp, c, -__fmul_rn(L.rM[i], c));
@@ -356,9 +340,16 @@ __global__ void __launch_bounds__(kDecideThreads, 3) decide_kernel(const Params 
       const float mc = __fmul_rn(L.rM[i], c);
       float4 o;
       o.x = L.rM[i] / p.T;
-      o.y = (mc + lg2(L.rS[i])) * kLn2;
-      o.z = 1.f;
-      o.w = -INFINITY;
+      if (p.topp) {
+        const float4 r = p.rstat[b * R + i];
+        o.y = (mc + lg2(r.y)) * kLn2;
+        o.z = r.z / r.y;
+        o.w = val_bf16(__float_as_uint(r.w));
+      } else {
+        o.y = (mc + lg2(L.rS[i])) * kLn2;
+        o.z = 1.f;
+        o.w = -INFINITY;
+      }
       reinterpret_cast<float4*>(p.out_row_stats)[b * R + i] = o;
     }
   }
@@ -420,6 +411,8 @@ __global__ void __launch_bounds__(kDecideThreads, 3) decide_kernel(const Params 
   fw.ip = 1.f / L.rS[j];
   fw.mcq = x.resid ? __fmul_rn(L.rM[K + 1 + j], c) : 0.f;
   fw.iq = x.resid ? 1.f / L.rS[K + 1 + j] : 0.f;
+  fw.tp = L.rT[j];
+  fw.tq = x.resid ? L.rT[K + 1 + j] : -INFINITY;
   fw.resid = x.resid;
   if (!bad) fast_cells<E>(fw, x, L, warp, lane);
   __syncthreads();
@@ -529,7 +522,8 @@ __global__ void __launch_bounds__(kDecideThreads, 3) decide_kernel(const Params 
     r.resid = x.resid ? 1 : 0;
     r.mp = L.rM[j];
     r.mq = x.resid ? L.rM[K + 1 + j] : 0.f;
-    r.taup = r.tauq = -INFINITY;
+    r.taup = L.rT[j];
+    r.tauq = x.resid ? L.rT[K + 1 + j] : -INFINITY;
     r.u = x.u;
     rf::flag(p.rf_ctl, p.rf_recs, p.B, r);
   }
@@ -596,10 +590,17 @@ bool fits(int64_t K, int64_t V) {
   return K >= 1 && K <= kMaxK && V >= 2 && V <= (int64_t)kMaxCluster * kMaxCellsPerCta * kCellElems;
 }
 
+bool fits_topp(int64_t K, int64_t V, int esz) { return fits(K, V) && esz == 2 && V % 8 == 0; }
+
 void plan(Params& p, int sms) {
   const int64_t rowbytes = p.V * p.esz;
   const int64_t rows = p.B * p.R;
-  if (rowbytes <= kChunkBytes / 2) {
+  if (p.topp) {
+    // whole rows, one CTA each at a time (persistent CTAs, see below)
+    p.NCH = 1;
+    p.CE = p.V;
+    p.RPI = 1;
+  } else if (rowbytes <= kChunkBytes / 2) {
     // short rows: groups of whole rows, about one chunk's worth each
     p.NCH = 1;
     p.CE = p.V;
@@ -628,6 +629,7 @@ void plan(Params& p, int sms) {
   int per_sm = (int)((200 * 1024) / (2 * (int64_t)p.stage_bytes));
   per_sm = per_sm < 1 ? 1 : (per_sm > 4 ? 4 : per_sm);
   p.rows_grid = (int64_t)sms * per_sm;
+  if (p.topp) p.rows_grid = (int64_t)sms * 4;  // the top-p row pass: four CTAs per SM
   if (p.rows_grid > p.items) p.rows_grid = p.items;
   p.ncell = (int)((p.V + kCellElems - 1) / kCellElems);
   int d = (p.ncell + 31) / 32;
@@ -670,7 +672,10 @@ cudaError_t raise_smem_limit_v2(const void* kernel, size_t bytes) {
   return e;
 }
 
-size_t part_bytes(const Params& p) { return ((size_t)(p.B * p.R * p.NCH) * sizeof(float2) + 255) / 256 * 256; }
+size_t part_bytes(const Params& p) {
+  const size_t b = p.topp ? (size_t)(p.B * p.R) * sizeof(float4) : (size_t)(p.B * p.R * p.NCH) * sizeof(float2);
+  return (b + 255) / 256 * 256;
+}
 size_t scratch_bytes(const Params& p) { return part_bytes(p) + (size_t)p.B * 2 * p.K * sizeof(float); }
 
 cudaError_t launch(const Params& p, int dtype, cudaStream_t stream) {

@@ -66,9 +66,10 @@ __device__ __forceinline__ bool df_pos(df a) { return a.h > 0.f || (a.h == 0.f &
 // k = round(32 xh) and |r| <= 1/64, 2^(k/32) = 2^floor(k/32) * 2^((k mod 32)/32)
 // from a table of double-floats, and 2^r = e^t, t = r ln 2, from its Taylor
 // series to t^5 (the first omitted term is below 3e-15 for |t| < 0.011).
-// Values below 2^-150 are returned as 0.
+// The power of two is applied as an exact multiply; values below 2^-126 are
+// returned as 0 (as the fp32 path's flush-to-zero exp2 does).
 __device__ __forceinline__ df df_exp2(float xh, float xl, const float* tab_hi, const float* tab_lo) {
-  if (!(xh >= -150.f)) return df{0.f, 0.f};
+  if (!(xh >= -126.f)) return df{0.f, 0.f};
   constexpr float kLn2Hi = 0.693147182464599609375f;      // fl(ln 2)
   constexpr float kLn2Lo = -1.904654323148236017e-09f;     // ln 2 - fl(ln 2)
   const float kf = rintf(__fmul_rn(xh, 32.f));
@@ -91,7 +92,9 @@ __device__ __forceinline__ df df_exp2(float xh, float xl, const float* tab_hi, c
   df r = fast_two_sum(Th, p.h);
   const float corr = __fadd_rn(__fadd_rn(p.l, __fmul_rn(Th, sl)), __fmaf_rn(Tl, t.h, Tl));
   r = fast_two_sum(r.h, __fadd_rn(r.l, corr));
-  return df{ldexpf(r.h, n), ldexpf(r.l, n)};
+  if (n < -126) return df{0.f, 0.f};
+  const float scale = __int_as_float((n + 127) << 23);  // 2^n, exact
+  return df{__fmul_rn(r.h, scale), __fmul_rn(r.l, scale)};
 }
 
 }  // namespace sv

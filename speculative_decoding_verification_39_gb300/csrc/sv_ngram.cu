@@ -20,6 +20,7 @@
 
 #include "../../include/specverify.h"
 #include "sv_device.cuh"
+#include "sv_sample_impl.h"
 
 namespace sv {
 namespace ng {
@@ -131,7 +132,9 @@ cudaError_t launch_pdl(const void* kernel, unsigned grid, void** args, cudaStrea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelExC(&cfg, kernel, args);
+  const cudaError_t e = cudaLaunchKernelExC(&cfg, kernel, args);
+  if (e == cudaSuccess) note_launches(1);
+  return e;
 }
 
 }  // namespace

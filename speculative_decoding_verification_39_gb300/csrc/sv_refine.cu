@@ -1,5 +1,5 @@
 // sv_refine.cu — the refine kernel: sampling draws that an fp32 draw could not
-// settle, redone in double-float arithmetic over the whole GPU (sm_103a).
+// settle, redone in double-float arithmetic (sm_103a).
 //
 // The draw ("Speculative Decoding —— LLM推理优化技术（一）" §2.1-2.3, kwkr.cn
 // "投机解码" §3.1, §3.4): after a rejection at j, the token is the smallest t
@@ -12,13 +12,24 @@
 // over the nucleus in double-float, and the residual weights as
 // max(0, e_p - (S_p/S_q) e_q), proportional to max(0, p' - q').
 //
-// One CTA per SM, launched cooperatively, so that the CTAs can wait for one
-// another at grid barriers (bounded: a wait gives up after 2 s and the call
-// reports SV_ERR_TIMEOUT). Each CTA owns one contiguous range of every row;
-// every flagged draw of the call is handled in the same three phases —
-// normaliser partials, range totals, the crossing — so that the number of
-// barriers does not grow with the number of flagged draws.
+// One thread-block cluster of CL CTAs per flagged draw (CL up to 16); CTA r
+// of the cluster owns elements [r*RL, (r+1)*RL) of the draw's rows. Per draw:
+//  1. every CTA evaluates e_p (and e_q) over its range once, keeps the
+//     double-float values in shared memory and sums them; the CTAs exchange
+//     the sums through distributed shared memory, so that every CTA holds the
+//     same S_p / S_q;
+//  2. every CTA sums the weights of its range in chunks of 8m elements and
+//     scans the chunk sums; the CTAs exchange their range totals, giving the
+//     base of each range, Z and u*Z; the CTA whose range crosses u*Z finds
+//     its thread whose chunks cross, and that thread walks them element by
+//     element. A residual of zero mass repeats step 2 with w = e_p.
+// Clusters take flagged draws in turn (draw f on cluster f mod clusters).
+// Where the range is too long for the double-float values to stay in shared
+// memory, step 2 evaluates them again from global memory.
 #include <climits>
+#include <map>
+#include <mutex>
+#include <tuple>
 
 #include "sv_device.cuh"
 #include "sv_df.cuh"
@@ -29,9 +40,7 @@ namespace rf {
 namespace {
 
 constexpr int kWarps = kThreads / 32;
-constexpr int kRecFloats = 12;  // per (flagged draw, CTA) partials
-constexpr int kGroup = 4;       // flagged draws whose loads a thread keeps in flight together
-constexpr int kPer = 4;         // elements per row and draw a thread loads at a time
+constexpr int kMaxChunks = 2048;  // chunk sums kept per CTA
 
 template <typename E>
 __device__ __forceinline__ float load_elem(const char* row, int64_t e) {
@@ -40,12 +49,64 @@ __device__ __forceinline__ float load_elem(const char* row, int64_t e) {
   return __ldg(reinterpret_cast<const float*>(row) + e);
 }
 
+// The 8 elements of a group as stored words (bf16: one 16-byte vector, fp32:
+// two), so that a loop over the elements can pick element k with selects
+// instead of indexing a register array.
+template <typename E>
+struct Raw;
+template <>
+struct Raw<uint16_t> {
+  uint4 a;
+  __device__ __forceinline__ float at(int k) const {
+    const uint32_t w = k < 4 ? (k < 2 ? a.x : a.y) : (k < 6 ? a.z : a.w);
+    return __uint_as_float((k & 1) ? (w & 0xFFFF0000u) : (w << 16));
+  }
+};
+template <>
+struct Raw<float> {
+  uint4 a, b;
+  __device__ __forceinline__ float at(int k) const {
+    const uint4& v = k < 4 ? a : b;
+    const int j = k & 3;
+    return __uint_as_float(j < 2 ? (j == 0 ? v.x : v.y) : (j == 2 ? v.z : v.w));
+  }
+};
+
+// Elements e..e+7 of a row as stored words (-inf from hi on).
+template <typename E>
+__device__ __forceinline__ void load_raw(const char* row, int64_t e, int64_t hi, bool vec, Raw<E>& r) {
+  if constexpr (sizeof(E) == 2) {
+    if (vec && e + 8 <= hi) {
+      r.a = __ldg(reinterpret_cast<const uint4*>(row + e * 2));
+    } else {
+      const unsigned short* s = reinterpret_cast<const unsigned short*>(row);
+      uint32_t w[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const uint32_t l0 = e + 2 * k < hi ? (uint32_t)__ldg(s + e + 2 * k) : 0xFF80u;
+        const uint32_t l1 = e + 2 * k + 1 < hi ? (uint32_t)__ldg(s + e + 2 * k + 1) : 0xFF80u;
+        w[k] = l0 | (l1 << 16);
+      }
+      r.a = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  } else {
+    if (vec && e + 8 <= hi) {
+      r.a = __ldg(reinterpret_cast<const uint4*>(row + e * 4));
+      r.b = __ldg(reinterpret_cast<const uint4*>(row + e * 4 + 16));
+    } else {
+      const float* s = reinterpret_cast<const float*>(row);
+      uint32_t w[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) w[k] = e + k < hi ? __float_as_uint(__ldg(s + e + k)) : 0xFF800000u;
+      r.a = make_uint4(w[0], w[1], w[2], w[3]);
+      r.b = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
+}
+
 struct Ctx {
-  const char* prow;
-  const char* qrow;
   float mp, mq, taup, tauq;
   df rho;
-  bool resid;  // weights max(0, e_p - rho e_q); otherwise e_p
   float c_hi, c_lo;
   const float* th;
   const float* tl;
@@ -57,28 +118,15 @@ struct Ctx {
     const float xl = __fadd_rn(__fmaf_rn(d.h, c_hi, -xh), __fmaf_rn(d.h, c_lo, __fmul_rn(d.l, c_hi)));
     return df_exp2(xh, xl, th, tl);
   }
-  // the weight of an element with target logit lp and draft logit lq
-  __device__ __forceinline__ df w_of(float lp, float lq) const {
-    const df ep = e(lp, mp, taup);
-    if (!resid) return ep;
-    const df r = df_sub(ep, df_mul(rho, e(lq, mq, tauq)));
+  // the residual weight from the two e values
+  __device__ __forceinline__ df resid_w(df ep, df eq) const {
+    const df r = df_sub(ep, df_mul(rho, eq));
     return df_pos(r) ? r : df{0.f, 0.f};
-  }
-  template <typename E>
-  __device__ __forceinline__ df w(int64_t v) const {
-    return w_of(load_elem<E>(prow, v), resid ? load_elem<E>(qrow, v) : -INFINITY);
   }
 };
 
-__device__ __forceinline__ df warp_sum_df(df v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    df t;
-    t.h = __shfl_xor_sync(0xffffffffu, v.h, o);
-    t.l = __shfl_xor_sync(0xffffffffu, v.l, o);
-    v = df_add(v, t);
-  }
-  return v;
+__device__ __forceinline__ df shfl_xor_df(df v, int o) {
+  return df{__shfl_xor_sync(0xffffffffu, v.h, o), __shfl_xor_sync(0xffffffffu, v.l, o)};
 }
 __device__ __forceinline__ df warp_incl_scan_df(df v, int lane) {
 #pragma unroll
@@ -91,387 +139,321 @@ __device__ __forceinline__ df warp_incl_scan_df(df v, int lane) {
   return v;
 }
 
-// Sum over the CTA, in a fixed order; every thread gets it.
-__device__ __forceinline__ df block_sum_df(df v, float* sh, int tid) {
-  v = warp_sum_df(v);
-  const int lane = tid & 31, warp = tid >> 5;
-  __syncthreads();
-  if (lane == 0) {
-    sh[2 * warp] = v.h;
-    sh[2 * warp + 1] = v.l;
-  }
-  __syncthreads();
-  df s{0.f, 0.f};
-  for (int w = 0; w < kWarps; ++w) s = df_add(s, df{sh[2 * w], sh[2 * w + 1]});
-  return s;
-}
-
-// Over the G CTAs' partials of one flagged draw (record fields oh, oh+1 as a
-// double-float, ol the last-positive index; ol < 0: none), in CTA order, one
-// CTA per thread (G <= kThreads): every thread gets the total, the exclusive
-// prefix of CTA `me`, the first CTA whose inclusive prefix exceeds u*total
-// (-1: none, or u < 0 to skip) and the largest last-positive index. All loads
-// are issued at once.
-struct Scan {
-  df total, excl_me;
-  int owner, last;
+// Shared state of a CTA besides the dynamic arrays.
+struct Shared {
+  float xs[2][4];                // exchange slots, read by the other CTAs of the cluster
+  float wh[kWarps], wl[kWarps];  // per-warp partials
+  float wh2[kWarps], wl2[kWarps];
+  int wi[kWarps];
+  float bh[4], bl[4];            // values broadcast to the CTA
+  int bi[4];
+  float th[32], tl[32];          // 2^(i/32) as double-floats
 };
-__device__ Scan cta_scan(const float* part, int f, int G, int oh, int ol, float u, int me, float* wh, float* wl,
-                         int* wi, int* wj) {
+
+// Sums of two double-floats over the CTA (fixed order); every thread gets both.
+__device__ __forceinline__ void block_sum2(df& a, df& b, Shared& s) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const float* q = part + ((int64_t)f * G + tid) * kRecFloats;
-  df v{0.f, 0.f};
-  int lt = -1;
-  if (tid < G) {
-    v = df{__ldcg(q + oh), __ldcg(q + oh + 1)};
-    if (ol >= 0) lt = __float_as_int(__ldcg(q + ol));
-  }
-  df incl = warp_incl_scan_df(v, lane);
-  int lm = lt;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(0xffffffffu, lm, o));
-  __syncthreads();
-  if (lane == 31) {
-    wh[warp] = incl.h;
-    wl[warp] = incl.l;
+  for (int o = 16; o > 0; o >>= 1) {
+    a = df_add(a, shfl_xor_df(a, o));
+    b = df_add(b, shfl_xor_df(b, o));
   }
-  if (lane == 0) wi[warp] = lm;
+  if (lane == 0) {
+    s.wh[warp] = a.h;
+    s.wl[warp] = a.l;
+    s.wh2[warp] = b.h;
+    s.wl2[warp] = b.l;
+  }
   __syncthreads();
-  df base{0.f, 0.f}, total{0.f, 0.f};
-  int last = -1;
+  df x{0.f, 0.f}, y{0.f, 0.f};
+#pragma unroll 1
   for (int w = 0; w < kWarps; ++w) {
-    const df tw{wh[w], wl[w]};
-    if (w < warp) base = df_add(base, tw);
-    total = df_add(total, tw);
-    last = max(last, wi[w]);
+    x = df_add(x, df{s.wh[w], s.wl[w]});
+    y = df_add(y, df{s.wh2[w], s.wl2[w]});
   }
-  incl = df_add(base, incl);
-  Scan r;
-  r.total = total;
-  r.last = last;
-  const df target = df_mul_f(total, u < 0.f ? 0.f : u);
-  const uint32_t m = __ballot_sync(0xffffffffu, tid < G && u >= 0.f && df_gt(incl, target));
+  a = x;
+  b = y;
   __syncthreads();
-  if (lane == 0) wj[warp] = m ? warp * 32 + __ffs(m) - 1 : INT_MAX;
-  if (tid == me) {
-    const df ex = df_sub(incl, v);
-    wh[kWarps] = ex.h;
-    wl[kWarps] = ex.l;
-  }
-  __syncthreads();
-  int own = INT_MAX;
-  for (int w = 0; w < kWarps; ++w) own = min(own, wj[w]);
-  r.owner = own == INT_MAX ? -1 : own;
-  r.excl_me = df{wh[kWarps], wl[kWarps]};
-  __syncthreads();  // the scratch may be reused by the next call
-  return r;
 }
 
-// Every CTA waits until all have arrived k times; false if the wait gave up
-// (or another CTA's did).
-__device__ bool grid_barrier(uint32_t* ctl, uint32_t k, int* sh_ok) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&ctl[1], 1u);
-    const uint32_t target = k * gridDim.x;
-    int ok = 1;
-    const uint64_t t0 = globaltimer_ns();
-    while (ld_acquire_gpu(&ctl[1]) < target) {
-      if (ld_relaxed_gpu(&ctl[3])) {
-        ok = 0;
-        break;
-      }
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
-        atomicExch(&ctl[3], 1u);
-        ok = 0;
-        break;
-      }
-    }
-    __threadfence();
-    *sh_ok = ok;
-  }
-  __syncthreads();
-  return *sh_ok != 0;
-}
-
+// Draws f = cluster, cluster + clusters, ... of the flagged list.
 template <typename E>
 __global__ void __launch_bounds__(kThreads, 1) refine_kernel(const Params p) {
-  __shared__ float red[2 * kWarps];
-  __shared__ Rec rec[kMaxBatch];
-  __shared__ float rho_h[kMaxBatch], rho_l[kMaxBatch];
-  __shared__ int zero[kMaxBatch];
-  __shared__ int lastw[kWarps];
-  __shared__ float wt_h[kWarps + 1], wt_l[kWarps + 1];
-  __shared__ int wsi[kWarps], wsj[kWarps];
-  __shared__ int sh_ok, sh_tok;
-  grid_dependency_sync(true);
+  extern __shared__ __align__(16) float dyn[];
+  __shared__ Shared s;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int G = gridDim.x, cta = blockIdx.x;
-  const int64_t V = p.V;
+  if (tid < 32) {
+    s.th[tid] = p.tab_hi[tid];
+    s.tl[tid] = p.tab_lo[tid];
+  }
+  __syncthreads();
+  grid_dependency_sync(true);
   uint32_t total = ld_acquire_gpu(&p.ctl[0]);
   if (total > (uint32_t)p.B) total = (uint32_t)p.B;
-  if (cta == 0 && tid == 0 && total && p.stats) atomicAdd(p.stats, total);
-  // this CTA's range of every row: [lo, hi), a multiple of 8 elements long
-  const int64_t RL = ((V + G - 1) / G + 7) / 8 * 8;
-  const int64_t lo = min((int64_t)cta * RL, V), hi = min(lo + RL, V);
-  uint32_t nbar = 0;
-  bool ok = true;
+  if (total == 0) return;  // the same word for every CTA: nothing to redo, no cluster barrier taken
+  if (blockIdx.x == 0 && tid == 0 && p.stats) atomicAdd(p.stats, total);
+  const int CL = p.CL;
+  const uint32_t rank = cluster_rank();
+  const uint32_t clus = cluster_id_x(), nclus = cluster_count_x();
+  const int64_t V = p.V;
+  const int64_t lo = min((int64_t)rank * p.RL, V), hi = min(lo + p.RL, V);
+  const int NG = (int)((hi - lo + 7) / 8);  // groups of 8 elements in this CTA's range
+  const int NGc = (int)(p.RL / 8);          // stride of the e arrays
+  const int m = p.m;
+  const int NC = (NG + m - 1) / m;          // chunks of m groups in this range
+  const bool cache = p.cache != 0, vec = p.vec != 0;
+  // dynamic shared memory: [cache] e_p and e_q as hi/lo arrays (element k of
+  // group g at k*NGc + g, so that a warp's 32 groups hit 32 banks); the chunk sums
+  const int ca = cache ? 8 * NGc : 0;
+  float* cph = dyn;
+  float* cpl = cph + ca;
+  float* cqh = cpl + ca;
+  float* cql = cqh + ca;
+  float* csh = cql + ca;
+  float* csl = csh + p.NC;
   Ctx x;
   x.c_hi = p.c_hi;
   x.c_lo = p.c_lo;
-  x.th = p.tab_hi;
-  x.tl = p.tab_lo;
-  auto setup = [&](const Rec& r, bool resid) {
-    x.prow = p.target + ((r.b * (int64_t)(p.K + 1) + r.j) * V) * p.esz;
-    x.qrow = r.resid ? p.draft + ((r.b * (int64_t)p.K + r.j) * V) * p.esz : x.prow;
+  x.th = s.th;
+  x.tl = s.tl;
+  x.rho = df{0.f, 0.f};
+  int xc = 0;  // exchanges so far: slot xc & 1 is free to write
+  for (uint32_t f = clus; f < total; f += nclus) {
+    const Rec r = p.recs[f];
+    const char* prow = p.target + ((r.b * (int64_t)(p.K + 1) + r.j) * V) * p.esz;
+    const char* qrow = r.resid ? p.draft + ((r.b * (int64_t)p.K + r.j) * V) * p.esz : prow;
     x.mp = r.mp;
     x.mq = r.mq;
     x.taup = r.taup;
     x.tauq = r.tauq;
-    x.resid = resid;
-  };
-  for (uint32_t f0 = 0; f0 < total && ok; f0 += kMaxBatch) {
-    const int nb = (int)min((uint32_t)kMaxBatch, total - f0);
-    for (int f = tid; f < nb; f += kThreads) rec[f] = p.recs[f0 + f];
-    __syncthreads();
-    // ---- phase 1: the residual draws' normalisers, per range ----------------
-    // Draws go four at a time: every thread first loads its elements of all
-    // four (so that their latencies overlap), then sums.
-    for (int g0 = 0; g0 < nb; g0 += kGroup) {
-      df sp[kGroup], sq[kGroup];
-#pragma unroll
-      for (int q = 0; q < kGroup; ++q) sp[q] = sq[q] = df{0.f, 0.f};
-      for (int64_t v0 = lo + tid; v0 < hi; v0 += kPer * kThreads) {
-        float lp[kGroup][kPer], lq[kGroup][kPer];
-#pragma unroll
-        for (int q = 0; q < kGroup; ++q) {
-          const bool on = g0 + q < nb && rec[g0 + q].resid;
-          const Rec& r = rec[on ? g0 + q : g0];
-          const char* pr = p.target + ((r.b * (int64_t)(p.K + 1) + r.j) * V) * p.esz;
-          const char* qr = p.draft + ((r.b * (int64_t)p.K + (r.resid ? r.j : 0)) * V) * p.esz;
-#pragma unroll
-          for (int u = 0; u < kPer; ++u) {
-            const int64_t v = v0 + (int64_t)u * kThreads;
-            lp[q][u] = (on && v < hi) ? load_elem<E>(pr, v) : -INFINITY;
-            lq[q][u] = (on && v < hi) ? load_elem<E>(qr, v) : -INFINITY;
-          }
-        }
-#pragma unroll
-        for (int q = 0; q < kGroup; ++q) {
-          if (!(g0 + q < nb && rec[g0 + q].resid)) continue;
-          setup(rec[g0 + q], false);
-#pragma unroll
-          for (int u = 0; u < kPer; ++u) {
-            sp[q] = df_add(sp[q], x.e(lp[q][u], x.mp, x.taup));
-            sq[q] = df_add(sq[q], x.e(lq[q][u], x.mq, x.tauq));
-          }
-        }
+    bool resid = r.resid != 0;
+    // the weight of element k of group g: from the kept e values or evaluated
+    // again from global memory
+    auto weight1 = [&](int g, int k) -> df {
+      if (cache) {
+        const df ep{cph[k * NGc + g], cpl[k * NGc + g]};
+        return resid ? x.resid_w(ep, df{cqh[k * NGc + g], cql[k * NGc + g]}) : ep;
       }
-#pragma unroll
-      for (int q = 0; q < kGroup; ++q) {
-        if (!(g0 + q < nb && rec[g0 + q].resid)) continue;  // uniform: rec is in shared memory
-        const df a = block_sum_df(sp[q], red, tid);
-        const df bq = block_sum_df(sq[q], red, tid);
+      const int64_t v = lo + 8 * (int64_t)g + k;
+      const df ep = x.e(v < hi ? load_elem<E>(prow, v) : -INFINITY, x.mp, x.taup);
+      if (!resid) return ep;
+      return x.resid_w(ep, x.e(v < hi ? load_elem<E>(qrow, v) : -INFINITY, x.mq, x.tauq));
+    };
+    __syncthreads();  // the previous draw is done with the shared arrays
+    // ---- step 1: e over the range (kept), and the residual's normalisers ----
+    if (resid || cache) {
+      df sp{0.f, 0.f}, sq{0.f, 0.f};
+      // group g is processed while group g + kThreads is loading; the element
+      // loop is not unrolled, so the double-float exp is one copy of code
+      Raw<E> cp, cq, np, nq;
+      if (tid < NG) {
+        load_raw<E>(prow, lo + 8 * (int64_t)tid, hi, vec, cp);
+        if (resid) load_raw<E>(qrow, lo + 8 * (int64_t)tid, hi, vec, cq);
+      }
+      for (int g = tid; g < NG; g += kThreads) {
+        const int gn = g + kThreads;
+        if (gn < NG) {
+          load_raw<E>(prow, lo + 8 * (int64_t)gn, hi, vec, np);
+          if (resid) load_raw<E>(qrow, lo + 8 * (int64_t)gn, hi, vec, nq);
+        }
+#pragma unroll 1
+        for (int k = 0; k < 8; ++k) {
+          const df ep = x.e(cp.at(k), x.mp, x.taup);
+          sp = df_add(sp, ep);
+          if (cache) {
+            cph[k * NGc + g] = ep.h;
+            cpl[k * NGc + g] = ep.l;
+          }
+          if (resid) {
+            const df eq = x.e(cq.at(k), x.mq, x.tauq);
+            sq = df_add(sq, eq);
+            if (cache) {
+              cqh[k * NGc + g] = eq.h;
+              cql[k * NGc + g] = eq.l;
+            }
+          }
+        }
+        cp = np;
+        cq = nq;
+      }
+      if (resid) {  // uniform: the record is the cluster's
+        block_sum2(sp, sq, s);
+        const int b = xc++ & 1;
         if (tid == 0) {
-          float* qq = p.part + ((int64_t)(g0 + q) * G + cta) * kRecFloats;
-          qq[0] = a.h;
-          qq[1] = a.l;
-          qq[2] = bq.h;
-          qq[3] = bq.l;
+          s.xs[b][0] = sp.h;
+          s.xs[b][1] = sp.l;
+          s.xs[b][2] = sq.h;
+          s.xs[b][3] = sq.l;
         }
-      }
-    }
-    ok = grid_barrier(p.ctl, ++nbar, &sh_ok);
-    if (!ok) break;
-    for (int f = 0; f < nb; ++f) {
-      if (!rec[f].resid) continue;  // uniform: rec is in shared memory
-      const Scan sa = cta_scan(p.part, f, G, 0, -1, -1.f, 0, wt_h, wt_l, wsi, wsj);
-      const Scan sb = cta_scan(p.part, f, G, 2, -1, -1.f, 0, wt_h, wt_l, wsi, wsj);
-      if (tid == 0) {
-        const df r = df_div(sa.total, sb.total);
-        rho_h[f] = r.h;
-        rho_l[f] = r.l;
-      }
-    }
-    __syncthreads();
-    // ---- phase 2: range totals of the weights; a second pass, from p itself,
-    // settles residuals of zero mass ----------------------------------------
-    // per (draw, CTA) record of 12 floats: [0..3] S_p, S_q; [4..5] total and
-    // [6] last positive index of pass 0; [7..8] and [9] of pass 1
-    for (int pass = 0; pass < 2 && ok; ++pass) {
-      int any = 0;
-      for (int g0 = 0; g0 < nb; g0 += kGroup) {
-        df t[kGroup];
-        int last[kGroup];
-        bool in[kGroup];
+        cluster_sync();
+        if (warp == 0) {
+          float a[4] = {0.f, 0.f, 0.f, 0.f};
+          if (lane < CL) {
 #pragma unroll
-        for (int q = 0; q < kGroup; ++q) {
-          t[q] = df{0.f, 0.f};
-          last[q] = -1;
-          in[q] = g0 + q < nb && (pass == 0 || (rec[g0 + q].resid && zero[g0 + q]));
-          any |= in[q];
-        }
-        for (int64_t v0 = lo + tid; v0 < hi; v0 += kPer * kThreads) {
-          float lp[kGroup][kPer], lq[kGroup][kPer];
-#pragma unroll
-          for (int q = 0; q < kGroup; ++q) {
-            const Rec& r = rec[in[q] ? g0 + q : g0];
-            const bool rs = in[q] && pass == 0 && r.resid;
-            const char* pr = p.target + ((r.b * (int64_t)(p.K + 1) + r.j) * V) * p.esz;
-            const char* qr = p.draft + ((r.b * (int64_t)p.K + (r.resid ? r.j : 0)) * V) * p.esz;
-#pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-              const int64_t v = v0 + (int64_t)u * kThreads;
-              lp[q][u] = (in[q] && v < hi) ? load_elem<E>(pr, v) : -INFINITY;
-              lq[q][u] = (rs && v < hi) ? load_elem<E>(qr, v) : -INFINITY;
-            }
+            for (int i = 0; i < 4; ++i) a[i] = dsmem_ld_f32(&s.xs[b][i], (uint32_t)lane);
           }
-#pragma unroll
-          for (int q = 0; q < kGroup; ++q) {
-            if (!in[q]) continue;
-            setup(rec[g0 + q], pass == 0 && rec[g0 + q].resid);
-            x.rho = df{rho_h[g0 + q], rho_l[g0 + q]};
-#pragma unroll
-            for (int u = 0; u < kPer; ++u) {
-              const df w = x.w_of(lp[q][u], lq[q][u]);
-              if (df_pos(w)) last[q] = (int)(v0 + (int64_t)u * kThreads);
-              t[q] = df_add(t[q], w);
-            }
+          df Sp{0.f, 0.f}, Sq{0.f, 0.f};
+          for (int q = 0; q < CL; ++q) {  // in rank order, the same in every CTA
+            Sp = df_add(Sp, df{__shfl_sync(0xffffffffu, a[0], q), __shfl_sync(0xffffffffu, a[1], q)});
+            Sq = df_add(Sq, df{__shfl_sync(0xffffffffu, a[2], q), __shfl_sync(0xffffffffu, a[3], q)});
+          }
+          if (lane == 0) {
+            const df rr = df_div(Sp, Sq);
+            s.bh[0] = rr.h;
+            s.bl[0] = rr.l;
           }
         }
-#pragma unroll
-        for (int q = 0; q < kGroup; ++q) {
-          if (!in[q]) continue;  // uniform: rec and zero are in shared memory
-          int l = last[q];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) l = max(l, __shfl_xor_sync(0xffffffffu, l, o));
-          const df tt = block_sum_df(t[q], red, tid);
-          if (lane == 0) lastw[warp] = l;
-          __syncthreads();
-          if (tid == 0) {
-            int l2 = -1;
-            for (int w = 0; w < kWarps; ++w) l2 = max(l2, lastw[w]);
-            float* qq = p.part + ((int64_t)(g0 + q) * G + cta) * kRecFloats;
-            qq[4 + 3 * pass] = tt.h;
-            qq[5 + 3 * pass] = tt.l;
-            qq[6 + 3 * pass] = __int_as_float(l2);
-          }
-          __syncthreads();
-        }
-      }
-      if (pass == 1 && !any) break;
-      ok = grid_barrier(p.ctl, ++nbar, &sh_ok);
-      if (!ok) break;
-      // ---- the crossing of each draw this pass settles --------------------------
-      for (int f = 0; f < nb; ++f) {
-        const bool in_pass = pass == 0 || (rec[f].resid && zero[f]);
-        if (!in_pass) continue;
-        const Scan sc = cta_scan(p.part, f, G, 4 + 3 * pass, 6 + 3 * pass, rec[f].u, cta, wt_h, wt_l, wsi, wsj);
-        const df Z = sc.total;
-        if (pass == 0) {
-          const int z = rec[f].resid && !df_pos(Z);
-          if (tid == 0) zero[f] = z;
-          if (z) continue;  // settled in the second pass
-        }
-        const df target = df_mul_f(Z, rec[f].u);
-        const df Pme = sc.excl_me;
-        const int owner = sc.owner;
-        const Rec& r = rec[f];
-        int32_t* out = p.out_tokens + (int64_t)r.b * (p.K + 1) + r.j;
-        if (owner < 0) {
-          // u*Z at or past the last partial sum: the last positive weight
-          if (cta == 0 && tid == 0) *out = sc.last;
-          continue;
-        }
-        if (cta != owner) continue;
-        setup(r, pass == 0 && r.resid);
-        x.rho = df{rho_h[f], rho_l[f]};
-        // pieces of 256 elements, one per warp, kWarps at a time
-        df base = Pme;
-        int tok = -1;
-        if (tid == 0) sh_tok = -1;
         __syncthreads();
-        for (int64_t s0 = lo; s0 < hi && tok < 0; s0 += 256 * kWarps) {
-          const int64_t e = s0 + (int64_t)warp * 256 + lane * 8;
-          float lp[8], lq[8];
-#pragma unroll
+        x.rho = df{s.bh[0], s.bl[0]};
+      }
+    }
+    // ---- step 2: chunk sums, the cluster's scan, the crossing ------------------
+    int32_t* out = p.out_tokens + (int64_t)r.b * (p.K + 1) + r.j;
+    for (int pass = 0; pass < 2; ++pass) {
+      int lastp = -1;  // the last positive weight this thread saw
+      for (int c = tid; c < NC; c += kThreads) {
+        df cs{0.f, 0.f};
+        for (int i = 0; i < m; ++i) {
+          const int g = c * m + i;
+          if (g >= NG) break;
+#pragma unroll 1
           for (int k = 0; k < 8; ++k) {
-            lp[k] = e + k < hi ? load_elem<E>(x.prow, e + k) : -INFINITY;
-            lq[k] = (e + k < hi && x.resid) ? load_elem<E>(x.qrow, e + k) : -INFINITY;
+            const df w = weight1(g, k);
+            cs = df_add(cs, w);
+            if (df_pos(w)) lastp = (int)(lo + 8 * (int64_t)g + k);
           }
-          df w[8];
-          df sl{0.f, 0.f};
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            w[k] = x.w_of(lp[k], lq[k]);
-            sl = df_add(sl, w[k]);
-          }
-          const df incl = warp_incl_scan_df(sl, lane);
-          if (lane == 31) {
-            wt_h[warp] = incl.h;
-            wt_l[warp] = incl.l;
-          }
-          __syncthreads();
-          // the bases of the pieces, in order; the first piece that crosses
-          df bw = base;
-          int cw = -1;
-          for (int q = 0; q < kWarps; ++q) {
-            const df nb2 = df_add(bw, df{wt_h[q], wt_l[q]});
-            if (q == warp) {
-              // this warp's base is bw
-              const uint32_t m = __ballot_sync(0xffffffffu, df_gt(df_add(bw, incl), target));
-              if (m && cw < 0) {
-                int t = -1;
-                if (lane == __ffs(m) - 1) {
-                  df C = df_add(bw, df_sub(incl, sl));
-                  for (int k = 0; k < 8 && t < 0; ++k) {
-                    C = df_add(C, w[k]);
-                    if (df_gt(C, target)) t = (int)(e + k);
-                  }
-                  for (int k = 7; k >= 0 && t < 0; --k)  // rounding between scan and walk
-                    if (df_pos(w[k])) t = (int)(e + k);
-                }
-                const uint32_t fm = __ballot_sync(0xffffffffu, t >= 0);
-                const int tv = __shfl_sync(0xffffffffu, t, fm ? __ffs(fm) - 1 : 0);
-                if (fm && lane == 0) sh_tok = tv;
-              }
-            }
-            if (cw < 0 && df_gt(nb2, target)) cw = q;
-            bw = nb2;
-          }
-          __syncthreads();
-          if (cw >= 0) tok = sh_tok;
-          base = bw;
-          __syncthreads();
         }
-        if (tok < 0)  // rounding between the ranks' totals and the walk: the range's last positive weight
-          tok = __float_as_int(__ldcg(p.part + ((int64_t)f * G + cta) * kRecFloats + 6 + 3 * pass));
-        if (tid == 0) *out = tok;
+        csh[c] = cs.h;
+        csl[c] = cs.l;
       }
       __syncthreads();
+      // thread t scans chunks [c0, c1): a contiguous run, in element order
+      const int cpt = (NC + kThreads - 1) / kThreads;
+      const int c0 = min(tid * cpt, NC), c1 = min(c0 + cpt, NC);
+      df run{0.f, 0.f};
+      for (int c = c0; c < c1; ++c) run = df_add(run, df{csh[c], csl[c]});
+      df incl = warp_incl_scan_df(run, lane);
+      int lm = lastp;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lm = max(lm, __shfl_xor_sync(0xffffffffu, lm, o));
+      if (lane == 31) {
+        s.wh[warp] = incl.h;
+        s.wl[warp] = incl.l;
+      }
+      if (lane == 0) s.wi[warp] = lm;
+      __syncthreads();
+      df below{0.f, 0.f}, tot{0.f, 0.f};
+      int L = -1;
+#pragma unroll 1
+      for (int w = 0; w < kWarps; ++w) {
+        const df tw{s.wh[w], s.wl[w]};
+        if (w < warp) below = df_add(below, tw);
+        tot = df_add(tot, tw);
+        L = max(L, s.wi[w]);
+      }
+      incl = df_add(below, incl);  // this CTA's sum up to the end of thread t's run
+      // exchange the range totals and last positive indices
+      const int b = xc++ & 1;
+      if (tid == 0) {
+        s.xs[b][0] = tot.h;
+        s.xs[b][1] = tot.l;
+        s.xs[b][2] = __int_as_float(L);
+      }
+      cluster_sync();
+      if (warp == 0) {
+        float a0 = 0.f, a1 = 0.f;
+        int a2 = -1;
+        if (lane < CL) {
+          a0 = dsmem_ld_f32(&s.xs[b][0], (uint32_t)lane);
+          a1 = dsmem_ld_f32(&s.xs[b][1], (uint32_t)lane);
+          a2 = dsmem_ld_s32(&s.xs[b][2], (uint32_t)lane);
+        }
+        df Z{0.f, 0.f}, base{0.f, 0.f};
+        int Lall = -1;
+        for (int q = 0; q < CL; ++q) {  // in rank order, the same in every CTA
+          const df t{__shfl_sync(0xffffffffu, a0, q), __shfl_sync(0xffffffffu, a1, q)};
+          if (q < (int)rank) base = df_add(base, t);
+          Z = df_add(Z, t);
+          Lall = max(Lall, __shfl_sync(0xffffffffu, a2, q));
+        }
+        const df target = df_mul_f(Z, r.u);
+        df acc{0.f, 0.f};
+        int owner = -1;
+        for (int q = 0; q < CL; ++q) {
+          acc = df_add(acc, df{__shfl_sync(0xffffffffu, a0, q), __shfl_sync(0xffffffffu, a1, q)});
+          if (owner < 0 && df_gt(acc, target)) owner = q;
+        }
+        if (lane == 0) {
+          s.bh[1] = Z.h;
+          s.bl[1] = Z.l;
+          s.bh[2] = base.h;
+          s.bl[2] = base.l;
+          s.bh[3] = target.h;
+          s.bl[3] = target.l;
+          s.bi[0] = owner;
+          s.bi[1] = Lall;
+        }
+      }
+      __syncthreads();
+      if (pass == 0 && resid && !df_pos(df{s.bh[1], s.bl[1]})) {
+        resid = false;  // a residual of zero mass: the draw is from p itself
+        continue;
+      }
+      const int owner = s.bi[0];
+      if (owner < 0) {
+        // u*Z at or past the last partial sum: the last positive weight
+        if (rank == 0 && tid == 0) *out = s.bi[1];
+        break;
+      }
+      if ((int)rank != owner) break;
+      const df base{s.bh[2], s.bl[2]}, target{s.bh[3], s.bl[3]};
+      const uint32_t mk = __ballot_sync(0xffffffffu, c0 < c1 && df_gt(df_add(base, incl), target));
+      if (lane == 0) s.wi[warp] = mk ? warp * 32 + __ffs(mk) - 1 : INT_MAX;
+      __syncthreads();
+      int first = INT_MAX;
+      for (int w = 0; w < kWarps; ++w) first = min(first, s.wi[w]);
+      if (first == INT_MAX) {
+        // rounding between the cluster's totals and this CTA's scan: the
+        // range's last positive weight
+        if (tid == 0) *out = L;
+      } else if (tid == first) {
+        df C = df_add(base, df_sub(incl, run));
+        int t = -1, lw = -1;
+        for (int c = c0; c < c1 && t < 0; ++c) {
+          for (int i = 0; i < m && t < 0; ++i) {
+            const int g = c * m + i;
+            if (g >= NG) break;
+#pragma unroll 1
+            for (int k = 0; k < 8; ++k) {
+              const df w = weight1(g, k);
+              if (df_pos(w)) lw = (int)(lo + 8 * (int64_t)g + k);
+              C = df_add(C, w);
+              if (df_gt(C, target)) {
+                t = (int)(lo + 8 * (int64_t)g + k);
+                break;
+              }
+            }
+          }
+        }
+        if (t < 0) t = lw >= 0 ? lw : L;  // rounding between the scan and the walk
+        *out = t;
+      }
+      break;
     }
-    if (!ok) break;
-    ok = grid_barrier(p.ctl, ++nbar, &sh_ok);  // the partials may be reused
   }
+  cluster_sync();  // no CTA leaves while another may still read its exchange slots
   // ---- the last CTA out leaves the control words at zero ------------------------
-  __syncthreads();
   if (tid == 0) {
-    if (!ok) atomicOr(p.status, kStatusTimeout);
     __threadfence();
-    if (atomicAdd(&p.ctl[2], 1u) == (uint32_t)G - 1) {
+    if (atomicAdd(&p.ctl[1], 1u) == gridDim.x - 1) {
       p.ctl[0] = 0;
-      p.ctl[1] = 0;
-      p.ctl[3] = 0;
       __threadfence();
-      p.ctl[2] = 0;
+      p.ctl[1] = 0;
     }
   }
 }
 
 }  // namespace
-
-size_t part_bytes(int grid) { return (size_t)kMaxBatch * grid * kRecFloats * sizeof(float); }
 
 void fill_table(Params& p, float temperature) {
   for (int i = 0; i < 32; ++i) {
@@ -484,15 +466,125 @@ void fill_table(Params& p, float temperature) {
   p.c_lo = (float)(cd - (double)p.c_hi);
 }
 
-cudaError_t launch(const Params& p, int grid, cudaStream_t stream) {
-  if (grid > kThreads) grid = kThreads;  // one CTA per thread in cta_scan
+namespace {
+
+// Launch shape per (device, V, element size).
+struct Shape {
+  int CL = 0, m = 1, NC = 0, cache = 0, clusters = 0;
+  int64_t RL = 0;
+  size_t smem = 0;
+};
+std::mutex g_mu;
+std::map<std::tuple<int, int64_t, int>, Shape> g_shapes;
+
+// The most dynamic shared memory the kernel may ask for on this device (the
+// attribute is raised once per device and kernel).
+template <typename E>
+cudaError_t prepare(int dev, size_t& budget) {
+  static std::map<int, size_t> done;
+  auto it = done.find(dev);
+  if (it != done.end()) {
+    budget = it->second;
+    return cudaSuccess;
+  }
+  int optin = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  const size_t b = (size_t)optin > sizeof(Shared) + 2048 ? (size_t)optin - sizeof(Shared) - 2048 : 0;
+  e = cudaFuncSetAttribute(refine_kernel<E>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)b);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(refine_kernel<E>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e != cudaSuccess) {
+    cudaGetLastError();  // only portable sizes then
+  }
+  done[dev] = b;
+  budget = b;
+  return cudaSuccess;
+}
+
+// CL: the smallest power of two that gives each CTA at most 4096 elements,
+// capped at kMaxCluster, halved until the device can hold such a cluster.
+template <typename E>
+cudaError_t plan(int dev, int64_t V, Shape& sh) {
+  size_t budget = 0;
+  cudaError_t e = prepare<E>(dev, budget);
+  if (e != cudaSuccess) return e;
+  int want = 1;
+  while (want < kMaxCluster && (int64_t)want * 4096 < V) want <<= 1;
+  for (int CL = want; CL >= 1; CL >>= 1) {
+    Shape t;
+    t.CL = CL;
+    t.RL = ((V + CL - 1) / CL + 7) / 8 * 8;
+    const int64_t NGc = t.RL / 8;
+    t.m = (int)((NGc + kMaxChunks - 1) / kMaxChunks);
+    t.NC = (int)((NGc + t.m - 1) / t.m);
+    const size_t sums = (size_t)t.NC * 8;
+    t.cache = (size_t)NGc * 128 + sums <= budget;
+    t.smem = (t.cache ? (size_t)NGc * 128 : 0) + sums;
+    if (t.smem > budget) continue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)CL);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = t.smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, refine_kernel<E>, &cfg) != cudaSuccess) {
+      cudaGetLastError();
+      n = 0;
+    }
+    if (n < 1) continue;
+    t.clusters = n;
+    sh = t;
+    return cudaSuccess;
+  }
+  return cudaErrorInvalidConfiguration;
+}
+
+}  // namespace
+
+cudaError_t launch(Params& p, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  Shape sh;
+  {
+    std::lock_guard<std::mutex> lk(g_mu);
+    const auto key = std::make_tuple(dev, p.V, p.esz);
+    auto it = g_shapes.find(key);
+    if (it != g_shapes.end()) {
+      sh = it->second;
+    } else {
+      e = p.esz == 2 ? plan<uint16_t>(dev, p.V, sh) : plan<float>(dev, p.V, sh);
+      if (e != cudaSuccess) return e;
+      g_shapes[key] = sh;
+    }
+  }
+  p.CL = sh.CL;
+  p.RL = sh.RL;
+  p.m = sh.m;
+  p.NC = sh.NC;
+  p.cache = sh.cache;
+  p.vec = (reinterpret_cast<uintptr_t>(p.target) % 16 == 0 && reinterpret_cast<uintptr_t>(p.draft) % 16 == 0 &&
+           (p.V * p.esz) % 16 == 0)
+              ? 1
+              : 0;
+  const int64_t clusters = p.B < sh.clusters ? p.B : sh.clusters;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)grid);
+  cfg.gridDim = dim3((unsigned)(clusters * sh.CL));
   cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = sh.smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)sh.CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
@@ -501,7 +593,7 @@ cudaError_t launch(const Params& p, int grid, cudaStream_t stream) {
     return p.esz == 2 ? cudaLaunchKernelEx(&c, refine_kernel<uint16_t>, p)
                       : cudaLaunchKernelEx(&c, refine_kernel<float>, p);
   };
-  cudaError_t e = go(cfg);
+  e = go(cfg);
   if (e != cudaSuccess) {  // without programmatic serialisation
     cudaGetLastError();
     cfg.numAttrs = 1;

@@ -1,5 +1,5 @@
 // sv_refine.h — the draws that fp32 cannot settle, redone in double-float
-// arithmetic over the whole GPU (sv_refine.cu). Not part of the public ABI.
+// arithmetic (sv_refine.cu). Not part of the public ABI.
 //
 // A sampling draw finds the smallest t with sum_{v<=t} w_v > u*Z in fp32.
 // When u*Z lands within kRefineMargin*Z of an edge of the chosen token's CDF
@@ -20,9 +20,10 @@ namespace rf {
 // every weight and normaliser) shifts the CDF by up to a few 1e-8 of Z;
 // with the running sums in double-float, 1e-7 of Z leaves room for both.
 constexpr float kRefineMargin = 1e-7f;
-// Flagged draws handled together in one pass of the refine kernel.
-constexpr int kMaxBatch = 64;
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+// Largest thread-block cluster the refine kernel asks for (a non-portable
+// size; smaller ones are used where the device cannot schedule it).
+constexpr int kMaxCluster = 16;
 
 // One flagged draw: sequence b drew position j from target row (b, j)
 // (minus draft row (b, j) after a rejection) with uniform u; M are the
@@ -35,7 +36,7 @@ struct Rec {
 };
 
 // Control words of the refine kernel, zero between calls: [0] flagged
-// draws, [1] grid-barrier arrivals, [2] CTAs finished, [3] abort.
+// draws, [1] CTAs finished, [2..3] unused.
 constexpr int kCtlWords = 4;
 
 struct Params {
@@ -46,11 +47,16 @@ struct Params {
   float c_hi, c_lo;    // log2(e)/T as a double-float
   float tab_hi[32], tab_lo[32];
   uint32_t* ctl;       // kCtlWords words
-  uint32_t* status;    // sticky status word of the call's scratch
   uint32_t* stats;     // nullable: a running count of the draws refined
   Rec* recs;           // [B]
-  float* part;         // [kMaxBatch][grid][8]
   int32_t* out_tokens; // [B, K+1]
+  // launch shape (filled by launch())
+  int CL;      // CTAs per draw: one thread-block cluster
+  int m;       // groups of 8 elements per chunk
+  int NC;      // chunks per CTA
+  int cache;   // 1: the double-float e values of the range stay in shared memory
+  int vec;     // 1: rows start on 16-byte boundaries (128-bit loads)
+  int64_t RL;  // elements per CTA, a multiple of 8
 };
 
 // Appends a flagged draw (device side; any thread).
@@ -59,9 +65,10 @@ __device__ __forceinline__ void flag(uint32_t* ctl, Rec* recs, int64_t B, const 
   if (slot < (uint32_t)B) recs[slot] = r;
 }
 
-size_t part_bytes(int grid);
 void fill_table(Params& p, float temperature);
-cudaError_t launch(const Params& p, int grid, cudaStream_t stream);
+// Plans the launch shape for p.V / p.esz on the current device and launches
+// one grid of clusters (as many as can be resident, at most B) on `stream`.
+cudaError_t launch(Params& p, cudaStream_t stream);
 
 }  // namespace rf
 }  // namespace sv

@@ -265,9 +265,261 @@ __global__ void __launch_bounds__(kRowsThreads, 4) rows_kernel(const Params p) {
   }
 }
 
+// ------------------------------------------------------------ top-p rows ---
+// With top-p < 1 ("Speculative Decoding —— LLM推理优化技术（一）" §4; kwkr.cn
+// "投机解码" §3.4: top-p applied to both p and q), each row also needs its
+// nucleus: the largest key tau (the order-preserving key of the bf16 logit;
+// equal logits share one) whose upper set {v : key(l_v) >= tau} holds mass
+// >= top_p * s, and that mass cum. One CTA per row at a time (persistent
+// CTAs, four per SM, taking rows g = blockIdx.x, + gridDim.x, ...); the row
+// streams through registers in batches of 32 KB, and per batch the CTA
+//  - raises its running max M (NaN-propagating) and rescales its running sum
+//    s = sum 2^(l c - fl(M c));
+//  - counts the elements whose keys lie in the window of kTpWin keys below
+//    key(M) (bin i holds key(M) - i); an element below the window costs one
+//    compare. When M rises the window slides up by as many keys: bins that
+//    fall off hold keys below the new window, and no later element can
+//    bring them back.
+// At the end of the row, bin i weighs count * 2^(val(key) c - fl(M c)); the
+// scan from the top key finds the cut. A row whose cut lies below the window
+// (a flat row) is read twice more: once for the masses of coarse bins of 256
+// keys below the window, once for the exact keys of the coarse bin that holds
+// the cut.
+constexpr int kTpThreads = 256;
+constexpr int kTpWarps = kTpThreads / 32;
+constexpr int kTpVecs = 8;    // 16-byte vectors per thread and batch: 32 KB per CTA
+constexpr int kTpWin = 256;   // exact keys counted while the row streams (one bin per thread)
+static_assert(kTpWin == kTpThreads, "one window bin per thread");
+
+struct TpShared {
+  union {
+    uint32_t u[kTpWin];
+    float f[kTpWin];
+  } hist;
+  float red[2][kTpWarps];
+  float bf[2];
+  int bi[2];
+};
+
+// Inclusive scan of v over the CTA in thread order; *total gets the sum.
+// `par` picks the partials buffer (alternating calls need no extra barrier).
+__device__ __forceinline__ float tp_scan(float v, float* total, TpShared& s, int& par) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const float incl = warp_incl_scan(v, lane);
+  if (lane == 31) s.red[par][warp] = incl;
+  __syncthreads();
+  float below = 0.f, t = 0.f;
+#pragma unroll
+  for (int w = 0; w < kTpWarps; ++w) {
+    if (w < warp) below += s.red[par][w];
+    t += s.red[par][w];
+  }
+  par ^= 1;
+  *total = t;
+  return below + incl;
+}
+
+// The lowest thread index whose flag is set (INT_MAX: none), for every thread.
+__device__ __forceinline__ int tp_first(bool flag, TpShared& s) {
+  if (threadIdx.x == 0) s.bi[0] = INT_MAX;
+  __syncthreads();
+  if (flag) atomicMin(&s.bi[0], (int)threadIdx.x);
+  __syncthreads();
+  const int r = s.bi[0];
+  __syncthreads();
+  return r;
+}
+
+// Every element of the row (8 at a time) to f(x[8]).
+template <typename F>
+__device__ __forceinline__ void tp_reread(const uint4* vp, int64_t nvec, F f) {
+  for (int64_t i = threadIdx.x; i < nvec; i += kTpThreads) {
+    float x[8];
+    Elem<uint16_t>::unpack(__ldg(vp + i), x);
+    f(x);
+  }
+}
+
+__global__ void __launch_bounds__(kTpThreads, 4) topp_rows_kernel(const Params p) {
+  __shared__ TpShared s;
+  grid_dependency_sync(true);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float c = p.c;
+  const int64_t rows = p.B * p.R;
+  const int64_t nvec = p.V / 8;  // V is a multiple of 8 and rows start 16-byte aligned
+  int par = 0;                   // which red[] buffer the next reduction uses
+  for (int64_t g = blockIdx.x; g < rows; g += gridDim.x) {
+    const char* row = row_of(p, g);
+    const uint4* vp = reinterpret_cast<const uint4*>(row);
+    s.hist.u[tid] = 0u;
+    __syncthreads();
+    float M = -INFINITY;    // block-uniform running max
+    uint32_t hi = 0u;       // key(M) once M > -inf
+    float tlo = INFINITY;   // smallest value in the window: x >= tlo <=> key(x) >= hi - kTpWin + 1
+    float sth = 0.f;        // this thread's sum against fl(M c)
+    bool valid = true;
+    // batches of kTpThreads * kTpVecs vectors (the loop bound is the same in
+    // every thread: the batch holds barriers)
+    for (int64_t b0 = 0; b0 < nvec; b0 += (int64_t)kTpThreads * kTpVecs) {
+      uint4 v[kTpVecs];
+#pragma unroll
+      for (int u = 0; u < kTpVecs; ++u) {
+        const int64_t i = b0 + tid + (int64_t)u * kTpThreads;
+        v[u] = i < nvec ? __ldg(vp + i) : make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+      }
+      float bm = Elem<uint16_t>::vmax(v[0]);
+#pragma unroll
+      for (int u = 1; u < kTpVecs; ++u) bm = fmax_nan(bm, Elem<uint16_t>::vmax(v[u]));
+      bm = warp_max_nan(bm);
+      if (lane == 0) s.red[par][warp] = bm;
+      __syncthreads();
+      float Mn = M;
+#pragma unroll
+      for (int w = 0; w < kTpWarps; ++w) Mn = fmax_nan(Mn, s.red[par][w]);
+      par ^= 1;
+      if (!(Mn < INFINITY)) {  // a NaN or +inf: the row is invalid (uniform)
+        M = Mn;
+        valid = false;
+        break;
+      }
+      if (Mn == -INFINITY) continue;  // only -inf so far (uniform)
+      if (Mn != M) {                  // uniform: every thread took the same max
+        if (M > -INFINITY) sth *= ex2(__fsub_rn(__fmul_rn(M, c), __fmul_rn(Mn, c)));
+        const uint32_t nhi = key_bf16(Mn);
+        if (M > -INFINITY && nhi != hi) {
+          // slide the window up by d keys: bin i now holds what bin i - d held
+          const uint32_t dk = nhi - hi;
+          const uint32_t t = (uint32_t)tid >= dk ? s.hist.u[tid - dk] : 0u;
+          __syncthreads();
+          s.hist.u[tid] = t;
+          __syncthreads();
+        }
+        hi = nhi;
+        M = Mn;
+        const uint32_t lo = hi >= (uint32_t)(kTpWin - 1) ? hi - (uint32_t)(kTpWin - 1) : 0u;
+        tlo = lo <= key_bf16(-INFINITY) ? -INFINITY : val_bf16(lo);
+      }
+      const float mref = __fmul_rn(M, c);
+#pragma unroll
+      for (int u = 0; u < kTpVecs; ++u) {
+        float x[8];
+        Elem<uint16_t>::unpack(v[u], x);
+        float a = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          a += ex2(fmaf(x[k], c, -mref));
+          if (x[k] >= tlo) atomicAdd(&s.hist.u[hi - key_bf16(x[k])], 1u);
+        }
+        sth += a;
+      }
+    }
+    __syncthreads();  // every count is in
+    float S = 0.f, cum = 0.f;
+    uint32_t tau = 0u;
+    if (valid && M > -INFINITY) {
+      const float mref = __fmul_rn(M, c);
+      float tot;
+      (void)tp_scan(sth, &S, s, par);
+      cum = S;
+      const float target = p.top_p * S;
+      const uint32_t lo = hi >= (uint32_t)(kTpWin - 1) ? hi - (uint32_t)(kTpWin - 1) : 0u;
+      // the window: bin t is key hi - t
+      const uint32_t cnt = (uint32_t)tid <= hi - lo ? s.hist.u[tid] : 0u;
+      float m = cnt ? (float)cnt * ex2(fmaf(val_bf16(hi - (uint32_t)tid), c, -mref)) : 0.f;
+      float incl = tp_scan(m, &tot, s, par);
+      int t = tp_first(incl >= target, s);
+      if (t != INT_MAX) {
+        if (tid == t) {
+          s.bi[1] = (int)(hi - (uint32_t)t);
+          s.bf[0] = incl;
+        }
+      } else if (lo == 0u) {  // every key seen: rounding left the mass short of top_p * s
+        if (tid == 0) {
+          s.bi[1] = 0;
+          s.bf[0] = tot;
+        }
+      } else {
+        // The cut lies below the window. Coarse bins: the masses of the keys
+        // below the window, 256 keys per bin (thread t takes bin 255 - t, so
+        // that thread order is descending keys).
+        const float above = tot;
+        s.hist.f[tid] = 0.f;
+        __syncthreads();
+        tp_reread(vp, nvec, [&](const float* x) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t key = key_bf16(x[k]);
+            if (key < lo) atomicAdd(&s.hist.f[key >> 8], ex2(fmaf(x[k], c, -mref)));
+          }
+        });
+        __syncthreads();
+        m = s.hist.f[kTpWin - 1 - tid];
+        incl = above + tp_scan(m, &tot, s, par);
+        t = tp_first(incl >= target, s);
+        if (t == INT_MAX) {  // rounding: keep everything
+          if (tid == 0) {
+            s.bi[1] = 0;
+            s.bf[0] = above + tot;
+          }
+        } else {
+          // the exact keys of coarse bin 255 - t (those below the window)
+          const uint32_t lo2 = (uint32_t)(kTpWin - 1 - t) << 8;
+          const uint32_t top2 = min(lo2 + 255u, lo - 1u);
+          if (tid == t) s.bf[1] = incl - m;  // the mass above the coarse bin
+          __syncthreads();
+          const float above2 = s.bf[1];
+          s.hist.u[tid] = 0u;
+          __syncthreads();
+          tp_reread(vp, nvec, [&](const float* x) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const uint32_t key = key_bf16(x[k]);
+              if (key >= lo2 && key <= top2) atomicAdd(&s.hist.u[top2 - key], 1u);
+            }
+          });
+          __syncthreads();
+          const uint32_t c2 = (uint32_t)tid <= top2 - lo2 ? s.hist.u[tid] : 0u;
+          m = c2 ? (float)c2 * ex2(fmaf(val_bf16(top2 - (uint32_t)tid), c, -mref)) : 0.f;
+          incl = above2 + tp_scan(m, &tot, s, par);
+          t = tp_first(incl >= target, s);
+          if (t != INT_MAX) {
+            if (tid == t) {
+              s.bi[1] = (int)(top2 - (uint32_t)t);
+              s.bf[0] = incl;
+            }
+          } else if (tid == 0) {  // rounding: the whole coarse bin
+            s.bi[1] = (int)lo2;
+            s.bf[0] = above2 + tot;
+          }
+        }
+      }
+      __syncthreads();
+      tau = (uint32_t)s.bi[1];
+      cum = s.bf[0];
+    }
+    if (tid == 0) {
+      p.rstat[g] = make_float4(M, S, cum, __uint_as_float(tau));
+      gather(p, g, row, 0, p.V, token_of(p, g));
+    }
+    __syncthreads();  // the histogram and red[] are free for the next row
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_rows(const Params& p, int dtype, cudaStream_t stream) {
+  if (p.topp) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.rows_grid);
+    cfg.blockDim = dim3(kTpThreads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, topp_rows_kernel, p);
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)p.items);
   cfg.blockDim = dim3(kRowsThreads);

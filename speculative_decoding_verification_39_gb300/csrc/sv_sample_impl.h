@@ -22,6 +22,10 @@ struct ScratchArea {
 // `data_bytes` of data for work on `stream`; returns an sv_status.
 typedef int (*ScratchGet)(void* ctx, cudaStream_t stream, size_t cnt_words, size_t data_bytes, ScratchArea* out);
 
+// Adds n to the count sv_launch_count reports (kernels launched by entry
+// points outside sv_api.cu).
+void note_launches(int n);
+
 int verify_sample_impl(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
                        const float* uniforms, int64_t B, int32_t K, int64_t V, int32_t dtype, float temperature,
                        float top_p, int32_t* out_tokens, int32_t* out_accept_len, float* out_row_stats,

@@ -54,7 +54,12 @@ struct Params {
   uint32_t row_slot;        // bytes of a stage per row of a group (RPI > 1)
   uint32_t stage_bytes;     // bytes of one shared-memory stage
   int64_t rows_grid;        // persistent CTAs of the row pass
-  float2* part;             // [B*R*NCH] {max raw logit, sum 2^(l*c - fl(max*c))}
+  float2* part;             // [B*R*NCH] {max raw logit, sum 2^(l*c - fl(max*c))} (top_p == 1)
+  // top-p < 1 (bf16 rows): the row pass takes whole rows, one CTA each, and
+  // writes each row's statistics whole
+  int topp;
+  float top_p;
+  float4* rstat;            // [B*R] {M, s, cum, tau key as bits} (topp)
   float* gz;                // [B, 2K] raw logit of x_i: target row i at [b*2K + i], draft row i at [b*2K + K + i]
   uint32_t* ctl;            // ctl[3]: sticky status bits
   uint32_t* rf_ctl;         // the refine kernel's control words (zero between calls)
@@ -70,6 +75,8 @@ struct Params {
 
 // Shapes this path takes (the rest go to the streaming kernel).
 bool fits(int64_t K, int64_t V);
+// With top-p < 1: bf16 rows whose byte length is a multiple of 16.
+bool fits_topp(int64_t K, int64_t V, int esz);
 // Fills the layout fields (CE, NCH, RPI, items, stage sizes, grids, D,
 // ncell, cpr, the table) from B, K, V, esz, T and the device's SM count.
 void plan(Params& p, int sms);

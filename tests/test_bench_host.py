@@ -61,13 +61,26 @@ def test_reference_arm_prints_one_contract_line():
 def test_config_names():
     assert bench.config_names("cfg2_v32000_bf16") == ["cfg2_v32000_bf16"]
     assert bench.config_names("cfg1_v1000_f32, la_sample_v32000_bf16") == ["cfg1_v1000_f32", "la_sample_v32000_bf16"]
-    every = list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS)
+    every = list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS) + list(bench.POOL_WORKLOADS)
     # the headline workload (the largest) first, then every other one, each once
     for spec in ("all", None):
         names = bench.config_names(spec)
         assert names[0] == "cfg3_v128256_bf16" and sorted(names) == sorted(every)
     with pytest.raises(KeyError):
         bench.config_names("cfg2_v32000_bf16,nope")
+    # the pool is a per_config record, never the line's own workload
+    assert bench.config_names("cfg2_v32000_bf16,ngram_pool_v32000") == ["cfg2_v32000_bf16", "ngram_pool_v32000"]
+    with pytest.raises(KeyError):
+        bench.config_names("ngram_pool_v32000")
+
+
+def test_pool_inputs_are_seeded_and_hit_the_keys():
+    w = bench.POOL_WORKLOADS["ngram_pool_v32000"]
+    a, la = bench.pool_inputs(w, 4)
+    b, lb = bench.pool_inputs(w, 4)
+    assert (a == b).all() and (la == lb).all()
+    assert a.shape == (4, w["B"], w["W"], w["N"]) and la.shape == (4, w["B"])
+    assert a[..., 0].max() < w["keys"] and la.max() < w["keys"] and a.max() < w["V"] and a.min() >= 0
 
 
 def test_launched_kernel_follows_the_library_rule():
@@ -76,7 +89,7 @@ def test_launched_kernel_follows_the_library_rule():
         greedy_path = 0
     for name, kernel in (("cfg1_v1000_f32", "verify_warp_kernel"), ("cfg3_v128256_bf16", "verify_kernel"),
                          ("cfg2_v32000_bf16", "rows_kernel"),
-                         ("cfg5_topp_v151936_bf16", "verify_kernel"), ("cfg4_greedy_v32000_bf16", "gr_rows_kernel"),
+                         ("cfg5_topp_v151936_bf16", "topp_rows_kernel"), ("cfg4_greedy_v32000_bf16", "gr_rows_kernel"),
                          ("la_sample_v32000_bf16", "la_rows_kernel"), ("md_sample_v32000_bf16", "md_rows_kernel")):
         cfg, mode = bench.workload(name)[:2]
         assert bench.launched_kernel(cfg, mode, A) == kernel, name
@@ -84,4 +97,12 @@ def test_launched_kernel_follows_the_library_rule():
     cfg, mode = bench.workload("cfg1_v1000_f32")[:2]
     assert bench.launched_kernel(cfg, mode, A) == "verify_warp_kernel"
     cfg, mode = bench.workload("cfg4_greedy_v32000_bf16")[:2]
+    assert bench.launched_kernel(cfg, mode, A) == "verify_kernel"
+
+
+def test_launched_kernel_topp_streaming_on_request():
+    class A:
+        sample_path = 1
+        greedy_path = 0
+    cfg, mode = bench.workload("cfg5_topp_v151936_bf16")[:2]
     assert bench.launched_kernel(cfg, mode, A) == "verify_kernel"

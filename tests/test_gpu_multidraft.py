@@ -31,6 +31,10 @@ CASES = {
     "bf16_v2000_g1_n6": MD.with_(B=30, V=2000, G=1, N=6, temperature=0.8, seed=4),
     "bf16_v500_g32_n3": MD.with_(B=6, V=500, G=32, N=3, seed=5),
     "bf16_v151936_g3_n3": MD.with_(B=4, V=151936, G=3, N=3, temperature=0.7, seed=6),
+    # the walk with the position's distribution in shared memory: at its
+    # largest row, and a row that is not a whole number of 16-byte vectors
+    "bf16_v51200_g4_n4": MD.with_(B=8, V=51200, G=4, N=4, seed=7),
+    "bf16_v32007_g7_n5": MD.with_(B=8, V=32007, seed=8),
 }
 
 

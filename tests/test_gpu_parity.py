@@ -41,6 +41,13 @@ SAMPLE_CASES = {
     "topp_ragged_bf16": C["cfg5_topp_v151936_bf16"].with_(B=6, K=3, V=20011, top_p=0.8),
     "topp_flat": C["cfg2_v32000_bf16"].with_(B=6, K=2, V=9000, target_sigma=0.05, draft_sigma=0.02, top_p=0.95,
                                              n_peaks=0),
+    # top-p row pass: clusters of 2, 4 and 16 CTAs per row; a flat row whose
+    # cut lies below the first window of keys; a nucleus of about one token
+    "topp_d2_v40000": C["cfg5_topp_v151936_bf16"].with_(B=6, K=3, V=40000),
+    "topp_d4_flat_v70000": C["cfg2_v32000_bf16"].with_(B=4, K=2, V=70000, target_sigma=0.05, draft_sigma=0.02,
+                                                       top_p=0.95, n_peaks=0),
+    "topp_d16_v200000": C["cfg5_topp_v151936_bf16"].with_(B=2, K=2, V=200000),
+    "topp_p005_v32000": C["cfg5_topp_v151936_bf16"].with_(B=8, K=4, V=32000, top_p=0.05),
     "hot_T2": C["cfg2_v32000_bf16"].with_(B=10, K=4, V=16384, temperature=2.0),
     # whole sequences in one CTA (2K+1 rows within 48 KB, rows 16-byte aligned);
     # rows of at most 1024 elements: one warp per sequence
