@@ -27,6 +27,14 @@ one-element torch kernel that ends the overlap, minus that kernel's own time.
 ``e2e`` repeats the metric through the public API with pinned host buffers,
 copies included. ``--impl reference`` times the CPU oracle (the baseline this
 project is checked against) on a bounded sample of the same workload.
+
+Two more per_config records are not verify calls of logits: the Lookahead
+n-gram pool (one insert and one lookup per step) and the verify on LM-head
+hidden states (the tcgen05 GEMM h.W^T of both heads, then the verify).
+
+``--calls N`` runs N plain calls of the first named workload (no graphs, no
+timing, no oracle) and exits: the command the ncu summaries under profiles/
+are taken with.
 """
 from __future__ import annotations
 
@@ -68,6 +76,13 @@ def log(*a):
 # token). First tokens and last tokens come from 64 ids, so that lookups find
 # n-grams; the other tokens are uniform over the vocabulary.
 POOL_WORKLOADS = {"ngram_pool_v32000": {"B": 32, "V": 32000, "N": 5, "cap": 7, "G": 7, "W": 7, "keys": 64}}
+
+# The verify on LM-head hidden states (reading c24): cfg2's verify shape
+# (B = 64, K = 5, V = 32000, T = 1) on hidden states of D = 4096, the hidden
+# size of the 7B models the pages use as targets and drafts; hidden states
+# N(0, 1) and heads N(0, 1/D), bf16, seeded.
+LMHEAD_WORKLOADS = {"lmhead_d4096_v32000": {"B": 64, "K": 5, "D": 4096, "V": 32000, "T": 1.0}}
+EXTRA_WORKLOADS = set(POOL_WORKLOADS) | set(LMHEAD_WORKLOADS)
 
 
 def find_config(name: str):
@@ -665,6 +680,166 @@ def measure_pool(args, name: str, steps: int, cpu_budget: float, counts: bool):
     return rec
 
 
+def lmhead_inputs(w: dict, dev, seed: int = 0) -> dict:
+    """Seeded LM-head inputs on the device: hidden states N(0,1), heads
+    N(0,1/D) (bf16), draft tokens drawn from the draft's own logits at T
+    (Gumbel-max), uniforms U(0,1)."""
+    import torch
+    B, K, D, V, T = w["B"], w["K"], w["D"], w["V"], w["T"]
+    g = torch.Generator(device=dev).manual_seed(seed)
+    ht = torch.randn(B, K + 1, D, device=dev, generator=g).to(torch.bfloat16)
+    hd = torch.randn(B, K, D, device=dev, generator=g).to(torch.bfloat16)
+    wt = (torch.randn(V, D, device=dev, generator=g) / math.sqrt(D)).to(torch.bfloat16)
+    wd = (torch.randn(V, D, device=dev, generator=g) / math.sqrt(D)).to(torch.bfloat16)
+    ld = hd.reshape(B * K, D).float() @ wd.float().T
+    gum = -torch.log(-torch.log(torch.rand(ld.shape, device=dev, generator=g).clamp_min(1e-30)))
+    x = (ld / T + gum).argmax(dim=1).to(torch.int32).reshape(B, K)
+    u = torch.rand(B, K + 1, device=dev, generator=g)
+    return {"ht": ht, "hd": hd, "wt": wt, "wd": wd, "x": x, "u": u}
+
+
+def measure_lmhead(args, name: str, steps: int, cpu_budget: float, counts: bool):
+    """The verify on LM-head hidden states: one call = the GEMM of both heads
+    on the tensor cores (2*(B(K+1)+BK)*V*D flops) and the verify of its fp32
+    logits. Timed over a CUDA graph of exactly ``steps`` calls; parity against
+    the oracle (fp64 logits) on the first sequences."""
+    import torch
+    import speculative_decoding_verification_39_gb300 as svpkg
+    w = LMHEAD_WORKLOADS[name]
+    B, K, D, V, T = w["B"], w["K"], w["D"], w["V"], w["T"]
+    dev = torch.device("cuda", torch.cuda.current_device())
+    log(f"[bench] {name}: B={B} K={K} D={D} V={V}")
+    inp = lmhead_inputs(w, dev)
+    stream = torch.cuda.Stream(dev)
+    args_t = (inp["ht"], inp["hd"], inp["wt"], inp["wd"], inp["x"], inp["u"], T)
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            out = svpkg.verify_sample_lmhead(*args_t)
+    stream.synchronize()
+    launches_before = svpkg.launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(steps):
+            out = svpkg.verify_sample_lmhead(*args_t)
+    captured = svpkg.launch_count() - launches_before
+    with ClockSampler(int(os.environ.get("LOCAL_RANK", "0"))) as clk:
+        t_pre = time.perf_counter()
+        with torch.cuda.stream(stream):
+            while time.perf_counter() - t_pre < 0.5:
+                graph.replay()
+                stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+    with torch.cuda.stream(stream):
+        if svpkg.get_status() != 0:
+            raise RuntimeError("device status set by the LM-head verify")
+    ms_per_step = ms / steps
+    flops = 2.0 * (B * (K + 1) + B * K) * V * D
+    tflops = flops / (ms_per_step / 1e3) / 1e12
+    peak = measured_bf16_tflops()
+    rec = {
+        "workload": {"workload": name, "mode": "lmhead_sample", "B": B, "K": K, "D": D, "V": V, "temperature": T,
+                     "hidden": "bf16", "l2": "heads (2 x 262 MB) larger than L2"},
+        "value": B * (K + 1) / (ms_per_step / 1e3),
+        "unit": "positions/s",
+        "ms_per_step": ms_per_step,
+        "steps": steps,
+        "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak[0], "unit": "TFLOP/s",
+                     "frac": tflops / peak[0], "peak_source": peak[1], "traffic": None,
+                     "algorithmic_flops_per_launch": flops, "kernel": "lmhead_kernel",
+                     "note": "whole call (the GEMM of both heads and the verify of its fp32 logits) against the "
+                             "GEMM's flops: a lower bound on the GEMM kernel's own rate",
+                     "timing": "CUDA events over one graph of the timed calls"},
+        "clocks": clk.summary(),
+        "gpu_launches": int(captured),
+    }
+    if counts or cpu_budget > 0:
+        import oracle
+        nb = 4
+        host = {k: (v[:nb] if k in ("ht", "hd", "x", "u") else v) for k, v in inp.items()}
+        host = {k: (v.view(torch.int16).cpu().numpy().view(np.uint16) if v.dtype == torch.bfloat16 else
+                    v.cpu().numpy()) for k, v in host.items()}
+        t0 = time.perf_counter()
+        ot, oa, om = oracle.verify_sample_lmhead(host["ht"], host["hd"], host["wt"], host["wd"], host["x"], host["u"],
+                                                 T)
+        el = time.perf_counter() - t0
+        gt, ga = out[0][:nb].cpu().numpy(), out[1][:nb].cpu().numpy()
+        if counts:
+            diff = (gt != ot).any(1) | (ga != oa)
+            near = om < 1e-6
+            rec["parity"] = {"sequences": nb, "mismatch": int(diff.sum()),
+                             "mismatch_away_from_near_tie": int((diff & ~near).sum()), "near_ties": int(near.sum()),
+                             "comparison": "tokens and accept lengths against the oracle's verify on fp64 logits "
+                                           "of the same bf16 hidden states and heads (differences only at "
+                                           "near-ties: the GPU accumulates in fp32)"}
+        if cpu_budget > 0:
+            rec["cpu_baseline"] = {"value": nb * (K + 1) / el, "unit": "positions/s", "cores": 1, "kind": "oracle",
+                                   "sample": f"{nb} sequences (fp64 GEMV of both heads, then the verify) in {el:.1f} s"}
+    del graph
+    return rec
+
+
+def measured_bf16_tflops():
+    """(bf16 TFLOP/s, source): the burst figure of MEASURED_PEAKS.json, else the fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            v = float(json.load(fh)["bf16_tflops"])
+        return v, "measured bf16_tflops (burst)"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback bf16"
+
+
+def run_calls(args, name: str):
+    """``--calls N``: N plain calls of one workload on the current stream, then
+    exit (for profilers: no graphs, no timing, no oracle)."""
+    import torch
+    import speculative_decoding_verification_39_gb300 as svpkg
+    torch.cuda.set_device(0)
+    svpkg.build()
+    svpkg.set_greedy_path(args.greedy_path)
+    svpkg.set_sample_path(args.sample_path)
+    dev = torch.device("cuda", 0)
+    n = args.calls
+    if name in POOL_WORKLOADS:
+        w = POOL_WORKLOADS[name]
+        ng, last = pool_inputs(w, n)
+        pool = svpkg.NgramPool(w["B"], w["V"], w["N"], w["cap"], device=dev)
+        ng, last = torch.from_numpy(ng).to(dev), torch.from_numpy(last).to(dev)
+        for i in range(n):
+            pool.insert(ng[i])
+            pool.lookup(last[i], w["G"])
+    elif name in LMHEAD_WORKLOADS:
+        w = LMHEAD_WORKLOADS[name]
+        inp = lmhead_inputs(w, dev)
+        for _ in range(n):
+            svpkg.verify_sample_lmhead(inp["ht"], inp["hd"], inp["wt"], inp["wd"], inp["x"], inp["u"], w["T"])
+    else:
+        cfg, mode = workload(name, args.batch)[:2]
+        host = host_inputs(cfg, mode)
+        keys = {"greedy": ("logits", "cand"), "lookahead": ("logits", "cand", "uniforms"),
+                "multidraft": ("target", "draft", "draft_tokens", "uniforms"),
+                "sample": ("target", "draft", "draft_tokens", "uniforms")}[mode]
+        t = [to_torch(host[k], torch).to(dev) for k in keys]
+        for _ in range(n):
+            if mode == "greedy":
+                svpkg.verify_greedy(*t)
+            elif mode == "lookahead":
+                svpkg.verify_lookahead_sample(*t, cfg.temperature)
+            elif mode == "multidraft":
+                svpkg.verify_multidraft_sample(*t, cfg.temperature)
+            else:
+                svpkg.verify_sample(*t, cfg.temperature, cfg.top_p)
+    torch.cuda.synchronize()
+    if svpkg.get_status() != 0:
+        raise RuntimeError("device status set")
+    log(f"[bench] {n} calls of {name}; refined draws so far: {svpkg.refined_draws()}")
+
+
 def run_gpu(args, names: list, rank: int, world: int):
     import torch
     import speculative_decoding_verification_39_gb300 as svpkg
@@ -675,6 +850,8 @@ def run_gpu(args, names: list, rank: int, world: int):
     svpkg.set_greedy_path(args.greedy_path)
     svpkg.set_sample_path(args.sample_path)
     head = names[0]
+    if head in EXTRA_WORKLOADS:
+        raise SystemExit(f"{head} is not a verify call of logits: name it after one (its record is a per_config one)")
     rec = measure(args, head, rank, world, args.steps, 0.0 if args.no_cpu_baseline else args.cpu_budget,
                   counts=not args.no_counts)
     cfg, mode = workload(head, args.batch)[:2]
@@ -707,6 +884,9 @@ def run_gpu(args, names: list, rank: int, world: int):
             if n in POOL_WORKLOADS:
                 r = measure_pool(args, n, max(args.steps, 100), 0.0 if args.no_cpu_baseline else 2.0,
                                  counts=not args.no_counts)
+            elif n in LMHEAD_WORKLOADS:
+                r = measure_lmhead(args, n, max(args.steps, 100), 0.0 if args.no_cpu_baseline else 2.0,
+                                   counts=not args.no_counts)
             else:
                 r = measure(args, n, rank, world, max(args.steps, 100), 0.0 if args.no_cpu_baseline else 2.0,
                             counts=not args.no_counts)
@@ -759,7 +939,8 @@ def run_reference(args, name: str):
 
 
 def all_names() -> list:
-    return list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS) + list(POOL_WORKLOADS)
+    return (list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS) + list(POOL_WORKLOADS) +
+            list(LMHEAD_WORKLOADS))
 
 
 def config_names(spec) -> list:
@@ -770,10 +951,8 @@ def config_names(spec) -> list:
         return [DEFAULT_CONFIG] + [n for n in all_names() if n != DEFAULT_CONFIG]
     names = [n.strip() for n in spec.split(",") if n.strip()]
     for n in names:
-        if n not in POOL_WORKLOADS:
+        if n not in EXTRA_WORKLOADS:
             find_config(n)  # KeyError for an unknown name, before any work
-    if names[0] in POOL_WORKLOADS:
-        raise KeyError(f"{names[0]} cannot be the line's own workload (it is not a verify call)")
     return names
 
 
@@ -799,9 +978,14 @@ def main():
     ap.add_argument("--l2-resident", action="store_true",
                     help="replay one input set, so that inputs that fit stay in L2 (reported as such; not an "
                          "HBM figure)")
+    ap.add_argument("--calls", type=int, default=0,
+                    help="run this many plain calls of the first named workload and exit (for profilers)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     names = config_names(args.config)
+    if args.calls > 0:
+        run_calls(args, names[0])
+        return
     if args.impl == "reference":
         run_reference(args, names[0])
         return

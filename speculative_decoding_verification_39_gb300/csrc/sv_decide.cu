@@ -36,7 +36,6 @@ namespace sv {
 namespace v2 {
 namespace {
 
-constexpr int kWarps = kDecideThreads / 32;  // the most warps a CTA has
 constexpr float kLn2 = 0.693147180559945309f;
 
 __device__ __forceinline__ int nwarps() { return (int)(blockDim.x >> 5); }
@@ -230,7 +229,7 @@ __device__ __forceinline__ void fast_cells(const FastW& fw, const DrawCtx& x, co
 }
 
 template <typename E>
-__global__ void __launch_bounds__(kDecideThreads, 3) decide_kernel(const Params p) {
+__global__ void __launch_bounds__(kDecideThreads, 4) decide_kernel(const Params p) {
   __shared__ Smem sm;
   extern __shared__ float dyn[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -439,22 +438,17 @@ __global__ void __launch_bounds__(kDecideThreads, 3) decide_kernel(const Params 
   __syncthreads();
   cluster_sync();  // (1) rank totals visible
   if (warp == 0 && !bad) {
-    // The ranks' running sums, in rank order, identical in every CTA.
-    df P{0.f, 0.f}, Pme{0.f, 0.f};
-    int owner = -1;
-    df tots[kMaxCluster];
-    for (int q = 0; q < D; ++q) {
-      tots[q] = df{dsmem_ld_f32(&sm.x_tot_h, q), dsmem_ld_f32(&sm.x_tot_l, q)};
-      P = df_add(P, tots[q]);
-    }
-    const df Z = P;
+    // The ranks' running sums, in rank order, identical in every CTA: lane q
+    // reads rank q's total, one warp scan gives every prefix at once.
+    const df mine = lane < D ? df{dsmem_ld_f32(&sm.x_tot_h, (uint32_t)lane), dsmem_ld_f32(&sm.x_tot_l, (uint32_t)lane)}
+                             : df{0.f, 0.f};
+    const df incl = warp_incl_scan_df(mine, lane);
+    const df Z{__shfl_sync(0xffffffffu, incl.h, 31), __shfl_sync(0xffffffffu, incl.l, 31)};
     const df target = df_mul_f(Z, x.u);
-    P = df{0.f, 0.f};
-    for (int q = 0; q < D; ++q) {
-      if (q == (int)rank) Pme = P;
-      P = df_add(P, tots[q]);
-      if (owner < 0 && df_gt(P, target)) owner = q;
-    }
+    const df excl = df_sub(incl, mine);
+    const df Pme{__shfl_sync(0xffffffffu, excl.h, (int)rank), __shfl_sync(0xffffffffu, excl.l, (int)rank)};
+    const uint32_t om = __ballot_sync(0xffffffffu, lane < D && df_gt(incl, target));
+    const int owner = om ? __ffs(om) - 1 : -1;
     const bool need_precise_all = !df_pos(Z) || owner < 0;
     if ((int)rank == owner && !need_precise_all) {
       // the crossing cell: the first whose inclusive sum exceeds the target
@@ -587,7 +581,8 @@ cudaError_t launch_decide(const Params& p, int dtype, cudaStream_t stream) {
 cudaError_t launch_rows(const Params& p, int dtype, cudaStream_t stream);
 
 bool fits(int64_t K, int64_t V) {
-  return K >= 1 && K <= kMaxK && V >= 2 && V <= (int64_t)kMaxCluster * kMaxCellsPerCta * kCellElems;
+  // within what portable clusters of 8 cover (larger clusters only spread the work thinner)
+  return K >= 1 && K <= kMaxK && V >= 2 && V <= (int64_t)8 * kMaxCellsPerCta * kCellElems;
 }
 
 bool fits_topp(int64_t K, int64_t V, int esz) { return fits(K, V) && esz == 2 && V % 8 == 0; }
@@ -634,7 +629,7 @@ void plan(Params& p, int sms) {
   p.ncell = (int)((p.V + kCellElems - 1) / kCellElems);
   int d = (p.ncell + 31) / 32;
   d = d < 1 ? 1 : (d > kMaxCluster ? kMaxCluster : d);
-  // cluster sizes of 1, 2, 4 or 8
+  // cluster sizes of 1, 2, 4, 8 or 16
   int dd = 1;
   while (dd < d) dd <<= 1;
   p.D = dd;
@@ -668,6 +663,9 @@ cudaError_t raise_smem_limit_v2(const void* kernel, size_t bytes) {
   if (e != cudaSuccess) return e;
   (void)bytes;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - 1024);
+  if (e != cudaSuccess) return e;
+  // clusters of 16 (a non-portable size) for the decide kernel's long rows
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
   if (e == cudaSuccess) done.insert({kernel, dev});
   return e;
 }

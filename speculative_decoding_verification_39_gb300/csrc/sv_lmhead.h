@@ -12,7 +12,7 @@ namespace lm {
 constexpr int kTileM = 128;  // rows of hidden states per CTA (TMEM lanes)
 constexpr int kTileN = 128;  // vocabulary entries per CTA (TMEM columns)
 constexpr int kTileK = 64;   // hidden dimension per shared-memory stage
-constexpr int kThreads = 128;
+constexpr int kThreads = 256;
 
 struct Params {
   const uint16_t* h[2];  // bf16 hidden states: [Mrows[i], D] (target rows, then draft rows)

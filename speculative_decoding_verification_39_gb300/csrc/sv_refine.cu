@@ -147,10 +147,12 @@ struct Shared {
   int wi[kWarps];
   float bh[4], bl[4];            // values broadcast to the CTA
   int bi[4];
+  float sh[2], sl[2];            // block_sum2's results
   float th[32], tl[32];          // 2^(i/32) as double-floats
 };
 
-// Sums of two double-floats over the CTA (fixed order); every thread gets both.
+// Sums of two double-floats over the CTA (a fixed shuffle tree, the same in
+// every CTA); every thread gets both.
 __device__ __forceinline__ void block_sum2(df& a, df& b, Shared& s) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 #pragma unroll
@@ -165,14 +167,24 @@ __device__ __forceinline__ void block_sum2(df& a, df& b, Shared& s) {
     s.wl2[warp] = b.l;
   }
   __syncthreads();
-  df x{0.f, 0.f}, y{0.f, 0.f};
-#pragma unroll 1
-  for (int w = 0; w < kWarps; ++w) {
-    x = df_add(x, df{s.wh[w], s.wl[w]});
-    y = df_add(y, df{s.wh2[w], s.wl2[w]});
+  if (warp == 0) {
+    df x = lane < kWarps ? df{s.wh[lane], s.wl[lane]} : df{0.f, 0.f};
+    df y = lane < kWarps ? df{s.wh2[lane], s.wl2[lane]} : df{0.f, 0.f};
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      x = df_add(x, shfl_xor_df(x, o));
+      y = df_add(y, shfl_xor_df(y, o));
+    }
+    if (lane == 0) {
+      s.sh[0] = x.h;
+      s.sl[0] = x.l;
+      s.sh[1] = y.h;
+      s.sl[1] = y.l;
+    }
   }
-  a = x;
-  b = y;
+  __syncthreads();
+  a = df{s.sh[0], s.sl[0]};
+  b = df{s.sh[1], s.sl[1]};
   __syncthreads();
 }
 
@@ -256,20 +268,28 @@ __global__ void __launch_bounds__(kThreads, 1) refine_kernel(const Params p) {
           load_raw<E>(prow, lo + 8 * (int64_t)gn, hi, vec, np);
           if (resid) load_raw<E>(qrow, lo + 8 * (int64_t)gn, hi, vec, nq);
         }
+        // two elements per iteration: independent chains for the scheduler,
+        // while the exp stays a few copies of code
 #pragma unroll 1
-        for (int k = 0; k < 8; ++k) {
-          const df ep = x.e(cp.at(k), x.mp, x.taup);
-          sp = df_add(sp, ep);
+        for (int k = 0; k < 8; k += 2) {
+          const df ep0 = x.e(cp.at(k), x.mp, x.taup);
+          const df ep1 = x.e(cp.at(k + 1), x.mp, x.taup);
+          sp = df_add(sp, df_add(ep0, ep1));
           if (cache) {
-            cph[k * NGc + g] = ep.h;
-            cpl[k * NGc + g] = ep.l;
+            cph[k * NGc + g] = ep0.h;
+            cpl[k * NGc + g] = ep0.l;
+            cph[(k + 1) * NGc + g] = ep1.h;
+            cpl[(k + 1) * NGc + g] = ep1.l;
           }
           if (resid) {
-            const df eq = x.e(cq.at(k), x.mq, x.tauq);
-            sq = df_add(sq, eq);
+            const df eq0 = x.e(cq.at(k), x.mq, x.tauq);
+            const df eq1 = x.e(cq.at(k + 1), x.mq, x.tauq);
+            sq = df_add(sq, df_add(eq0, eq1));
             if (cache) {
-              cqh[k * NGc + g] = eq.h;
-              cql[k * NGc + g] = eq.l;
+              cqh[k * NGc + g] = eq0.h;
+              cql[k * NGc + g] = eq0.l;
+              cqh[(k + 1) * NGc + g] = eq1.h;
+              cql[(k + 1) * NGc + g] = eq1.l;
             }
           }
         }
@@ -287,15 +307,16 @@ __global__ void __launch_bounds__(kThreads, 1) refine_kernel(const Params p) {
         }
         cluster_sync();
         if (warp == 0) {
-          float a[4] = {0.f, 0.f, 0.f, 0.f};
-          if (lane < CL) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) a[i] = dsmem_ld_f32(&s.xs[b][i], (uint32_t)lane);
-          }
+          // lane q holds rank q's sums; one shuffle tree, the same in every CTA
           df Sp{0.f, 0.f}, Sq{0.f, 0.f};
-          for (int q = 0; q < CL; ++q) {  // in rank order, the same in every CTA
-            Sp = df_add(Sp, df{__shfl_sync(0xffffffffu, a[0], q), __shfl_sync(0xffffffffu, a[1], q)});
-            Sq = df_add(Sq, df{__shfl_sync(0xffffffffu, a[2], q), __shfl_sync(0xffffffffu, a[3], q)});
+          if (lane < CL) {
+            Sp = df{dsmem_ld_f32(&s.xs[b][0], (uint32_t)lane), dsmem_ld_f32(&s.xs[b][1], (uint32_t)lane)};
+            Sq = df{dsmem_ld_f32(&s.xs[b][2], (uint32_t)lane), dsmem_ld_f32(&s.xs[b][3], (uint32_t)lane)};
+          }
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) {
+            Sp = df_add(Sp, shfl_xor_df(Sp, o));
+            Sq = df_add(Sq, shfl_xor_df(Sq, o));
           }
           if (lane == 0) {
             const df rr = df_div(Sp, Sq);
@@ -317,10 +338,12 @@ __global__ void __launch_bounds__(kThreads, 1) refine_kernel(const Params p) {
           const int g = c * m + i;
           if (g >= NG) break;
 #pragma unroll 1
-          for (int k = 0; k < 8; ++k) {
-            const df w = weight1(g, k);
-            cs = df_add(cs, w);
-            if (df_pos(w)) lastp = (int)(lo + 8 * (int64_t)g + k);
+          for (int k = 0; k < 8; k += 2) {
+            const df w0 = weight1(g, k);
+            const df w1 = weight1(g, k + 1);
+            cs = df_add(cs, df_add(w0, w1));
+            if (df_pos(w0)) lastp = (int)(lo + 8 * (int64_t)g + k);
+            if (df_pos(w1)) lastp = (int)(lo + 8 * (int64_t)g + k + 1);
           }
         }
         csh[c] = cs.h;
@@ -361,28 +384,24 @@ __global__ void __launch_bounds__(kThreads, 1) refine_kernel(const Params p) {
       }
       cluster_sync();
       if (warp == 0) {
-        float a0 = 0.f, a1 = 0.f;
+        // lane q holds rank q's total: one warp scan gives Z, this rank's
+        // base and the owner (the first rank whose running sum passes u*Z)
+        df t{0.f, 0.f};
         int a2 = -1;
         if (lane < CL) {
-          a0 = dsmem_ld_f32(&s.xs[b][0], (uint32_t)lane);
-          a1 = dsmem_ld_f32(&s.xs[b][1], (uint32_t)lane);
+          t = df{dsmem_ld_f32(&s.xs[b][0], (uint32_t)lane), dsmem_ld_f32(&s.xs[b][1], (uint32_t)lane)};
           a2 = dsmem_ld_s32(&s.xs[b][2], (uint32_t)lane);
         }
-        df Z{0.f, 0.f}, base{0.f, 0.f};
-        int Lall = -1;
-        for (int q = 0; q < CL; ++q) {  // in rank order, the same in every CTA
-          const df t{__shfl_sync(0xffffffffu, a0, q), __shfl_sync(0xffffffffu, a1, q)};
-          if (q < (int)rank) base = df_add(base, t);
-          Z = df_add(Z, t);
-          Lall = max(Lall, __shfl_sync(0xffffffffu, a2, q));
-        }
+        const df inc = warp_incl_scan_df(t, lane);
+        const df Z{__shfl_sync(0xffffffffu, inc.h, 31), __shfl_sync(0xffffffffu, inc.l, 31)};
+        const df exc = df_sub(inc, t);
+        const df base{__shfl_sync(0xffffffffu, exc.h, (int)rank), __shfl_sync(0xffffffffu, exc.l, (int)rank)};
+        int Lall = a2;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Lall = max(Lall, __shfl_xor_sync(0xffffffffu, Lall, o));
         const df target = df_mul_f(Z, r.u);
-        df acc{0.f, 0.f};
-        int owner = -1;
-        for (int q = 0; q < CL; ++q) {
-          acc = df_add(acc, df{__shfl_sync(0xffffffffu, a0, q), __shfl_sync(0xffffffffu, a1, q)});
-          if (owner < 0 && df_gt(acc, target)) owner = q;
-        }
+        const uint32_t om = __ballot_sync(0xffffffffu, lane < CL && df_gt(inc, target));
+        const int owner = om ? __ffs(om) - 1 : -1;
         if (lane == 0) {
           s.bh[1] = Z.h;
           s.bl[1] = Z.l;
@@ -416,27 +435,37 @@ __global__ void __launch_bounds__(kThreads, 1) refine_kernel(const Params p) {
         // rounding between the cluster's totals and this CTA's scan: the
         // range's last positive weight
         if (tid == 0) *out = L;
-      } else if (tid == first) {
-        df C = df_add(base, df_sub(incl, run));
+        break;
+      }
+      if (tid == first) {  // where the crossing thread's run starts, in this CTA's sum
+        const df ex = df_sub(incl, run);
+        s.bh[0] = ex.h;
+        s.bl[0] = ex.l;
+      }
+      __syncthreads();
+      if (warp == 0) {
+        // warp 0 walks that run 32 elements at a time: the first element whose
+        // running sum passes u*Z
+        const int fc0 = min(first * cpt, NC), fc1 = min(fc0 + cpt, NC);
+        const int64_t E0 = lo + 8 * (int64_t)fc0 * m, E1 = min(lo + 8 * (int64_t)fc1 * m, hi);
+        df C = df_add(base, df{s.bh[0], s.bl[0]});
         int t = -1, lw = -1;
-        for (int c = c0; c < c1 && t < 0; ++c) {
-          for (int i = 0; i < m && t < 0; ++i) {
-            const int g = c * m + i;
-            if (g >= NG) break;
-#pragma unroll 1
-            for (int k = 0; k < 8; ++k) {
-              const df w = weight1(g, k);
-              if (df_pos(w)) lw = (int)(lo + 8 * (int64_t)g + k);
-              C = df_add(C, w);
-              if (df_gt(C, target)) {
-                t = (int)(lo + 8 * (int64_t)g + k);
-                break;
-              }
-            }
+        for (int64_t e0 = E0; e0 < E1 && t < 0; e0 += 32) {
+          const int64_t e = e0 + lane;
+          df w{0.f, 0.f};
+          if (e < E1) {
+            const int off = (int)(e - lo);
+            w = weight1(off >> 3, off & 7);
           }
+          const df Ce = df_add(C, warp_incl_scan_df(w, lane));
+          const uint32_t pos = __ballot_sync(0xffffffffu, df_pos(w));
+          if (pos) lw = (int)(e0 + 31 - __clz(pos));
+          const uint32_t cr = __ballot_sync(0xffffffffu, e < E1 && df_gt(Ce, target));
+          if (cr) t = (int)(e0 + __ffs(cr) - 1);
+          C = df{__shfl_sync(0xffffffffu, Ce.h, 31), __shfl_sync(0xffffffffu, Ce.l, 31)};
         }
-        if (t < 0) t = lw >= 0 ? lw : L;  // rounding between the scan and the walk
-        *out = t;
+        // rounding between the scan and the walk: the run's last positive weight
+        if (lane == 0) *out = t >= 0 ? t : (lw >= 0 ? lw : L);
       }
       break;
     }

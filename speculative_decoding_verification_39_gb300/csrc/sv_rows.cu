@@ -301,6 +301,26 @@ struct TpShared {
   int bi[2];
 };
 
+// key_bf16 of the value whose stored 16 bits are h.
+__device__ __forceinline__ uint32_t key16(uint32_t h) {
+  if (h == 0x8000u) h = 0u;
+  return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+}
+
+// The lowest key of the window whose top key is hi.
+__device__ __forceinline__ uint32_t lo_key(uint32_t hi) {
+  return hi >= (uint32_t)(kTpWin - 1) ? hi - (uint32_t)(kTpWin - 1) : 0u;
+}
+
+// Adds 1 to the shared-memory counter at `addr` when `p` holds (predicated,
+// no branch; the address is not touched otherwise).
+__device__ __forceinline__ void red_add_if(uint32_t addr, bool p) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t@q red.shared.add.u32 [%0], 1;\n\t}" ::"r"(addr),
+      "r"((int)p)
+      : "memory");
+}
+
 // Inclusive scan of v over the CTA in thread order; *total gets the sum.
 // `par` picks the partials buffer (alternating calls need no extra barrier).
 __device__ __forceinline__ float tp_scan(float v, float* total, TpShared& s, int& par) {
@@ -355,7 +375,6 @@ __global__ void __launch_bounds__(kTpThreads, 4) topp_rows_kernel(const Params p
     __syncthreads();
     float M = -INFINITY;    // block-uniform running max
     uint32_t hi = 0u;       // key(M) once M > -inf
-    float tlo = INFINITY;   // smallest value in the window: x >= tlo <=> key(x) >= hi - kTpWin + 1
     float sth = 0.f;        // this thread's sum against fl(M c)
     bool valid = true;
     // batches of kTpThreads * kTpVecs vectors (the loop bound is the same in
@@ -396,21 +415,38 @@ __global__ void __launch_bounds__(kTpThreads, 4) topp_rows_kernel(const Params p
         }
         hi = nhi;
         M = Mn;
-        const uint32_t lo = hi >= (uint32_t)(kTpWin - 1) ? hi - (uint32_t)(kTpWin - 1) : 0u;
-        tlo = lo <= key_bf16(-INFINITY) ? -INFINITY : val_bf16(lo);
       }
       const float mref = __fmul_rn(M, c);
+      // Window of positive values only (the usual case): the key of a
+      // positive value is its 16 bits | 0x8000, so the bin of an element is
+      // (M's bits) - (its bits), in the window iff below kTpWin as an
+      // unsigned number (negative values, sign bit set, wrap far past it).
+      // Every lane runs the same predicated code: no divergence.
+      const bool positive = lo_key(hi) > 0x8000u;
+      const uint32_t hb = positive ? hi - 0x8000u : hi;
+      const uint32_t hbase = smem_u32(s.hist.u) + hb * 4u;  // bin of bits (or key) k at hbase - 4k
 #pragma unroll
       for (int u = 0; u < kTpVecs; ++u) {
         float x[8];
         Elem<uint16_t>::unpack(v[u], x);
         float a = 0.f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          a += ex2(fmaf(x[k], c, -mref));
-          if (x[k] >= tlo) atomicAdd(&s.hist.u[hi - key_bf16(x[k])], 1u);
-        }
+        for (int k = 0; k < 8; ++k) a += ex2(fmaf(x[k], c, -mref));
         sth += a;
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        if (positive) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t h = (k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu);
+            red_add_if(hbase - 4u * h, hb - h < (uint32_t)kTpWin);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t key = key16((k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu));
+            red_add_if(hbase - 4u * key, hb - key < (uint32_t)kTpWin);
+          }
+        }
       }
     }
     __syncthreads();  // every count is in

@@ -25,7 +25,7 @@ constexpr int kDecideThreads = 256;
 constexpr int kMaxK = 1024;         // draft tokens per sequence on this path
 constexpr int kCellElems = 256;     // inverse-CDF cell: 32 lanes x 8 elements
 constexpr int kMaxCellsPerCta = 512;
-constexpr int kMaxCluster = 8;      // portable cluster size
+constexpr int kMaxCluster = 16;     // CTAs per sequence in the decide kernel (above 8: a non-portable size)
 constexpr int kMaxChunks = 64;      // chunks per row
 constexpr int kMaxRowsPerItem = 64; // whole short rows per work item of the row pass
 // Chunks hold at most this many bytes of a row.

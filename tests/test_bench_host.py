@@ -61,17 +61,18 @@ def test_reference_arm_prints_one_contract_line():
 def test_config_names():
     assert bench.config_names("cfg2_v32000_bf16") == ["cfg2_v32000_bf16"]
     assert bench.config_names("cfg1_v1000_f32, la_sample_v32000_bf16") == ["cfg1_v1000_f32", "la_sample_v32000_bf16"]
-    every = list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS) + list(bench.POOL_WORKLOADS)
+    every = (list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS) +
+             list(bench.POOL_WORKLOADS) + list(bench.LMHEAD_WORKLOADS))
     # the headline workload (the largest) first, then every other one, each once
     for spec in ("all", None):
         names = bench.config_names(spec)
         assert names[0] == "cfg3_v128256_bf16" and sorted(names) == sorted(every)
     with pytest.raises(KeyError):
         bench.config_names("cfg2_v32000_bf16,nope")
-    # the pool is a per_config record, never the line's own workload
-    assert bench.config_names("cfg2_v32000_bf16,ngram_pool_v32000") == ["cfg2_v32000_bf16", "ngram_pool_v32000"]
-    with pytest.raises(KeyError):
-        bench.config_names("ngram_pool_v32000")
+    # the pool and the LM-head verify are per_config records (or --calls targets)
+    assert bench.config_names("cfg2_v32000_bf16,ngram_pool_v32000,lmhead_d4096_v32000") == [
+        "cfg2_v32000_bf16", "ngram_pool_v32000", "lmhead_d4096_v32000"]
+    assert bench.config_names("ngram_pool_v32000") == ["ngram_pool_v32000"]
 
 
 def test_pool_inputs_are_seeded_and_hit_the_keys():

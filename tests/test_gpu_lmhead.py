@@ -37,8 +37,10 @@ def make(B, K, D, V, T, seed):
     return bf(ht), bf(hd), bf(wt), bf(wd), lt, ld, toks, U
 
 
+# (shapes: one, two and three 128-row tiles of positions per pass; more rows
+# than one pass takes (500 target rows: a pass of 384, then 116); ragged V)
 @pytest.mark.parametrize("B,K,D,V,T", [(4, 3, 128, 1000, 3.0), (40, 5, 256, 4099, 6.0), (1, 1, 64, 130, 2.0),
-                                       (64, 5, 512, 32000, 16.0)])
+                                       (64, 5, 512, 32000, 16.0), (100, 4, 128, 700, 4.0)])
 def test_lmhead_logits_and_verify(B, K, D, V, T):
     ht, hd, wt, wd, lt, ld, toks, U = make(B, K, D, V, T, seed=B + D)
     out_t, out_a, lg = svpkg.verify_sample_lmhead(to_dev(ht), to_dev(hd), to_dev(wt), to_dev(wd), to_dev(toks),
