@@ -150,7 +150,7 @@ struct FastW {
 };
 
 __device__ __forceinline__ df warp_incl_scan_df(df v, int lane) {
-#pragma unroll
+#pragma unroll 1  // once per CTA, cold in the instruction cache
   for (int o = 1; o < 32; o <<= 1) {
     df t;
     t.h = __shfl_up_sync(0xffffffffu, v.h, o);

@@ -644,8 +644,10 @@ __device__ void cells_global(const WF& wf, int64_t CE, int cbeg, int cend, float
 // The crossing, from the cell sums in sh.cells[0, ncells): one warp scans
 // them, finds the cell holding u * Z and walks it. Returns the token to every
 // consumer thread (-1 when every weight is zero).
+// Out of line: it runs once per draw, and inlined into the streaming kernel
+// its double-float arithmetic pushed registers of the streaming loop to spill.
 template <typename E, class WF>
-__device__ int64_t cdf_cross(const WF& wf, int64_t V, float u, Shared& sh, int tid) {
+__device__ __noinline__ int64_t cdf_cross(const WF& wf, int64_t V, float u, Shared& sh, int tid) {
   const int warp = tid >> 5, lane = tid & 31;
   const int64_t CE = cell_elems(V);
   const int64_t m = CE / 256;
@@ -658,7 +660,8 @@ __device__ int64_t cdf_cross(const WF& wf, int64_t V, float u, Shared& sh, int t
     df ls{0.f, 0.f};
     for (int cc = c0; cc < c1; ++cc) ls = df_add(ls, df{sh.cells[cc], 0.f});
     df incl = ls;
-#pragma unroll
+    // (not unrolled: this runs once per draw, cold in the instruction cache)
+#pragma unroll 1
     for (int o = 1; o < 32; o <<= 1) {
       df t2;
       t2.h = __shfl_up_sync(0xffffffffu, incl.h, o);

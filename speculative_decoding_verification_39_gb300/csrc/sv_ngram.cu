@@ -75,6 +75,82 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32) insert_kernel(Pool P, const
   }
 }
 
+// The same insertions with the step's keys staged in shared memory (W <= 32,
+// N <= 33, cap <= 32): one round of loads brings every involved key's count
+// and slots and the step's n-grams in, the warp resolves the W n-grams in
+// order there (an n-gram sees the ones before it under its key), and one
+// round of stores writes back the keys that changed. Per warp, in dynamic
+// shared memory (words): cnt[W] | key[W] | tok[W][N] | ent[W][cap][N-1].
+__device__ __forceinline__ int stage_words(int W, int N, int cap) { return 2 * W + W * N + W * cap * (N - 1); }
+
+__global__ void __launch_bounds__(kWarpsPerCta * 32) insert_staged_kernel(Pool P, const int32_t* ngrams, int W) {
+  extern __shared__ int32_t stage[];
+  grid_dependency_sync(true);
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
+  const int64_t b = (int64_t)blockIdx.x * (blockDim.x >> 5) + wib;
+  if (b >= P.B) return;
+  const int N = P.N, T = N - 1, cap = P.cap;
+  int32_t* cnt = stage + (int64_t)wib * stage_words(W, N, cap);
+  int32_t* key = cnt + W;
+  int32_t* tok = key + W;
+  int32_t* ent = tok + W * N;
+  // the step's n-grams
+  for (int i = lane; i < W * N; i += 32) tok[i] = ngrams[b * (int64_t)W * N + i];
+  __syncwarp();
+  // lane w: its n-gram's key (-1: some token outside [0, V)) and the first
+  // n-gram of the step under the same key (its representative)
+  int k = -1, rep = -1;
+  if (lane < W) {
+    bool ok = true;
+    for (int t = 0; t < N; ++t) {
+      const int32_t v = tok[lane * N + t];
+      ok = ok && v >= 0 && (int64_t)v < P.V;
+    }
+    k = ok ? tok[lane * N] : -1;
+  }
+  for (int w = 0; w < W; ++w) {
+    const int kw = __shfl_sync(0xffffffffu, k, w);
+    if (lane < W && rep < 0 && k >= 0 && kw == k) rep = w;
+  }
+  if (lane < W) key[lane] = rep == lane ? k : -1;  // only representatives load and store
+  __syncwarp();
+  // one round of loads: the representatives' counts and slots
+  if (lane < W && key[lane] >= 0) cnt[lane] = (int32_t)P.dir[b * P.V + key[lane]];
+  for (int i = lane; i < W * cap * T; i += 32) {
+    const int r = i / (cap * T), rest = i - r * cap * T;
+    if (key[r] >= 0) ent[i] = P.slot(b, key[r], rest / T)[rest % T];
+  }
+  __syncwarp();
+  // in order, in shared memory
+  uint32_t dirty = 0;  // representatives whose key changed
+  for (int w = 0; w < W; ++w) {
+    const int kw = __shfl_sync(0xffffffffu, k, w);
+    const int r = __shfl_sync(0xffffffffu, rep, w);
+    if (kw < 0) continue;  // an n-gram with a token outside [0, V): ignored
+    const uint32_t n = (uint32_t)cnt[r];
+    const int held = n < (uint32_t)cap ? (int)n : cap;
+    bool dup = false;
+    for (int h = 0; h < held && !dup; ++h) {
+      const int s = (int)((n - 1 - (uint32_t)h) % (uint32_t)cap);
+      const bool differs = lane < T && ent[(r * cap + s) * T + lane] != tok[w * N + 1 + lane];
+      dup = !__any_sync(0xffffffffu, differs);
+    }
+    if (dup) continue;  // already held: it keeps its place
+    const int s = (int)(n % (uint32_t)cap);
+    if (lane < T) ent[(r * cap + s) * T + lane] = tok[w * N + 1 + lane];
+    __syncwarp();
+    if (lane == 0) cnt[r] = (int32_t)(n + 1);
+    __syncwarp();
+    dirty |= 1u << r;
+  }
+  // one round of stores: the changed keys' slots and counts
+  for (int i = lane; i < W * cap * T; i += 32) {
+    const int r = i / (cap * T), rest = i - r * cap * T;
+    if ((dirty >> r) & 1u) P.slot(b, key[r], rest / T)[rest % T] = ent[i];
+  }
+  if (lane < W && ((dirty >> lane) & 1u)) P.dir[b * P.V + key[lane]] = (uint32_t)cnt[lane];
+}
+
 __global__ void __launch_bounds__(kWarpsPerCta * 32) lookup_kernel(Pool P, const int32_t* last, int G,
                                                                     int32_t* cand, int32_t* count) {
   grid_dependency_sync(true);
@@ -122,10 +198,11 @@ Pool make_pool(void* mem, int64_t B, int64_t V, int32_t N, int32_t cap) {
   return P;
 }
 
-cudaError_t launch_pdl(const void* kernel, unsigned grid, void** args, cudaStream_t st) {
+cudaError_t launch_pdl(const void* kernel, unsigned grid, void** args, cudaStream_t st, size_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kWarpsPerCta * 32);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -165,6 +242,12 @@ extern "C" int sv_ngram_pool_insert(void* pool, int64_t B, int64_t V, int32_t N,
   int W_ = W;
   void* args[] = {&P, &ngrams, &W_};
   const unsigned grid = (unsigned)((B + sv::ng::kWarpsPerCta - 1) / sv::ng::kWarpsPerCta);
+  const size_t staged = (size_t)sv::ng::kWarpsPerCta * (size_t)(2 * W + W * N + W * cap * (N - 1)) * 4;
+  if (W <= 32 && N <= 33 && cap <= 32 && staged <= 48 * 1024)
+    return sv::ng::launch_pdl(reinterpret_cast<const void*>(sv::ng::insert_staged_kernel), grid, args,
+                              static_cast<cudaStream_t>(stream), staged) == cudaSuccess
+               ? SV_OK
+               : SV_ERR_CUDA;
   return sv::ng::launch_pdl(reinterpret_cast<const void*>(sv::ng::insert_kernel), grid, args,
                             static_cast<cudaStream_t>(stream)) == cudaSuccess
              ? SV_OK

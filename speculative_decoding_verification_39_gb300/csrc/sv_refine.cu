@@ -128,8 +128,11 @@ struct Ctx {
 __device__ __forceinline__ df shfl_xor_df(df v, int o) {
   return df{__shfl_xor_sync(0xffffffffu, v.h, o), __shfl_xor_sync(0xffffffffu, v.l, o)};
 }
+// (The shuffle loops of this file are not unrolled: the code after the
+// element loops runs once per launch, cold in the instruction cache, where
+// fewer distinct instructions matter more than the loop's few extra ones.)
 __device__ __forceinline__ df warp_incl_scan_df(df v, int lane) {
-#pragma unroll
+#pragma unroll 1
   for (int o = 1; o < 32; o <<= 1) {
     df t;
     t.h = __shfl_up_sync(0xffffffffu, v.h, o);
@@ -155,7 +158,7 @@ struct Shared {
 // every CTA); every thread gets both.
 __device__ __forceinline__ void block_sum2(df& a, df& b, Shared& s) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-#pragma unroll
+#pragma unroll 1
   for (int o = 16; o > 0; o >>= 1) {
     a = df_add(a, shfl_xor_df(a, o));
     b = df_add(b, shfl_xor_df(b, o));
@@ -170,7 +173,7 @@ __device__ __forceinline__ void block_sum2(df& a, df& b, Shared& s) {
   if (warp == 0) {
     df x = lane < kWarps ? df{s.wh[lane], s.wl[lane]} : df{0.f, 0.f};
     df y = lane < kWarps ? df{s.wh2[lane], s.wl2[lane]} : df{0.f, 0.f};
-#pragma unroll
+#pragma unroll 1
     for (int o = 16; o > 0; o >>= 1) {
       x = df_add(x, shfl_xor_df(x, o));
       y = df_add(y, shfl_xor_df(y, o));
@@ -313,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1) refine_kernel(const Params p) {
             Sp = df{dsmem_ld_f32(&s.xs[b][0], (uint32_t)lane), dsmem_ld_f32(&s.xs[b][1], (uint32_t)lane)};
             Sq = df{dsmem_ld_f32(&s.xs[b][2], (uint32_t)lane), dsmem_ld_f32(&s.xs[b][3], (uint32_t)lane)};
           }
-#pragma unroll
+#pragma unroll 1
           for (int o = 16; o > 0; o >>= 1) {
             Sp = df_add(Sp, shfl_xor_df(Sp, o));
             Sq = df_add(Sq, shfl_xor_df(Sq, o));
@@ -365,16 +368,30 @@ __global__ void __launch_bounds__(kThreads, 1) refine_kernel(const Params p) {
       }
       if (lane == 0) s.wi[warp] = lm;
       __syncthreads();
-      df below{0.f, 0.f}, tot{0.f, 0.f};
-      int L = -1;
-#pragma unroll 1
-      for (int w = 0; w < kWarps; ++w) {
-        const df tw{s.wh[w], s.wl[w]};
-        if (w < warp) below = df_add(below, tw);
-        tot = df_add(tot, tw);
-        L = max(L, s.wi[w]);
+      if (warp == 0) {
+        // the warps' totals scanned by one warp: each warp's base, the CTA's
+        // total and its last positive index
+        const df tw = lane < kWarps ? df{s.wh[lane], s.wl[lane]} : df{0.f, 0.f};
+        int lw = lane < kWarps ? s.wi[lane] : -1;
+        const df wi = warp_incl_scan_df(tw, lane);
+        const df we = df_sub(wi, tw);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lw = max(lw, __shfl_xor_sync(0xffffffffu, lw, o));
+        __syncwarp();
+        if (lane < kWarps) {
+          s.wh2[lane] = we.h;
+          s.wl2[lane] = we.l;
+        }
+        if (lane == 31) {
+          s.sh[0] = wi.h;
+          s.sl[0] = wi.l;
+          s.bi[2] = lw;
+        }
       }
-      incl = df_add(below, incl);  // this CTA's sum up to the end of thread t's run
+      __syncthreads();
+      const df tot{s.sh[0], s.sl[0]};
+      const int L = s.bi[2];
+      incl = df_add(df{s.wh2[warp], s.wl2[warp]}, incl);  // this CTA's sum up to the end of thread t's run
       // exchange the range totals and last positive indices
       const int b = xc++ & 1;
       if (tid == 0) {

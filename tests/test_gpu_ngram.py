@@ -22,9 +22,14 @@ def built():
     yield
 
 
+# (the insert stages a step's keys in shared memory when W <= 32, N <= 33,
+# cap <= 32 and eight warps' stages fit 48 KB: the first four shapes; the
+# others take the direct path)
 @pytest.mark.parametrize("B,V,N,cap,G,W,keys", [(5, 40, 4, 3, 4, 6, 3), (3, 1000, 5, 7, 7, 7, 2),
                                                  (2, 9, 2, 1, 2, 3, 9), (33, 32000, 5, 7, 7, 7, 4),
-                                                 (4, 100, 40, 5, 3, 4, 2)])
+                                                 (3, 60, 33, 32, 6, 32, 3),
+                                                 (4, 100, 40, 5, 3, 4, 2), (3, 50, 3, 40, 5, 5, 2),
+                                                 (2, 200, 4, 4, 4, 40, 3)])
 def test_pool_matches_oracle(B, V, N, cap, G, W, keys):
     rng = np.random.default_rng(B * 1000 + N)
     ref = oracle.NgramPool(B, V, N, cap)
