@@ -241,13 +241,19 @@ KERNEL_SOURCES = {
     "rows_kernel": ("sv_rows.cu", "sv_v2.h", "sv_device.cuh"),
     "topp_rows_kernel": ("sv_rows.cu", "sv_v2.h", "sv_device.cuh"),
     "refine_kernel": ("sv_refine.cu", "sv_refine.h", "sv_df.cuh", "sv_device.cuh"),
-    "decide_kernel": ("sv_decide.cu", "sv_df.cuh", "sv_v2.h", "sv_device.cuh"),
+    "decide_kernel": ("sv_decide.cu", "sv_df.cuh", "sv_v2.h", "sv_refine.h", "sv_device.cuh"),
     "verify_kernel": ("sv_kernels.cu", "sv_device.cuh", "sv_kernels.h"),
     "verify_warp_kernel": ("sv_kernels.cu", "sv_device.cuh", "sv_kernels.h"),
     "verify_seq_kernel": ("sv_kernels.cu", "sv_device.cuh", "sv_kernels.h"),
     "gr_rows_kernel": ("sv_greedy_rows.cu", "sv_greedy_rows.h", "sv_device.cuh"),
     "la_rows_kernel": ("sv_lookahead.cu", "sv_lookahead.h", "sv_device.cuh"),
     "md_rows_kernel": ("sv_multidraft.cu", "sv_multidraft.h", "sv_rowstat.cuh", "sv_device.cuh"),
+    "md_walk_res_kernel": ("sv_multidraft.cu", "sv_multidraft.h", "sv_rowstat.cuh", "sv_device.cuh"),
+    "gr_match_kernel": ("sv_greedy_rows.cu", "sv_greedy_rows.h", "sv_device.cuh"),
+    "la_walk_kernel": ("sv_lookahead.cu", "sv_lookahead.h", "sv_device.cuh"),
+    "insert_staged_kernel": ("sv_ngram.cu", "sv_device.cuh", "sv_sample_impl.h"),
+    "lookup_kernel": ("sv_ngram.cu", "sv_device.cuh", "sv_sample_impl.h"),
+    "lmhead_kernel": ("sv_lmhead.cu", "sv_lmhead.h", "sv_device.cuh"),
 }
 
 
