@@ -218,7 +218,20 @@ __device__ __forceinline__ void fast_cells(const FastW& fw, const DrawCtx& x, co
     const int64_t e = (int64_t)cell * kCellElems + lane * 8;
     float lp[8], lq[8];
     load8<E>(x.prow, e, x.V, lp);
-    if (fw.resid) load8<E>(x.qrow, e, x.V, lq);
+    if (fw.resid) {
+      // the draft's logits matter only where the target's lie in its
+      // nucleus (a weight is 0 where p' is): with top-p most vectors need
+      // none; without it (tp = -inf) every vector does
+      bool need = false;
+#pragma unroll
+      for (int k = 0; k < 8; ++k) need |= lp[k] >= fw.tp;
+      if (need) {
+        load8<E>(x.qrow, e, x.V, lq);
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) lq[k] = -INFINITY;
+      }
+    }
     float w[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) w[k] = fw.w(lp[k], fw.resid ? lq[k] : 0.f);
@@ -369,6 +382,10 @@ __global__ void __launch_bounds__(kDecideThreads, 4) decide_kernel(const Params 
   x.qrow.g = x.resid ? p.draft + ((b * K + j) * V) * p.esz : x.prow.g;
   x.prow.sm = x.qrow.sm = L.slice;
   x.prow.s0 = x.prow.s1 = x.qrow.s0 = x.qrow.s1 = 0;
+  // the rows whose slices are copied: the target's, and the draft's after a
+  // rejection without top-p (with top-p the draft's few logits inside the
+  // target's nucleus are read directly)
+  const int ncopy = x.resid && !p.topp ? 2 : 1;
   if (p.prefetch && !bad && ce > cb) {
     // This CTA's slice of the draw rows, HBM/L2 -> shared memory: the
     // 16-byte aligned part of [cb*256, ce*256) of each row, one bulk copy
@@ -378,7 +395,7 @@ __global__ void __launch_bounds__(kDecideThreads, 4) decide_kernel(const Params 
     const uint32_t cap = (uint32_t)(p.cpr * kCellElems * p.esz);
     RowView* rv[2] = {&x.prow, &x.qrow};
     uint32_t total = 0;
-    for (int k = 0; k < (x.resid ? 2 : 1); ++k) {
+    for (int k = 0; k < ncopy; ++k) {
       const uintptr_t a0 = reinterpret_cast<uintptr_t>(rv[k]->g + e_lo * p.esz);
       const uintptr_t a1 = reinterpret_cast<uintptr_t>(rv[k]->g + e_hi * p.esz);
       const uintptr_t A = (a0 + 15) & ~uintptr_t(15), Z = a1 & ~uintptr_t(15);
@@ -391,7 +408,7 @@ __global__ void __launch_bounds__(kDecideThreads, 4) decide_kernel(const Params 
     }
     if (tid == 0) {
       mbar_arrive_expect_tx(&sm.slice_bar, total);
-      for (int k = 0; k < (x.resid ? 2 : 1); ++k)
+      for (int k = 0; k < ncopy; ++k)
         if (rv[k]->s1 > rv[k]->s0)
           bulk_g2s(const_cast<char*>(rv[k]->sm), rv[k]->g + rv[k]->s0 * p.esz,
                    (uint32_t)((rv[k]->s1 - rv[k]->s0) * p.esz), &sm.slice_bar);
@@ -544,7 +561,7 @@ __global__ void __launch_bounds__(kDecideThreads, 4) decide_kernel(const Params 
 
 size_t decide_smem_bytes(const Params& p) {
   size_t b = sizeof(float) * layout_floats(p.K, p.R, p.cpr) + 16;
-  if (p.prefetch) b += 2 * (size_t)p.cpr * kCellElems * p.esz;
+  if (p.prefetch) b += (p.topp ? 1 : 2) * (size_t)p.cpr * kCellElems * p.esz;
   return b;
 }
 
@@ -627,7 +644,11 @@ void plan(Params& p, int sms) {
   if (p.topp) p.rows_grid = (int64_t)sms * 4;  // the top-p row pass: four CTAs per SM
   if (p.rows_grid > p.items) p.rows_grid = p.items;
   p.ncell = (int)((p.V + kCellElems - 1) / kCellElems);
-  int d = (p.ncell + 31) / 32;
+  // about 32 cells per rank (one warp scan of its cell sums); with top-p,
+  // where only the target row's slice is copied, about 80, so that the
+  // clusters are smaller and more of them reside at once
+  const int per_rank = p.topp ? 80 : 32;
+  int d = (p.ncell + per_rank - 1) / per_rank;
   d = d < 1 ? 1 : (d > kMaxCluster ? kMaxCluster : d);
   // cluster sizes of 1, 2, 4, 8 or 16
   int dd = 1;
@@ -637,8 +658,8 @@ void plan(Params& p, int sms) {
   // threads: one warp per cell of the slice, 2 to 8 warps
   int w = p.cpr < 2 ? 2 : (p.cpr > 8 ? 8 : p.cpr);
   p.dthreads = w * 32;
-  // the slice copies when the two rows' slices fit 96 KB
-  p.prefetch = 2 * (int64_t)p.cpr * kCellElems * p.esz <= 96 * 1024 ? 1 : 0;
+  // the slice copies when the copied rows' slices fit 96 KB
+  p.prefetch = (p.topp ? 1 : 2) * (int64_t)p.cpr * kCellElems * p.esz <= 96 * 1024 ? 1 : 0;
   for (int i = 0; i < 32; ++i) {
     const double v = exp2((double)i / 32.0);
     p.tab_hi[i] = (float)v;

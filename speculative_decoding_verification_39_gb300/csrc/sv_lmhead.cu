@@ -4,24 +4,36 @@
 // §2.1-2.3 takes the target's and the draft's logits as given; with the
 // models' last hidden states h and their LM heads W instead, the logits are
 // h · Wᵀ (one row per position, one column per vocabulary entry). This kernel
-// computes them on the fifth-generation tensor cores:
+// computes them on the fifth-generation tensor cores, as D = W_tile · hᵀ:
 //
 //  - one CTA (256 threads) per 128-entry tile of the vocabulary of one head
-//    (blockIdx.y: 0 target, 1 draft), covering up to 384 positions per pass in
-//    three 128 x 128 fp32 accumulators in tensor memory (512 columns,
-//    allocated by warp 0 with tcgen05.alloc), so that W is read once;
-//  - the hidden dimension goes in 64-wide slices through two shared-memory
-//    stages (the W tile, then the h tiles, each 128 rows x 128 bytes in the
-//    128-byte-swizzled K-major layout): while one thread issues the slice's
-//    tcgen05.mma (K = 16 each, bf16 inputs, fp32 accumulate) and commits them
-//    to the stage's mbarrier, every thread loads the next slice into the
-//    other stage, waiting (bounded) only for the MMAs that last read it;
+//    (blockIdx.y: 0 target, 1 draft); the tile is the MMA's A operand (M =
+//    128, one tensor-memory lane per vocabulary entry) and up to 384
+//    positions per pass are its B operand (N = 256, then the rest), so that
+//    a pass holds every position's accumulator (fp32, 384 of the 512
+//    tensor-memory columns) and W is read once;
+//  - the hidden dimension goes in 64-wide slices through a ring of three
+//    shared-memory stages (the W tile, then up to three 128-row h tiles,
+//    each 128 rows x 128 bytes in the 128-byte-swizzled K-major layout that
+//    the tensor copy writes). One thread issues the tensor copies
+//    (cp.async.bulk.tensor, completing on the stage's "full" mbarrier),
+//    another the tcgen05.mma (K = 16 each, bf16 inputs, fp32 accumulate),
+//    whose commit frees the stage on its "empty" mbarrier;
+//  - with clusters of two CTAs (neighbouring vocabulary tiles, the same
+//    positions), each CTA copies half of the h tiles and the copy engine
+//    multicasts them into both CTAs' stages, halving the h traffic from L2;
+//    a stage is then free once both CTAs' MMAs have read it;
 //  - the epilogue: warp w reads tensor-memory lanes 32(w mod 4) .. +31 (one
-//    position per thread) with tcgen05.ld and writes the fp32 logits.
+//    vocabulary entry per thread) 32 positions at a time with tcgen05.ld, and
+//    the warp's stores to one position's row are 128 contiguous bytes.
+// Every mbarrier wait is bounded; a wait that runs out sets the status word
+// and the kernel winds down, freeing its tensor memory.
 //
 // Products of bf16 values are exact in fp32 and the accumulation is fp32, so
 // the logits equal h · Wᵀ up to fp32 summation rounding (exactly, when the
 // partial sums are integers below 2^24).
+#include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched through the runtime
+
 #include "sv_device.cuh"
 #include "sv_lmhead.h"
 
@@ -29,22 +41,18 @@ namespace sv {
 namespace lm {
 namespace {
 
-constexpr uint32_t kTileBytes = kTileM * kTileK * 2;  // 16 KB, the same for the W tile
-constexpr int kMT = 3;                                 // M tiles per pass: 3 x 128 TMEM columns
-constexpr int kStages = 2;
-constexpr uint32_t kStageBytes = kTileBytes * (1 + kMT);  // the W tile, then the h tiles
-constexpr uint32_t kTmemCols = 512;                    // the power of two above 3 x 128
-constexpr int kChunksPerThread = (1 + kMT) * kTileM * 8 / kThreads;
-static_assert((1 + kMT) * kTileM * 8 % kThreads == 0, "whole chunks per thread");
-// Byte offset of the 16-byte chunk kc (elements 8kc..8kc+7) of row `row` of a
-// 128 x 64 bf16 tile in the 128-byte-swizzled K-major layout: each row is one
-// 128-byte line (the whole 64-wide slice), its chunks permuted by XOR with
-// (row mod 8), so that the eight rows of an 8-row group, which the tensor
-// core reads together, fall on different banks. 8-row groups are 1024 bytes
-// apart; the tile starts on a 1024-byte boundary.
-__device__ __forceinline__ uint32_t tile_off(int row, int kc) {
-  return (uint32_t)(row * 128 + ((kc ^ (row & 7)) << 4));
-}
+constexpr uint32_t kTileBytes = kTileM * kTileK * 2;       // 16 KB: one 128 x 64 bf16 box
+constexpr int kMT = 3;                                      // h tiles (128 positions each) per pass
+constexpr int kPass = kMT * kTileM;                         // positions per pass
+constexpr int kStages = 3;
+constexpr uint32_t kStageBytes = kTileBytes * (1 + kMT);    // the W tile, then the h tiles
+constexpr uint32_t kTmemCols = 512;                         // the power of two above 384
+constexpr int kSmemBytes = (int)(kStages * kStageBytes) + 1024;  // + the 1024-byte alignment
+
+struct Maps {
+  CUtensorMap h[2];  // [Mrows, D] per head, 128 x 64 boxes
+  CUtensorMap w[2];  // [V, D] per head, 128 x 64 boxes
+};
 
 // Shared-memory matrix descriptor of a 128-byte-swizzled K-major operand:
 // start address (>> 4; advanced by 32 bytes per K step of 16 inside the
@@ -62,25 +70,56 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
 
 // Instruction descriptor of kind::f16: fp32 accumulator (bits 4-5 = 1), A and
 // B bf16 (bits 7-9 = 1, 10-12 = 1), both K-major (bits 15, 16 = 0),
-// N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc =
-    (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTileN >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28 (M = 128).
+__device__ __forceinline__ uint32_t idesc(uint32_t n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((uint32_t)(kTileM >> 4) << 24);
+}
 
-__device__ __forceinline__ void mma_bf16(uint32_t taddr, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+__device__ __forceinline__ void mma_bf16(uint32_t taddr, uint64_t adesc, uint64_t bdesc, uint32_t id,
                                          uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(taddr),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "l"(adesc), "l"(bdesc), "r"(id), "r"(accumulate)
       : "memory");
 }
+// Arrive (once) on this CTA's mbarrier when every MMA this thread issued so far is done.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
 }
+// The same on the mbarrier at this offset in every CTA of `mask`.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(mask)
+      : "memory");
+}
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void proxy_fence_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// The 128 x 64 box at (x = column, y = row) of `map` into `dst` (1024-byte
+// aligned), completing on `bar`; x is a multiple of 64 elements (128 bytes).
+__device__ __forceinline__ void tma_load(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+      "[%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// The same box into `dst` of every CTA in `mask`, completing on each one's `bar`.
+__device__ __forceinline__ void tma_load_mc(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar,
+                                            uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 
 // 32 consecutive fp32 columns of this thread's tensor-memory lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
@@ -100,158 +139,235 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
 }
 
-// Chunk c of a stage load: tile t = c / 1024 (0: the W tile, 1..3: h tiles),
-// row (c / 8) % 128 of it, 16-byte chunk c % 8 of the 64-wide slice.
-__global__ void __launch_bounds__(kThreads, 1) lmhead_kernel(const Params p) {
+// CS: CTAs per cluster: 1, or 2 with the h tiles multicast between them.
+template <int CS>
+__global__ void __launch_bounds__(kThreads, 1) lmhead_kernel(const __grid_constant__ Maps maps, const Params p) {
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ uint64_t bar[kStages];
+  __shared__ uint64_t full[kStages], empty[kStages], accb;
   __shared__ uint32_t tmem_base;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int head = blockIdx.y;
   const int64_t M = p.Mrows[head];
-  const int64_t n0 = (int64_t)blockIdx.x * kTileN;
-  const uint16_t* H = p.h[head];
-  const uint16_t* W = p.w[head];
-  const int64_t V = p.V, D = p.D;
+  const int64_t n0 = (int64_t)blockIdx.x * kTileM;
+  const int64_t V = p.V;
+  const uint32_t rank = CS > 1 ? cluster_rank() : 0u;
+  const uint16_t mask = (uint16_t)((1u << CS) - 1u);
+  const CUtensorMap* hm = &maps.h[head];
+  const CUtensorMap* wm = &maps.w[head];
   grid_dependency_sync(true);
-  if (M <= 0) return;  // (uniform per CTA, before any allocation)
+  if (M <= 0) return;  // the same for both CTAs of a cluster (one head), before any allocation
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base)),
-                 "r"((uint32_t)kTmemCols)
+                 "r"(kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
+  if (tid == 32) {
+    prefetch_map(wm);
+    prefetch_map(hm);
+  }
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&bar[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);    // the producer's arrival (plus the stage's bytes)
+      mbar_init(&empty[s], CS);  // one MMA commit per CTA of the cluster
+    }
+    mbar_init(&accb, 1);
     fence_mbar_init();
   }
   tc_fence_before();
-  __syncthreads();
+  if (CS > 1)
+    cluster_sync();  // the peer's barriers are initialised before any copy or commit reaches them
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t taddr = tmem_base;
   // the stages on a 1024-byte boundary (the swizzle atom)
   uint8_t* sbase = smem + ((1024u - (smem_u32(smem) & 1023u)) & 1023u);
-  const int nk = (int)(D / kTileK);
-  uint32_t par[kStages] = {0u, 0u};  // the parity of each barrier's next completion
-  bool ok = true;
-
-  for (int64_t mg = 0; mg < M && ok; mg += (int64_t)kMT * kTileM) {
-    const int nt = (int)min((int64_t)kMT, (M - mg + kTileM - 1) / kTileM);  // M tiles in this group
-    // slice kb of the W tile and the nt h tiles into stage s: every thread
-    // loads its 16 chunks first, then stores them (loads in flight together)
-    auto load = [&](int kb, int s) {
-      uint8_t* st = sbase + (size_t)s * kStageBytes;
-      uint4 v[kChunksPerThread];
-#pragma unroll
-      for (int i = 0; i < kChunksPerThread; ++i) {
-        const int c = tid + i * kThreads;
-        const int t = c >> 10, row = (c >> 3) & (kTileM - 1), kc = c & 7;
-        const int64_t k0 = (int64_t)kb * kTileK + kc * 8;
-        v[i] = make_uint4(0u, 0u, 0u, 0u);
-        if (t == 0) {
-          if (n0 + row < V) v[i] = __ldg(reinterpret_cast<const uint4*>(W + (n0 + row) * D + k0));
-        } else if (t <= nt) {
-          const int64_t m = mg + (int64_t)(t - 1) * kTileM + row;
-          if (m < M) v[i] = __ldg(reinterpret_cast<const uint4*>(H + m * D + k0));
+  const uint32_t sb = smem_u32(sbase);
+  const int nk = (int)(p.D / kTileK);
+  uint32_t it0 = 0;  // slices of all earlier passes (the position in the stage ring)
+  uint32_t pass = 0;
+  bool ok = true;    // this thread's waits all ended in time
+  for (int64_t mg = 0; mg < M; mg += kPass, it0 += (uint32_t)nk, ++pass) {
+    const int rows = (int)min((int64_t)kPass, M - mg);
+    const int nt = (rows + kTileM - 1) / kTileM;
+    if (warp == 0 && lane == 0) {
+      // producer: slice kb of the W tile and the pass's h tiles into stage it % kStages
+      for (int kb = 0; kb < nk; ++kb) {
+        const uint32_t it = it0 + (uint32_t)kb, s = it % kStages, use = it / kStages;
+        if (use > 0 && !mbar_wait(&empty[s], (use - 1u) & 1u)) {
+          ok = false;
+          break;
         }
-      }
-#pragma unroll
-      for (int i = 0; i < kChunksPerThread; ++i) {
-        const int c = tid + i * kThreads;
-        const int t = c >> 10, row = (c >> 3) & (kTileM - 1), kc = c & 7;
-        if (t <= nt) *reinterpret_cast<uint4*>(st + (size_t)t * kTileBytes + tile_off(row, kc)) = v[i];
-      }
-    };
-    load(0, 0);
-    proxy_fence_smem();  // the tensor cores read shared memory through the async proxy
-    __syncthreads();
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb & 1;
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t st = smem_u32(sbase) + (uint32_t)s * kStageBytes;
+        uint8_t* st = sbase + s * kStageBytes;
+        mbar_arrive_expect_tx(&full[s], kTileBytes * (uint32_t)(1 + nt));
+        tma_load(st, wm, kb * kTileK, (int)n0, &full[s]);
         for (int t = 0; t < nt; ++t) {
+          uint8_t* dst = st + (size_t)(1 + t) * kTileBytes;
+          const int y = (int)(mg + (int64_t)t * kTileM);
+          if (CS == 1)
+            tma_load(dst, hm, kb * kTileK, y, &full[s]);
+          else if (t % CS == (int)rank)
+            tma_load_mc(dst, hm, kb * kTileK, y, &full[s], mask);
+        }
+      }
+    } else if (warp == 1 && lane == 0) {
+      // MMA issuer: positions 0..255 of the pass (N = na) to columns 0.., the
+      // rest (N = nb) to columns 256..
+      const uint32_t na = (uint32_t)min(256, (rows + 15) & ~15);
+      const uint32_t nb = rows > 256 ? (uint32_t)((rows - 256 + 15) & ~15) : 0u;
+      for (int kb = 0; kb < nk; ++kb) {
+        const uint32_t it = it0 + (uint32_t)kb, s = it % kStages, use = it / kStages;
+        if (!mbar_wait(&full[s], use & 1u)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = sb + s * kStageBytes;
 #pragma unroll
-          for (int j = 0; j < kTileK / 16; ++j)  // K = 16 per instruction: 32 bytes of each 128-byte row
-            mma_bf16(taddr + (uint32_t)(t * kTileN), smem_desc(st + (uint32_t)(t + 1) * kTileBytes + j * 32),
-                     smem_desc(st + j * 32), kIdesc, (kb > 0 || j > 0) ? 1u : 0u);
+        for (int j = 0; j < kTileK / 16; ++j) {  // K = 16 per instruction: 32 bytes of each 128-byte row
+          const uint64_t a = smem_desc(st + (uint32_t)j * 32u);
+          const uint32_t acc = (kb > 0 || j > 0) ? 1u : 0u;
+          mma_bf16(taddr, a, smem_desc(st + kTileBytes + (uint32_t)j * 32u), idesc(na), acc);
+          if (nb)
+            mma_bf16(taddr + 256u, a, smem_desc(st + kTileBytes + 256u * 128u + (uint32_t)j * 32u), idesc(nb), acc);
         }
-        mma_commit(&bar[s]);
+        if (CS > 1)
+          mma_commit_mc(&empty[s], mask);
+        else
+          mma_commit(&empty[s]);
       }
-      if (kb + 1 < nk) {
-        if (kb >= 1) {
-          // stage s ^ 1 was read by the MMAs of slice kb - 1: let them finish
-          ok = __syncthreads_and(mbar_wait(&bar[s ^ 1], par[s ^ 1]));
-          par[s ^ 1] ^= 1u;
-          if (!ok) break;
-        }
-        load(kb + 1, s ^ 1);
-        proxy_fence_smem();
-        __syncthreads();
-      }
+      mma_commit(&accb);  // every MMA this pass issued (also after a failed wait)
     }
-    // the last one or two commits, in order
-    for (int kb = (nk >= 2 ? nk - 2 : nk - 1); kb < nk && ok; ++kb) {
-      const int s = kb & 1;
-      ok = __syncthreads_and(mbar_wait(&bar[s], par[s]));
-      par[s] ^= 1u;
+    __syncwarp();
+    const bool got = mbar_wait(&accb, pass & 1u);
+    if (!__syncthreads_and(got && ok)) {
+      ok = false;
+      break;
     }
     tc_fence_after();
-    if (!ok) break;
-    // epilogue: warp w reads TMEM lanes 32(w % 4) .. +31 of M tiles w / 4
-    // and w / 4 + 2 (one position per thread), 32 columns at a time
+    // epilogue: warp w reads lanes 32(w % 4) .. +31 (vocabulary entries) and
+    // chunks w / 4, w / 4 + 2, ... of 32 columns (positions)
     const int q = warp & 3;
-    for (int t = warp >> 2; t < nt; t += 2) {
-      const int64_t m = mg + (int64_t)t * kTileM + q * 32 + lane;
-      float* out = p.out[head] + m * V;
+    const int64_t n = n0 + q * 32 + lane;
+    float* out = p.out[head];
+    const int nch = (rows + 31) >> 5;
 #pragma unroll 1
-      for (int c0 = 0; c0 < kTileN; c0 += 32) {
-        float v[32];
-        tmem_ld32(taddr + ((uint32_t)(q * 32) << 16) + (uint32_t)(t * kTileN + c0), v);
-        if (m < M) {
+    for (int ch = warp >> 2; ch < nch; ch += 2) {
+      float v[32];
+      tmem_ld32(taddr + ((uint32_t)(q * 32) << 16) + (uint32_t)(ch * 32), v);
+      if (n < V) {
+        const int64_t m0 = mg + (int64_t)ch * 32;
+        float* o = out + m0 * V + n;
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const int64_t n = n0 + c0 + k;
-            if (n < V) out[n] = v[k];
-          }
-        }
+        for (int k = 0; k < 32; ++k)
+          if (m0 + k < M) o[(int64_t)k * V] = v[k];
       }
     }
-    // the accumulators and stages are free for the next group
+    // the accumulators are free for the next pass
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
   }
-  if (!ok && tid == 0) atomicOr(p.status, kStatusTimeout);
+  // Before this CTA exits, every commit (its own and the peer's) has arrived
+  // on its barriers: the producer waits for the last use of each stage.
+  if (ok && warp == 0 && lane == 0) {
+    for (uint32_t it = it0 > (uint32_t)kStages ? it0 - (uint32_t)kStages : 0u; it < it0; ++it) {
+      if (!mbar_wait(&empty[it % kStages], (it / kStages) & 1u)) {
+        ok = false;
+        break;
+      }
+    }
+  }
   tc_fence_before();
-  __syncthreads();
+  const bool all_ok = __syncthreads_and(ok);
+  if (!all_ok && tid == 0) atomicOr(p.status, kStatusTimeout);
+  if (CS > 1) cluster_sync();  // no copy or commit of the peer reaches this CTA after it exits
   if (warp == 0) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"((uint32_t)kTmemCols)
-                 : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols) : "memory");
   }
 }
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver (through the runtime: no link
+// against the driver library); null when the driver has none.
+EncodeTiled encoder() {
+  static const EncodeTiled fn = []() -> EncodeTiled {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    return reinterpret_cast<EncodeTiled>(f);
+  }();
+  return fn;
+}
+
+// A row-major [rows, D] bf16 matrix in 128 x 64 boxes, 128-byte swizzle;
+// rows past the end read as zeros.
+bool encode_rows(CUtensorMap* map, const uint16_t* base, int64_t rows, int64_t D) {
+  const EncodeTiled enc = encoder();
+  if (!enc) return false;
+  const cuuint64_t dim[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+  const cuuint64_t stride[1] = {(cuuint64_t)D * 2u};
+  const cuuint32_t box[2] = {(cuuint32_t)kTileK, (cuuint32_t)kTileM};
+  const cuuint32_t estride[2] = {1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dim, stride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_maps(Maps& maps, const Params& p) {
+  for (int i = 0; i < 2; ++i) {
+    if (p.Mrows[i] <= 0) return false;
+    if (!encode_rows(&maps.h[i], p.h[i], p.Mrows[i], p.D) || !encode_rows(&maps.w[i], p.w[i], p.V, p.D))
+      return false;
+  }
+  return true;
+}
+
+template <int CS>
+cudaError_t launch_cs(const Maps& maps, const Params& p, cudaStream_t stream) {
+  const unsigned tiles = (unsigned)((p.V + kTileM - 1) / kTileM);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((tiles + CS - 1) / CS * CS, 2u);  // whole clusters (a tile past V stores nothing)
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;  // one CTA per SM: its 512 tensor-memory columns are always free
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  int na = 1;
+  if (CS > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CS;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    na = 2;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  cudaError_t e = cudaFuncSetAttribute(lmhead_kernel<CS>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, lmhead_kernel<CS>, maps, p);
+}
+
+constexpr int kCluster = 2;  // CTAs per cluster of the product launch
 
 }  // namespace
 
 bool fits(int64_t D) { return D >= kTileK && D % kTileK == 0; }
 
 cudaError_t launch(const Params& p, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)((p.V + kTileN - 1) / kTileN), 2u);
-  cfg.blockDim = dim3(kThreads);
-  // two stages of 64 KB; one CTA per SM, so that its 512 TMEM columns are
-  // always free
-  const int smem = (int)(kStages * kStageBytes + 1024);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cudaError_t e = cudaFuncSetAttribute(lmhead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, lmhead_kernel, p);
+  Maps maps;
+  if (!encode_maps(maps, p)) return cudaErrorNotSupported;
+  return launch_cs<kCluster>(maps, p, stream);
 }
 
 }  // namespace lm

@@ -9,8 +9,7 @@
 namespace sv {
 namespace lm {
 
-constexpr int kTileM = 128;  // rows of hidden states per CTA (TMEM lanes)
-constexpr int kTileN = 128;  // vocabulary entries per CTA (TMEM columns)
+constexpr int kTileM = 128;  // rows of a tile: a CTA's vocabulary entries (tensor-memory lanes), or positions
 constexpr int kTileK = 64;   // hidden dimension per shared-memory stage
 constexpr int kThreads = 256;
 

@@ -272,7 +272,7 @@ __global__ void __launch_bounds__(kRowsThreads, 4) rows_kernel(const Params p) {
 // equal logits share one) whose upper set {v : key(l_v) >= tau} holds mass
 // >= top_p * s, and that mass cum. One CTA per row at a time (persistent
 // CTAs, four per SM, taking rows g = blockIdx.x, + gridDim.x, ...); the row
-// streams through registers in batches of 32 KB, and per batch the CTA
+// streams through registers in batches of 24 KB, and per batch the CTA
 //  - raises its running max M (NaN-propagating) and rescales its running sum
 //    s = sum 2^(l c - fl(M c));
 //  - counts the elements whose keys lie in the window of kTpWin keys below
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(kRowsThreads, 4) rows_kernel(const Params p) {
 // the cut.
 constexpr int kTpThreads = 256;
 constexpr int kTpWarps = kTpThreads / 32;
-constexpr int kTpVecs = 8;    // 16-byte vectors per thread and batch: 32 KB per CTA
+constexpr int kTpVecs = 6;    // 16-byte vectors per thread and batch: 24 KB per CTA
 constexpr int kTpWin = 256;   // exact keys counted while the row streams (one bin per thread)
 static_assert(kTpWin == kTpThreads, "one window bin per thread");
 
@@ -299,6 +299,7 @@ struct TpShared {
   float red[2][kTpWarps];
   float bf[2];
   int bi[2];
+  uint32_t spare[32];  // the counts of elements outside the window (one word per lane, never read)
 };
 
 // key_bf16 of the value whose stored 16 bits are h.
@@ -312,13 +313,44 @@ __device__ __forceinline__ uint32_t lo_key(uint32_t hi) {
   return hi >= (uint32_t)(kTpWin - 1) ? hi - (uint32_t)(kTpWin - 1) : 0u;
 }
 
-// Adds 1 to the shared-memory counter at `addr` when `p` holds (predicated,
-// no branch; the address is not touched otherwise).
-__device__ __forceinline__ void red_add_if(uint32_t addr, bool p) {
-  asm volatile(
-      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %1, 0;\n\t@q red.shared.add.u32 [%0], 1;\n\t}" ::"r"(addr),
-      "r"((int)p)
-      : "memory");
+// Adds 1 to the shared-memory counter at `addr` when x >= lo, otherwise to
+// `spare` (a word of this lane's own, never read): the address is selected,
+// the atomic is unconditional, so the code has no branch (a predicated
+// atomic is guarded by one). A NaN compares false.
+__device__ __forceinline__ void red_add_ge(uint32_t addr, uint32_t spare, float x, float lo) {
+  const uint32_t a = x >= lo ? addr : spare;
+  asm volatile("red.shared.add.u32 [%0], 1;" ::"r"(a) : "memory");
+}
+
+// (s0, s1) += (a0, a1): the packed fp32 pair add, rounded exactly as two
+// scalar adds.
+__device__ __forceinline__ void add_x2(float& s0, float& s1, float a0, float a1) {
+  asm("{\n\t.reg .b64 ss, aa;\n\tmov.b64 ss, {%0, %1};\n\tmov.b64 aa, {%2, %3};\n\t"
+      "add.rn.f32x2 ss, ss, aa;\n\tmov.b64 {%0, %1}, ss;\n\t}"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
+// One batch of the streaming pass: the exp2 sum of every element against
+// mref into (s[0], s[1]), and a count at hbase - 4 * bin(h) for every element
+// x >= lo_val (the window: keys follow the values). kPos: the window holds
+// positive values only, so the bin is (M's bits) - (the element's bits);
+// otherwise it is key(M) - key (hbase is set up to match).
+template <bool kPos>
+__device__ __forceinline__ void tp_batch(const uint4* v, float c, float mref, float lo_val, uint32_t hbase,
+                                         uint32_t spare, float* s) {
+#pragma unroll
+  for (int u = 0; u < kTpVecs; ++u) {
+    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float x0 = bf_lo(w[j]), x1 = bf_hi(w[j]);
+      add_x2(s[0], s[1], ex2(fmaf(x0, c, -mref)), ex2(fmaf(x1, c, -mref)));
+      const uint32_t h0 = w[j] & 0xFFFFu, h1 = w[j] >> 16;
+      red_add_ge(hbase - 4u * (kPos ? h0 : key16(h0)), spare, x0, lo_val);
+      red_add_ge(hbase - 4u * (kPos ? h1 : key16(h1)), spare, x1, lo_val);
+    }
+  }
 }
 
 // Inclusive scan of v over the CTA in thread order; *total gets the sum.
@@ -368,6 +400,7 @@ __global__ void __launch_bounds__(kTpThreads, 4) topp_rows_kernel(const Params p
   const int64_t rows = p.B * p.R;
   const int64_t nvec = p.V / 8;  // V is a multiple of 8 and rows start 16-byte aligned
   int par = 0;                   // which red[] buffer the next reduction uses
+  const uint32_t spare = smem_u32(&s.spare[lane]);
   for (int64_t g = blockIdx.x; g < rows; g += gridDim.x) {
     const char* row = row_of(p, g);
     const uint4* vp = reinterpret_cast<const uint4*>(row);
@@ -417,37 +450,22 @@ __global__ void __launch_bounds__(kTpThreads, 4) topp_rows_kernel(const Params p
         M = Mn;
       }
       const float mref = __fmul_rn(M, c);
-      // Window of positive values only (the usual case): the key of a
-      // positive value is its 16 bits | 0x8000, so the bin of an element is
-      // (M's bits) - (its bits), in the window iff below kTpWin as an
-      // unsigned number (negative values, sign bit set, wrap far past it).
-      // Every lane runs the same predicated code: no divergence.
-      const bool positive = lo_key(hi) > 0x8000u;
-      const uint32_t hb = positive ? hi - 0x8000u : hi;
-      const uint32_t hbase = smem_u32(s.hist.u) + hb * 4u;  // bin of bits (or key) k at hbase - 4k
-#pragma unroll
-      for (int u = 0; u < kTpVecs; ++u) {
-        float x[8];
-        Elem<uint16_t>::unpack(v[u], x);
-        float a = 0.f;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) a += ex2(fmaf(x[k], c, -mref));
-        sth += a;
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-        if (positive) {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t h = (k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu);
-            red_add_if(hbase - 4u * h, hb - h < (uint32_t)kTpWin);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t key = key16((k & 1) ? (w[k >> 1] >> 16) : (w[k >> 1] & 0xFFFFu));
-            red_add_if(hbase - 4u * key, hb - key < (uint32_t)kTpWin);
-          }
-        }
-      }
+      // The window [lo, hi] of keys holds exactly the elements x >= val(lo)
+      // (x <= M always). Of positive values only (the usual case), the key
+      // of an element is its 16 bits | 0x8000, so its bin is (M's bits) -
+      // (its bits). Every lane runs the same predicated code: no divergence.
+      // (Keys below that of -inf, 0x7F, are NaN patterns: a window that
+      // reaches them takes every value.)
+      const uint32_t lo = lo_key(hi);
+      const float lo_val = lo > 0x7Fu ? val_bf16(lo) : -INFINITY;
+      const bool positive = lo > 0x8000u;
+      const uint32_t hbase = smem_u32(s.hist.u) + (positive ? hi - 0x8000u : hi) * 4u;
+      float acc[2] = {0.f, 0.f};
+      if (positive)
+        tp_batch<true>(v, c, mref, lo_val, hbase, spare, acc);
+      else
+        tp_batch<false>(v, c, mref, lo_val, hbase, spare, acc);
+      sth += acc[0] + acc[1];
     }
     __syncthreads();  // every count is in
     float S = 0.f, cum = 0.f;

@@ -41,8 +41,9 @@ SAMPLE_CASES = {
     "topp_ragged_bf16": C["cfg5_topp_v151936_bf16"].with_(B=6, K=3, V=20011, top_p=0.8),
     "topp_flat": C["cfg2_v32000_bf16"].with_(B=6, K=2, V=9000, target_sigma=0.05, draft_sigma=0.02, top_p=0.95,
                                              n_peaks=0),
-    # top-p row pass: clusters of 2, 4 and 16 CTAs per row; a flat row whose
-    # cut lies below the first window of keys; a nucleus of about one token
+    # top-p decide: clusters of 2, 4 and 16 CTAs per sequence; a flat row
+    # whose cut lies below the row pass's first window of keys (and whose
+    # nucleus spans the row); a nucleus of about one token
     "topp_d2_v40000": C["cfg5_topp_v151936_bf16"].with_(B=6, K=3, V=40000),
     "topp_d4_flat_v70000": C["cfg2_v32000_bf16"].with_(B=4, K=2, V=70000, target_sigma=0.05, draft_sigma=0.02,
                                                        top_p=0.95, n_peaks=0),
