@@ -141,10 +141,11 @@ __device__ __forceinline__ void load8(const RowView& r, int64_t e, int64_t V, fl
 struct FastW {
   float c, mcp, ip, mcq, iq, tp, tq;
   bool resid;
+  // (the cut selects the exponent, -inf outside the nucleus: no branch)
   __device__ __forceinline__ float w(float lp, float lq) const {
-    const float ep = lp >= tp ? ex2(fmaf(lp, c, -mcp)) : 0.f;
+    const float ep = ex2(lp >= tp ? fmaf(lp, c, -mcp) : -INFINITY);
     if (!resid) return ep;
-    const float eq = lq >= tq ? ex2(fmaf(lq, c, -mcq)) : 0.f;
+    const float eq = ex2(lq >= tq ? fmaf(lq, c, -mcq) : -INFINITY);
     return fmaxf(0.f, fmaf(ep, ip, -eq * iq));
   }
 };
