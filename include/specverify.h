@@ -206,8 +206,10 @@ int sv_verify_multidraft_sample(const void* target, const void* draft, const int
  *            (target rows, then draft rows); without it the library keeps a
  *            workspace per (device, stream), freed by sv_release().
  * The products of bf16 values are exact in fp32 and the sums are fp32: the
- * logits equal h · Wᵀ up to fp32 summation rounding. Three kernels run on
- * `stream`: the GEMM, then the verify's.
+ * logits equal h · Wᵀ up to fp32 summation rounding. On `stream`: the GEMM
+ * (its operands read by tensor copies), then the kernels sv_verify_sample
+ * runs on fp32 logits of this shape. SV_ERR_CUDA also when the driver offers
+ * no tensor-map encoder.
  */
 int sv_verify_sample_lmhead(const void* h_target, const void* h_draft, const void* w_target, const void* w_draft,
                             const int32_t* draft_tokens, const float* uniforms, int64_t B, int32_t K, int64_t D,
