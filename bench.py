@@ -282,6 +282,14 @@ def profiled_traffic(workload_name: str, kernel: str = "verify_kernel"):
     return float(m.group(1))
 
 
+def pool_traffic(workload_name: str):
+    """DRAM bytes of one pool step (its insert and its lookup launch) from the
+    two committed ncu summaries, or None if either is missing or stale."""
+    a = profiled_traffic(workload_name, "insert_staged_kernel")
+    b = profiled_traffic(workload_name, "lookup_kernel")
+    return None if a is None or b is None else a + b
+
+
 def launched_kernel(cfg, mode, args) -> str:
     """The streaming kernel (the one that reads the logits) the library
     launches for this workload, by the library's own selection rule."""
@@ -663,8 +671,8 @@ def measure_pool(args, name: str, steps: int, cpu_budget: float, counts: bool):
         "ms_per_step": ms_per_step,
         "steps": steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": None,
-                     "algorithmic_bytes_per_launch": step_bytes, "kernel": "insert_kernel + lookup_kernel",
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": pool_traffic(name),
+                     "algorithmic_bytes_per_launch": step_bytes, "kernel": "insert_staged_kernel + lookup_kernel",
                      "note": "a few KB per step: the pool is latency-bound (two dependent launches per step), "
                              "not bandwidth-bound",
                      "timing": "CUDA events over one graph of the timed steps"},
@@ -756,7 +764,8 @@ def measure_lmhead(args, name: str, steps: int, cpu_budget: float, counts: bool)
         "ms_per_step": ms_per_step,
         "steps": steps,
         "roofline": {"bound": "tensor", "achieved": tflops, "peak": peak[0], "unit": "TFLOP/s",
-                     "frac": tflops / peak[0], "peak_source": peak[1], "traffic": None,
+                     "frac": tflops / peak[0], "peak_source": peak[1],
+                     "traffic": profiled_traffic(name, "lmhead_kernel"),
                      "algorithmic_flops_per_launch": flops, "kernel": "lmhead_kernel",
                      "note": "whole call (the GEMM of both heads and the verify of its fp32 logits) against the "
                              "GEMM's flops: a lower bound on the GEMM kernel's own rate",

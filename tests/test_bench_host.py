@@ -107,3 +107,18 @@ def test_launched_kernel_topp_streaming_on_request():
         greedy_path = 0
     cfg, mode = bench.workload("cfg5_topp_v151936_bf16")[:2]
     assert bench.launched_kernel(cfg, mode, A) == "verify_kernel"
+
+
+def test_every_record_has_current_profiled_traffic():
+    # Every workload's streaming kernel (and the pool's and the LM head's
+    # kernels) has an ncu summary under profiles/ taken on the sources as they
+    # are: a kernel changed since its capture reads as None here.
+    class A:
+        sample_path = 0
+        greedy_path = 0
+    for name in list(sg.CONFIGS) + list(sg.LOOKAHEAD_CONFIGS) + list(sg.MULTIDRAFT_CONFIGS):
+        cfg, mode = bench.workload(name)[:2]
+        kernel = bench.launched_kernel(cfg, mode, A)
+        assert bench.profiled_traffic(name, kernel) is not None, (name, kernel)
+    assert bench.profiled_traffic("lmhead_d4096_v32000", "lmhead_kernel") is not None
+    assert bench.pool_traffic("ngram_pool_v32000") is not None
