@@ -272,16 +272,19 @@ __global__ void __launch_bounds__(kRowsThreads, 4) rows_kernel(const Params p) {
 // equal logits share one) whose upper set {v : key(l_v) >= tau} holds mass
 // >= top_p * s, and that mass cum. One CTA per row at a time (persistent
 // CTAs, four per SM, taking rows g = blockIdx.x, + gridDim.x, ...); the row
-// streams through registers in batches of 24 KB, and per batch the CTA
-//  - raises its running max M (NaN-propagating) and rescales its running sum
-//    s = sum 2^(l c - fl(M c));
-//  - counts the elements whose keys lie in the window of kTpWin keys below
-//    key(M) (bin i holds key(M) - i); an element below the window costs one
-//    compare. When M rises the window slides up by as many keys: bins that
-//    fall off hold keys below the new window, and no later element can
-//    bring them back.
-// At the end of the row, bin i weighs count * 2^(val(key) c - fl(M c)); the
-// scan from the top key finds the cut. A row whose cut lies below the window
+// streams through registers in batches of 24 KB, and per batch each warp
+// (on its own, with no barrier across the CTA)
+//  - raises its running max M_w (NaN-propagating) and rescales its lanes'
+//    running sums s = sum 2^(l c - fl(M_w c));
+//  - counts its elements whose keys lie in its window of kTpWin keys below
+//    key(M_w) (bin i holds key(M_w) - i). When M_w rises the window slides
+//    up by as many keys: bins that fall off hold keys below the new window,
+//    and no later element can bring them back.
+// At the end of the row the CTA takes M = max M_w, rescales the sums to
+// fl(M c) and merges the windows: as M_w <= M, warp w's window reaches at
+// least as low as the row's window of kTpWin keys below key(M), so it holds
+// every element of its own that lies in it. Bin i of the row's window weighs
+// count * 2^(val(key) c - fl(M c)); the scan from the top key finds the cut. A row whose cut lies below the window
 // (a flat row) is read twice more: once for the masses of coarse bins of 256
 // keys below the window, once for the exact keys of the coarse bin that holds
 // the cut.
@@ -299,7 +302,9 @@ struct TpShared {
   float red[2][kTpWarps];
   float bf[2];
   int bi[2];
-  uint32_t spare[32];  // the counts of elements outside the window (one word per lane, never read)
+  uint32_t spare[32];                // the counts of elements outside the window (one word per lane, never read)
+  uint32_t whist[kTpWarps][kTpWin];  // each warp's window of keys below its running max
+  float wm[kTpWarps];                // each warp's max of the row
 };
 
 // key_bf16 of the value whose stored 16 bits are h.
@@ -404,14 +409,15 @@ __global__ void __launch_bounds__(kTpThreads, 4) topp_rows_kernel(const Params p
   for (int64_t g = blockIdx.x; g < rows; g += gridDim.x) {
     const char* row = row_of(p, g);
     const uint4* vp = reinterpret_cast<const uint4*>(row);
-    s.hist.u[tid] = 0u;
-    __syncthreads();
-    float M = -INFINITY;    // block-uniform running max
-    uint32_t hi = 0u;       // key(M) once M > -inf
-    float sth = 0.f;        // this thread's sum against fl(M c)
-    bool valid = true;
-    // batches of kTpThreads * kTpVecs vectors (the loop bound is the same in
-    // every thread: the batch holds barriers)
+    uint32_t* wh = s.whist[warp];
+#pragma unroll
+    for (int k = 0; k < kTpWin / 32; ++k) wh[lane + 32 * k] = 0u;
+    __syncwarp();
+    float Mw = -INFINITY;  // this warp's running max (the same in its lanes)
+    uint32_t hw = 0u;      // key(Mw) once Mw > -inf
+    float sth = 0.f;       // this thread's sum against fl(Mw c)
+    // batches of kTpThreads * kTpVecs vectors; each warp keeps its own max and
+    // window, so a batch takes no barrier across the CTA
     for (int64_t b0 = 0; b0 < nvec; b0 += (int64_t)kTpThreads * kTpVecs) {
       uint4 v[kTpVecs];
 #pragma unroll
@@ -422,44 +428,43 @@ __global__ void __launch_bounds__(kTpThreads, 4) topp_rows_kernel(const Params p
       float bm = Elem<uint16_t>::vmax(v[0]);
 #pragma unroll
       for (int u = 1; u < kTpVecs; ++u) bm = fmax_nan(bm, Elem<uint16_t>::vmax(v[u]));
-      bm = warp_max_nan(bm);
-      if (lane == 0) s.red[par][warp] = bm;
-      __syncthreads();
-      float Mn = M;
-#pragma unroll
-      for (int w = 0; w < kTpWarps; ++w) Mn = fmax_nan(Mn, s.red[par][w]);
-      par ^= 1;
-      if (!(Mn < INFINITY)) {  // a NaN or +inf: the row is invalid (uniform)
-        M = Mn;
-        valid = false;
+      const float Mn = fmax_nan(Mw, warp_max_nan(bm));
+      if (!(Mn < INFINITY)) {  // a NaN or +inf: the row is invalid
+        Mw = Mn;
         break;
       }
-      if (Mn == -INFINITY) continue;  // only -inf so far (uniform)
-      if (Mn != M) {                  // uniform: every thread took the same max
-        if (M > -INFINITY) sth *= ex2(__fsub_rn(__fmul_rn(M, c), __fmul_rn(Mn, c)));
+      if (Mn == -INFINITY) continue;  // only -inf so far
+      if (Mn != Mw) {
+        if (Mw > -INFINITY) sth *= ex2(__fsub_rn(__fmul_rn(Mw, c), __fmul_rn(Mn, c)));
         const uint32_t nhi = key_bf16(Mn);
-        if (M > -INFINITY && nhi != hi) {
-          // slide the window up by d keys: bin i now holds what bin i - d held
-          const uint32_t dk = nhi - hi;
-          const uint32_t t = (uint32_t)tid >= dk ? s.hist.u[tid - dk] : 0u;
-          __syncthreads();
-          s.hist.u[tid] = t;
-          __syncthreads();
+        if (Mw > -INFINITY && nhi != hw) {
+          // slide the window up by dk keys: bin i now holds what bin i - dk held
+          const uint32_t dk = nhi - hw;
+          uint32_t t[kTpWin / 32];
+#pragma unroll
+          for (int k = 0; k < kTpWin / 32; ++k) {
+            const uint32_t i = (uint32_t)(lane + 32 * k);
+            t[k] = i >= dk ? wh[i - dk] : 0u;
+          }
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < kTpWin / 32; ++k) wh[lane + 32 * k] = t[k];
+          __syncwarp();
         }
-        hi = nhi;
-        M = Mn;
+        hw = nhi;
+        Mw = Mn;
       }
-      const float mref = __fmul_rn(M, c);
-      // The window [lo, hi] of keys holds exactly the elements x >= val(lo)
-      // (x <= M always). Of positive values only (the usual case), the key
-      // of an element is its 16 bits | 0x8000, so its bin is (M's bits) -
-      // (its bits). Every lane runs the same predicated code: no divergence.
+      const float mref = __fmul_rn(Mw, c);
+      // The window [lo, hw] of keys holds exactly the elements x >= val(lo)
+      // (x <= Mw always). Of positive values only (the usual case), the key
+      // of an element is its 16 bits | 0x8000, so its bin is (Mw's bits) -
+      // (its bits). Every lane runs the same code: no divergence.
       // (Keys below that of -inf, 0x7F, are NaN patterns: a window that
       // reaches them takes every value.)
-      const uint32_t lo = lo_key(hi);
+      const uint32_t lo = lo_key(hw);
       const float lo_val = lo > 0x7Fu ? val_bf16(lo) : -INFINITY;
       const bool positive = lo > 0x8000u;
-      const uint32_t hbase = smem_u32(s.hist.u) + (positive ? hi - 0x8000u : hi) * 4u;
+      const uint32_t hbase = smem_u32(wh) + (positive ? hw - 0x8000u : hw) * 4u;
       float acc[2] = {0.f, 0.f};
       if (positive)
         tp_batch<true>(v, c, mref, lo_val, hbase, spare, acc);
@@ -467,18 +472,41 @@ __global__ void __launch_bounds__(kTpThreads, 4) topp_rows_kernel(const Params p
         tp_batch<false>(v, c, mref, lo_val, hbase, spare, acc);
       sth += acc[0] + acc[1];
     }
-    __syncthreads();  // every count is in
+    if (lane == 0) s.wm[warp] = Mw;
+    __syncthreads();  // every count and every warp's max is in
+    // the row's max (a NaN or +inf in any warp: the row is invalid)
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kTpWarps; ++w) M = fmax_nan(M, s.wm[w]);
+    const bool valid = M < INFINITY;
+    uint32_t hi = 0u;
     float S = 0.f, cum = 0.f;
     uint32_t tau = 0u;
     if (valid && M > -INFINITY) {
       const float mref = __fmul_rn(M, c);
+      hi = key_bf16(M);
+      // this thread's sum against fl(M c) (its warp's reference is at most that)
+      sth = Mw > -INFINITY ? sth * ex2(__fsub_rn(__fmul_rn(Mw, c), mref)) : 0.f;
       float tot;
       (void)tp_scan(sth, &S, s, par);
       cum = S;
       const float target = p.top_p * S;
       const uint32_t lo = hi >= (uint32_t)(kTpWin - 1) ? hi - (uint32_t)(kTpWin - 1) : 0u;
-      // the window: bin t is key hi - t
-      const uint32_t cnt = (uint32_t)tid <= hi - lo ? s.hist.u[tid] : 0u;
+      // the window: bin t is key hi - t, the warps' windows merged (warp w's
+      // bin j holds key key(M_w) - j; as M_w <= M, its window reaches at
+      // least as low as the row's, so it counted every element of its own
+      // in the row's window)
+      uint32_t cnt = 0u;
+      if ((uint32_t)tid <= hi - lo) {
+#pragma unroll
+        for (int w = 0; w < kTpWarps; ++w) {
+          const float mw = s.wm[w];
+          if (mw > -INFINITY) {
+            const uint32_t j = (uint32_t)tid - (hi - key_bf16(mw));  // wraps past kTpWin when below bin 0
+            if (j < (uint32_t)kTpWin) cnt += s.whist[w][j];
+          }
+        }
+      }
       float m = cnt ? (float)cnt * ex2(fmaf(val_bf16(hi - (uint32_t)tid), c, -mref)) : 0.f;
       float incl = tp_scan(m, &tot, s, par);
       int t = tp_first(incl >= target, s);
