@@ -199,7 +199,8 @@ int sv_verify_multidraft_sample(const void* target, const void* draft, const int
  *            the positions whose logits sv_verify_sample would take.
  *   w_target, w_draft [V, D] bf16: the two LM heads (row v is vocabulary
  *            entry v).
- *   D a multiple of 64; the four arrays 16-byte aligned.
+ *   D a multiple of 64, below 2^31; B*(2K+1) < 2^31; the four arrays
+ *            16-byte aligned.
  *   draft_tokens, uniforms, B, K, V, temperature (> 0), top_p, out_tokens,
  *   out_accept_len: as for sv_verify_sample.
  *   out_logits nullable [B*(K+1) + B*K, V] fp32: where to put the logits

@@ -629,6 +629,9 @@ extern "C" int sv_verify_sample_lmhead(const void* h_target, const void* h_draft
                                        int32_t* out_tokens, int32_t* out_accept_len, float* out_logits,
                                        void* stream) {
   if (B < 0 || K < 1 || V < 2 || V >= kMaxV || K > (1 << 20) || !sv::lm::fits(D)) return SV_ERR_ARG;
+  // the tensor copies address rows and columns with signed 32-bit coordinates
+  if (B > (int64_t(1) << 31) || B * (2 * (int64_t)K + 1) >= (int64_t(1) << 31) || D >= (int64_t(1) << 31))
+    return SV_ERR_ARG;
   if (!(temperature > 0.f) || std::isinf(temperature)) return SV_ERR_ARG;
   if (!(top_p > 0.f && top_p <= 1.f)) return SV_ERR_ARG;
   if (B == 0) return SV_OK;

@@ -97,6 +97,18 @@ def test_host_argument_checks(lib):
     assert md(p, None, p, p, 4, 7, 5, 100, 1, 1.0, p, p, None, None, None) == -1  # no draft
     assert md(p, q, p, p, 4, 7, 5, 100, 1, 1.0, p, p, None, None, None) == -2    # misaligned draft
     assert md(None, None, None, None, 0, 7, 5, 100, 1, 1.0, None, None, None, None, None) == 0
+    # the verify on hidden states: its argument checks come before any device work
+    lm = lib.sv_verify_sample_lmhead
+    assert lm(p, p, p, p, p, p, 2, 1, 100, 50, 1.0, 1.0, p, p, None, None) == -1       # D not a multiple of 64
+    assert lm(p, p, p, p, p, p, 2, 1, 64, 50, 0.0, 1.0, p, p, None, None) == -1        # T = 0
+    assert lm(p, p, p, p, p, p, 2, 1, 64, 50, 1.0, 0.0, p, p, None, None) == -1        # top_p = 0
+    assert lm(p, p, p, p, p, p, 2, 0, 64, 50, 1.0, 1.0, p, p, None, None) == -1        # K < 1
+    assert lm(p, p, p, p, p, p, 2, 1, 64, 1, 1.0, 1.0, p, p, None, None) == -1         # V < 2
+    assert lm(p, p, p, p, p, p, 1 << 30, 1, 64, 50, 1.0, 1.0, p, p, None, None) == -1  # B(2K+1) >= 2^31
+    assert lm(None, p, p, p, p, p, 2, 1, 64, 50, 1.0, 1.0, p, p, None, None) == -1     # no target states
+    assert lm(p, p, p, None, p, p, 2, 1, 64, 50, 1.0, 1.0, p, p, None, None) == -1     # no draft head
+    assert lm(q, p, p, p, p, p, 2, 1, 64, 50, 1.0, 1.0, p, p, None, None) == -2        # misaligned states
+    assert lm(None, None, None, None, None, None, 0, 1, 64, 50, 1.0, 1.0, None, None, None, None) == 0
     assert lib.sv_set_greedy_path(2) == -1 and lib.sv_set_greedy_path(-1) == -1
     assert lib.sv_set_launch_shape(7, 1) == -1
     assert lib.sv_set_launch_shape(0, 0) == 0
